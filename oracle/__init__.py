@@ -1,0 +1,200 @@
+"""CPU oracle for the fused MXFP4 MoE layer forward -- TEST INFRASTRUCTURE.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
+leg may import this package.  It wraps ``moe_oracle.cpp`` (plain C++17, fp64,
+brute force), which shares no code with the GPU library.
+
+Functions and the passages they follow (reference page titles):
+  route      -- top-k with renormalised softmax weights; the shared expert's
+                weight sigmoid(fp32(logit)) * scale ("[sglang] SGLang MoE
+                shared expert: fuse 3 kernels into 1", kernel change).
+  sort       -- prepare_moe_input's expert_offsets / a_map / c_map ("[SGLang]
+                CUTLASS MoE", section 1) and the virtual experts of kBlockN rows
+                ("[sglang] ... MXFP4 decode MoE ... shape templates",
+                sections 1 and 5, including the expert_offset slice).
+  forward    -- the dataflow of the "[SGLang] CUTLASS MoE" structure diagram
+                with MXFP8 activations, MXFP4 weights, silu_and_mul (section 4)
+                and apply_shuffle_mul_sum (section 5).
+  quantize_* -- the OCP MX v1.0 conversion rule for E2M1 / E4M3 blocks of 32.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "moe_oracle.cpp")
+_SO = os.path.join(_HERE, "_build", "liboracle.so")
+_lib = None
+
+FMT_E2M1 = 0
+FMT_E4M3 = 1
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with g++ (no fast-math, no FMA contraction)."""
+    if not force and os.path.exists(_SO) and os.path.getmtime(_SO) >= os.path.getmtime(_SRC):
+        return _SO
+    os.makedirs(os.path.dirname(_SO), exist_ok=True)
+    tmp = _SO + ".tmp%d" % os.getpid()
+    cmd = ["g++", "-std=c++17", "-O2", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math",
+           "-o", tmp, _SRC]
+    subprocess.check_call(cmd)
+    os.replace(tmp, _SO)
+    return _SO
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        build()
+        L = ctypes.CDLL(_SO)
+        P = ctypes.c_void_p
+        i32, i64, dbl = ctypes.c_int, ctypes.c_int64, ctypes.c_double
+        L.oracle_e2m1_value.restype = dbl
+        L.oracle_e2m1_value.argtypes = [i32]
+        L.oracle_e4m3_value.restype = dbl
+        L.oracle_e4m3_value.argtypes = [i32]
+        L.oracle_e8m0_value.restype = dbl
+        L.oracle_e8m0_value.argtypes = [i32]
+        L.oracle_bf16_rne.restype = ctypes.c_uint16
+        L.oracle_bf16_rne.argtypes = [dbl]
+        L.oracle_mx_quantize_block.restype = None
+        L.oracle_mx_quantize_block.argtypes = [P, i32, i32, P, P]
+        L.oracle_quantize_mxfp4.restype = None
+        L.oracle_quantize_mxfp4.argtypes = [P, i64, i64, P, P]
+        L.oracle_quantize_mxfp8_bf16.restype = None
+        L.oracle_quantize_mxfp8_bf16.argtypes = [P, i64, i64, P, P]
+        L.oracle_route.restype = None
+        L.oracle_route.argtypes = [i32, i32, i32, P, i32, P, dbl, P, P]
+        L.oracle_sort.restype = i32
+        L.oracle_sort.argtypes = [i32, i32, P, i32, i32, i32, i32, i32, P, P, P, P, P]
+        L.oracle_forward.restype = i32
+        L.oracle_forward.argtypes = [i32] * 8 + [P] * 8 + [i32] + [P] * 7
+        _lib = L
+    return _lib
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+# ------------------------------------------------------------------ formats
+def e2m1_value(code: int) -> float:
+    return lib().oracle_e2m1_value(int(code))
+
+
+def e4m3_value(code: int) -> float:
+    return lib().oracle_e4m3_value(int(code))
+
+
+def e8m0_value(code: int) -> float:
+    return lib().oracle_e8m0_value(int(code))
+
+
+def bf16_rne(d: float) -> int:
+    return int(lib().oracle_bf16_rne(float(d)))
+
+
+def mx_quantize_block(values, fmt: int):
+    """One MX block (any length): returns (codes uint8[n], scale_code int)."""
+    v = _c(values, np.float64)
+    codes = np.zeros(v.size, np.uint8)
+    sc = np.zeros(1, np.uint8)
+    lib().oracle_mx_quantize_block(_p(v), v.size, fmt, _p(codes), _p(sc))
+    return codes, int(sc[0])
+
+
+def quantize_mxfp4(w):
+    """fp32 [rows, K] -> (packed E2M1 codes uint8 [rows, K/2], E8M0 uint8 [rows, K/32])."""
+    w = _c(w, np.float32)
+    rows, K = w.shape
+    codes = np.zeros((rows, K // 2), np.uint8)
+    scales = np.zeros((rows, K // 32), np.uint8)
+    lib().oracle_quantize_mxfp4(_p(w), rows, K, _p(codes), _p(scales))
+    return codes, scales
+
+
+def quantize_mxfp8_bf16(x_bits):
+    """bf16 bits uint16 [rows, K] -> (E4M3 codes uint8 [rows, K], E8M0 uint8 [rows, K/32])."""
+    x = _c(x_bits, np.uint16)
+    rows, K = x.shape
+    codes = np.zeros((rows, K), np.uint8)
+    scales = np.zeros((rows, K // 32), np.uint8)
+    lib().oracle_quantize_mxfp8_bf16(_p(x), rows, K, _p(codes), _p(scales))
+    return codes, scales
+
+
+# ------------------------------------------------------------------ routing
+def route(logits, top_k: int, num_shared: int = 0, shared_logit=None, shared_scale: float = 1.0):
+    """logits fp32 [T, Eg] -> (ids int32 [T, k+S], weights float64 [T, k+S])."""
+    lg = _c(logits, np.float32)
+    T, Eg = lg.shape
+    kp = top_k + num_shared
+    ids = np.zeros((T, kp), np.int32)
+    w = np.zeros((T, kp), np.float64)
+    sl = None if num_shared == 0 else _c(shared_logit, np.uint16).reshape(T, num_shared)
+    lib().oracle_route(T, Eg, top_k, _p(lg), num_shared, _p(sl), float(shared_scale), _p(ids), _p(w))
+    return ids, w
+
+
+def sort(ids, E_global: int, E_local: int, expert_offset: int, num_shared: int, block_n: int):
+    """ids int32 [T, k'] -> dict with counts, offsets, a_map, c_map, vinfo [num_v, 4], num_v."""
+    ids = _c(ids, np.int32)
+    T, kp = ids.shape
+    Et = E_local + num_shared
+    counts = np.zeros(Et, np.int32)
+    offsets = np.zeros(Et + 1, np.int32)
+    c_map = np.zeros(T * kp, np.int32)
+    a_map = np.full(T * kp, -1, np.int32)
+    vmax = Et + (T * kp) // block_n + 1
+    vinfo = np.zeros((vmax, 4), np.int32)
+    nv = lib().oracle_sort(T, kp, _p(ids), E_global, E_local, expert_offset, num_shared, block_n,
+                           _p(counts), _p(offsets), _p(a_map), _p(c_map), _p(vinfo))
+    R = int(offsets[-1])
+    return dict(counts=counts, offsets=offsets, a_map=a_map[:R].copy(), c_map=c_map,
+                vinfo=vinfo[:nv].copy(), num_v=int(nv))
+
+
+# ------------------------------------------------------------------ forward
+def forward(x_bits, ids, w, wmap, w1, w1s, w2, w2s, *, H: int, I: int, E_global: int, E_local: int,
+            expert_offset: int, num_shared: int, tokens=None, want_act: bool = False, want_xq: bool = False):
+    """Layer forward for ``tokens`` (default: all).
+
+    x_bits uint16 [T, H] (bf16); ids int32 [T, k']; w float64 [T, k'];
+    wmap int32 [E_local + S] -> index into the compact weight arrays
+    w1 [n, 2I, H/2], w1s [n, 2I, H/32], w2 [n, H, I/2], w2s [n, H, I/32].
+    Returns dict(out_f64, out_bf16 (uint16 bits), [act, act_sf], [xq, xq_sf]).
+    """
+    x = _c(x_bits, np.uint16)
+    ids = _c(ids, np.int32)
+    w = _c(w, np.float64)
+    T, kp = ids.shape
+    toks = _c(np.arange(T) if tokens is None else tokens, np.int32)
+    n = toks.size
+    out = np.zeros((n, H), np.float64)
+    outb = np.zeros((n, H), np.uint16)
+    act = np.zeros((n, kp, I), np.uint8) if want_act else None
+    acts = np.zeros((n, kp, I // 32), np.uint8) if want_act else None
+    xq = np.zeros((n, H), np.uint8) if want_xq else None
+    xqs = np.zeros((n, H // 32), np.uint8) if want_xq else None
+    arrs = [_c(a, np.uint8) for a in (w1, w1s, w2, w2s)]
+    wm = _c(wmap, np.int32)
+    rc = lib().oracle_forward(T, H, I, kp, E_global, E_local, expert_offset, num_shared, _p(x), _p(ids), _p(w),
+                              _p(wm), *[_p(a) for a in arrs], n, _p(toks), _p(out), _p(outb), _p(act), _p(acts),
+                              _p(xq), _p(xqs))
+    if rc != 0:
+        raise ValueError("oracle_forward: a routed expert has no weights in wmap")
+    res = dict(out_f64=out, out_bf16=outb)
+    if want_act:
+        res.update(act=act, act_sf=acts)
+    if want_xq:
+        res.update(xq=xq, xq_sf=xqs)
+    return res
