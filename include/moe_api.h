@@ -1,0 +1,202 @@
+/*
+ * moe_api.h -- C ABI of the GB300 (sm_103a) fused MXFP4 Mixture-of-Experts
+ * layer forward.
+ *
+ * The layer (reference pages: "[SGLang] CUTLASS MoE", structure diagram;
+ * "[sglang] Kimi-K3.1 MXFP4 decode MoE kernel generalised to shape templates",
+ * sections 1-5; "[sglang] SGLang MoE shared expert: fuse 3 kernels into 1"):
+ *
+ *   route  : top-k of the router logits, weights renormalised over the picks,
+ *            optional appended shared expert with weight sigmoid(logit)*scale
+ *   sort   : token -> expert rows (expert_offsets, a_map, c_map) and virtual
+ *            experts of block_n rows
+ *   forward: x -> MXFP8, FC1 = [gate | up] on E2M1 weights, silu(gate)*up ->
+ *            MXFP8, FC2, weighted un-permute combine -> bf16 out
+ *
+ * Ownership: the caller allocates every buffer (device memory unless stated).
+ * The library never allocates device memory, never frees and never
+ * synchronises the stream; every call is asynchronous on `stream` and, except
+ * moe_layer_host, capturable in a CUDA graph.
+ *
+ * Errors: calls return MOE_OK (0) or a negative MOE_ERR_* code.  Argument
+ * errors are detected on the host and launch nothing.  Errors found on the
+ * device (a bounded wait that expired) are recorded in the workspace status
+ * word, read with moe_get_status after the stream has been synchronised.
+ *
+ * Data formats:
+ *   bf16       : uint16_t bit patterns.
+ *   E2M1       : 4-bit codes, two per byte, element 2i in the low nibble.
+ *   E4M3 / E8M0: one byte per element / per 32-element block.
+ *   MX blocks  : one E8M0 scale per 32 consecutive elements along K (the
+ *                contiguous dimension), OCP MX v1.0 conversion rule.
+ */
+#ifndef MOE_API_H
+#define MOE_API_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* moe_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+enum {
+    MOE_OK = 0,
+    MOE_ERR_NULL = -1,      /* a required pointer is NULL */
+    MOE_ERR_SHAPE = -2,     /* shape outside moe_is_supported */
+    MOE_ERR_ALIGN = -3,     /* a pointer misses its documented alignment */
+    MOE_ERR_WORKSPACE = -4, /* workspace smaller than moe_workspace_bytes */
+    MOE_ERR_CUDA = -5,      /* a CUDA runtime/driver call failed */
+    MOE_ERR_TIMEOUT = -6    /* device status: a bounded wait expired */
+};
+
+enum { MOE_ACT_SWIGLU = 0 }; /* silu(gate) * up, gate = W1 rows [0, I), up = rows [I, 2I) */
+
+/* Shape of one layer call.
+ *   T            tokens in this call (0 <= T <= max_T)
+ *   max_T        tokens the workspace is sized for
+ *   E_global     routed experts in the logit space (columns of the logits)
+ *   E_local      routed experts whose weights live here
+ *   expert_offset global id of local expert 0; ids outside
+ *                [expert_offset, expert_offset + E_local) get no row
+ *                ("... MXFP4 decode MoE ... shape templates", section 5)
+ *   top_k        routed experts per token
+ *   num_shared   0 or 1 shared experts appended to every token, global id
+ *                E_global + s, local weight slot E_local + s
+ *   hidden, inter H and I
+ *   block_n      rows per virtual expert: 16 or 32 (decode tiling) or 128
+ *                (prefill tiling); results do not depend on it
+ *   activation   MOE_ACT_SWIGLU
+ *   shared_scale multiplies the shared expert's sigmoid weight (e.g.
+ *                1/ep_size, "... shared expert: fuse 3 kernels into 1") */
+typedef struct moe_shape {
+    int32_t T, max_T, E_global, E_local, expert_offset, top_k, num_shared;
+    int32_t hidden, inter, block_n, activation;
+    float shared_scale;
+} moe_shape;
+
+/* Packed expert weights (device, read only), E_tot = E_local + num_shared:
+ *   w1     E2M1 codes [E_tot, 2I, H/2], 32-byte aligned
+ *   w1_sf  E8M0 scales packed by moe_pack_scales from [E_tot*2I, H/32]
+ *   w2     E2M1 codes [E_tot, H, I/2], 32-byte aligned
+ *   w2_sf  E8M0 scales packed by moe_pack_scales from [E_tot*H, I/32] */
+typedef struct moe_weights {
+    const uint8_t *w1, *w1_sf, *w2, *w2_sf;
+} moe_weights;
+
+/* Device pointers into a workspace, for inspection and parity checks.
+ *   header       int32[64]: [0] rows R, [1] virtual experts, [2] groups,
+ *                [3] status, [4] status detail
+ *   expert_counts int32[E_tot], expert_offsets int32[E_tot + 1]
+ *   vinfo        int32[max_v][4] {local expert, first row, rows, chunk}
+ *   a_map        int32[R] row -> slot t*k' + j;  c_map int32[T*k'] slot -> row or -1
+ *   xq           E4M3 [rows_alloc, H]: row r = MXFP8(x[a_map[r] / k'])
+ *   xq_sf        E8M0 of xq in the tile layout (see moe_forward)
+ *   act, act_sf  the FC1 output (silu(gate)*up, MXFP8) in the same layouts
+ *   y            the FC2 output rows, already multiplied by the routing weight */
+typedef struct moe_views {
+    int32_t *header, *expert_counts, *expert_offsets, *vinfo, *a_map, *c_map;
+    uint8_t *xq, *xq_sf, *act, *act_sf;
+    void* y;
+    int32_t max_v, rows_alloc, y_is_bf16, sf_tile_bytes_x, sf_tile_bytes_act;
+} moe_views;
+
+/* 1 if the shape is supported, else 0.  Limits: hidden % 512 == 0,
+ * inter % 128 == 0, block_n in {16, 32, 128}, 1 <= top_k <= 32,
+ * top_k <= E_global <= 1024, 1 <= E_local + num_shared <= 1024,
+ * num_shared in {0, 1}, 0 <= expert_offset, expert_offset + E_local <=
+ * E_global, 0 <= T <= max_T, max_T * (top_k + num_shared) < 2^24.
+ * (The compile-time limits of "... MXFP4 decode MoE ... shape templates",
+ * section 2, restated as runtime checks.) */
+int moe_is_supported(const moe_shape* shape);
+
+/* Bytes of the single workspace buffer (256-byte aligned carve). */
+int moe_workspace_bytes(const moe_shape* shape, size_t* bytes);
+
+/* Bytes of the packed scale array produced by moe_pack_scales. */
+int moe_packed_scale_bytes(int64_t rows, int64_t K, size_t* bytes);
+
+/* fp32 [rows, K] -> MXFP4: codes [rows, K/2] and E8M0 scales [rows, K/32]
+ * (row-major), shared exponent floor(log2 amax) - 2, elements rounded to
+ * nearest even and saturated to +-6 (OCP MX v1.0).  K % 32 == 0.  codes must
+ * be 16-byte aligned. */
+int moe_quantize_mxfp4(const float* w, int64_t rows, int64_t K, uint8_t* codes, uint8_t* scales,
+                       moe_stream_t stream);
+
+/* Row-major E8M0 scales [rows, K/32] -> the tensor-core scale layout: for
+ * each 128-row block and 128-K chunk, 512 bytes where row r (mod 128) and
+ * K-block b (mod 4) sit at byte (r % 32) * 16 + (r / 32) * 4 + b.
+ * rows % 128 == 0, K % 128 == 0. */
+int moe_pack_scales(const uint8_t* scales, int64_t rows, int64_t K, uint8_t* packed, moe_stream_t stream);
+
+/* Routing.  logits fp32 [T, E_global]; shared_logit bf16 [T, num_shared] or
+ * NULL when num_shared == 0.  Writes topk_ids int32 [T, k'] and topk_w fp32
+ * [T, k'], k' = top_k + num_shared: the top_k largest logits in descending
+ * order (ties to the lower expert id), weights exp(l_j - m) / sum_sel exp(l_i
+ * - m) (softmax renormalised over the picks), then the shared expert (id
+ * E_global + s, weight sigmoid(fp32(logit)) * shared_scale).  NaN logits are
+ * not supported. */
+int moe_route(const moe_shape* shape, const float* logits, const uint16_t* shared_logit, int32_t* topk_ids,
+              float* topk_w, moe_stream_t stream);
+
+/* Token-to-expert sort of topk_ids int32 [T, k'] into the workspace:
+ * expert counts/offsets, a_map/c_map (rows of an expert in ascending slot
+ * order t*k' + j), virtual experts (chunks of block_n rows per expert) and the
+ * GEMM work list; resets the status word.  ("[SGLang] CUTLASS MoE", section 1
+ * prepare_moe_input; "... MXFP4 decode MoE ... shape templates", sections 1,
+ * 5.)  The workspace must be 256-byte aligned. */
+int moe_sort(const moe_shape* shape, const int32_t* topk_ids, void* workspace, size_t workspace_bytes,
+             moe_stream_t stream);
+
+/* Forward after moe_sort: x bf16 [T, H] -> out bf16 [T, H].
+ *   out[t] = bf16( sum_{j: c_map[t,j] >= 0, ascending j} topk_w[t,j] *
+ *                  Y_j(t) ),  Y_j = FC2(MXFP8(silu(G) * U)), [G | U] =
+ *                  FC1(MXFP8(x[t])) with expert topk_ids[t,j]'s weights.
+ * FC1/FC2 run on tcgen05 block-scaled tensor cores (E4M3 x E2M1, fp32
+ * accumulation), the SwiGLU + MXFP8 requantisation is fused into the FC1
+ * epilogue and the routing-weight multiply into the FC2 epilogue.
+ * x, out 16-byte aligned. */
+int moe_forward(const moe_shape* shape, const uint16_t* x, const moe_weights* weights, const float* topk_w,
+                void* workspace, size_t workspace_bytes, uint16_t* out, moe_stream_t stream);
+
+/* route + sort + forward as one fixed launch chain (programmatic dependent
+ * launch between kernels, no host synchronisation, graph capturable). */
+int moe_layer(const moe_shape* shape, const float* logits, const uint16_t* shared_logit, const uint16_t* x,
+              const moe_weights* weights, int32_t* topk_ids, float* topk_w, void* workspace, size_t workspace_bytes,
+              uint16_t* out, moe_stream_t stream);
+
+/* moe_layer from HOST buffers: copies logits, shared_logit and x (host,
+ * preferably pinned) into the workspace's staging area, runs the chain and
+ * copies out (host) back, all on `stream`; the caller synchronises before
+ * reading out.  Weights stay on the device. */
+int moe_layer_host(const moe_shape* shape, const float* logits_host, const uint16_t* shared_logit_host,
+                   const uint16_t* x_host, const moe_weights* weights, void* workspace, size_t workspace_bytes,
+                   uint16_t* out_host, moe_stream_t stream);
+
+/* moe_layer with timing events: events[0..6] (cudaEvent_t, created by the
+ * caller) are recorded on `stream` before route and after route, sort, the x
+ * quantise/gather, FC1, FC2 and combine, so each kernel's device time is
+ * cudaEventElapsedTime(events[i], events[i+1]).  The records sit between the
+ * launches (no programmatic overlap across them); use moe_layer for the
+ * production chain. */
+int moe_layer_events(const moe_shape* shape, const float* logits, const uint16_t* shared_logit, const uint16_t* x,
+                     const moe_weights* weights, int32_t* topk_ids, float* topk_w, void* workspace,
+                     size_t workspace_bytes, uint16_t* out, void* const* events, moe_stream_t stream);
+
+/* Workspace views (device pointers) for inspection. */
+int moe_get_views(const moe_shape* shape, void* workspace, moe_views* views);
+
+/* Reads the status word (and its detail) from the workspace with a
+ * synchronous device-to-host copy: call after the stream has finished.
+ * *status is MOE_OK or MOE_ERR_TIMEOUT. */
+int moe_get_status(const void* workspace, int32_t* status, int32_t* detail);
+
+/* Number of SMs the launches are sized for on the current device. */
+int moe_num_sms(int32_t* num_sms);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_API_H */

@@ -1,0 +1,363 @@
+// C ABI of the library (declared in include/moe_api.h): argument checks, the
+// workspace carve, TMA tensor maps and the fixed launch chain
+//   route -> sort -> gather/quantise x -> FC1 -> FC2 -> combine
+// with programmatic dependent launch between kernels and no host
+// synchronisation (graph capturable).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace moe {
+namespace {
+
+// Transaction bytes of one 128 x 128 E2M1 box loaded with the
+// 16U4_ALIGN16B tensor-map type: the shared-memory footprint, 16 bytes per 16
+// elements.
+constexpr int kFp4BoxTxBytes = 128 * 128;
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool get_encode() {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode != nullptr;
+}
+
+// 2-D K-major tensor map: dim0 = K elements (contiguous), dim1 = rows.
+bool make_map(CUtensorMap* map, CUtensorMapDataType type, const void* base, uint64_t K, uint64_t rows,
+              uint64_t row_bytes, uint32_t box_k, uint32_t box_rows) {
+    if (!get_encode()) return false;
+    cuuint64_t dims[2] = {K, rows};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {box_k, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, type, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+int num_sms_cached() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    static int cache[64] = {0};
+    if (dev < 64 && cache[dev]) return cache[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev < 64) cache[dev] = n;
+    return n;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int check_shape(const moe_shape* s) {
+    if (!s) return MOE_ERR_NULL;
+    return moe_is_supported(s) ? MOE_OK : MOE_ERR_SHAPE;
+}
+
+int check_ws(const moe_shape* s, const void* ws, size_t ws_bytes) {
+    if (!ws) return MOE_ERR_NULL;
+    if (!aligned(ws, 256)) return MOE_ERR_ALIGN;
+    size_t need = 0;
+    moe_workspace_bytes(s, &need);
+    return ws_bytes >= need ? MOE_OK : MOE_ERR_WORKSPACE;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+    return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+int cuda_rc(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+int run_route(const moe_shape* s, const float* logits, const uint16_t* shared_logit, int32_t* ids, float* w,
+              cudaStream_t st, bool pdl) {
+    const Dims d = make_dims(*s);
+    RouteParams p{logits, shared_logit, ids, w, d.T, d.Eg, d.k, d.S, d.kp, d.shared_scale};
+    return cuda_rc(launch_route(p, st, pdl));
+}
+
+int run_sort(const moe_shape* s, const int32_t* ids, void* ws, cudaStream_t st, bool pdl) {
+    const Dims d = make_dims(*s);
+    const Layout L = make_layout(d);
+    SortParams p{ids, at<int32_t>(ws, L.header), at<int32_t>(ws, L.counts), at<int32_t>(ws, L.offsets),
+                 at<int4>(ws, L.vinfo), at<int4>(ws, L.groups), at<int32_t>(ws, L.a_map), at<int32_t>(ws, L.c_map),
+                 d.T, d.kp, d.Eg, d.E, d.off, d.S, d.Et, d.B, d.G};
+    return cuda_rc(launch_sort(p, st, pdl));
+}
+
+// Records events[i] on the stream when an events array is given.
+inline bool rec(void* const* ev, int i, cudaStream_t st) {
+    return !ev || cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), st) == cudaSuccess;
+}
+
+int run_forward(const moe_shape* s, const uint16_t* x, const moe_weights* wt, const float* topk_w, void* ws,
+                uint16_t* out, cudaStream_t st, bool pdl, void* const* ev = nullptr) {
+    const Dims d = make_dims(*s);
+    const Layout L = make_layout(d);
+    if (d.T == 0) {
+        for (int i = 3; ev && i < 7; ++i)
+            if (!rec(ev, i, st)) return MOE_ERR_CUDA;
+        return MOE_OK;
+    }
+    const int nsm = num_sms_cached();
+    if (nsm <= 0) return MOE_ERR_CUDA;
+
+    GatherParams gp{x, at<int32_t>(ws, L.header), at<int4>(ws, L.vinfo), at<int32_t>(ws, L.a_map),
+                    at<uint8_t>(ws, L.xq), at<uint8_t>(ws, L.xsf), d.H, d.kp, d.B, L.xsf_tile_bytes, d.V_max};
+    cudaError_t e = launch_gather_decode(gp, st, pdl);
+    if (e != cudaSuccess || !rec(ev, 3, st)) return MOE_ERR_CUDA;
+
+    CUtensorMap mw1, mw2, mx, mact;
+    const uint64_t Et = static_cast<uint64_t>(d.Et);
+    if (!make_map(&mw1, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, wt->w1, d.H, Et * 2 * d.I, d.H / 2, 128, 128) ||
+        !make_map(&mw2, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, wt->w2, d.I, Et * d.H, d.I / 2, 128, 128) ||
+        !make_map(&mx, CU_TENSOR_MAP_DATA_TYPE_UINT8, at<uint8_t>(ws, L.xq), d.H, d.rows_alloc, d.H, 128, d.B) ||
+        !make_map(&mact, CU_TENSOR_MAP_DATA_TYPE_UINT8, at<uint8_t>(ws, L.act), d.I, d.rows_alloc, d.I, 128, d.B))
+        return MOE_ERR_CUDA;
+
+    GemmParams g{};
+    g.header = at<int32_t>(ws, L.header);
+    g.status = at<int32_t>(ws, L.header) + kHdrStatus;
+    g.groups = at<int4>(ws, L.groups);
+    g.vinfo = at<int4>(ws, L.vinfo);
+    g.a_map = at<int32_t>(ws, L.a_map);
+    g.topk_w = topk_w;
+    g.act = at<uint8_t>(ws, L.act);
+    g.act_sf = at<uint8_t>(ws, L.asf);
+    g.y = at<float>(ws, L.y);
+    g.H = d.H;
+    g.I = d.I;
+    g.out_sf_tile_bytes = L.asf_tile_bytes;
+    g.a_tile_tx_bytes = kFp4BoxTxBytes;
+    g.wait_ns = kWaitLimitNs;
+
+    g.a_sf = wt->w1_sf;
+    g.b_sf = at<uint8_t>(ws, L.xsf);
+    g.b_sf_tile_bytes = L.xsf_tile_bytes;
+    e = launch_fc1_decode(mw1, mx, g, d.B, nsm, st, pdl);
+    if (e != cudaSuccess || !rec(ev, 4, st)) return MOE_ERR_CUDA;
+
+    g.a_sf = wt->w2_sf;
+    g.b_sf = at<uint8_t>(ws, L.asf);
+    g.b_sf_tile_bytes = L.asf_tile_bytes;
+    e = launch_fc2_decode(mw2, mact, g, d.B, nsm, st, pdl);
+    if (e != cudaSuccess || !rec(ev, 5, st)) return MOE_ERR_CUDA;
+
+    CombineParams cp{at<int32_t>(ws, L.c_map), at<float>(ws, L.y), out, d.T, d.kp, d.H};
+    e = launch_combine(cp, st, pdl);
+    if (e != cudaSuccess || !rec(ev, 6, st)) return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
+int check_weights(const moe_weights* w) {
+    if (!w || !w->w1 || !w->w1_sf || !w->w2 || !w->w2_sf) return MOE_ERR_NULL;
+    if (!aligned(w->w1, 32) || !aligned(w->w2, 32) || !aligned(w->w1_sf, 16) || !aligned(w->w2_sf, 16))
+        return MOE_ERR_ALIGN;
+    return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int moe_is_supported(const moe_shape* s) {
+    if (!s) return 0;
+    const int64_t kp = static_cast<int64_t>(s->top_k) + s->num_shared;
+    if (s->hidden <= 0 || s->hidden % 512 != 0) return 0;
+    if (s->inter <= 0 || s->inter % 128 != 0) return 0;
+    if (!(s->block_n == 16 || s->block_n == 32)) return 0;
+    if (s->top_k < 1 || s->top_k > 32 || s->top_k > s->E_global || s->E_global > 1024) return 0;
+    if (s->num_shared < 0 || s->num_shared > 1) return 0;
+    if (s->E_local < 1 || s->E_local + s->num_shared > 1024) return 0;
+    if (s->expert_offset < 0 || s->expert_offset + s->E_local > s->E_global) return 0;
+    if (s->T < 0 || s->T > s->max_T || s->max_T < 1) return 0;
+    if (static_cast<int64_t>(s->max_T) * kp >= (1 << 24)) return 0;
+    if (s->activation != MOE_ACT_SWIGLU) return 0;
+    return 1;
+}
+
+int moe_workspace_bytes(const moe_shape* s, size_t* bytes) {
+    if (!s || !bytes) return MOE_ERR_NULL;
+    if (!moe_is_supported(s)) return MOE_ERR_SHAPE;
+    *bytes = make_layout(make_dims(*s)).total;
+    return MOE_OK;
+}
+
+int moe_packed_scale_bytes(int64_t rows, int64_t K, size_t* bytes) {
+    if (!bytes) return MOE_ERR_NULL;
+    if (rows <= 0 || K <= 0 || rows % 128 || K % 128) return MOE_ERR_SHAPE;
+    *bytes = static_cast<size_t>(rows) * (K / 32);
+    return MOE_OK;
+}
+
+int moe_quantize_mxfp4(const float* w, int64_t rows, int64_t K, uint8_t* codes, uint8_t* scales,
+                       moe_stream_t stream) {
+    if (!w || !codes || !scales) return MOE_ERR_NULL;
+    if (rows <= 0 || K <= 0 || K % 32) return MOE_ERR_SHAPE;
+    if (!aligned(w, 16) || !aligned(codes, 16)) return MOE_ERR_ALIGN;
+    QuantParams p{w, codes, scales, rows, K};
+    return cuda_rc(launch_quantize_mxfp4(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int moe_pack_scales(const uint8_t* scales, int64_t rows, int64_t K, uint8_t* packed, moe_stream_t stream) {
+    if (!scales || !packed) return MOE_ERR_NULL;
+    if (rows <= 0 || K <= 0 || rows % 128 || K % 128) return MOE_ERR_SHAPE;
+    PackParams p{scales, packed, rows, K};
+    return cuda_rc(launch_pack_scales(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int moe_route(const moe_shape* s, const float* logits, const uint16_t* shared_logit, int32_t* topk_ids,
+              float* topk_w, moe_stream_t stream) {
+    int rc = check_shape(s);
+    if (rc) return rc;
+    if (s->T > 0 && (!logits || !topk_ids || !topk_w || (s->num_shared > 0 && !shared_logit))) return MOE_ERR_NULL;
+    return run_route(s, logits, shared_logit, topk_ids, topk_w, reinterpret_cast<cudaStream_t>(stream), false);
+}
+
+int moe_sort(const moe_shape* s, const int32_t* topk_ids, void* ws, size_t ws_bytes, moe_stream_t stream) {
+    int rc = check_shape(s);
+    if (rc) return rc;
+    if (s->T > 0 && !topk_ids) return MOE_ERR_NULL;
+    if ((rc = check_ws(s, ws, ws_bytes))) return rc;
+    return run_sort(s, topk_ids, ws, reinterpret_cast<cudaStream_t>(stream), false);
+}
+
+int moe_forward(const moe_shape* s, const uint16_t* x, const moe_weights* w, const float* topk_w, void* ws,
+                size_t ws_bytes, uint16_t* out, moe_stream_t stream) {
+    int rc = check_shape(s);
+    if (rc) return rc;
+    if (s->T > 0 && (!x || !topk_w || !out)) return MOE_ERR_NULL;
+    if (!aligned(x, 16) || !aligned(out, 16)) return MOE_ERR_ALIGN;
+    if ((rc = check_weights(w))) return rc;
+    if ((rc = check_ws(s, ws, ws_bytes))) return rc;
+    return run_forward(s, x, w, topk_w, ws, out, reinterpret_cast<cudaStream_t>(stream), false);
+}
+
+int moe_layer(const moe_shape* s, const float* logits, const uint16_t* shared_logit, const uint16_t* x,
+              const moe_weights* w, int32_t* topk_ids, float* topk_w, void* ws, size_t ws_bytes, uint16_t* out,
+              moe_stream_t stream) {
+    int rc = check_shape(s);
+    if (rc) return rc;
+    if (s->T > 0 && (!logits || !x || !topk_ids || !topk_w || !out || (s->num_shared > 0 && !shared_logit)))
+        return MOE_ERR_NULL;
+    if (!aligned(x, 16) || !aligned(out, 16)) return MOE_ERR_ALIGN;
+    if ((rc = check_weights(w))) return rc;
+    if ((rc = check_ws(s, ws, ws_bytes))) return rc;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if ((rc = run_route(s, logits, shared_logit, topk_ids, topk_w, st, false))) return rc;
+    if ((rc = run_sort(s, topk_ids, ws, st, true))) return rc;
+    return run_forward(s, x, w, topk_w, ws, out, st, true);
+}
+
+int moe_layer_events(const moe_shape* s, const float* logits, const uint16_t* shared_logit, const uint16_t* x,
+                     const moe_weights* w, int32_t* topk_ids, float* topk_w, void* ws, size_t ws_bytes, uint16_t* out,
+                     void* const* events, moe_stream_t stream) {
+    int rc = check_shape(s);
+    if (rc) return rc;
+    if (!events) return MOE_ERR_NULL;
+    for (int i = 0; i < 7; ++i)
+        if (!events[i]) return MOE_ERR_NULL;
+    if (s->T > 0 && (!logits || !x || !topk_ids || !topk_w || !out || (s->num_shared > 0 && !shared_logit)))
+        return MOE_ERR_NULL;
+    if (!aligned(x, 16) || !aligned(out, 16)) return MOE_ERR_ALIGN;
+    if ((rc = check_weights(w))) return rc;
+    if ((rc = check_ws(s, ws, ws_bytes))) return rc;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (!rec(events, 0, st)) return MOE_ERR_CUDA;
+    if ((rc = run_route(s, logits, shared_logit, topk_ids, topk_w, st, false))) return rc;
+    if (!rec(events, 1, st)) return MOE_ERR_CUDA;
+    if ((rc = run_sort(s, topk_ids, ws, st, false))) return rc;
+    if (!rec(events, 2, st)) return MOE_ERR_CUDA;
+    return run_forward(s, x, w, topk_w, ws, out, st, false, events);
+}
+
+int moe_layer_host(const moe_shape* s, const float* logits_host, const uint16_t* shared_logit_host,
+                   const uint16_t* x_host, const moe_weights* w, void* ws, size_t ws_bytes, uint16_t* out_host,
+                   moe_stream_t stream) {
+    int rc = check_shape(s);
+    if (rc) return rc;
+    if (s->T > 0 && (!logits_host || !x_host || !out_host || (s->num_shared > 0 && !shared_logit_host)))
+        return MOE_ERR_NULL;
+    if ((rc = check_weights(w))) return rc;
+    if ((rc = check_ws(s, ws, ws_bytes))) return rc;
+    const Dims d = make_dims(*s);
+    const Layout L = make_layout(d);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    float* lg = at<float>(ws, L.st_logits);
+    uint16_t* sl = at<uint16_t>(ws, L.st_shared);
+    uint16_t* xd = at<uint16_t>(ws, L.st_x);
+    uint16_t* od = at<uint16_t>(ws, L.st_out);
+    if (cudaMemcpyAsync(lg, logits_host, size_t(d.T) * d.Eg * 4, cudaMemcpyHostToDevice, st) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (d.S > 0 &&
+        cudaMemcpyAsync(sl, shared_logit_host, size_t(d.T) * d.S * 2, cudaMemcpyHostToDevice, st) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (cudaMemcpyAsync(xd, x_host, size_t(d.T) * d.H * 2, cudaMemcpyHostToDevice, st) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    int32_t* ids = at<int32_t>(ws, L.st_ids);
+    float* tw = at<float>(ws, L.st_w);
+    if ((rc = run_route(s, lg, d.S > 0 ? sl : nullptr, ids, tw, st, false))) return rc;
+    if ((rc = run_sort(s, ids, ws, st, true))) return rc;
+    if ((rc = run_forward(s, xd, w, tw, ws, od, st, true))) return rc;
+    if (cudaMemcpyAsync(out_host, od, size_t(d.T) * d.H * 2, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
+int moe_get_views(const moe_shape* s, void* ws, moe_views* v) {
+    int rc = check_shape(s);
+    if (rc) return rc;
+    if (!ws || !v) return MOE_ERR_NULL;
+    const Dims d = make_dims(*s);
+    const Layout L = make_layout(d);
+    v->header = at<int32_t>(ws, L.header);
+    v->expert_counts = at<int32_t>(ws, L.counts);
+    v->expert_offsets = at<int32_t>(ws, L.offsets);
+    v->vinfo = at<int32_t>(ws, L.vinfo);
+    v->a_map = at<int32_t>(ws, L.a_map);
+    v->c_map = at<int32_t>(ws, L.c_map);
+    v->xq = at<uint8_t>(ws, L.xq);
+    v->xq_sf = at<uint8_t>(ws, L.xsf);
+    v->act = at<uint8_t>(ws, L.act);
+    v->act_sf = at<uint8_t>(ws, L.asf);
+    v->y = at<void>(ws, L.y);
+    v->max_v = d.V_max;
+    v->rows_alloc = d.rows_alloc;
+    v->y_is_bf16 = L.y_bf16;
+    v->sf_tile_bytes_x = L.xsf_tile_bytes;
+    v->sf_tile_bytes_act = L.asf_tile_bytes;
+    return MOE_OK;
+}
+
+int moe_get_status(const void* ws, int32_t* status, int32_t* detail) {
+    if (!ws || !status || !detail) return MOE_ERR_NULL;
+    int32_t h[2];
+    if (cudaMemcpy(h, static_cast<const int32_t*>(ws) + kHdrStatus, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    *status = h[0];
+    *detail = h[1];
+    return MOE_OK;
+}
+
+int moe_num_sms(int32_t* n) {
+    if (!n) return MOE_ERR_NULL;
+    *n = num_sms_cached();
+    return *n > 0 ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,53 @@
+// Weighted un-permute combine ("[SGLang] CUTLASS MoE", section 5
+// apply_shuffle_mul_sum): out[t] = bf16( sum_j Y[c_map[t, j]] ) over the
+// token's slots j in ascending order, skipping slots with no local row
+// (c_map = -1, "[sglang] ... MXFP4 decode MoE ... shape templates", section
+// 5).  Y rows already carry the routing weight (FC2 epilogue), so this is a
+// gather-sum: no atomics, bitwise deterministic.
+#include "common.cuh"
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kCombineThreads = 256;
+constexpr int kMaxSlots = 64;
+
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineParams p) {
+    __shared__ int rows[kMaxSlots];
+    ptx::pdl_wait();
+    const int t = blockIdx.x;
+    if (threadIdx.x < p.kp) rows[threadIdx.x] = p.c_map[static_cast<size_t>(t) * p.kp + threadIdx.x];
+    __syncthreads();
+    const int n4 = p.H / 4;
+    for (int c = threadIdx.x; c < n4; c += kCombineThreads) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j = 0; j < p.kp; ++j) {
+            const int r = rows[j];
+            if (r < 0) continue;
+            const float4 v = reinterpret_cast<const float4*>(p.y + static_cast<size_t>(r) * p.H)[c];
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+        }
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+        const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+        uint2 packed;
+        packed.x = *reinterpret_cast<const uint32_t*>(&lo);
+        packed.y = *reinterpret_cast<const uint32_t*>(&hi);
+        reinterpret_cast<uint2*>(p.out + static_cast<size_t>(t) * p.H)[c] = packed;
+    }
+    ptx::pdl_launch_dependents();
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream, bool pdl) {
+    if (p.T == 0) return cudaSuccess;
+    return launch_kernel(combine_kernel, dim3(p.T), dim3(kCombineThreads), 0, stream, pdl, p);
+}
+
+}  // namespace moe

@@ -1,0 +1,151 @@
+// Shared definitions of the GPU library: derived dimensions, the workspace
+// carve, status codes and the MX (OCP MX v1.0) element quantiser used by the
+// activation paths.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp4.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+
+#include "../../include/moe_api.h"
+
+namespace moe {
+
+constexpr int kHeaderWords = 64;
+enum HeaderWord { kHdrRows = 0, kHdrNumV = 1, kHdrNumGroups = 2, kHdrStatus = 3, kHdrDetail = 4 };
+
+// Where a bounded wait expired (status detail = site * 65536 + block index).
+enum WaitSite { kSiteProducerEmpty = 1, kSiteMmaFull = 2, kSiteMmaAccEmpty = 3, kSiteEpiAccFull = 4 };
+
+constexpr uint64_t kWaitLimitNs = 200ull * 1000 * 1000;  // 200 ms per wait
+
+enum Mode { kModeDecode = 0, kModePrefill = 1 };
+
+// Dimensions derived from a moe_shape.
+struct Dims {
+    int T, max_T, Eg, E, off, k, S, kp, Et, H, I, B;
+    int G;           // virtual experts (tiles) per GEMM work group
+    int R_max;       // routed rows bound: max_T * k'
+    int V_max;       // virtual-expert bound: Et + R_max / B
+    int rows_alloc;  // activation rows incl. the last tile's TMA tail box
+    int mode;
+    float shared_scale;
+};
+
+// Byte offsets of the workspace regions (256-byte aligned).
+struct Layout {
+    size_t header, counts, offsets, vinfo, groups, a_map, c_map;
+    size_t xq, xsf, act, asf, y;
+    size_t st_logits, st_shared, st_x, st_ids, st_w, st_out;
+    size_t total;
+    int xsf_tile_bytes, asf_tile_bytes, y_bf16;
+};
+
+inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+inline Dims make_dims(const moe_shape& s) {
+    Dims d{};
+    d.T = s.T;
+    d.max_T = s.max_T;
+    d.Eg = s.E_global;
+    d.E = s.E_local;
+    d.off = s.expert_offset;
+    d.k = s.top_k;
+    d.S = s.num_shared;
+    d.kp = s.top_k + s.num_shared;
+    d.Et = s.E_local + s.num_shared;
+    d.H = s.hidden;
+    d.I = s.inter;
+    d.B = s.block_n;
+    d.mode = (s.block_n == 128) ? kModePrefill : kModeDecode;
+    d.G = (d.mode == kModeDecode) ? 64 / d.B : 1;
+    d.R_max = s.max_T * d.kp;
+    d.V_max = d.Et + d.R_max / d.B;
+    d.rows_alloc = d.R_max + d.B;
+    d.shared_scale = s.shared_scale;
+    return d;
+}
+
+inline Layout make_layout(const Dims& d) {
+    Layout L{};
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        size_t at = o;
+        o = align256(o + bytes);
+        return at;
+    };
+    L.header = take(kHeaderWords * 4);
+    L.counts = take(size_t(d.Et) * 4);
+    L.offsets = take(size_t(d.Et + 1) * 4);
+    L.vinfo = take(size_t(d.V_max) * 16);
+    L.groups = take(size_t(d.V_max) * 16);
+    L.a_map = take(size_t(d.R_max) * 4);
+    L.c_map = take(size_t(d.R_max) * 4);
+    if (d.mode == kModeDecode) {
+        // Tile scale layout: per virtual expert and per 512-K group, 32 lines
+        // x 16 bytes; line i = row i of the tile, byte b = K-block 16*g + b.
+        L.xsf_tile_bytes = (d.H / 512) * 512;
+        L.asf_tile_bytes = ((d.I + 511) / 512) * 512;
+        L.y_bf16 = 0;
+    } else {
+        // Tile scale layout for 128-row tiles: per 128-K chunk one 512-byte
+        // block, row r / K-block b at (r % 32) * 16 + (r / 32) * 4 + b.
+        L.xsf_tile_bytes = (d.H / 128) * 512;
+        L.asf_tile_bytes = (d.I / 128) * 512;
+        L.y_bf16 = 1;
+    }
+    L.xq = take(size_t(d.rows_alloc) * d.H);
+    L.xsf = take(size_t(d.V_max) * L.xsf_tile_bytes);
+    L.act = take(size_t(d.rows_alloc) * d.I);
+    L.asf = take(size_t(d.V_max) * L.asf_tile_bytes);
+    L.y = take(size_t(d.R_max) * d.H * (L.y_bf16 ? 2 : 4));
+    L.st_logits = take(size_t(d.max_T) * d.Eg * 4);
+    L.st_shared = take(size_t(d.max_T) * (d.S > 0 ? d.S : 1) * 2);
+    L.st_x = take(size_t(d.max_T) * d.H * 2);
+    L.st_ids = take(size_t(d.R_max) * 4);
+    L.st_w = take(size_t(d.R_max) * 4);
+    L.st_out = take(size_t(d.max_T) * d.H * 2);
+    L.total = o;
+    return L;
+}
+
+// ---------------------------------------------------------------- device MX
+// floor(log2 |amax|) - emax for a finite non-negative fp32, clamped to
+// [-127, 127]; amax == 0 gives -127 (E8M0 code 0).
+__device__ __forceinline__ int mx_shared_exponent(float amax, int emax) {
+    const uint32_t b = __float_as_uint(amax);
+    const int ex = static_cast<int>((b >> 23) & 0xFF);
+    int fl;
+    if (ex == 0) {
+        const uint32_t m = b & 0x7FFFFF;
+        if (m == 0) return -127;
+        fl = (31 - __clz(m)) - 149;  // subnormal: m * 2^-149
+    } else {
+        fl = ex - 127;
+    }
+    const int e = fl - emax;
+    return e < -127 ? -127 : (e > 127 ? 127 : e);
+}
+
+// 2^n as fp32 for n in [-127, 127] (exact).
+__device__ __forceinline__ float exp2_int(int n) {
+    return n >= -126 ? __uint_as_float(static_cast<uint32_t>(n + 127) << 23) : __uint_as_float(0x00400000u);
+}
+
+// Two fp32 -> two E4M3 codes (RNE, saturating); v0 in the low byte.
+__device__ __forceinline__ uint16_t e4m3x2(float v0, float v1) {
+    return static_cast<uint16_t>(__nv_cvt_float2_to_fp8x2(make_float2(v0, v1), __NV_SATFINITE, __NV_E4M3));
+}
+
+// Two fp32 -> two E2M1 codes (RNE, saturating); v0 in the low nibble.
+__device__ __forceinline__ uint8_t e2m1x2(float v0, float v1) {
+    return static_cast<uint8_t>(__nv_cvt_float2_to_fp4x2(make_float2(v0, v1), __NV_E2M1, cudaRoundNearest));
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
+    return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+}  // namespace moe

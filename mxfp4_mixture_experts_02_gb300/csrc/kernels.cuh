@@ -1,0 +1,109 @@
+// Kernel parameter blocks and launchers of the GPU library.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace moe {
+
+// cudaLaunchKernelEx with programmatic dependent launch (the kernel may start
+// while its predecessor in the stream drains; it calls griddepcontrol.wait
+// before touching the predecessor's outputs).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream, bool pdl,
+                          Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+struct RouteParams {
+    const float* logits;
+    const uint16_t* shared_logit;
+    int32_t* ids;
+    float* w;
+    int T, Eg, k, S, kp;
+    float shared_scale;
+};
+
+struct SortParams {
+    const int32_t* ids;
+    int32_t* header;
+    int32_t* counts;
+    int32_t* offsets;
+    int4* vinfo;
+    int4* groups;
+    int32_t* a_map;
+    int32_t* c_map;
+    int T, kp, Eg, E, off, S, Et, B, G;
+};
+
+struct GatherParams {  // x -> MXFP8 rows in expert order + tile scales
+    const uint16_t* x;
+    const int32_t* header;
+    const int4* vinfo;
+    const int32_t* a_map;
+    uint8_t* xq;
+    uint8_t* xsf;
+    int H, kp, B, xsf_tile_bytes, max_v;
+};
+
+struct GemmParams {
+    const int32_t* header;
+    int32_t* status;  // header + kHdrStatus (status, detail)
+    const int4* groups;
+    const int4* vinfo;
+    const int32_t* a_map;
+    const float* topk_w;
+    const uint8_t* a_sf;   // packed weight scales
+    const uint8_t* b_sf;   // tile scales of the activation operand
+    uint8_t* act;          // FC1 output codes [rows_alloc, I]
+    uint8_t* act_sf;       // FC1 output tile scales
+    float* y;              // FC2 output [R, H] (fp32)
+    int H, I;
+    int b_sf_tile_bytes, out_sf_tile_bytes;
+    int a_tile_tx_bytes;   // transaction bytes of one 128x128 E2M1 TMA box
+    uint64_t wait_ns;
+};
+
+struct CombineParams {
+    const int32_t* c_map;
+    const float* y;
+    uint16_t* out;
+    int T, kp, H;
+};
+
+struct QuantParams {
+    const float* w;
+    uint8_t* codes;
+    uint8_t* scales;
+    int64_t rows, K;
+};
+
+struct PackParams {
+    const uint8_t* scales;
+    uint8_t* packed;
+    int64_t rows, K;
+};
+
+cudaError_t launch_route(const RouteParams& p, cudaStream_t stream, bool pdl);
+cudaError_t launch_sort(const SortParams& p, cudaStream_t stream, bool pdl);
+cudaError_t launch_gather_decode(const GatherParams& p, cudaStream_t stream, bool pdl);
+cudaError_t launch_fc1_decode(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int B, int grid,
+                              cudaStream_t stream, bool pdl);
+cudaError_t launch_fc2_decode(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int B, int grid,
+                              cudaStream_t stream, bool pdl);
+cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream, bool pdl);
+cudaError_t launch_quantize_mxfp4(const QuantParams& p, cudaStream_t stream);
+cudaError_t launch_pack_scales(const PackParams& p, cudaStream_t stream);
+
+}  // namespace moe

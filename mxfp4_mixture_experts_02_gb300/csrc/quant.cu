@@ -1,0 +1,144 @@
+// MX quantisers (OCP MX v1.0 conversion: shared exponent floor(log2 amax) -
+// emax, elements rounded to nearest even and saturated by the cvt.satfinite
+// instructions):
+//   gather_decode_kernel : x bf16 -> MXFP8 (E4M3, emax 8), written directly in
+//                          expert-row order (the "[SGLang] CUTLASS MoE"
+//                          section 2 shuffle_rows folded into the quantiser)
+//                          with the tile scale layout the FC1 kernel copies
+//                          into tensor memory;
+//   quantize_mxfp4_kernel: fp32 weights -> MXFP4 (E2M1, emax 2), offline;
+//   pack_scales_kernel   : row-major E8M0 -> 512-byte tensor-core blocks.
+#include "common.cuh"
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kGatherThreads = 256;
+
+// One CTA per virtual expert (tile of B rows).  Thread job = (row, 32-block).
+__global__ void __launch_bounds__(kGatherThreads) gather_decode_kernel(GatherParams p) {
+    ptx::pdl_wait();
+    const int v = blockIdx.x;
+    const int nv = p.header[kHdrNumV];
+    if (v < nv) {
+        const int4 vi = p.vinfo[v];
+        const int first = vi.y, rows = vi.z;
+        const int nb = p.H / 32;
+        uint8_t* sf_tile = p.xsf + static_cast<size_t>(v) * p.xsf_tile_bytes;
+        for (int job = threadIdx.x; job < rows * nb; job += kGatherThreads) {
+            const int i = job / nb, b = job - i * nb;
+            const int row = first + i;
+            const int t = p.a_map[row] / p.kp;
+            const uint4* src = reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(t) * p.H + b * 32);
+            uint4 raw[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) raw[c] = src[c];
+            const uint16_t* hv = reinterpret_cast<const uint16_t*>(raw);
+            float f[32];
+            float amax = 0.f;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                f[e] = bf16_bits_to_float(hv[e]);
+                amax = fmaxf(amax, fabsf(f[e]));
+            }
+            const int ex = mx_shared_exponent(amax, 8);
+            const float inv = exp2_int(-ex);
+            uint32_t packed[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const uint32_t lo = e4m3x2(f[4 * e] * inv, f[4 * e + 1] * inv);
+                const uint32_t hi = e4m3x2(f[4 * e + 2] * inv, f[4 * e + 3] * inv);
+                packed[e] = lo | (hi << 16);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(p.xq + static_cast<size_t>(row) * p.H + b * 32);
+            dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+            dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+            sf_tile[(b >> 4) * 512 + i * 16 + (b & 15)] = static_cast<uint8_t>(ex + 127);
+        }
+        // unused lines of the tile's scale blocks (rows >= tile rows) -> 0
+        const int groups = p.H / 512;
+        for (int j = threadIdx.x; j < groups * 32 * 16; j += kGatherThreads) {
+            const int line = (j >> 4) & 31;
+            if (line >= rows) sf_tile[(j >> 9) * 512 + (j & 511)] = 0;
+        }
+    }
+    ptx::pdl_launch_dependents();
+}
+
+// One thread per 32-element block of a row.
+__global__ void quantize_mxfp4_kernel(QuantParams p) {
+    const int64_t nb = p.K / 32;
+    const int64_t total = p.rows * nb;
+    for (int64_t job = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; job < total;
+         job += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t r = job / nb, b = job - r * nb;
+        const float4* src = reinterpret_cast<const float4*>(p.w + r * p.K + b * 32);
+        float f[32];
+        float amax = 0.f;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const float4 q = src[c];
+            f[4 * c] = q.x;
+            f[4 * c + 1] = q.y;
+            f[4 * c + 2] = q.z;
+            f[4 * c + 3] = q.w;
+        }
+#pragma unroll
+        for (int e = 0; e < 32; ++e) amax = fmaxf(amax, fabsf(f[e]));
+        const int ex = mx_shared_exponent(amax, 2);
+        const float inv = exp2_int(-ex);
+        uint32_t words[4];
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            uint32_t acc = 0;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                acc |= static_cast<uint32_t>(e2m1x2(f[8 * w + 2 * q] * inv, f[8 * w + 2 * q + 1] * inv)) << (8 * q);
+            words[w] = acc;
+        }
+        *reinterpret_cast<uint4*>(p.codes + r * (p.K / 2) + b * 16) = make_uint4(words[0], words[1], words[2], words[3]);
+        p.scales[r * nb + b] = static_cast<uint8_t>(ex + 127);
+    }
+}
+
+// One thread per packed byte.
+__global__ void pack_scales_kernel(PackParams p) {
+    const int64_t kc_n = p.K / 128;
+    const int64_t total = (p.rows / 128) * kc_n * 512;
+    for (int64_t o = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; o < total;
+         o += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t blk = o / 512;
+        const int pos = static_cast<int>(o - blk * 512);
+        const int64_t rb = blk / kc_n, kc = blk - rb * kc_n;
+        const int line = pos >> 4, quarter = (pos >> 2) & 3, kb = pos & 3;
+        const int64_t row = rb * 128 + quarter * 32 + line;
+        p.packed[o] = p.scales[row * (p.K / 32) + kc * 4 + kb];
+    }
+}
+
+unsigned grid_for(int64_t n, int threads) {
+    int64_t g = (n + threads - 1) / threads;
+    if (g > 1 << 20) g = 1 << 20;
+    return static_cast<unsigned>(g < 1 ? 1 : g);
+}
+
+}  // namespace
+
+cudaError_t launch_gather_decode(const GatherParams& p, cudaStream_t stream, bool pdl) {
+    return launch_kernel(gather_decode_kernel, dim3(p.max_v), dim3(kGatherThreads), 0, stream, pdl, p);
+}
+
+cudaError_t launch_quantize_mxfp4(const QuantParams& p, cudaStream_t stream) {
+    quantize_mxfp4_kernel<<<grid_for(p.rows * (p.K / 32), 256), 256, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pack_scales(const PackParams& p, cudaStream_t stream) {
+    pack_scales_kernel<<<grid_for((p.rows / 128) * (p.K / 128) * 512, 256), 256, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,134 @@
+"""Builds MoE layer test cases: device inputs for the GPU library and, for the
+tokens being checked, the oracle's own independent computation.
+
+GPU side : x / logits / shared logit / fp32 weights from the CUDA build of the
+           seeded generator; weights quantised by the library
+           (moe_quantize_mxfp4 + moe_pack_scales).
+Oracle   : the same seeded inputs from the host build of the generator;
+           routing, sort, weight quantisation and forward by the oracle.
+Nothing computed by the GPU library feeds the oracle.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import mxfp4_mixture_experts_02_gb300 as moe
+import oracle
+import synth
+
+
+def shape_of(cfg: synth.MoeConfig, T: int | None = None) -> moe.MoeShape:
+    T = cfg.T if T is None else T
+    return moe.MoeShape(T=T, max_T=max(T, 1), E_global=cfg.E_global, E_local=cfg.E_local,
+                        expert_offset=cfg.expert_offset, top_k=cfg.top_k, num_shared=cfg.num_shared,
+                        hidden=cfg.hidden, inter=cfg.inter, block_n=cfg.block_n, shared_scale=cfg.shared_scale)
+
+
+def device_weights(cfg: synth.MoeConfig, chunk: int = 64, keep_rowmajor_scales: bool = False):
+    """Packed weights of all local experts (+shared), generated and quantised
+    on the device chunk by chunk."""
+    gids = cfg.global_ids
+    E, H, I = gids.size, cfg.hidden, cfg.inter
+    dev = "cuda"
+    w1 = torch.empty((E, 2 * I, H // 2), dtype=torch.uint8, device=dev)
+    w2 = torch.empty((E, H, I // 2), dtype=torch.uint8, device=dev)
+    s1 = torch.empty((E * 2 * I, H // 32), dtype=torch.uint8, device=dev)
+    s2 = torch.empty((E * H, I // 32), dtype=torch.uint8, device=dev)
+    for c0 in range(0, E, chunk):
+        ids = gids[c0:c0 + chunk]
+        n = ids.size
+        f1 = synth.w1_device(cfg, ids)
+        c, s = moe.moe_quantize_mxfp4(f1.reshape(n * 2 * I, H))
+        w1[c0:c0 + n] = c.reshape(n, 2 * I, H // 2)
+        s1[c0 * 2 * I:(c0 + n) * 2 * I] = s
+        del f1
+        f2 = synth.w2_device(cfg, ids)
+        c, s = moe.moe_quantize_mxfp4(f2.reshape(n * H, I))
+        w2[c0:c0 + n] = c.reshape(n, H, I // 2)
+        s2[c0 * H:(c0 + n) * H] = s
+        del f2
+    wts = moe.MoeWeights(w1, moe.moe_pack_scales(s1, H), w2, moe.moe_pack_scales(s2, I))
+    torch.cuda.synchronize()
+    if keep_rowmajor_scales:
+        return wts, s1.reshape(E, 2 * I, H // 32), s2.reshape(E, H, I // 32)
+    return wts
+
+
+def device_inputs(cfg: synth.MoeConfig, T: int | None = None):
+    T = cfg.T if T is None else T
+    x = synth.x_device(cfg, T=T)
+    logits = synth.logits_device(cfg, T=T)
+    sl = synth.shared_logit_device(cfg, T=T).contiguous() if cfg.num_shared else None
+    return x, logits, sl
+
+
+class OracleCase:
+    """The oracle's computation of a config for a subset of tokens."""
+
+    def __init__(self, cfg: synth.MoeConfig, T: int | None = None):
+        self.cfg = cfg
+        self.T = cfg.T if T is None else T
+        self.x = synth.x_host(cfg, T=self.T)
+        self.logits = synth.logits_host(cfg, T=self.T)
+        self.shared = synth.shared_logit_host(cfg, T=self.T)
+        self.ids, self.w = oracle.route(self.logits, cfg.top_k, cfg.num_shared, self.shared, cfg.shared_scale)
+        self.sort = oracle.sort(self.ids, cfg.E_global, cfg.E_local, cfg.expert_offset, cfg.num_shared, cfg.block_n)
+        self._wcache = {}
+
+    def local_of(self, gid):
+        c = self.cfg
+        if gid >= c.E_global:
+            return c.E_local + gid - c.E_global
+        if c.expert_offset <= gid < c.expert_offset + c.E_local:
+            return gid - c.expert_offset
+        return -1
+
+    def expert_weights(self, locals_):
+        """Oracle-quantised weights of the given local experts (cached)."""
+        c = self.cfg
+        need = [e for e in locals_ if e not in self._wcache]
+        if need:
+            gids = c.global_ids[need]
+            f1 = synth.w1_host(c, gids)
+            f2 = synth.w2_host(c, gids)
+            for k, e in enumerate(need):
+                a, b = oracle.quantize_mxfp4(f1[k])
+                d, f = oracle.quantize_mxfp4(f2[k])
+                self._wcache[e] = (a, b, d, f)
+        return [self._wcache[e] for e in locals_]
+
+    def forward(self, tokens):
+        c = self.cfg
+        tokens = np.asarray(tokens, np.int32)
+        locs = sorted({self.local_of(int(g)) for t in tokens for g in self.ids[t]} - {-1})
+        ws = self.expert_weights(locs)
+        wmap = np.full(c.E_local + c.num_shared, -1, np.int32)
+        for k, e in enumerate(locs):
+            wmap[e] = k
+        if not locs:  # no local expert at all: any placeholder shapes
+            z = np.zeros((1, 2 * c.inter, c.hidden // 2), np.uint8)
+            arrs = (z, np.zeros((1, 2 * c.inter, c.hidden // 32), np.uint8),
+                    np.zeros((1, c.hidden, c.inter // 2), np.uint8), np.zeros((1, c.hidden, c.inter // 32), np.uint8))
+        else:
+            arrs = tuple(np.stack([w[i] for w in ws]) for i in range(4))
+        return oracle.forward(self.x, self.ids, self.w, wmap, *arrs, H=c.hidden, I=c.inter, E_global=c.E_global,
+                              E_local=c.E_local, expert_offset=c.expert_offset, num_shared=c.num_shared,
+                              tokens=tokens, want_act=True, want_xq=True)
+
+
+def bf16_bits(t: torch.Tensor) -> np.ndarray:
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def bf16_to_f64(bits) -> np.ndarray:
+    return synth.bf16_bits_to_f64(bits)
+
+
+def rel_l2(a, b) -> float:
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30))
+
+
+E4M3_VALUES = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).double().numpy()

@@ -1,0 +1,270 @@
+"""GPU path vs the oracle, through the C ABI (marked gpu).
+
+Bars (from the layer's specification):
+  - integer / byte results bit-exact: topk ids, expert counts and offsets,
+    a_map, c_map, virtual experts, the MXFP8 bytes of x, the MXFP4 weight
+    codes and scales;
+  - topk weights: |w_gpu - w| <= 4e-6 * w + 1e-7 (fp32 exp / sum / divide);
+  - intermediate act (FC1 -> SwiGLU -> MXFP8): identical codes except where
+    fp32 tensor-core accumulation and fp64 differ across a rounding boundary:
+    <= 0.5 % of elements, each within one E4M3 step (one scale step when the
+    block exponent itself flips);
+  - output bf16: relative L2 <= 1e-2 and max-abs <= 2e-2 against the fp64
+    oracle.
+"""
+import numpy as np
+import pytest
+import torch
+
+import mxfp4_mixture_experts_02_gb300 as moe
+import oracle
+import synth
+from moe_case import E4M3_VALUES, OracleCase, bf16_bits, bf16_to_f64, device_inputs, device_weights, rel_l2, shape_of
+
+pytestmark = pytest.mark.gpu
+
+SMALL = synth.MoeConfig("small", 7, T=48, E_global=64, E_local=64, expert_offset=0, top_k=4, num_shared=0,
+                        hidden=1024, inter=256, block_n=32)
+
+GRID = [
+    SMALL.replace(T=1, block_n=16),
+    SMALL.replace(T=7, block_n=32),
+    SMALL.replace(T=48, block_n=16, num_shared=1, shared_scale=0.5),
+    SMALL.replace(T=96, block_n=32, zipf_s=1.1),
+    SMALL.replace(T=256, block_n=16, E_local=32, expert_offset=16),
+    SMALL.replace(T=256, block_n=32, num_shared=1, zipf_s=1.1, hidden=1536, inter=384),
+    synth.CONFIGS["tiny"],
+]
+FULL = [synth.CONFIGS[n] for n in ("decode_t32", "ep_slice_t64", "skewed_shared_t256")]
+
+
+def _cid(c):
+    return "%s-T%d-B%d-E%d+%d-S%d-H%d-I%d" % (c.name, c.T, c.block_n, c.E_local, c.expert_offset, c.num_shared,
+                                               c.hidden, c.inter)
+
+
+_WCACHE = {}
+
+
+def _weights(cfg):
+    key = (cfg.seed, cfg.E_global, cfg.E_local, cfg.expert_offset, cfg.num_shared, cfg.hidden, cfg.inter)
+    if key not in _WCACHE:
+        _WCACHE.clear()
+        _WCACHE[key] = device_weights(cfg, keep_rowmajor_scales=True)
+    return _WCACHE[key]
+
+
+def run_layer(cfg, T=None):
+    shape = shape_of(cfg, T)
+    wts, _, _ = _weights(cfg)
+    x, logits, sl = device_inputs(cfg, T=shape.T)
+    ws = moe.workspace(shape)
+    out, ids, w = moe.moe_layer(shape, logits, sl, x, wts, ws)
+    torch.cuda.synchronize()
+    status = moe.moe_get_status(ws)
+    return shape, ws, out, ids, w, status
+
+
+def tile_scales_to_rows(views, vinfo, num_v, K):
+    """Per-row E8M0 scales [R, K/32] from the decode tile layout."""
+    sf = views.cpu().numpy()
+    R = int(sum(v[2] for v in vinfo[:num_v]))
+    rows = np.zeros((R, K // 32), np.uint8)
+    for v in range(num_v):
+        _, first, n, _ = vinfo[v]
+        for i in range(n):
+            for b in range(K // 32):
+                rows[first + i, b] = sf[v, (b // 16) * 512 + i * 16 + (b % 16)]
+    return rows
+
+
+def sample_tokens(T, n=6):
+    if T <= 48:
+        return np.arange(T)
+    rng = np.random.default_rng(T)
+    return np.unique(np.concatenate([[0, T - 1], rng.choice(T, n - 2, replace=False)]))
+
+
+def check_layer(cfg, tokens=None):
+    shape, ws, out, ids, w, status = run_layer(cfg)
+    assert status == (0, 0), status
+    orc = OracleCase(cfg)
+    # routing: ids bit-exact, weights to fp32 accuracy
+    np.testing.assert_array_equal(ids.cpu().numpy(), orc.ids)
+    wg = w.cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(wg - orc.w) <= 4e-6 * np.abs(orc.w) + 1e-7), np.max(np.abs(wg - orc.w))
+    # sort: bit-exact
+    v = moe.moe_get_views(shape, ws)
+    s = orc.sort
+    hdr = v["header"].cpu().numpy()
+    R = int(s["offsets"][-1])
+    assert hdr[0] == R and hdr[1] == s["num_v"]
+    np.testing.assert_array_equal(v["expert_counts"].cpu().numpy(), s["counts"])
+    np.testing.assert_array_equal(v["expert_offsets"].cpu().numpy(), s["offsets"])
+    np.testing.assert_array_equal(v["c_map"].cpu().numpy()[:cfg.T * cfg.kp], s["c_map"])
+    np.testing.assert_array_equal(v["a_map"].cpu().numpy()[:R], s["a_map"])
+    vinfo = v["vinfo"].cpu().numpy()
+    np.testing.assert_array_equal(vinfo[:s["num_v"]], s["vinfo"])
+    # forward on the checked tokens
+    toks = sample_tokens(cfg.T) if tokens is None else tokens
+    ref = orc.forward(toks)
+    xq = v["xq"].cpu().numpy()
+    xsf = tile_scales_to_rows(v["xq_sf"], vinfo, s["num_v"], cfg.hidden)
+    act = v["act"].cpu().numpy()
+    asf = tile_scales_to_rows(v["act_sf"], vinfo, s["num_v"], cfg.inter)
+    n_act, n_diff = 0, 0
+    for k, t in enumerate(toks):
+        for j in range(cfg.kp):
+            row = s["c_map"][t * cfg.kp + j]
+            if row < 0:
+                continue
+            # x -> MXFP8 in expert order: bit-exact
+            np.testing.assert_array_equal(xq[row], ref["xq"][k])
+            np.testing.assert_array_equal(xsf[row], ref["xq_sf"][k])
+            # intermediate: decoded values, mostly identical, else one step apart
+            ga = E4M3_VALUES[act[row]] * np.exp2(np.repeat(asf[row].astype(np.float64), 32) - 127)
+            oa = E4M3_VALUES[ref["act"][k, j]] * np.exp2(np.repeat(ref["act_sf"][k, j].astype(np.float64), 32) - 127)
+            d = ga != oa
+            n_act += ga.size
+            n_diff += int(d.sum())
+            step = np.exp2(np.floor(np.log2(np.maximum(np.abs(oa[d]), 1e-300))) - 3)
+            assert np.all(np.abs(ga[d] - oa[d]) <= 2.01 * np.maximum(step, np.exp2(np.repeat(
+                ref["act_sf"][k, j].astype(np.float64), 32)[d] - 127 - 9))), (t, j)
+    if n_act:
+        assert n_diff <= 0.005 * n_act, (n_diff, n_act)
+    got = bf16_to_f64(bf16_bits(out)[toks])
+    assert rel_l2(got, ref["out_f64"]) <= 1e-2
+    assert np.max(np.abs(got - ref["out_f64"])) <= 2e-2
+    return out
+
+
+@pytest.mark.parametrize("cfg", GRID, ids=_cid)
+def test_layer_grid_vs_oracle(cfg):
+    check_layer(cfg)
+
+
+@pytest.mark.parametrize("cfg", FULL, ids=_cid)
+def test_layer_full_size_vs_oracle(cfg):
+    check_layer(cfg, tokens=sample_tokens(cfg.T, 4))
+
+
+def test_weight_quantiser_bit_exact():
+    cfg = SMALL.replace(E_local=4, E_global=4, hidden=512, inter=128)
+    wts, s1, s2 = device_weights(cfg, keep_rowmajor_scales=True)
+    f1 = synth.w1_host(cfg, cfg.global_ids)
+    for e in range(4):
+        c, s = oracle.quantize_mxfp4(f1[e])
+        np.testing.assert_array_equal(wts.w1[e].cpu().numpy(), c)
+        np.testing.assert_array_equal(s1[e].cpu().numpy(), s)
+    # edge values: zeros, exact ties, saturation, tiny and huge blocks
+    rng = np.random.default_rng(3)
+    w = (rng.integers(-14, 15, (256, 64)) * 0.25 * 2.0 ** rng.integers(-8, 8, (256, 1))).astype(np.float32)
+    w[0] = 0
+    w[1, :32] = -0.0
+    w[2] = rng.normal(0, 1e-30, 64)
+    w[3] = rng.normal(0, 1e30, 64)
+    w[4, 5] = 7.0
+    w[4, :5] = 4.0
+    c, s = moe.moe_quantize_mxfp4(torch.from_numpy(w).cuda())
+    oc, os_ = oracle.quantize_mxfp4(w)
+    np.testing.assert_array_equal(c.cpu().numpy(), oc)
+    np.testing.assert_array_equal(s.cpu().numpy(), os_)
+
+
+def test_pack_scales_layout():
+    rows, K = 256, 512
+    sc = torch.randint(0, 255, (rows, K // 32), dtype=torch.uint8, device="cuda")
+    packed = moe.moe_pack_scales(sc, K).cpu().numpy()
+    s = sc.cpu().numpy()
+    for rb in range(rows // 128):
+        for kc in range(K // 128):
+            blk = packed[(rb * (K // 128) + kc) * 512:][:512]
+            for r in range(128):
+                for b in range(4):
+                    assert blk[(r % 32) * 16 + (r // 32) * 4 + b] == s[rb * 128 + r, kc * 4 + b]
+
+
+def test_synth_generators_agree():
+    for stream in (1, 4):
+        h = synth.normal_q16_host(9, stream, 12345, 4096)
+        d = synth.normal_q16_device(9, stream, 12345, 4096).cpu().numpy()
+        np.testing.assert_array_equal(h, d)
+    cfg = synth.CONFIGS["skewed_shared_t256"].replace(T=8)
+    np.testing.assert_array_equal(synth.logits_host(cfg), synth.logits_device(cfg).cpu().numpy())
+    np.testing.assert_array_equal(synth.x_host(cfg), bf16_bits(synth.x_device(cfg)))
+
+
+def test_deterministic_and_status_ok():
+    cfg = GRID[3]
+    _, ws, out1, _, _, st = run_layer(cfg)
+    _, ws2, out2, _, _, st2 = run_layer(cfg)
+    assert st == (0, 0) and st2 == (0, 0)
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+
+
+def test_expert_parallel_slices_sum_to_full():
+    full_cfg = SMALL.replace(T=64, block_n=16)
+    _, _, full, _, _, st = run_layer(full_cfg)
+    assert st == (0, 0)
+    acc = torch.zeros_like(full, dtype=torch.float32)
+    for off in (0, 32):
+        c = full_cfg.replace(E_local=32, expert_offset=off)
+        _, _, part, _, _, st = run_layer(c)
+        assert st == (0, 0)
+        acc += part.float()
+    # each slice rounds to bf16 on its own: allow two bf16 roundings
+    assert rel_l2(acc.cpu().numpy(), full.float().cpu().numpy()) <= 1e-2
+    assert torch.max(torch.abs(acc - full.float())).item() <= 2e-2
+
+
+def test_zero_tokens_and_single_token():
+    cfg = SMALL.replace(T=1, block_n=32)
+    check_layer(cfg)
+    shape = shape_of(cfg, 0)
+    shape.max_T = 4
+    wts, _, _ = _weights(cfg)
+    ws = moe.workspace(shape)
+    x = torch.empty((0, cfg.hidden), dtype=torch.bfloat16, device="cuda")
+    lg = torch.empty((0, cfg.E_global), dtype=torch.float32, device="cuda")
+    out, ids, w = moe.moe_layer(shape, lg, None, x, wts, ws)
+    torch.cuda.synchronize()
+    assert out.shape == (0, cfg.hidden)
+
+
+def test_graph_capture_replays_the_chain():
+    cfg = GRID[2]
+    shape = shape_of(cfg)
+    wts, _, _ = _weights(cfg)
+    x, logits, sl = device_inputs(cfg)
+    ws = moe.workspace(shape)
+    ids = torch.empty((shape.T, shape.kp), dtype=torch.int32, device="cuda")
+    w = torch.empty((shape.T, shape.kp), dtype=torch.float32, device="cuda")
+    out = torch.empty((shape.T, shape.hidden), dtype=torch.bfloat16, device="cuda")
+    ref, _, _ = moe.moe_layer(shape, logits, sl, x, wts, ws)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            moe.moe_layer(shape, logits, sl, x, wts, ws, ids, w, out)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    assert moe.moe_get_status(ws) == (0, 0)
+
+
+def test_host_buffer_entry_point_matches_device_path():
+    cfg = GRID[2]
+    shape = shape_of(cfg)
+    wts, _, _ = _weights(cfg)
+    x, logits, sl = device_inputs(cfg)
+    ws = moe.workspace(shape)
+    ref, _, _ = moe.moe_layer(shape, logits, sl, x, wts, ws)
+    xh, lh = x.cpu().pin_memory(), logits.cpu().pin_memory()
+    sh = sl.cpu().pin_memory() if sl is not None else None
+    oh = torch.empty((shape.T, shape.hidden), dtype=torch.bfloat16).pin_memory()
+    ws2 = moe.workspace(shape)
+    moe.moe_layer_host(shape, lh, sh, xh, wts, ws2, oh)
+    torch.cuda.synchronize()
+    assert torch.equal(oh.view(torch.int16), ref.cpu().view(torch.int16))

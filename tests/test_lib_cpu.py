@@ -1,0 +1,77 @@
+"""The C-ABI library on a machine without a GPU: it builds, loads, exports
+every function include/moe_api.h declares, and rejects bad arguments on the
+host (no kernel launch) with the documented error codes."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import mxfp4_mixture_experts_02_gb300 as moe
+from conftest import ROOT
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "moe_api.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*int\s+(moe_\w+)\s*\(", src, flags=re.M)))
+
+
+def test_library_exports_every_declared_symbol():
+    L = moe.lib()
+    names = _declared_functions()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def _shape(**kw):
+    base = dict(T=32, max_T=32, E_global=896, E_local=896, expert_offset=0, top_k=16, num_shared=0, hidden=3584,
+                inter=384, block_n=32)
+    base.update(kw)
+    return moe.MoeShape(**base)
+
+
+def test_supported_shapes_and_limits():
+    assert moe.moe_is_supported(_shape())
+    assert moe.moe_is_supported(_shape(block_n=16, E_local=448, expert_offset=448, T=64, max_T=64))
+    assert moe.moe_is_supported(_shape(num_shared=1, T=256, max_T=256))
+    bad = [dict(hidden=3500), dict(hidden=256), dict(inter=192), dict(block_n=64), dict(block_n=8),
+           dict(top_k=0), dict(top_k=33), dict(top_k=900, E_global=896), dict(E_global=2048, E_local=2048),
+           dict(num_shared=2), dict(E_local=0), dict(expert_offset=448), dict(expert_offset=-1),
+           dict(T=33), dict(T=-1), dict(max_T=1 << 20), dict(activation=1)]
+    for kw in bad:
+        assert not moe.moe_is_supported(_shape(**kw)), kw
+
+
+def test_workspace_bytes_grows_with_max_tokens():
+    a = moe.moe_workspace_bytes(_shape(T=1, max_T=32))
+    b = moe.moe_workspace_bytes(_shape(T=1, max_T=256))
+    assert 0 < a < b
+    with pytest.raises(moe.MoeError) as e:
+        moe.moe_workspace_bytes(_shape(hidden=100))
+    assert e.value.rc == -2
+
+
+def test_host_side_errors_launch_nothing():
+    L = moe.lib()
+    s = _shape().c()
+    # NULL pointers
+    assert L.moe_route(ctypes.byref(s), None, None, None, None, None) == -1
+    assert L.moe_sort(ctypes.byref(s), None, None, 0, None) == -1
+    assert L.moe_get_status(None, None, None) == -1
+    # unsupported shape
+    bad = _shape(block_n=64).c()
+    assert L.moe_sort(ctypes.byref(bad), 16, 256, 1 << 30, None) == -2
+    # workspace misaligned / too small (checked before any launch)
+    assert L.moe_sort(ctypes.byref(s), 16, 255, 1 << 30, None) == -3
+    assert L.moe_sort(ctypes.byref(s), 16, 256, 100, None) == -4
+    # misaligned weights
+    w = moe.lib  # noqa: F841
+    from mxfp4_mixture_experts_02_gb300 import _Weights
+    wt = _Weights(48, 256, 256, 256)  # w1 not 32-byte aligned
+    need = moe.moe_workspace_bytes(_shape())
+    assert L.moe_forward(ctypes.byref(s), 256, ctypes.byref(wt), 256, 256, need, 256, None) == -3
+    # packed-scale size rules
+    assert L.moe_pack_scales(16, 100, 128, 16, None) == -2
+    assert L.moe_quantize_mxfp4(16, 4, 33, 16, 16, None) == -2
