@@ -15,9 +15,10 @@ namespace moe {
 namespace {
 
 // Transaction bytes of one 128 x 128 E2M1 box loaded with the
-// 16U4_ALIGN16B tensor-map type: the shared-memory footprint, 16 bytes per 16
-// elements.
-constexpr int kFp4BoxTxBytes = 128 * 128;
+// 16U4_ALIGN16B tensor-map type: the packed bytes read from global memory
+// (8 bytes per 16 elements), not the 16-byte-per-16-element shared-memory
+// footprint.
+constexpr int kFp4BoxTxBytes = 128 * 128 / 2;
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;

@@ -83,19 +83,13 @@ inline Layout make_layout(const Dims& d) {
     L.groups = take(size_t(d.V_max) * 16);
     L.a_map = take(size_t(d.R_max) * 4);
     L.c_map = take(size_t(d.R_max) * 4);
-    if (d.mode == kModeDecode) {
-        // Tile scale layout: per virtual expert and per 512-K group, 32 lines
-        // x 16 bytes; line i = row i of the tile, byte b = K-block 16*g + b.
-        L.xsf_tile_bytes = (d.H / 512) * 512;
-        L.asf_tile_bytes = ((d.I + 511) / 512) * 512;
-        L.y_bf16 = 0;
-    } else {
-        // Tile scale layout for 128-row tiles: per 128-K chunk one 512-byte
-        // block, row r / K-block b at (r % 32) * 16 + (r / 32) * 4 + b.
-        L.xsf_tile_bytes = (d.H / 128) * 512;
-        L.asf_tile_bytes = (d.I / 128) * 512;
-        L.y_bf16 = 1;
-    }
+    // Tile scale layout: per virtual expert and 128-K chunk one 512-byte
+    // block, tile row r / K-block b at (r % 32) * 16 + (r / 32) * 4 + b: one
+    // tcgen05.cp .32x128b.warpx4 puts it in 4 TMEM columns, row r at lane
+    // r % 32, column r / 32, byte b.
+    L.xsf_tile_bytes = (d.H / 128) * 512;
+    L.asf_tile_bytes = (d.I / 128) * 512;
+    L.y_bf16 = (d.mode == kModeDecode) ? 0 : 1;
     L.xq = take(size_t(d.rows_alloc) * d.H);
     L.xsf = take(size_t(d.V_max) * L.xsf_tile_bytes);
     L.act = take(size_t(d.rows_alloc) * d.I);

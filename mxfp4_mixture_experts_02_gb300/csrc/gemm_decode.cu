@@ -47,7 +47,7 @@ struct Cfg {
     static constexpr int kOffSFB = kOffSFA + NA * 512;
     static constexpr int kStageBytes = ((kOffSFB + G * 512) + 1023) & ~1023;
     static constexpr int kAccCols = NA * G * B;       // fp32 columns of one accumulator buffer
-    static constexpr int kSfCols = 4 * NA + 4 * G;    // TMEM columns of one stage's scale blocks
+    static constexpr int kSfCols = ((4 * NA + 4 * G) + 15) & ~15;  // TMEM columns of one stage's scale blocks
     static constexpr int kSfBase = 2 * kAccCols;
     static constexpr int kTmemCols = 512;
     static constexpr int kBarBytes = (2 * STAGES + 5) * 8 + 16;
@@ -173,7 +173,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     for (int j = 0; j < G; ++j)
                         if (j < nt)
                             ptx::bulk_load(st + C::kOffSFB + j * 512,
-                                           p.b_sf + static_cast<size_t>(v0 + j) * p.b_sf_tile_bytes + (kc >> 2) * 512,
+                                           p.b_sf + static_cast<size_t>(v0 + j) * p.b_sf_tile_bytes + kc * 512,
                                            512, &sh.full[stage]);
                     if (++stage == STAGES) {
                         stage = 0;
@@ -229,7 +229,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         for (int j = 0; j < G; ++j) {
                             if (j >= nt) continue;
                             const uint64_t bdesc = ptx::sdesc_sw128(ptx::smem_u32(st + C::kOffB + j * C::kBTile) + kk * 32);
-                            const uint32_t sfb = sf + 4 * NA + 4 * j + (kc & 3);
+                            const uint32_t sfb = sf + 4 * NA + 4 * j;
 #pragma unroll
                             for (int a = 0; a < NA; ++a) {
                                 const uint64_t adesc = ptx::sdesc_sw128(ptx::smem_u32(st + a * C::kATile) + kk * 32);
@@ -261,6 +261,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const int g = it / MT, mt = it - g * MT;
             const int4 grp = p.groups[g];
             const int v0 = grp.y, nt = grp.z;
+            // FC2: lane i holds the routing weight of tile row i, loaded before
+            // the accumulator wait so the dependent loads overlap the MMAs.
+            float wrow[G];
+            if constexpr (!FC1) {
+#pragma unroll
+                for (int j = 0; j < G; ++j) {
+                    wrow[j] = 0.f;
+                    if (j < nt) {
+                        const int4 vi = p.vinfo[v0 + j];
+                        if (lane < vi.z) wrow[j] = p.topk_w[p.a_map[vi.y + lane]];
+                    }
+                }
+            }
             if (!wait_or_abort(&sh.accfull[abuf], aphase, p.wait_ns, sh.abort_flag)) {
                 if (lane == 0 && !*sh.abort_flag) record_timeout(p, sh.abort_flag, kSiteEpiAccFull);
                 break;
@@ -282,7 +295,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     }
                     ptx::tmem_wait_ld();
                     uint8_t* sf_tile = p.act_sf + static_cast<size_t>(v0 + j) * p.out_sf_tile_bytes;
-                    const int sf_off = ((mt * 128 + 32 * q) >> 9) * 512 + (((mt * 128 + 32 * q) >> 5) & 15);
+                    const int sf_off = ((mt * 128 + 32 * q) >> 7) * 512 + (((mt * 128 + 32 * q) >> 5) & 3);
 #pragma unroll
                     for (int n = 0; n < B; ++n) {
                         if (n < rows) {
@@ -301,13 +314,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     else
                         ptx::tmem_ld16(acc + j * B, yr);
                     ptx::tmem_wait_ld();
+                    float wj = 0.f;
+#pragma unroll
+                    for (int jj = 0; jj < G; ++jj)
+                        if (jj == j) wj = wrow[jj];
 #pragma unroll
                     for (int n = 0; n < B; ++n) {
-                        if (n < rows) {
-                            const int row = first + n;
-                            const float w = p.topk_w[p.a_map[row]];
-                            p.y[static_cast<size_t>(row) * p.H + f] = __uint_as_float(yr[n]) * w;
-                        }
+                        const float w = __shfl_sync(0xffffffffu, wj, n);
+                        if (n < rows) p.y[static_cast<size_t>(first + n) * p.H + f] = __uint_as_float(yr[n]) * w;
                     }
                 }
             }

@@ -5,7 +5,10 @@
 //                          expert-row order (the "[SGLang] CUTLASS MoE"
 //                          section 2 shuffle_rows folded into the quantiser)
 //                          with the tile scale layout the FC1 kernel copies
-//                          into tensor memory;
+//                          into tensor memory: per virtual expert and 128-K
+//                          chunk one 512-byte block, tile row i / K-block b
+//                          at byte i * 16 + b (the 128-row block layout with
+//                          only the first 32-row group populated);
 //   quantize_mxfp4_kernel: fp32 weights -> MXFP4 (E2M1, emax 2), offline;
 //   pack_scales_kernel   : row-major E8M0 -> 512-byte tensor-core blocks.
 #include "common.cuh"
@@ -56,13 +59,14 @@ __global__ void __launch_bounds__(kGatherThreads) gather_decode_kernel(GatherPar
             uint4* dst = reinterpret_cast<uint4*>(p.xq + static_cast<size_t>(row) * p.H + b * 32);
             dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
             dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-            sf_tile[(b >> 4) * 512 + i * 16 + (b & 15)] = static_cast<uint8_t>(ex + 127);
+            sf_tile[(b >> 2) * 512 + i * 16 + (b & 3)] = static_cast<uint8_t>(ex + 127);
         }
-        // unused lines of the tile's scale blocks (rows >= tile rows) -> 0
-        const int groups = p.H / 512;
-        for (int j = threadIdx.x; j < groups * 32 * 16; j += kGatherThreads) {
-            const int line = (j >> 4) & 31;
-            if (line >= rows) sf_tile[(j >> 9) * 512 + (j & 511)] = 0;
+        // every other byte of the tile's scale blocks -> 0 (rows >= tile rows,
+        // and the row groups 32..127 an N <= 32 MMA never reads)
+        const int bytes = (p.H / 128) * 512;
+        for (int j = threadIdx.x; j < bytes; j += kGatherThreads) {
+            const int line = (j >> 4) & 31, col = j & 15;
+            if (line >= rows || col >= 4) sf_tile[j] = 0;
         }
     }
     ptx::pdl_launch_dependents();

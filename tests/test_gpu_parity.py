@@ -74,7 +74,7 @@ def tile_scales_to_rows(views, vinfo, num_v, K):
         _, first, n, _ = vinfo[v]
         for i in range(n):
             for b in range(K // 32):
-                rows[first + i, b] = sf[v, (b // 16) * 512 + i * 16 + (b % 16)]
+                rows[first + i, b] = sf[v, (b // 4) * 512 + i * 16 + (b % 4)]
     return rows
 
 
