@@ -126,6 +126,9 @@ def setup_layer(cfg, device):
         w2[c0:c0 + n] = c.reshape(n, H, I // 2)
         s2[c0 * H:(c0 + n) * H] = s
     weights = moe.MoeWeights(w1, moe.moe_pack_scales(s1, H), w2, moe.moe_pack_scales(s2, I))
+    del s1, s2
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()  # drop the fp32 generation chunks
     x = synth.x_device(cfg, device)
     logits = synth.logits_device(cfg, device)
     sl = synth.shared_logit_device(cfg, device).contiguous() if cfg.num_shared else None
