@@ -265,6 +265,10 @@ def moe_layer_events(shape: MoeShape, logits, shared_logit, x, weights: MoeWeigh
     """moe_layer with 7 torch.cuda.Events recorded at the stage boundaries
     (before route, after route / sort / gather / FC1 / FC2 / combine)."""
     _check_cuda(logits, shared_logit, x, ws)
+    stream = torch.cuda.current_stream(x.device)
+    for ev in events:
+        if not ev.cuda_event:  # torch creates the CUDA event on its first record
+            ev.record(stream)
     arr = (ctypes.c_void_p * 7)(*[ev.cuda_event for ev in events])
     s, w = shape.c(), weights.c()
     _call("moe_layer_events", ctypes.byref(s), logits.data_ptr(), _ptr(shared_logit), x.data_ptr(), ctypes.byref(w),
