@@ -112,23 +112,25 @@ def setup_layer(cfg, device):
                          hidden=cfg.hidden, inter=cfg.inter, block_n=cfg.block_n, shared_scale=cfg.shared_scale)
     gids = cfg.global_ids
     E, H, I = gids.size, cfg.hidden, cfg.inter
-    w1 = torch.empty((E, 2 * I, H // 2), dtype=torch.uint8, device=device)
-    w2 = torch.empty((E, H, I // 2), dtype=torch.uint8, device=device)
-    s1 = torch.empty((E * 2 * I, H // 32), dtype=torch.uint8, device=device)
-    s2 = torch.empty((E * H, I // 32), dtype=torch.uint8, device=device)
+    c1 = torch.empty((E, 2 * I, H // 2), dtype=torch.uint8, device=device)
+    c2 = torch.empty((E, H, I // 2), dtype=torch.uint8, device=device)
+    s1 = torch.empty((E, 2 * I, H // 32), dtype=torch.uint8, device=device)
+    s2 = torch.empty((E, H, I // 32), dtype=torch.uint8, device=device)
     for c0 in range(0, E, 64):
         ids = gids[c0:c0 + 64]
         n = ids.size
         c, s = moe.moe_quantize_mxfp4(synth.w1_device(cfg, ids, device).reshape(n * 2 * I, H))
-        w1[c0:c0 + n] = c.reshape(n, 2 * I, H // 2)
-        s1[c0 * 2 * I:(c0 + n) * 2 * I] = s
+        c1[c0:c0 + n] = c.reshape(n, 2 * I, H // 2)
+        s1[c0:c0 + n] = s.reshape(n, 2 * I, H // 32)
         c, s = moe.moe_quantize_mxfp4(synth.w2_device(cfg, ids, device).reshape(n * H, I))
-        w2[c0:c0 + n] = c.reshape(n, H, I // 2)
-        s2[c0 * H:(c0 + n) * H] = s
-    weights = moe.MoeWeights(w1, moe.moe_pack_scales(s1, H), w2, moe.moe_pack_scales(s2, I))
-    del s1, s2
+        c2[c0:c0 + n] = c.reshape(n, H, I // 2)
+        s2[c0:c0 + n] = s.reshape(n, H, I // 32)
+    p1, q1 = moe.moe_pack_weights(c1, s1, True)
+    p2, q2 = moe.moe_pack_weights(c2, s2, False)
+    weights = moe.MoeWeights(p1, q1, p2, q2)
+    del c1, c2, s1, s2, c, s
     torch.cuda.synchronize()
-    torch.cuda.empty_cache()  # drop the fp32 generation chunks
+    torch.cuda.empty_cache()  # drop the fp32 generation chunks and row-major copies
     x = synth.x_device(cfg, device)
     logits = synth.logits_device(cfg, device)
     sl = synth.shared_logit_device(cfg, device).contiguous() if cfg.num_shared else None

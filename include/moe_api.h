@@ -77,11 +77,12 @@ typedef struct moe_shape {
     float shared_scale;
 } moe_shape;
 
-/* Packed expert weights (device, read only), E_tot = E_local + num_shared:
- *   w1     E2M1 codes [E_tot, 2I, H/2], 32-byte aligned
- *   w1_sf  E8M0 scales packed by moe_pack_scales from [E_tot*2I, H/32]
- *   w2     E2M1 codes [E_tot, H, I/2], 32-byte aligned
- *   w2_sf  E8M0 scales packed by moe_pack_scales from [E_tot*H, I/32] */
+/* Packed expert weights (device, read only), E_tot = E_local + num_shared,
+ * produced by moe_pack_weights from row-major MXFP4 (moe_quantize_mxfp4):
+ *   w1, w1_sf  W1 [E_tot, 2I, H] packed with pair_halves = 1 (gate/up tiles
+ *              of the same features adjacent)
+ *   w2, w2_sf  W2 [E_tot, H, I] packed with pair_halves = 0
+ * Codes 32-byte aligned, scales 16-byte aligned. */
 typedef struct moe_weights {
     const uint8_t *w1, *w1_sf, *w2, *w2_sf;
 } moe_weights;
@@ -115,9 +116,6 @@ int moe_is_supported(const moe_shape* shape);
 /* Bytes of the single workspace buffer (256-byte aligned carve). */
 int moe_workspace_bytes(const moe_shape* shape, size_t* bytes);
 
-/* Bytes of the packed scale array produced by moe_pack_scales. */
-int moe_packed_scale_bytes(int64_t rows, int64_t K, size_t* bytes);
-
 /* fp32 [rows, K] -> MXFP4: codes [rows, K/2] and E8M0 scales [rows, K/32]
  * (row-major), shared exponent floor(log2 amax) - 2, elements rounded to
  * nearest even and saturated to +-6 (OCP MX v1.0).  K % 32 == 0.  codes must
@@ -125,11 +123,22 @@ int moe_packed_scale_bytes(int64_t rows, int64_t K, size_t* bytes);
 int moe_quantize_mxfp4(const float* w, int64_t rows, int64_t K, uint8_t* codes, uint8_t* scales,
                        moe_stream_t stream);
 
-/* Row-major E8M0 scales [rows, K/32] -> the tensor-core scale layout: for
- * each 128-row block and 128-K chunk, 512 bytes where row r (mod 128) and
- * K-block b (mod 4) sit at byte (r % 32) * 16 + (r / 32) * 4 + b.
- * rows % 128 == 0, K % 128 == 0. */
-int moe_pack_scales(const uint8_t* scales, int64_t rows, int64_t K, uint8_t* packed, moe_stream_t stream);
+/* Tile-major packing of one weight matrix per expert for the tensor-core
+ * path.  Input: row-major E2M1 codes [experts, N, K/2] and E8M0 scales
+ * [experts, N, K/32] (moe_quantize_mxfp4).  A row block holds 128 rows, or
+ * with pair_halves = 1 the 128 rows b*128.. of the first half [0, N/2)
+ * followed by the 128 rows N/2 + b*128.. of the second half (W1: gate and up
+ * rows of the same features).  Output, for each expert e, row block b and
+ * 128-K chunk c in that order:
+ *   packed_codes : the block's rows x 64 bytes (the chunk's 128 codes of each
+ *                  row, row-major), contiguous;
+ *   packed_scales: per 128-row group of the block a 512-byte block, row r /
+ *                  K-block j of the chunk at byte (r % 32) * 16 + (r / 32) * 4
+ *                  + j (the tensor-memory scale layout, one tcgen05.cp each).
+ * Sizes equal the inputs'.  N % 128 == 0 (N % 256 == 0 with pair_halves),
+ * K % 128 == 0. */
+int moe_pack_weights(const uint8_t* codes, const uint8_t* scales, int64_t experts, int64_t N, int64_t K,
+                     int32_t pair_halves, uint8_t* packed_codes, uint8_t* packed_scales, moe_stream_t stream);
 
 /* Routing.  logits fp32 [T, E_global]; shared_logit bf16 [T, num_shared] or
  * NULL when num_shared == 0.  Writes topk_ids int32 [T, k'] and topk_w fp32

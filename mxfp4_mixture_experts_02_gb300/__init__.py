@@ -18,7 +18,7 @@ from . import build as _build
 
 __all__ = [
     "MoeShape", "MoeWeights", "MoeError", "lib", "moe_is_supported", "moe_workspace_bytes",
-    "moe_packed_scale_bytes", "moe_quantize_mxfp4", "moe_pack_scales", "moe_route", "moe_sort", "moe_forward",
+    "moe_quantize_mxfp4", "moe_pack_weights", "moe_route", "moe_sort", "moe_forward",
     "moe_layer", "moe_layer_host", "moe_layer_events", "moe_get_views", "moe_get_status", "moe_num_sms", "quantize_expert_weights",
     "workspace", "MOE_OK", "MOE_ERR_TIMEOUT",
 ]
@@ -92,10 +92,10 @@ _lib = None
 _SIGS = {
     "moe_is_supported": [ctypes.c_void_p],
     "moe_workspace_bytes": [ctypes.c_void_p, ctypes.c_void_p],
-    "moe_packed_scale_bytes": [ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p],
     "moe_quantize_mxfp4": [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
                            ctypes.c_void_p],
-    "moe_pack_scales": [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p],
+    "moe_pack_weights": [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                         ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p],
     "moe_route": [ctypes.c_void_p] * 6,
     "moe_sort": [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p],
     "moe_forward": [ctypes.c_void_p] * 5 + [ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p],
@@ -164,12 +164,6 @@ def moe_workspace_bytes(shape: MoeShape) -> int:
     return n.value
 
 
-def moe_packed_scale_bytes(rows: int, K: int) -> int:
-    n = ctypes.c_size_t(0)
-    _call("moe_packed_scale_bytes", rows, K, ctypes.byref(n))
-    return n.value
-
-
 def moe_num_sms() -> int:
     n = ctypes.c_int32(0)
     _call("moe_num_sms", ctypes.byref(n))
@@ -192,25 +186,33 @@ def moe_quantize_mxfp4(w: torch.Tensor):
     return codes, scales
 
 
-def moe_pack_scales(scales: torch.Tensor, K: int) -> torch.Tensor:
-    """Row-major E8M0 [rows, K/32] -> tensor-core scale blocks (same byte count)."""
-    _check_cuda(scales)
-    rows = scales.shape[0]
-    packed = torch.empty(moe_packed_scale_bytes(rows, K), dtype=torch.uint8, device=scales.device)
-    _call("moe_pack_scales", scales.data_ptr(), rows, K, packed.data_ptr(), _stream(scales.device))
-    return packed
+def moe_pack_weights(codes: torch.Tensor, scales: torch.Tensor, pair_halves: bool):
+    """Row-major MXFP4 of one weight matrix per expert -- codes uint8 [E, N, K/2],
+    scales uint8 [E, N, K/32] -- to the tile-major layout the GEMMs stream
+    (see moe_api.h).  Returns (packed_codes, packed_scales), flat uint8."""
+    _check_cuda(codes, scales)
+    E, N, K2 = codes.shape
+    pc = torch.empty(codes.numel(), dtype=torch.uint8, device=codes.device)
+    ps = torch.empty(scales.numel(), dtype=torch.uint8, device=codes.device)
+    _call("moe_pack_weights", codes.data_ptr(), scales.data_ptr(), E, N, 2 * K2, 1 if pair_halves else 0,
+          pc.data_ptr(), ps.data_ptr(), _stream(codes.device))
+    return pc, ps
 
 
-def quantize_expert_weights(w1: torch.Tensor, w2: torch.Tensor, keep_rowmajor_scales: bool = False):
-    """fp32 W1 [E, 2I, H] and W2 [E, H, I] (device) -> MoeWeights (and, if asked,
-    the row-major scales (w1_sf, w2_sf) for inspection)."""
+def quantize_expert_weights(w1: torch.Tensor, w2: torch.Tensor, keep_rowmajor: bool = False):
+    """fp32 W1 [E, 2I, H] and W2 [E, H, I] (device) -> packed MoeWeights (and, if
+    asked, the row-major codes and scales (c1, s1, c2, s2) for inspection)."""
     E, I2, H = w1.shape
     I = w2.shape[2]
     c1, s1 = moe_quantize_mxfp4(w1.reshape(E * I2, H))
     c2, s2 = moe_quantize_mxfp4(w2.reshape(E * H, I))
-    wts = MoeWeights(c1.reshape(E, I2, H // 2), moe_pack_scales(s1, H), c2.reshape(E, H, I // 2), moe_pack_scales(s2, I))
-    if keep_rowmajor_scales:
-        return wts, (s1.reshape(E, I2, H // 32), s2.reshape(E, H, I // 32))
+    c1, s1 = c1.reshape(E, I2, H // 2), s1.reshape(E, I2, H // 32)
+    c2, s2 = c2.reshape(E, H, I // 2), s2.reshape(E, H, I // 32)
+    p1, q1 = moe_pack_weights(c1, s1, True)
+    p2, q2 = moe_pack_weights(c2, s2, False)
+    wts = MoeWeights(p1, q1, p2, q2)
+    if keep_rowmajor:
+        return wts, (c1, s1, c2, s2)
     return wts
 
 

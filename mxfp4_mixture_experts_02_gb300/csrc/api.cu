@@ -14,11 +14,9 @@
 namespace moe {
 namespace {
 
-// Transaction bytes of one 128 x 128 E2M1 box loaded with the
-// 16U4_ALIGN16B tensor-map type: the packed bytes read from global memory
-// (8 bytes per 16 elements), not the 16-byte-per-16-element shared-memory
-// footprint.
-constexpr int kFp4BoxTxBytes = 128 * 128 / 2;
+// A 16U4_ALIGN16B box completes its packed global byte count (8 bytes per 16
+// E2M1 elements), not its 16-byte-per-16-element shared-memory footprint.
+constexpr int kFp4BytesPer128Row = 64;
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
@@ -122,8 +120,13 @@ int run_forward(const moe_shape* s, const uint16_t* x, const moe_weights* wt, co
 
     CUtensorMap mw1, mw2, mx, mact;
     const uint64_t Et = static_cast<uint64_t>(d.Et);
-    if (!make_map(&mw1, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, wt->w1, d.H, Et * 2 * d.I, d.H / 2, 128, 128) ||
-        !make_map(&mw2, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, wt->w2, d.I, Et * d.H, d.I / 2, 128, 128) ||
+    // Tile-major packed weights viewed as rows of 128 E2M1 codes (64 bytes):
+    // an FC1 stage is one 256-row box (gate + up tile), an FC2 stage a
+    // 128-row box, each one contiguous run of global memory.
+    if (!make_map(&mw1, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, wt->w1, 128, Et * 2 * d.I * (d.H / 128),
+                  kFp4BytesPer128Row, 128, 256) ||
+        !make_map(&mw2, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, wt->w2, 128, Et * d.H * (d.I / 128),
+                  kFp4BytesPer128Row, 128, 128) ||
         !make_map(&mx, CU_TENSOR_MAP_DATA_TYPE_UINT8, at<uint8_t>(ws, L.xq), d.H, d.rows_alloc, d.H, 128, d.B) ||
         !make_map(&mact, CU_TENSOR_MAP_DATA_TYPE_UINT8, at<uint8_t>(ws, L.act), d.I, d.rows_alloc, d.I, 128, d.B))
         return MOE_ERR_CUDA;
@@ -141,16 +144,17 @@ int run_forward(const moe_shape* s, const uint16_t* x, const moe_weights* wt, co
     g.H = d.H;
     g.I = d.I;
     g.out_sf_tile_bytes = L.asf_tile_bytes;
-    g.a_tile_tx_bytes = kFp4BoxTxBytes;
     g.wait_ns = kWaitLimitNs;
 
     g.a_sf = wt->w1_sf;
+    g.a_tx_bytes = 256 * kFp4BytesPer128Row;
     g.b_sf = at<uint8_t>(ws, L.xsf);
     g.b_sf_tile_bytes = L.xsf_tile_bytes;
     e = launch_fc1_decode(mw1, mx, g, d.B, nsm, st, pdl);
     if (e != cudaSuccess || !rec(ev, 4, st)) return MOE_ERR_CUDA;
 
     g.a_sf = wt->w2_sf;
+    g.a_tx_bytes = 128 * kFp4BytesPer128Row;
     g.b_sf = at<uint8_t>(ws, L.asf);
     g.b_sf_tile_bytes = L.asf_tile_bytes;
     e = launch_fc2_decode(mw2, mact, g, d.B, nsm, st, pdl);
@@ -199,13 +203,6 @@ int moe_workspace_bytes(const moe_shape* s, size_t* bytes) {
     return MOE_OK;
 }
 
-int moe_packed_scale_bytes(int64_t rows, int64_t K, size_t* bytes) {
-    if (!bytes) return MOE_ERR_NULL;
-    if (rows <= 0 || K <= 0 || rows % 128 || K % 128) return MOE_ERR_SHAPE;
-    *bytes = static_cast<size_t>(rows) * (K / 32);
-    return MOE_OK;
-}
-
 int moe_quantize_mxfp4(const float* w, int64_t rows, int64_t K, uint8_t* codes, uint8_t* scales,
                        moe_stream_t stream) {
     if (!w || !codes || !scales) return MOE_ERR_NULL;
@@ -215,11 +212,13 @@ int moe_quantize_mxfp4(const float* w, int64_t rows, int64_t K, uint8_t* codes, 
     return cuda_rc(launch_quantize_mxfp4(p, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-int moe_pack_scales(const uint8_t* scales, int64_t rows, int64_t K, uint8_t* packed, moe_stream_t stream) {
-    if (!scales || !packed) return MOE_ERR_NULL;
-    if (rows <= 0 || K <= 0 || rows % 128 || K % 128) return MOE_ERR_SHAPE;
-    PackParams p{scales, packed, rows, K};
-    return cuda_rc(launch_pack_scales(p, reinterpret_cast<cudaStream_t>(stream)));
+int moe_pack_weights(const uint8_t* codes, const uint8_t* scales, int64_t experts, int64_t N, int64_t K,
+                     int32_t pair_halves, uint8_t* packed_codes, uint8_t* packed_scales, moe_stream_t stream) {
+    if (!codes || !scales || !packed_codes || !packed_scales) return MOE_ERR_NULL;
+    if (experts <= 0 || N <= 0 || K <= 0 || K % 128 || N % (pair_halves ? 256 : 128)) return MOE_ERR_SHAPE;
+    if (!aligned(codes, 16) || !aligned(packed_codes, 16)) return MOE_ERR_ALIGN;
+    PackParams p{codes, scales, packed_codes, packed_scales, experts, N, K, pair_halves ? 1 : 0};
+    return cuda_rc(launch_pack_weights(p, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int moe_route(const moe_shape* s, const float* logits, const uint16_t* shared_logit, int32_t* topk_ids,

@@ -12,19 +12,39 @@ namespace moe {
 
 namespace {
 
-constexpr int kCombineThreads = 256;
+constexpr int kCombineThreads = 128;   // one float4 of the hidden dim per thread
 constexpr int kMaxSlots = 64;
 
+// Block (chunk of 512 hidden columns, token).  The token's rows are read
+// once into shared memory; each thread sums its float4 over the slots in
+// ascending order, issuing the loads of 4 slots before adding them.
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineParams p) {
     __shared__ int rows[kMaxSlots];
     ptx::pdl_wait();
-    const int t = blockIdx.x;
+    const int t = blockIdx.y;
     if (threadIdx.x < p.kp) rows[threadIdx.x] = p.c_map[static_cast<size_t>(t) * p.kp + threadIdx.x];
     __syncthreads();
-    const int n4 = p.H / 4;
-    for (int c = threadIdx.x; c < n4; c += kCombineThreads) {
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int j = 0; j < p.kp; ++j) {
+    const int c = blockIdx.x * kCombineThreads + threadIdx.x;  // float4 column
+    if (c < p.H / 4) {
+        const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+        float4 acc = zero;
+        int j = 0;
+        for (; j + 4 <= p.kp; j += 4) {
+            float4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int r = rows[j + u];
+                v[u] = r >= 0 ? reinterpret_cast<const float4*>(p.y + static_cast<size_t>(r) * p.H)[c] : zero;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                acc.x += v[u].x;
+                acc.y += v[u].y;
+                acc.z += v[u].z;
+                acc.w += v[u].w;
+            }
+        }
+        for (; j < p.kp; ++j) {
             const int r = rows[j];
             if (r < 0) continue;
             const float4 v = reinterpret_cast<const float4*>(p.y + static_cast<size_t>(r) * p.H)[c];
@@ -47,7 +67,8 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineParams 
 
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream, bool pdl) {
     if (p.T == 0) return cudaSuccess;
-    return launch_kernel(combine_kernel, dim3(p.T), dim3(kCombineThreads), 0, stream, pdl, p);
+    const dim3 grid((p.H / 4 + kCombineThreads - 1) / kCombineThreads, p.T);
+    return launch_kernel(combine_kernel, grid, dim3(kCombineThreads), 0, stream, pdl, p);
 }
 
 }  // namespace moe

@@ -146,11 +146,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 int fr[G];
 #pragma unroll
                 for (int j = 0; j < G; ++j) fr[j] = (j < nt) ? p.vinfo[v0 + j].y : 0;
-                const int rowA0 = FC1 ? e * 2 * p.I + mt * 128 : e * p.H + mt * 128;
-                const int rowA1 = e * 2 * p.I + p.I + mt * 128;
-                const int blkA0 = FC1 ? e * (2 * p.I / 128) + mt : e * (p.H / 128) + mt;
-                const int blkA1 = e * (2 * p.I / 128) + p.I / 128 + mt;
-                const uint32_t tx = NA * p.a_tile_tx_bytes + nt * (C::kBTile + 512) + NA * 512;
+                // tile-major packed weights: (expert, row block, K chunk) tiles
+                const int64_t tile0 = (static_cast<int64_t>(e) * MT + mt) * KC;
+                const uint32_t tx = p.a_tx_bytes + nt * (C::kBTile + 512) + NA * 512;
                 for (int kc = 0; kc < KC; ++kc) {
                     if (!wait_or_abort(&sh.empty[stage], phase ^ 1, p.wait_ns, sh.abort_flag)) {
                         if (!*sh.abort_flag) record_timeout(p, sh.abort_flag, kSiteProducerEmpty);
@@ -159,16 +157,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     }
                     uint8_t* st = smem + stage * C::kStageBytes;
                     ptx::mbar_arrive_expect_tx(&sh.full[stage], tx);
-                    ptx::tma_load_2d(st, &tmA, &sh.full[stage], kc * 128, rowA0);
-                    if (FC1) ptx::tma_load_2d(st + C::kATile, &tmA, &sh.full[stage], kc * 128, rowA1);
+                    ptx::tma_load_2d(st, &tmA, &sh.full[stage], 0, static_cast<int32_t>((tile0 + kc) * (NA * 128)));
 #pragma unroll
                     for (int j = 0; j < G; ++j)
                         if (j < nt) ptx::tma_load_2d(st + C::kOffB + j * C::kBTile, &tmB, &sh.full[stage], kc * 128, fr[j]);
-                    ptx::bulk_load(st + C::kOffSFA, p.a_sf + (static_cast<size_t>(blkA0) * KC + kc) * 512, 512,
+                    ptx::bulk_load(st + C::kOffSFA, p.a_sf + static_cast<size_t>(tile0 + kc) * (NA * 512), NA * 512,
                                    &sh.full[stage]);
-                    if (FC1)
-                        ptx::bulk_load(st + C::kOffSFA + 512, p.a_sf + (static_cast<size_t>(blkA1) * KC + kc) * 512,
-                                       512, &sh.full[stage]);
 #pragma unroll
                     for (int j = 0; j < G; ++j)
                         if (j < nt)

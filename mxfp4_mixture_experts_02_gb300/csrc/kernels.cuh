@@ -71,7 +71,7 @@ struct GemmParams {
     float* y;              // FC2 output [R, H] (fp32)
     int H, I;
     int b_sf_tile_bytes, out_sf_tile_bytes;
-    int a_tile_tx_bytes;   // transaction bytes of one 128x128 E2M1 TMA box
+    int a_tx_bytes;        // transaction bytes of a stage's weight box (packed E2M1 bytes)
     uint64_t wait_ns;
 };
 
@@ -90,9 +90,12 @@ struct QuantParams {
 };
 
 struct PackParams {
+    const uint8_t* codes;
     const uint8_t* scales;
-    uint8_t* packed;
-    int64_t rows, K;
+    uint8_t* packed_codes;
+    uint8_t* packed_scales;
+    int64_t experts, N, K;
+    int pair;
 };
 
 cudaError_t launch_route(const RouteParams& p, cudaStream_t stream, bool pdl);
@@ -104,6 +107,6 @@ cudaError_t launch_fc2_decode(const CUtensorMap& tmA, const CUtensorMap& tmB, co
                               cudaStream_t stream, bool pdl);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream, bool pdl);
 cudaError_t launch_quantize_mxfp4(const QuantParams& p, cudaStream_t stream);
-cudaError_t launch_pack_scales(const PackParams& p, cudaStream_t stream);
+cudaError_t launch_pack_weights(const PackParams& p, cudaStream_t stream);
 
 }  // namespace moe

@@ -10,7 +10,10 @@
 //                          at byte i * 16 + b (the 128-row block layout with
 //                          only the first 32-row group populated);
 //   quantize_mxfp4_kernel: fp32 weights -> MXFP4 (E2M1, emax 2), offline;
-//   pack_scales_kernel   : row-major E8M0 -> 512-byte tensor-core blocks.
+//   pack_codes_kernel,
+//   pack_scales_kernel   : row-major MXFP4 -> tile-major codes (one contiguous
+//                          run per TMA box) and 512-byte tensor-memory scale
+//                          blocks, offline.
 #include "common.cuh"
 #include "kernels.cuh"
 #include "ptx.cuh"
@@ -108,18 +111,46 @@ __global__ void quantize_mxfp4_kernel(QuantParams p) {
     }
 }
 
-// One thread per packed byte.
-__global__ void pack_scales_kernel(PackParams p) {
-    const int64_t kc_n = p.K / 128;
-    const int64_t total = (p.rows / 128) * kc_n * 512;
+// Source row of row rr of row block b (see moe_pack_weights).
+__device__ __forceinline__ int64_t packed_src_row(int64_t b, int rr, int64_t N, int pair) {
+    if (!pair) return b * 128 + rr;
+    return rr < 128 ? b * 128 + rr : N / 2 + b * 128 + (rr - 128);
+}
+
+// Codes: one thread per 16-byte piece of the output.
+__global__ void pack_codes_kernel(PackParams p) {
+    const int RB = p.pair ? 256 : 128;
+    const int64_t NB = p.N / RB, KC = p.K / 128;
+    const int64_t total = p.experts * p.N * (p.K / 2) / 16;
     for (int64_t o = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; o < total;
          o += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int64_t blk = o / 512;
-        const int pos = static_cast<int>(o - blk * 512);
-        const int64_t rb = blk / kc_n, kc = blk - rb * kc_n;
+        const int64_t tile = o / (RB * 4);
+        const int within = static_cast<int>(o - tile * RB * 4);
+        const int rr = within >> 2, piece = within & 3;
+        const int64_t e = tile / (NB * KC), rem = tile - e * NB * KC;
+        const int64_t b = rem / KC, c = rem - b * KC;
+        const int64_t row = e * p.N + packed_src_row(b, rr, p.N, p.pair);
+        reinterpret_cast<uint4*>(p.packed_codes)[o] =
+            *reinterpret_cast<const uint4*>(p.codes + row * (p.K / 2) + c * 64 + piece * 16);
+    }
+}
+
+// Scales: one thread per output byte.
+__global__ void pack_scales_kernel(PackParams p) {
+    const int RB = p.pair ? 256 : 128;
+    const int64_t NB = p.N / RB, KC = p.K / 128;
+    const int64_t total = p.experts * p.N * (p.K / 32);
+    for (int64_t o = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; o < total;
+         o += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t tile = o / (RB * 4);
+        const int within = static_cast<int>(o - tile * RB * 4);
+        const int grp = within >> 9, pos = within & 511;
         const int line = pos >> 4, quarter = (pos >> 2) & 3, kb = pos & 3;
-        const int64_t row = rb * 128 + quarter * 32 + line;
-        p.packed[o] = p.scales[row * (p.K / 32) + kc * 4 + kb];
+        const int rr = grp * 128 + quarter * 32 + line;
+        const int64_t e = tile / (NB * KC), rem = tile - e * NB * KC;
+        const int64_t b = rem / KC, c = rem - b * KC;
+        const int64_t row = e * p.N + packed_src_row(b, rr, p.N, p.pair);
+        p.packed_scales[o] = p.scales[row * (p.K / 32) + c * 4 + kb];
     }
 }
 
@@ -140,8 +171,9 @@ cudaError_t launch_quantize_mxfp4(const QuantParams& p, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
-cudaError_t launch_pack_scales(const PackParams& p, cudaStream_t stream) {
-    pack_scales_kernel<<<grid_for((p.rows / 128) * (p.K / 128) * 512, 256), 256, 0, stream>>>(p);
+cudaError_t launch_pack_weights(const PackParams& p, cudaStream_t stream) {
+    pack_codes_kernel<<<grid_for(p.experts * p.N * (p.K / 2) / 16, 256), 256, 0, stream>>>(p);
+    pack_scales_kernel<<<grid_for(p.experts * p.N * (p.K / 32), 256), 256, 0, stream>>>(p);
     return cudaGetLastError();
 }
 

@@ -2,14 +2,15 @@
 // shared expert.
 //
 // One warp per token.  Lane l holds the logits of experts l, l+32, ... in
-// registers (coalesced loads of the token's row).  Each of the k rounds takes
-// a warp-wide argmax of (logit, -id) with butterfly shuffles, so ties go to
-// the lower expert id, and removes the winner.  Weights: exp(l_j - l_0) / sum
-// over the picks (softmax renormalised over the selected experts).  The
-// shared expert gets id E_global + s and weight sigmoid(fp32(bf16 logit)) *
-// scale, computed in fp32 in the same kernel ("[sglang] SGLang MoE shared
-// expert: fuse 3 kernels into 1": the sigmoid and the bf16->fp32 cast fused
-// into the append).
+// registers (coalesced loads of the token's row) and keeps its best untaken
+// entry.  Each of the k rounds is two warp reductions: the maximum of an
+// order-preserving integer key of the logit, then the smallest expert id
+// among the lanes holding that maximum (ties go to the lower id); only the
+// winning lane rescans its entries.  Weights: exp(l_j - l_0) / sum over the
+// picks (softmax renormalised over the selected experts).  The shared expert
+// gets id E_global + s and weight sigmoid(fp32(bf16 logit)) * scale, computed
+// in fp32 in the same kernel ("[sglang] SGLang MoE shared expert: fuse 3
+// kernels into 1": the sigmoid and the bf16->fp32 cast fused into the append).
 #include "common.cuh"
 #include "kernels.cuh"
 #include "ptx.cuh"
@@ -21,9 +22,19 @@ namespace {
 constexpr int kRouteWarps = 8;
 constexpr int kMaxPerLane = 32;  // E_global <= 1024
 
-__device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
-    return va > vb || (va == vb && ia < ib);
+// Monotone map of a finite fp32 to uint32 (a < b  <=>  key(a) < key(b));
+// -0 is folded onto +0 so that equal values tie.
+__device__ __forceinline__ uint32_t order_key(float f) {
+    uint32_t u = __float_as_uint(f);
+    if (u == 0x80000000u) u = 0;
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
+
+__device__ __forceinline__ float key_value(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k ^ 0x80000000u) : ~k);
+}
+
+constexpr uint32_t kNoId = 0xFFFFFFFFu;
 
 __global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(RouteParams p) {
     ptx::pdl_wait();
@@ -31,46 +42,43 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(RouteParams p) 
     const int t = blockIdx.x * kRouteWarps + (threadIdx.x >> 5);
     if (t < p.T) {
         const float* row = p.logits + static_cast<size_t>(t) * p.Eg;
-        const int nper = (p.Eg + 31) / 32;
-        float v[kMaxPerLane];
+        uint32_t key[kMaxPerLane];
+        uint32_t avail = 0;
 #pragma unroll
         for (int i = 0; i < kMaxPerLane; ++i) {
             const int e = lane + 32 * i;
-            v[i] = (i < nper && e < p.Eg) ? row[e] : -INFINITY;
+            const bool in = e < p.Eg;
+            key[i] = in ? order_key(row[e]) : 0u;
+            if (in) avail |= 1u << i;
         }
-        uint32_t taken = 0;
-        for (int i = 0; i < kMaxPerLane; ++i)
-            if (i >= nper || lane + 32 * i >= p.Eg) taken |= 1u << i;
-
-        float my_val = 0.f;
-        int my_id = 0;
+        // best untaken entry of this lane (lower index wins ties = lower id)
+        auto lane_best = [&](uint32_t& bk, uint32_t& bid) {
+            bk = 0;
+            bid = kNoId;
+#pragma unroll
+            for (int i = 0; i < kMaxPerLane; ++i)
+                if (((avail >> i) & 1u) && (bid == kNoId || key[i] > bk)) {
+                    bk = key[i];
+                    bid = static_cast<uint32_t>(lane + 32 * i);
+                }
+        };
+        uint32_t bk, bid;
+        lane_best(bk, bid);
+        uint32_t my_key = 0, my_id = 0;
         for (int j = 0; j < p.k; ++j) {
-            // lane-local best among untaken entries (lower index = lower id)
-            float bv = -INFINITY;
-            int bi = 0x7FFFFFFF;
-#pragma unroll
-            for (int i = 0; i < kMaxPerLane; ++i) {
-                const int e = lane + 32 * i;
-                if (!((taken >> i) & 1u) && better(v[i], e, bv, bi)) {
-                    bv = v[i];
-                    bi = e;
-                }
+            // lanes without candidates hold bid = kNoId and never win
+            const uint32_t kmax = __reduce_max_sync(0xffffffffu, bid == kNoId ? 0u : bk);
+            const uint32_t win = __reduce_min_sync(0xffffffffu, (bid != kNoId && bk == kmax) ? bid : kNoId);
+            if (lane == static_cast<int>(win & 31)) {
+                avail &= ~(1u << (win >> 5));
+                lane_best(bk, bid);
             }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-                const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-                if (better(ov, oi, bv, bi)) {
-                    bv = ov;
-                    bi = oi;
-                }
-            }
-            if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
             if (lane == j) {
-                my_val = bv;
-                my_id = bi;
+                my_key = kmax;
+                my_id = win;
             }
         }
+        const float my_val = key_value(my_key);
         const float m = __shfl_sync(0xffffffffu, my_val, 0);
         const float ex = (lane < p.k) ? expf(my_val - m) : 0.f;
         float sum = ex;
@@ -78,7 +86,7 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(RouteParams p) 
         for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
         const size_t base = static_cast<size_t>(t) * p.kp;
         if (lane < p.k) {
-            p.ids[base + lane] = my_id;
+            p.ids[base + lane] = static_cast<int32_t>(my_id);
             p.w[base + lane] = ex / sum;
         }
         if (lane < p.S) {

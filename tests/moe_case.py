@@ -3,7 +3,7 @@ tokens being checked, the oracle's own independent computation.
 
 GPU side : x / logits / shared logit / fp32 weights from the CUDA build of the
            seeded generator; weights quantised by the library
-           (moe_quantize_mxfp4 + moe_pack_scales).
+           (moe_quantize_mxfp4 + moe_pack_weights).
 Oracle   : the same seeded inputs from the host build of the generator;
            routing, sort, weight quantisation and forward by the oracle.
 Nothing computed by the GPU library feeds the oracle.
@@ -25,33 +25,33 @@ def shape_of(cfg: synth.MoeConfig, T: int | None = None) -> moe.MoeShape:
                         hidden=cfg.hidden, inter=cfg.inter, block_n=cfg.block_n, shared_scale=cfg.shared_scale)
 
 
-def device_weights(cfg: synth.MoeConfig, chunk: int = 64, keep_rowmajor_scales: bool = False):
+def device_weights(cfg: synth.MoeConfig, chunk: int = 64, keep_rowmajor: bool = False):
     """Packed weights of all local experts (+shared), generated and quantised
-    on the device chunk by chunk."""
+    on the device chunk by chunk, packed by the library."""
     gids = cfg.global_ids
     E, H, I = gids.size, cfg.hidden, cfg.inter
     dev = "cuda"
-    w1 = torch.empty((E, 2 * I, H // 2), dtype=torch.uint8, device=dev)
-    w2 = torch.empty((E, H, I // 2), dtype=torch.uint8, device=dev)
-    s1 = torch.empty((E * 2 * I, H // 32), dtype=torch.uint8, device=dev)
-    s2 = torch.empty((E * H, I // 32), dtype=torch.uint8, device=dev)
+    c1 = torch.empty((E, 2 * I, H // 2), dtype=torch.uint8, device=dev)
+    c2 = torch.empty((E, H, I // 2), dtype=torch.uint8, device=dev)
+    s1 = torch.empty((E, 2 * I, H // 32), dtype=torch.uint8, device=dev)
+    s2 = torch.empty((E, H, I // 32), dtype=torch.uint8, device=dev)
     for c0 in range(0, E, chunk):
         ids = gids[c0:c0 + chunk]
         n = ids.size
-        f1 = synth.w1_device(cfg, ids)
-        c, s = moe.moe_quantize_mxfp4(f1.reshape(n * 2 * I, H))
-        w1[c0:c0 + n] = c.reshape(n, 2 * I, H // 2)
-        s1[c0 * 2 * I:(c0 + n) * 2 * I] = s
-        del f1
-        f2 = synth.w2_device(cfg, ids)
-        c, s = moe.moe_quantize_mxfp4(f2.reshape(n * H, I))
-        w2[c0:c0 + n] = c.reshape(n, H, I // 2)
-        s2[c0 * H:(c0 + n) * H] = s
-        del f2
-    wts = moe.MoeWeights(w1, moe.moe_pack_scales(s1, H), w2, moe.moe_pack_scales(s2, I))
+        c, s = moe.moe_quantize_mxfp4(synth.w1_device(cfg, ids).reshape(n * 2 * I, H))
+        c1[c0:c0 + n] = c.reshape(n, 2 * I, H // 2)
+        s1[c0:c0 + n] = s.reshape(n, 2 * I, H // 32)
+        c, s = moe.moe_quantize_mxfp4(synth.w2_device(cfg, ids).reshape(n * H, I))
+        c2[c0:c0 + n] = c.reshape(n, H, I // 2)
+        s2[c0:c0 + n] = s.reshape(n, H, I // 32)
+    p1, q1 = moe.moe_pack_weights(c1, s1, True)
+    p2, q2 = moe.moe_pack_weights(c2, s2, False)
+    wts = moe.MoeWeights(p1, q1, p2, q2)
     torch.cuda.synchronize()
-    if keep_rowmajor_scales:
-        return wts, s1.reshape(E, 2 * I, H // 32), s2.reshape(E, H, I // 32)
+    if keep_rowmajor:
+        return wts, (c1, s1, c2, s2)
+    del c1, c2, s1, s2
+    torch.cuda.empty_cache()
     return wts
 
 

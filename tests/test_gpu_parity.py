@@ -50,13 +50,13 @@ def _weights(cfg):
     key = (cfg.seed, cfg.E_global, cfg.E_local, cfg.expert_offset, cfg.num_shared, cfg.hidden, cfg.inter)
     if key not in _WCACHE:
         _WCACHE.clear()
-        _WCACHE[key] = device_weights(cfg, keep_rowmajor_scales=True)
+        _WCACHE[key] = device_weights(cfg)
     return _WCACHE[key]
 
 
 def run_layer(cfg, T=None):
     shape = shape_of(cfg, T)
-    wts, _, _ = _weights(cfg)
+    wts = _weights(cfg)
     x, logits, sl = device_inputs(cfg, T=shape.T)
     ws = moe.workspace(shape)
     out, ids, w = moe.moe_layer(shape, logits, sl, x, wts, ws)
@@ -150,11 +150,11 @@ def test_layer_full_size_vs_oracle(cfg):
 
 def test_weight_quantiser_bit_exact():
     cfg = SMALL.replace(E_local=4, E_global=4, hidden=512, inter=128)
-    wts, s1, s2 = device_weights(cfg, keep_rowmajor_scales=True)
+    _, (c1, s1, _, _) = device_weights(cfg, keep_rowmajor=True)
     f1 = synth.w1_host(cfg, cfg.global_ids)
     for e in range(4):
         c, s = oracle.quantize_mxfp4(f1[e])
-        np.testing.assert_array_equal(wts.w1[e].cpu().numpy(), c)
+        np.testing.assert_array_equal(c1[e].cpu().numpy(), c)
         np.testing.assert_array_equal(s1[e].cpu().numpy(), s)
     # edge values: zeros, exact ties, saturation, tiny and huge blocks
     rng = np.random.default_rng(3)
@@ -171,17 +171,29 @@ def test_weight_quantiser_bit_exact():
     np.testing.assert_array_equal(s.cpu().numpy(), os_)
 
 
-def test_pack_scales_layout():
-    rows, K = 256, 512
-    sc = torch.randint(0, 255, (rows, K // 32), dtype=torch.uint8, device="cuda")
-    packed = moe.moe_pack_scales(sc, K).cpu().numpy()
-    s = sc.cpu().numpy()
-    for rb in range(rows // 128):
-        for kc in range(K // 128):
-            blk = packed[(rb * (K // 128) + kc) * 512:][:512]
-            for r in range(128):
-                for b in range(4):
-                    assert blk[(r % 32) * 16 + (r // 32) * 4 + b] == s[rb * 128 + r, kc * 4 + b]
+@pytest.mark.parametrize("pair", [False, True])
+def test_pack_weights_layout(pair):
+    E, N, K = 2, 512, 384
+    codes = torch.randint(0, 255, (E, N, K // 2), dtype=torch.uint8, device="cuda")
+    scales = torch.randint(0, 255, (E, N, K // 32), dtype=torch.uint8, device="cuda")
+    pc, ps = moe.moe_pack_weights(codes, scales, pair)
+    pc, ps = pc.cpu().numpy(), ps.cpu().numpy()
+    c, s = codes.cpu().numpy(), scales.cpu().numpy()
+    RB = 256 if pair else 128
+    NB, KC = N // RB, K // 128
+    for e in range(E):
+        for b in range(NB):
+            rows = (list(range(b * 128, b * 128 + 128)) + list(range(N // 2 + b * 128, N // 2 + b * 128 + 128))
+                    if pair else list(range(b * 128, b * 128 + 128)))
+            for kc in range(KC):
+                tile = (e * NB + b) * KC + kc
+                tc = pc[tile * RB * 64:(tile + 1) * RB * 64].reshape(RB, 64)
+                np.testing.assert_array_equal(tc, c[e, rows, kc * 64:(kc + 1) * 64])
+                ts = ps[tile * RB * 4:(tile + 1) * RB * 4]
+                for rr, row in enumerate(rows):
+                    g, r = rr // 128, rr % 128
+                    for j in range(4):
+                        assert ts[g * 512 + (r % 32) * 16 + (r // 32) * 4 + j] == s[e, row, kc * 4 + j]
 
 
 def test_synth_generators_agree():
@@ -222,7 +234,7 @@ def test_zero_tokens_and_single_token():
     check_layer(cfg)
     shape = shape_of(cfg, 0)
     shape.max_T = 4
-    wts, _, _ = _weights(cfg)
+    wts = _weights(cfg)
     ws = moe.workspace(shape)
     x = torch.empty((0, cfg.hidden), dtype=torch.bfloat16, device="cuda")
     lg = torch.empty((0, cfg.E_global), dtype=torch.float32, device="cuda")
@@ -234,7 +246,7 @@ def test_zero_tokens_and_single_token():
 def test_graph_capture_replays_the_chain():
     cfg = GRID[2]
     shape = shape_of(cfg)
-    wts, _, _ = _weights(cfg)
+    wts = _weights(cfg)
     x, logits, sl = device_inputs(cfg)
     ws = moe.workspace(shape)
     ids = torch.empty((shape.T, shape.kp), dtype=torch.int32, device="cuda")
@@ -257,7 +269,7 @@ def test_graph_capture_replays_the_chain():
 def test_host_buffer_entry_point_matches_device_path():
     cfg = GRID[2]
     shape = shape_of(cfg)
-    wts, _, _ = _weights(cfg)
+    wts = _weights(cfg)
     x, logits, sl = device_inputs(cfg)
     ws = moe.workspace(shape)
     ref, _, _ = moe.moe_layer(shape, logits, sl, x, wts, ws)

@@ -72,6 +72,7 @@ def test_host_side_errors_launch_nothing():
     wt = _Weights(48, 256, 256, 256)  # w1 not 32-byte aligned
     need = moe.moe_workspace_bytes(_shape())
     assert L.moe_forward(ctypes.byref(s), 256, ctypes.byref(wt), 256, 256, need, 256, None) == -3
-    # packed-scale size rules
-    assert L.moe_pack_scales(16, 100, 128, 16, None) == -2
+    # packing size rules
+    assert L.moe_pack_weights(16, 16, 2, 100, 128, 0, 16, 16, None) == -2
+    assert L.moe_pack_weights(16, 16, 2, 128, 128, 1, 16, 16, None) == -2
     assert L.moe_quantize_mxfp4(16, 4, 33, 16, 16, None) == -2
