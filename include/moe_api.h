@@ -66,8 +66,9 @@ enum { MOE_ACT_SWIGLU = 0 }; /* silu(gate) * up, gate = W1 rows [0, I), up = row
  *   num_shared   0 or 1 shared experts appended to every token, global id
  *                E_global + s, local weight slot E_local + s
  *   hidden, inter H and I
- *   block_n      rows per virtual expert: 16 or 32 (decode tiling) or 128
- *                (prefill tiling); results do not depend on it
+ *   block_n      rows per virtual expert = token rows of a GEMM tile: 16 or
+ *                32 (decode tiling, fp32 FC2 rows) or 128 (prefill tiling,
+ *                bf16 FC2 rows); the layer's value does not depend on it
  *   activation   MOE_ACT_SWIGLU
  *   shared_scale multiplies the shared expert's sigmoid weight (e.g.
  *                1/ep_size, "... shared expert: fuse 3 kernels into 1") */
@@ -96,7 +97,8 @@ typedef struct moe_weights {
  *   xq           E4M3 [rows_alloc, H]: row r = MXFP8(x[a_map[r] / k'])
  *   xq_sf        E8M0 of xq in the tile layout (see moe_forward)
  *   act, act_sf  the FC1 output (silu(gate)*up, MXFP8) in the same layouts
- *   y            the FC2 output rows, already multiplied by the routing weight */
+ *   y            the FC2 output rows [R, H], already multiplied by the routing
+ *                weight: fp32 for block_n 16/32, bf16 for block_n 128 */
 typedef struct moe_views {
     int32_t *header, *expert_counts, *expert_offsets, *vinfo, *a_map, *c_map;
     uint8_t *xq, *xq_sf, *act, *act_sf;
@@ -125,18 +127,17 @@ int moe_quantize_mxfp4(const float* w, int64_t rows, int64_t K, uint8_t* codes, 
 
 /* Tile-major packing of one weight matrix per expert for the tensor-core
  * path.  Input: row-major E2M1 codes [experts, N, K/2] and E8M0 scales
- * [experts, N, K/32] (moe_quantize_mxfp4).  A row block holds 128 rows, or
- * with pair_halves = 1 the 128 rows b*128.. of the first half [0, N/2)
- * followed by the 128 rows N/2 + b*128.. of the second half (W1: gate and up
- * rows of the same features).  Output, for each expert e, row block b and
- * 128-K chunk c in that order:
- *   packed_codes : the block's rows x 64 bytes (the chunk's 128 codes of each
- *                  row, row-major), contiguous;
- *   packed_scales: per 128-row group of the block a 512-byte block, row r /
+ * [experts, N, K/32] (moe_quantize_mxfp4).  A row block holds 256 rows: rows
+ * b*256.. (pair_halves = 0, W2), or the 128 rows b*128.. of the first half
+ * [0, N/2) followed by the 128 rows N/2 + b*128.. of the second half
+ * (pair_halves = 1, W1: the gate and up rows of the same 128 features).
+ * Output, for each expert e, row block b and 128-K chunk c in that order:
+ *   packed_codes : the block's 256 rows x 64 bytes (the chunk's 128 codes of
+ *                  each row), one contiguous 16 KiB run;
+ *   packed_scales: two 512-byte blocks (block rows 0-127, 128-255), row r /
  *                  K-block j of the chunk at byte (r % 32) * 16 + (r / 32) * 4
  *                  + j (the tensor-memory scale layout, one tcgen05.cp each).
- * Sizes equal the inputs'.  N % 128 == 0 (N % 256 == 0 with pair_halves),
- * K % 128 == 0. */
+ * Sizes equal the inputs'.  N % 256 == 0, K % 128 == 0. */
 int moe_pack_weights(const uint8_t* codes, const uint8_t* scales, int64_t experts, int64_t N, int64_t K,
                      int32_t pair_halves, uint8_t* packed_codes, uint8_t* packed_scales, moe_stream_t stream);
 

@@ -114,19 +114,21 @@ int run_forward(const moe_shape* s, const uint16_t* x, const moe_weights* wt, co
     if (nsm <= 0) return MOE_ERR_CUDA;
 
     GatherParams gp{x, at<int32_t>(ws, L.header), at<int4>(ws, L.vinfo), at<int32_t>(ws, L.a_map),
-                    at<uint8_t>(ws, L.xq), at<uint8_t>(ws, L.xsf), d.H, d.kp, d.B, L.xsf_tile_bytes, d.V_max};
-    cudaError_t e = launch_gather_decode(gp, st, pdl);
+                    at<uint8_t>(ws, L.xq), at<uint8_t>(ws, L.xsf), d.H, d.kp, d.B, L.xsf_tile_bytes, d.V_max,
+                    d.V_max < 4 * nsm ? d.V_max : 4 * nsm};
+    cudaError_t e = launch_gather(gp, st, pdl);
     if (e != cudaSuccess || !rec(ev, 3, st)) return MOE_ERR_CUDA;
 
+    // Tile-major packed weights viewed as rows of 128 E2M1 codes (64 bytes):
+    // a GEMM stage is one 256-row box, one contiguous 16 KiB run of global
+    // memory.  Token operands: boxes of B rows x 128 K of the expert-ordered
+    // MXFP8 activations.
     CUtensorMap mw1, mw2, mx, mact;
     const uint64_t Et = static_cast<uint64_t>(d.Et);
-    // Tile-major packed weights viewed as rows of 128 E2M1 codes (64 bytes):
-    // an FC1 stage is one 256-row box (gate + up tile), an FC2 stage a
-    // 128-row box, each one contiguous run of global memory.
     if (!make_map(&mw1, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, wt->w1, 128, Et * 2 * d.I * (d.H / 128),
                   kFp4BytesPer128Row, 128, 256) ||
         !make_map(&mw2, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, wt->w2, 128, Et * d.H * (d.I / 128),
-                  kFp4BytesPer128Row, 128, 128) ||
+                  kFp4BytesPer128Row, 128, 256) ||
         !make_map(&mx, CU_TENSOR_MAP_DATA_TYPE_UINT8, at<uint8_t>(ws, L.xq), d.H, d.rows_alloc, d.H, 128, d.B) ||
         !make_map(&mact, CU_TENSOR_MAP_DATA_TYPE_UINT8, at<uint8_t>(ws, L.act), d.I, d.rows_alloc, d.I, 128, d.B))
         return MOE_ERR_CUDA;
@@ -140,27 +142,28 @@ int run_forward(const moe_shape* s, const uint16_t* x, const moe_weights* wt, co
     g.topk_w = topk_w;
     g.act = at<uint8_t>(ws, L.act);
     g.act_sf = at<uint8_t>(ws, L.asf);
-    g.y = at<float>(ws, L.y);
+    g.y = L.y_bf16 ? nullptr : at<float>(ws, L.y);
+    g.y_bf16 = L.y_bf16 ? at<uint16_t>(ws, L.y) : nullptr;
     g.H = d.H;
     g.I = d.I;
     g.out_sf_tile_bytes = L.asf_tile_bytes;
+    g.a_tx_bytes = 256 * kFp4BytesPer128Row;
     g.wait_ns = kWaitLimitNs;
 
     g.a_sf = wt->w1_sf;
-    g.a_tx_bytes = 256 * kFp4BytesPer128Row;
     g.b_sf = at<uint8_t>(ws, L.xsf);
     g.b_sf_tile_bytes = L.xsf_tile_bytes;
-    e = launch_fc1_decode(mw1, mx, g, d.B, nsm, st, pdl);
+    e = launch_gemm(true, mw1, mx, g, d.B, nsm, st, pdl);
     if (e != cudaSuccess || !rec(ev, 4, st)) return MOE_ERR_CUDA;
 
     g.a_sf = wt->w2_sf;
-    g.a_tx_bytes = 128 * kFp4BytesPer128Row;
     g.b_sf = at<uint8_t>(ws, L.asf);
     g.b_sf_tile_bytes = L.asf_tile_bytes;
-    e = launch_fc2_decode(mw2, mact, g, d.B, nsm, st, pdl);
+    e = launch_gemm(false, mw2, mact, g, d.B, nsm, st, pdl);
     if (e != cudaSuccess || !rec(ev, 5, st)) return MOE_ERR_CUDA;
 
-    CombineParams cp{at<int32_t>(ws, L.c_map), at<float>(ws, L.y), out, d.T, d.kp, d.H};
+    CombineParams cp{at<int32_t>(ws, L.c_map), L.y_bf16 ? nullptr : at<float>(ws, L.y),
+                     L.y_bf16 ? at<uint16_t>(ws, L.y) : nullptr, out, d.T, d.kp, d.H};
     e = launch_combine(cp, st, pdl);
     if (e != cudaSuccess || !rec(ev, 6, st)) return MOE_ERR_CUDA;
     return MOE_OK;
@@ -185,7 +188,7 @@ int moe_is_supported(const moe_shape* s) {
     const int64_t kp = static_cast<int64_t>(s->top_k) + s->num_shared;
     if (s->hidden <= 0 || s->hidden % 512 != 0) return 0;
     if (s->inter <= 0 || s->inter % 128 != 0) return 0;
-    if (!(s->block_n == 16 || s->block_n == 32)) return 0;
+    if (!(s->block_n == 16 || s->block_n == 32 || s->block_n == 128)) return 0;
     if (s->top_k < 1 || s->top_k > 32 || s->top_k > s->E_global || s->E_global > 1024) return 0;
     if (s->num_shared < 0 || s->num_shared > 1) return 0;
     if (s->E_local < 1 || s->E_local + s->num_shared > 1024) return 0;
@@ -215,7 +218,7 @@ int moe_quantize_mxfp4(const float* w, int64_t rows, int64_t K, uint8_t* codes, 
 int moe_pack_weights(const uint8_t* codes, const uint8_t* scales, int64_t experts, int64_t N, int64_t K,
                      int32_t pair_halves, uint8_t* packed_codes, uint8_t* packed_scales, moe_stream_t stream) {
     if (!codes || !scales || !packed_codes || !packed_scales) return MOE_ERR_NULL;
-    if (experts <= 0 || N <= 0 || K <= 0 || K % 128 || N % (pair_halves ? 256 : 128)) return MOE_ERR_SHAPE;
+    if (experts <= 0 || N <= 0 || K <= 0 || K % 128 || N % 256) return MOE_ERR_SHAPE;
     if (!aligned(codes, 16) || !aligned(packed_codes, 16)) return MOE_ERR_ALIGN;
     PackParams p{codes, scales, packed_codes, packed_scales, experts, N, K, pair_halves ? 1 : 0};
     return cuda_rc(launch_pack_weights(p, reinterpret_cast<cudaStream_t>(stream)));

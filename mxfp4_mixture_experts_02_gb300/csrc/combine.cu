@@ -63,10 +63,67 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineParams 
     ptx::pdl_launch_dependents();
 }
 
+// bf16 Y rows (prefill tiling): one uint4 (8 columns) per thread.
+__global__ void __launch_bounds__(kCombineThreads) combine_bf16_kernel(CombineParams p) {
+    __shared__ int rows[kMaxSlots];
+    ptx::pdl_wait();
+    const int t = blockIdx.y;
+    if (threadIdx.x < p.kp) rows[threadIdx.x] = p.c_map[static_cast<size_t>(t) * p.kp + threadIdx.x];
+    __syncthreads();
+    const int c = blockIdx.x * kCombineThreads + threadIdx.x;  // uint4 column (8 bf16)
+    if (c < p.H / 8) {
+        float acc[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) acc[u] = 0.f;
+        int j = 0;
+        for (; j + 4 <= p.kp; j += 4) {
+            uint4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int r = rows[j + u];
+                v[u] = r >= 0 ? reinterpret_cast<const uint4*>(p.y_bf16 + static_cast<size_t>(r) * p.H)[c]
+                              : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const uint32_t w4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    acc[2 * m] += __uint_as_float(w4[m] << 16);
+                    acc[2 * m + 1] += __uint_as_float(w4[m] & 0xFFFF0000u);
+                }
+            }
+        }
+        for (; j < p.kp; ++j) {
+            const int r = rows[j];
+            if (r < 0) continue;
+            const uint4 v = reinterpret_cast<const uint4*>(p.y_bf16 + static_cast<size_t>(r) * p.H)[c];
+            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                acc[2 * m] += __uint_as_float(w4[m] << 16);
+                acc[2 * m + 1] += __uint_as_float(w4[m] & 0xFFFF0000u);
+            }
+        }
+        uint32_t pk[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[2 * m], acc[2 * m + 1]);
+            pk[m] = *reinterpret_cast<const uint32_t*>(&b2);
+        }
+        reinterpret_cast<uint4*>(p.out + static_cast<size_t>(t) * p.H)[c] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    }
+    ptx::pdl_launch_dependents();
+}
+
 }  // namespace
 
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream, bool pdl) {
     if (p.T == 0) return cudaSuccess;
+    if (p.y_bf16) {
+        const dim3 grid((p.H / 8 + kCombineThreads - 1) / kCombineThreads, p.T);
+        return launch_kernel(combine_bf16_kernel, grid, dim3(kCombineThreads), 0, stream, pdl, p);
+    }
     const dim3 grid((p.H / 4 + kCombineThreads - 1) / kCombineThreads, p.T);
     return launch_kernel(combine_kernel, grid, dim3(kCombineThreads), 0, stream, pdl, p);
 }

@@ -26,7 +26,7 @@ enum Mode { kModeDecode = 0, kModePrefill = 1 };
 // Dimensions derived from a moe_shape.
 struct Dims {
     int T, max_T, Eg, E, off, k, S, kp, Et, H, I, B;
-    int G;           // virtual experts (tiles) per GEMM work group
+    int G;           // virtual experts per sort work group (1: a GEMM item is one tile)
     int R_max;       // routed rows bound: max_T * k'
     int V_max;       // virtual-expert bound: Et + R_max / B
     int rows_alloc;  // activation rows incl. the last tile's TMA tail box
@@ -60,7 +60,7 @@ inline Dims make_dims(const moe_shape& s) {
     d.I = s.inter;
     d.B = s.block_n;
     d.mode = (s.block_n == 128) ? kModePrefill : kModeDecode;
-    d.G = (d.mode == kModeDecode) ? 64 / d.B : 1;
+    d.G = 1;
     d.R_max = s.max_T * d.kp;
     d.V_max = d.Et + d.R_max / d.B;
     d.rows_alloc = d.R_max + d.B;

@@ -1,0 +1,349 @@
+// Grouped block-scaled GEMMs of the MoE layer (FC1 and FC2), one kernel
+// template for the decode tilings (token tiles of 16 / 32 rows) and the
+// prefill tiling (128-row token tiles).
+//
+// Work item = (virtual expert v: a tile of TM token rows of expert e,
+// weight block nb of 256 rows).  One tcgen05.mma kind::mxf8f6f4 block_scale
+// per 32-wide K step: A = the token tile (M = 128, E4M3, K-major), B = the
+// 256 weight rows (N = 256, E2M1, K-major), fp32 accumulator of 128 lanes x
+// 256 columns in TMEM, E8M0 scales (one per 32 K) copied into TMEM with
+// tcgen05.cp.  The weights are the N operand because an MMA instruction costs
+// the same for any N <= 256: 256 weight rows per instruction halves the
+// instruction count of a weight-streaming (decode) GEMM against 128 rows.
+//
+//   FC1: B = W1[e] gate rows f0..f0+127 and up rows I+f0.. (packed adjacent),
+//        K = H.  Epilogue: h = silu(gate) * up in fp32 and MXFP8 per token
+//        and 32 features -> act / act_sf ("[SGLang] CUTLASS MoE", section 4
+//        silu_and_mul, fused into the GEMM).
+//   FC2: B = W2[e] rows nb*256.., K = I.  Epilogue: times the routing weight
+//        of the row's slot -> Y rows (the multiply of section 5's
+//        apply_shuffle_mul_sum, fused).
+//
+// With TM < 128 only the tile's TM rows are loaded; the MMA still reads 128
+// rows, the rest alias the next stages' token tiles (their accumulator lanes
+// are never read).
+//
+// Warp roles (10 warps): 0..7 epilogue (warp w reads TMEM lane quadrant w % 4
+// and column half w / 4; with TM <= 32 only quadrant 0 holds tokens, so only
+// warps 0 and 4 work), 8 TMA producer (STAGES-deep ring), 9 TMEM allocator and
+// single-thread MMA issuer.  The epilogue releases the accumulator as soon as
+// its TMEM loads complete, so the next item's MMAs overlap the SwiGLU /
+// quantise / store math.  Every wait is bounded; on expiry the CTA records
+// MOE_ERR_TIMEOUT in the workspace status word, stops, lets its MMAs drain,
+// frees TMEM and exits.
+#include "common.cuh"
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kWarps = 10;
+constexpr int kThreads = kWarps * 32;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+
+template <int TM, int STAGES>
+struct Cfg {
+    static constexpr int kWTile = 256 * 128;           // 256 weight rows x 128 K (16-byte E2M1 chunks)
+    static constexpr int kOffSFW = kWTile;             // 2 x 512 B weight scales
+    static constexpr int kOffSFX = kWTile + 1024;      // 512 B token scales
+    static constexpr int kStageBytes = ((kWTile + 1536) + 1023) & ~1023;
+    static constexpr int kXTile = TM * 128;            // bytes of the loaded token rows
+    static constexpr int kXRegion = STAGES * kXTile + (TM < 128 ? 128 * 128 - kXTile : 0);
+    static constexpr int kOffX = STAGES * kStageBytes;
+    static constexpr int kOffBar = kOffX + kXRegion;
+    static constexpr int kSmemBytes = kOffBar + (2 * STAGES + 4) * 8 + 16 + 1024;
+    static constexpr int kAccCols = 256;
+    static constexpr int kSfCols = 16;                  // per stage: 4 token-scale + 8 weight-scale columns
+    static constexpr int kTmemCols = 512;
+    static constexpr int kEpiWarps = TM <= 32 ? 2 : 8;  // warps holding token lanes
+    static_assert(kAccCols + STAGES * kSfCols <= kTmemCols, "TMEM budget");
+    static_assert(kSmemBytes <= 232448, "shared memory budget");
+    static_assert(TM == 16 || TM == 32 || TM == 128, "token tile rows");
+};
+
+__device__ __forceinline__ void record_timeout(const GemmParams& p, volatile int* abort_flag, int site) {
+    *abort_flag = 1;
+    if (atomicCAS(p.status, 0, MOE_ERR_TIMEOUT) == 0) p.status[1] = site * 65536 + static_cast<int>(blockIdx.x);
+}
+
+// Bounded wait that also gives up as soon as another role of the CTA aborted.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, uint64_t limit_ns,
+                                              volatile int* abort_flag) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer();
+    while (true) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (ptx::globaltimer() - t0 > limit_ns) return false;
+    }
+}
+
+__device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
+
+// 32 fp32 -> MXFP8 (E4M3 codes in 8 words, E8M0 code returned).
+__device__ __forceinline__ uint32_t mxfp8_block(const float* v, uint32_t (&w)[8]) {
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    const int ex = mx_shared_exponent(amax, 8);
+    const float inv = exp2_int(-ex);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t lo = e4m3x2(v[4 * i] * inv, v[4 * i + 1] * inv);
+        const uint32_t hi = e4m3x2(v[4 * i + 2] * inv, v[4 * i + 3] * inv);
+        w[i] = lo | (hi << 16);
+    }
+    return static_cast<uint32_t>(ex + 127);
+}
+
+template <int TM, bool FC1, bool YBF16, int STAGES>
+__global__ void __launch_bounds__(kThreads, 1)
+    moe_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                    const GemmParams p) {
+    using C = Cfg<TM, STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+    uint64_t* empty = full + STAGES;
+    uint64_t* accfull = empty + STAGES;
+    uint64_t* accempty = accfull + 1;
+    uint64_t* done = accempty + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            ptx::mbar_init(&full[s], 1);
+            ptx::mbar_init(&empty[s], 1);
+        }
+        ptx::mbar_init(accfull, 1);
+        ptx::mbar_init(accempty, C::kEpiWarps);
+        ptx::mbar_init(done, 1);
+        *abort_flag = 0;
+        ptx::fence_mbarrier_init();
+    }
+    if (warp == kProducerWarp && lane == 0) {
+        ptx::tma_prefetch_desc(&tmW);
+        ptx::tma_prefetch_desc(&tmX);
+    }
+    if (warp == kMmaWarp) {
+        ptx::tmem_alloc(tmem_slot, C::kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    ptx::pdl_wait();
+    const int num_v = p.header[kHdrNumV];
+    const int NB = FC1 ? p.I / 128 : p.H / 256;  // 256-row weight blocks per expert
+    const int KC = FC1 ? p.H / 128 : p.I / 128;  // 128-wide K chunks
+    const int nitems = num_v * NB;
+
+    if (warp == kProducerWarp) {
+        if (lane == 0) {
+            // ---------------------------------------------------- TMA producer
+            uint32_t stage = 0, phase = 0;
+            bool ok = true;
+            for (int it = blockIdx.x; ok && it < nitems; it += gridDim.x) {
+                const int v = it / NB, nb = it - v * NB;
+                const int4 vi = p.vinfo[v];
+                const int e = vi.x, first = vi.y;
+                const int64_t tile0 = (static_cast<int64_t>(e) * NB + nb) * KC;
+                const uint32_t tx = 256 * 64 + C::kXTile + 1536;
+                for (int kc = 0; kc < KC; ++kc) {
+                    if (!wait_or_abort(&empty[stage], phase ^ 1, p.wait_ns, abort_flag)) {
+                        if (!*abort_flag) record_timeout(p, abort_flag, kSiteProducerEmpty);
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* st = smem + stage * C::kStageBytes;
+                    ptx::mbar_arrive_expect_tx(&full[stage], tx);
+                    ptx::tma_load_2d(st, &tmW, &full[stage], 0, static_cast<int32_t>((tile0 + kc) * 256));
+                    ptx::tma_load_2d(smem + C::kOffX + stage * C::kXTile, &tmX, &full[stage], kc * 128, first);
+                    ptx::bulk_load(st + C::kOffSFW, p.a_sf + static_cast<size_t>(tile0 + kc) * 1024, 1024, &full[stage]);
+                    ptx::bulk_load(st + C::kOffSFX, p.b_sf + static_cast<size_t>(v) * p.b_sf_tile_bytes + kc * 512, 512,
+                                   &full[stage]);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            // every issued stage lands before the CTA may exit (bounded)
+            for (int s = 0; s < STAGES; ++s) {
+                const uint32_t par = (static_cast<uint32_t>(s) < stage) ? phase : (phase ^ 1);
+                ptx::mbar_wait(&full[s], par, 10ull * 1000 * 1000);
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        if (lane == 0) {
+            // ---------------------------------------------------- MMA issuer
+            constexpr uint32_t kIdesc = ptx::idesc_mx(ptx::kFmtE4M3, ptx::kFmtE2M1, 128, 256);
+            uint32_t stage = 0, phase = 0, aphase = 0;
+            bool ok = true;
+            for (int it = blockIdx.x; ok && it < nitems; it += gridDim.x) {
+                if (!wait_or_abort(accempty, aphase ^ 1, p.wait_ns, abort_flag)) {
+                    if (!*abort_flag) record_timeout(p, abort_flag, kSiteMmaAccEmpty);
+                    break;
+                }
+                ptx::tc_fence_after();
+                for (int kc = 0; kc < KC; ++kc) {
+                    if (!wait_or_abort(&full[stage], phase, p.wait_ns, abort_flag)) {
+                        if (!*abort_flag) record_timeout(p, abort_flag, kSiteMmaFull);
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint8_t* st = smem + stage * C::kStageBytes;
+                    const uint32_t sf = tmem + C::kAccCols + stage * C::kSfCols;
+                    ptx::tc_cp_32x128b_warpx4(sf, ptx::sdesc_sf(ptx::smem_u32(st + C::kOffSFX)));
+                    ptx::tc_cp_32x128b_warpx4(sf + 4, ptx::sdesc_sf(ptx::smem_u32(st + C::kOffSFW)));
+                    ptx::tc_cp_32x128b_warpx4(sf + 8, ptx::sdesc_sf(ptx::smem_u32(st + C::kOffSFW + 512)));
+                    const uint32_t xa = ptx::smem_u32(smem + C::kOffX + stage * C::kXTile);
+                    const uint32_t wa = ptx::smem_u32(st);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        ptx::mma_mxf8f6f4(tmem, ptx::sdesc_sw128(xa + kk * 32), ptx::sdesc_sw128(wa + kk * 32),
+                                          ptx::idesc_with_sf_id(kIdesc, kk, kk), sf, sf + 4, (kc | kk) != 0);
+                    ptx::tc_commit(&empty[stage]);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (!ok) break;
+                ptx::tc_commit(accfull);
+                aphase ^= 1;
+            }
+            ptx::tc_commit(done);
+            ptx::mbar_wait(done, 0, 10ull * 1000 * 1000);
+        }
+    } else {
+        // -------------------------------------------------------- epilogue
+        const int q = warp & 3, half = warp >> 2;
+        const bool active = (TM > 32) || q == 0;
+        uint32_t aphase = 0;
+        for (int it = blockIdx.x; active && it < nitems; it += gridDim.x) {
+            const int v = it / NB, nb = it - v * NB;
+            const int4 vi = p.vinfo[v];
+            const int first = vi.y, rows = vi.z;
+            const int i = q * 32 + lane;  // token row of this lane within the tile
+            const bool valid = i < rows;
+            float w_row = 0.f;
+            if (!FC1 && valid) w_row = p.topk_w[p.a_map[first + i]];
+            if (!wait_or_abort(accfull, aphase, p.wait_ns, abort_flag)) {
+                if (lane == 0 && !*abort_flag) record_timeout(p, abort_flag, kSiteEpiAccFull);
+                break;
+            }
+            aphase ^= 1;
+            ptx::tc_fence_after();
+            const uint32_t tq = tmem + (static_cast<uint32_t>(32 * q) << 16);
+            uint32_t r[4][32];
+            if constexpr (FC1) {
+                // gate features half*64 .. +64 and the matching up features
+                ptx::tmem_ld32(tq + half * 64, r[0]);
+                ptx::tmem_ld32(tq + half * 64 + 32, r[1]);
+                ptx::tmem_ld32(tq + 128 + half * 64, r[2]);
+                ptx::tmem_ld32(tq + 128 + half * 64 + 32, r[3]);
+            } else {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tq + half * 128 + 32 * c, r[c]);
+            }
+            ptx::tmem_wait_ld();
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(accempty);  // accumulator free for the next item
+            if (valid) {
+                const int64_t row = first + i;
+                if constexpr (FC1) {
+                    const int f0 = nb * 128 + half * 64;  // first intermediate feature of this lane
+                    uint8_t* sf_tile = p.act_sf + static_cast<size_t>(v) * p.out_sf_tile_bytes + nb * 512 +
+                                       (i & 31) * 16 + (i >> 5) * 4 + half * 2;
+#pragma unroll
+                    for (int b = 0; b < 2; ++b) {
+                        float h[32];
+#pragma unroll
+                        for (int c = 0; c < 32; ++c)
+                            h[c] = silu(__uint_as_float(r[b][c])) * __uint_as_float(r[2 + b][c]);
+                        uint32_t wq[8];
+                        const uint32_t sc = mxfp8_block(h, wq);
+                        uint4* dst = reinterpret_cast<uint4*>(p.act + row * p.I + f0 + 32 * b);
+                        dst[0] = make_uint4(wq[0], wq[1], wq[2], wq[3]);
+                        dst[1] = make_uint4(wq[4], wq[5], wq[6], wq[7]);
+                        sf_tile[b] = static_cast<uint8_t>(sc);
+                    }
+                } else {
+                    const int n0 = nb * 256 + half * 128;  // first hidden column of this lane
+                    if constexpr (YBF16) {
+                        uint4* dst = reinterpret_cast<uint4*>(p.y_bf16 + row * p.H + n0);
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+#pragma unroll
+                            for (int g = 0; g < 4; ++g) {
+                                uint32_t pk[4];
+#pragma unroll
+                                for (int u = 0; u < 4; ++u) {
+                                    const __nv_bfloat162 b2 =
+                                        __floats2bfloat162_rn(__uint_as_float(r[c][8 * g + 2 * u]) * w_row,
+                                                              __uint_as_float(r[c][8 * g + 2 * u + 1]) * w_row);
+                                    pk[u] = *reinterpret_cast<const uint32_t*>(&b2);
+                                }
+                                dst[c * 4 + g] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                            }
+                    } else {
+                        float4* dst = reinterpret_cast<float4*>(p.y + row * p.H + n0);
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+#pragma unroll
+                            for (int g = 0; g < 8; ++g)
+                                dst[c * 8 + g] = make_float4(__uint_as_float(r[c][4 * g]) * w_row,
+                                                             __uint_as_float(r[c][4 * g + 1]) * w_row,
+                                                             __uint_as_float(r[c][4 * g + 2]) * w_row,
+                                                             __uint_as_float(r[c][4 * g + 3]) * w_row);
+                    }
+                }
+            }
+        }
+    }
+
+    ptx::pdl_launch_dependents();
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    if (warp == kMmaWarp) {
+        __syncwarp();
+        ptx::tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+template <int TM, bool FC1, bool YBF16, int STAGES>
+cudaError_t launch_impl(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmParams& p, int grid,
+                        cudaStream_t stream, bool pdl) {
+    using C = Cfg<TM, STAGES>;
+    auto kern = moe_gemm_kernel<TM, FC1, YBF16, STAGES>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (err != cudaSuccess) return err;
+    return launch_kernel(kern, dim3(grid), dim3(kThreads), C::kSmemBytes, stream, pdl, tmW, tmX, p);
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(bool fc1, const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmParams& p, int TM,
+                        int grid, cudaStream_t stream, bool pdl) {
+    if (fc1) {
+        if (TM == 16) return launch_impl<16, true, false, 5>(tmW, tmX, p, grid, stream, pdl);
+        if (TM == 32) return launch_impl<32, true, false, 5>(tmW, tmX, p, grid, stream, pdl);
+        return launch_impl<128, true, true, 4>(tmW, tmX, p, grid, stream, pdl);
+    }
+    if (TM == 16) return launch_impl<16, false, false, 5>(tmW, tmX, p, grid, stream, pdl);
+    if (TM == 32) return launch_impl<32, false, false, 5>(tmW, tmX, p, grid, stream, pdl);
+    return launch_impl<128, false, true, 4>(tmW, tmX, p, grid, stream, pdl);
+}
+
+}  // namespace moe

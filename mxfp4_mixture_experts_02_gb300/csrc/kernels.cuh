@@ -54,7 +54,7 @@ struct GatherParams {  // x -> MXFP8 rows in expert order + tile scales
     const int32_t* a_map;
     uint8_t* xq;
     uint8_t* xsf;
-    int H, kp, B, xsf_tile_bytes, max_v;
+    int H, kp, B, xsf_tile_bytes, max_v, grid;
 };
 
 struct GemmParams {
@@ -68,7 +68,8 @@ struct GemmParams {
     const uint8_t* b_sf;   // tile scales of the activation operand
     uint8_t* act;          // FC1 output codes [rows_alloc, I]
     uint8_t* act_sf;       // FC1 output tile scales
-    float* y;              // FC2 output [R, H] (fp32)
+    float* y;              // FC2 output [R, H], fp32 (decode tilings)
+    uint16_t* y_bf16;      // FC2 output [R, H], bf16 (prefill tiling)
     int H, I;
     int b_sf_tile_bytes, out_sf_tile_bytes;
     int a_tx_bytes;        // transaction bytes of a stage's weight box (packed E2M1 bytes)
@@ -77,7 +78,8 @@ struct GemmParams {
 
 struct CombineParams {
     const int32_t* c_map;
-    const float* y;
+    const float* y;         // fp32 rows, or NULL when y_bf16 is used
+    const uint16_t* y_bf16; // bf16 rows (prefill tiling)
     uint16_t* out;
     int T, kp, H;
 };
@@ -100,11 +102,9 @@ struct PackParams {
 
 cudaError_t launch_route(const RouteParams& p, cudaStream_t stream, bool pdl);
 cudaError_t launch_sort(const SortParams& p, cudaStream_t stream, bool pdl);
-cudaError_t launch_gather_decode(const GatherParams& p, cudaStream_t stream, bool pdl);
-cudaError_t launch_fc1_decode(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int B, int grid,
-                              cudaStream_t stream, bool pdl);
-cudaError_t launch_fc2_decode(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int B, int grid,
-                              cudaStream_t stream, bool pdl);
+cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream, bool pdl);
+cudaError_t launch_gemm(bool fc1, const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmParams& p, int TM,
+                        int grid, cudaStream_t stream, bool pdl);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream, bool pdl);
 cudaError_t launch_quantize_mxfp4(const QuantParams& p, cudaStream_t stream);
 cudaError_t launch_pack_weights(const PackParams& p, cudaStream_t stream);

@@ -1,14 +1,11 @@
 // MX quantisers (OCP MX v1.0 conversion: shared exponent floor(log2 amax) -
 // emax, elements rounded to nearest even and saturated by the cvt.satfinite
 // instructions):
-//   gather_decode_kernel : x bf16 -> MXFP8 (E4M3, emax 8), written directly in
+//   gather_kernel        : x bf16 -> MXFP8 (E4M3, emax 8), written directly in
 //                          expert-row order (the "[SGLang] CUTLASS MoE"
 //                          section 2 shuffle_rows folded into the quantiser)
 //                          with the tile scale layout the FC1 kernel copies
-//                          into tensor memory: per virtual expert and 128-K
-//                          chunk one 512-byte block, tile row i / K-block b
-//                          at byte i * 16 + b (the 128-row block layout with
-//                          only the first 32-row group populated);
+//                          into tensor memory;
 //   quantize_mxfp4_kernel: fp32 weights -> MXFP4 (E2M1, emax 2), offline;
 //   pack_codes_kernel,
 //   pack_scales_kernel   : row-major MXFP4 -> tile-major codes (one contiguous
@@ -24,15 +21,17 @@ namespace {
 
 constexpr int kGatherThreads = 256;
 
-// One CTA per virtual expert (tile of B rows).  Thread job = (row, 32-block).
-__global__ void __launch_bounds__(kGatherThreads) gather_decode_kernel(GatherParams p) {
+// CTAs walk the virtual experts (tiles of up to B rows).  Thread job =
+// (row, 32-block).  Tile scale layout: per 128-K chunk a 512-byte block,
+// tile row i / K-block b at byte (i % 32) * 16 + (i / 32) * 4 + b % 4.
+__global__ void __launch_bounds__(kGatherThreads) gather_kernel(GatherParams p) {
     ptx::pdl_wait();
-    const int v = blockIdx.x;
     const int nv = p.header[kHdrNumV];
-    if (v < nv) {
+    const int nb = p.H / 32;
+    const int bytes = (p.H / 128) * 512;
+    for (int v = blockIdx.x; v < nv; v += gridDim.x) {
         const int4 vi = p.vinfo[v];
         const int first = vi.y, rows = vi.z;
-        const int nb = p.H / 32;
         uint8_t* sf_tile = p.xsf + static_cast<size_t>(v) * p.xsf_tile_bytes;
         for (int job = threadIdx.x; job < rows * nb; job += kGatherThreads) {
             const int i = job / nb, b = job - i * nb;
@@ -62,14 +61,13 @@ __global__ void __launch_bounds__(kGatherThreads) gather_decode_kernel(GatherPar
             uint4* dst = reinterpret_cast<uint4*>(p.xq + static_cast<size_t>(row) * p.H + b * 32);
             dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
             dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-            sf_tile[(b >> 2) * 512 + i * 16 + (b & 3)] = static_cast<uint8_t>(ex + 127);
+            sf_tile[(b >> 2) * 512 + (i & 31) * 16 + (i >> 5) * 4 + (b & 3)] = static_cast<uint8_t>(ex + 127);
         }
-        // every other byte of the tile's scale blocks -> 0 (rows >= tile rows,
-        // and the row groups 32..127 an N <= 32 MMA never reads)
-        const int bytes = (p.H / 128) * 512;
+        // every other byte of the tile's scale blocks -> 0 (rows beyond the
+        // tile; the MMA reads 128 rows)
         for (int j = threadIdx.x; j < bytes; j += kGatherThreads) {
-            const int line = (j >> 4) & 31, col = j & 15;
-            if (line >= rows || col >= 4) sf_tile[j] = 0;
+            const int line = (j >> 4) & 31, grp = (j >> 2) & 3;
+            if (grp * 32 + line >= rows) sf_tile[j] = 0;
         }
     }
     ptx::pdl_launch_dependents();
@@ -111,15 +109,15 @@ __global__ void quantize_mxfp4_kernel(QuantParams p) {
     }
 }
 
-// Source row of row rr of row block b (see moe_pack_weights).
+// Source row of row rr of 256-row block b (see moe_pack_weights).
 __device__ __forceinline__ int64_t packed_src_row(int64_t b, int rr, int64_t N, int pair) {
-    if (!pair) return b * 128 + rr;
+    if (!pair) return b * 256 + rr;
     return rr < 128 ? b * 128 + rr : N / 2 + b * 128 + (rr - 128);
 }
 
 // Codes: one thread per 16-byte piece of the output.
 __global__ void pack_codes_kernel(PackParams p) {
-    const int RB = p.pair ? 256 : 128;
+    const int RB = 256;
     const int64_t NB = p.N / RB, KC = p.K / 128;
     const int64_t total = p.experts * p.N * (p.K / 2) / 16;
     for (int64_t o = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; o < total;
@@ -137,7 +135,7 @@ __global__ void pack_codes_kernel(PackParams p) {
 
 // Scales: one thread per output byte.
 __global__ void pack_scales_kernel(PackParams p) {
-    const int RB = p.pair ? 256 : 128;
+    const int RB = 256;
     const int64_t NB = p.N / RB, KC = p.K / 128;
     const int64_t total = p.experts * p.N * (p.K / 32);
     for (int64_t o = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; o < total;
@@ -162,8 +160,8 @@ unsigned grid_for(int64_t n, int threads) {
 
 }  // namespace
 
-cudaError_t launch_gather_decode(const GatherParams& p, cudaStream_t stream, bool pdl) {
-    return launch_kernel(gather_decode_kernel, dim3(p.max_v), dim3(kGatherThreads), 0, stream, pdl, p);
+cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream, bool pdl) {
+    return launch_kernel(gather_kernel, dim3(p.grid), dim3(kGatherThreads), 0, stream, pdl, p);
 }
 
 cudaError_t launch_quantize_mxfp4(const QuantParams& p, cudaStream_t stream) {

@@ -33,6 +33,8 @@ GRID = [
     SMALL.replace(T=96, block_n=32, zipf_s=1.1),
     SMALL.replace(T=256, block_n=16, E_local=32, expert_offset=16),
     SMALL.replace(T=256, block_n=32, num_shared=1, zipf_s=1.1, hidden=1536, inter=384),
+    SMALL.replace(T=200, block_n=128, top_k=8, num_shared=1, zipf_s=1.1),
+    SMALL.replace(T=64, block_n=128, E_local=32, expert_offset=32, hidden=1536, inter=384),
     synth.CONFIGS["tiny"],
 ]
 FULL = [synth.CONFIGS[n] for n in ("decode_t32", "ep_slice_t64", "skewed_shared_t256")]
@@ -66,7 +68,8 @@ def run_layer(cfg, T=None):
 
 
 def tile_scales_to_rows(views, vinfo, num_v, K):
-    """Per-row E8M0 scales [R, K/32] from the decode tile layout."""
+    """Per-row E8M0 scales [R, K/32] from the tile layout (per 128-K chunk a
+    512-byte block, tile row i / K-block b at (i % 32) * 16 + (i / 32) * 4 + b)."""
     sf = views.cpu().numpy()
     R = int(sum(v[2] for v in vinfo[:num_v]))
     rows = np.zeros((R, K // 32), np.uint8)
@@ -74,7 +77,7 @@ def tile_scales_to_rows(views, vinfo, num_v, K):
         _, first, n, _ = vinfo[v]
         for i in range(n):
             for b in range(K // 32):
-                rows[first + i, b] = sf[v, (b // 4) * 512 + i * 16 + (b % 4)]
+                rows[first + i, b] = sf[v, (b // 4) * 512 + (i % 32) * 16 + (i // 32) * 4 + (b % 4)]
     return rows
 
 
@@ -179,17 +182,16 @@ def test_pack_weights_layout(pair):
     pc, ps = moe.moe_pack_weights(codes, scales, pair)
     pc, ps = pc.cpu().numpy(), ps.cpu().numpy()
     c, s = codes.cpu().numpy(), scales.cpu().numpy()
-    RB = 256 if pair else 128
-    NB, KC = N // RB, K // 128
+    NB, KC = N // 256, K // 128
     for e in range(E):
         for b in range(NB):
             rows = (list(range(b * 128, b * 128 + 128)) + list(range(N // 2 + b * 128, N // 2 + b * 128 + 128))
-                    if pair else list(range(b * 128, b * 128 + 128)))
+                    if pair else list(range(b * 256, b * 256 + 256)))
             for kc in range(KC):
                 tile = (e * NB + b) * KC + kc
-                tc = pc[tile * RB * 64:(tile + 1) * RB * 64].reshape(RB, 64)
+                tc = pc[tile * 256 * 64:(tile + 1) * 256 * 64].reshape(256, 64)
                 np.testing.assert_array_equal(tc, c[e, rows, kc * 64:(kc + 1) * 64])
-                ts = ps[tile * RB * 4:(tile + 1) * RB * 4]
+                ts = ps[tile * 1024:(tile + 1) * 1024]
                 for rr, row in enumerate(rows):
                     g, r = rr // 128, rr % 128
                     for j in range(4):
