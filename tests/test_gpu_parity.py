@@ -37,7 +37,7 @@ GRID = [
     SMALL.replace(T=64, block_n=128, E_local=32, expert_offset=32, hidden=1536, inter=384),
     synth.CONFIGS["tiny"],
 ]
-FULL = [synth.CONFIGS[n] for n in ("decode_t32", "ep_slice_t64", "skewed_shared_t256")]
+FULL = [synth.CONFIGS[n] for n in ("decode_t32", "ep_slice_t64", "skewed_shared_t256", "prefill_t32768")]
 
 
 def _cid(c):
