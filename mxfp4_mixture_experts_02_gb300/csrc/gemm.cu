@@ -139,7 +139,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    ptx::pdl_wait();
+    // The work list comes from the sort, which has completed when this grid
+    // launches (the previous kernel's CTAs waited on it before triggering
+    // this launch).  Only the token operands -- written by the immediately
+    // preceding kernel -- need griddepcontrol.wait, which the producer issues
+    // after it has started streaming the first weight stages.
     const int num_v = p.header[kHdrNumV];
     const int NB = FC1 ? p.I / 128 : p.H / 256;  // 256-row weight blocks per expert
     const int KC = FC1 ? p.H / 128 : p.I / 128;  // 128-wide K chunks
@@ -148,15 +152,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kProducerWarp) {
         if (lane == 0) {
             // ---------------------------------------------------- TMA producer
+            // Weight tiles and weight scales of the first STAGES stages are
+            // issued before griddepcontrol.wait; their token tiles / token
+            // scales after it.  A stage's full barrier expects all its bytes.
             uint32_t stage = 0, phase = 0;
             bool ok = true;
+            const uint32_t tx = 256 * 64 + C::kXTile + 1536;
+            int pre_v[STAGES], pre_first[STAGES], pre_kc[STAGES];
+            int npre = 0;
+            bool waited = false;
+            // wait for the preceding kernel, then issue the deferred token loads
+            auto flush_prefetched = [&]() {
+                ptx::pdl_wait();
+                waited = true;
+#pragma unroll
+                for (int j = 0; j < STAGES; ++j) {
+                    if (j >= npre) break;
+                    ptx::tma_load_2d(smem + C::kOffX + j * C::kXTile, &tmX, &full[j], pre_kc[j] * 128, pre_first[j]);
+                    ptx::bulk_load(smem + j * C::kStageBytes + C::kOffSFX,
+                                   p.b_sf + static_cast<size_t>(pre_v[j]) * p.b_sf_tile_bytes + pre_kc[j] * 512, 512,
+                                   &full[j]);
+                }
+            };
             for (int it = blockIdx.x; ok && it < nitems; it += gridDim.x) {
                 const int v = it / NB, nb = it - v * NB;
                 const int4 vi = p.vinfo[v];
                 const int e = vi.x, first = vi.y;
                 const int64_t tile0 = (static_cast<int64_t>(e) * NB + nb) * KC;
-                const uint32_t tx = 256 * 64 + C::kXTile + 1536;
                 for (int kc = 0; kc < KC; ++kc) {
+                    // the ring is full of prefetched stages: their token loads
+                    // must be in flight before waiting for a free stage
+                    if (!waited && npre == STAGES) flush_prefetched();
                     if (!wait_or_abort(&empty[stage], phase ^ 1, p.wait_ns, abort_flag)) {
                         if (!*abort_flag) record_timeout(p, abort_flag, kSiteProducerEmpty);
                         ok = false;
@@ -165,16 +191,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint8_t* st = smem + stage * C::kStageBytes;
                     ptx::mbar_arrive_expect_tx(&full[stage], tx);
                     ptx::tma_load_2d(st, &tmW, &full[stage], 0, static_cast<int32_t>((tile0 + kc) * 256));
-                    ptx::tma_load_2d(smem + C::kOffX + stage * C::kXTile, &tmX, &full[stage], kc * 128, first);
                     ptx::bulk_load(st + C::kOffSFW, p.a_sf + static_cast<size_t>(tile0 + kc) * 1024, 1024, &full[stage]);
-                    ptx::bulk_load(st + C::kOffSFX, p.b_sf + static_cast<size_t>(v) * p.b_sf_tile_bytes + kc * 512, 512,
-                                   &full[stage]);
+                    if (!waited) {  // first lap: stage == npre
+                        pre_v[npre] = v;
+                        pre_first[npre] = first;
+                        pre_kc[npre] = kc;
+                        ++npre;
+                    } else {
+                        ptx::tma_load_2d(smem + C::kOffX + stage * C::kXTile, &tmX, &full[stage], kc * 128, first);
+                        ptx::bulk_load(st + C::kOffSFX, p.b_sf + static_cast<size_t>(v) * p.b_sf_tile_bytes + kc * 512,
+                                       512, &full[stage]);
+                    }
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1;
                     }
                 }
             }
+            if (!waited) flush_prefetched();  // fewer stages than the ring
             // every issued stage lands before the CTA may exit (bounded)
             for (int s = 0; s < STAGES; ++s) {
                 const uint32_t par = (static_cast<uint32_t>(s) < stage) ? phase : (phase ^ 1);

@@ -28,7 +28,8 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(GatherParams p) 
     ptx::pdl_wait();
     const int nv = p.header[kHdrNumV];
     const int nb = p.H / 32;
-    const int bytes = (p.H / 128) * 512;
+    // Bytes of rows beyond the tile stay as they are: the MMA reads 128 rows,
+    // but the accumulator lanes of rows past the tile are never read.
     for (int v = blockIdx.x; v < nv; v += gridDim.x) {
         const int4 vi = p.vinfo[v];
         const int first = vi.y, rows = vi.z;
@@ -62,12 +63,6 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(GatherParams p) 
             dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
             dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
             sf_tile[(b >> 2) * 512 + (i & 31) * 16 + (i >> 5) * 4 + (b & 3)] = static_cast<uint8_t>(ex + 127);
-        }
-        // every other byte of the tile's scale blocks -> 0 (rows beyond the
-        // tile; the MMA reads 128 rows)
-        for (int j = threadIdx.x; j < bytes; j += kGatherThreads) {
-            const int line = (j >> 4) & 31, grp = (j >> 2) & 3;
-            if (grp * 32 + line >= rows) sf_tile[j] = 0;
         }
     }
     ptx::pdl_launch_dependents();

@@ -23,7 +23,8 @@ constexpr int kRouteWarps = 8;
 constexpr int kMaxPerLane = 32;  // E_global <= 1024
 
 // Monotone map of a finite fp32 to uint32 (a < b  <=>  key(a) < key(b));
-// -0 is folded onto +0 so that equal values tie.
+// -0 is folded onto +0 so that equal values tie; every finite value and
+// -inf map above 0.
 __device__ __forceinline__ uint32_t order_key(float f) {
     uint32_t u = __float_as_uint(f);
     if (u == 0x80000000u) u = 0;
@@ -34,7 +35,28 @@ __device__ __forceinline__ float key_value(uint32_t k) {
     return __uint_as_float((k & 0x80000000u) ? (k ^ 0x80000000u) : ~k);
 }
 
-constexpr uint32_t kNoId = 0xFFFFFFFFu;
+// Best (largest key, lowest index on ties) of a lane's entries by a
+// pairwise tree; taken / absent entries hold key 0, which no finite logit
+// maps to.
+__device__ __forceinline__ void lane_best(const uint32_t (&key)[kMaxPerLane], uint32_t& bk, int& bi) {
+    uint32_t k[kMaxPerLane];
+    int ix[kMaxPerLane];
+#pragma unroll
+    for (int i = 0; i < kMaxPerLane; ++i) {
+        k[i] = key[i];
+        ix[i] = i;
+    }
+#pragma unroll
+    for (int w = kMaxPerLane / 2; w >= 1; w >>= 1)
+#pragma unroll
+        for (int i = 0; i < w; ++i)
+            if (k[i + w] > k[i]) {  // the upper half holds higher indices: ties keep the lower one
+                k[i] = k[i + w];
+                ix[i] = ix[i + w];
+            }
+    bk = k[0];
+    bi = ix[0];
+}
 
 __global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(RouteParams p) {
     ptx::pdl_wait();
@@ -43,35 +65,24 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(RouteParams p) 
     if (t < p.T) {
         const float* row = p.logits + static_cast<size_t>(t) * p.Eg;
         uint32_t key[kMaxPerLane];
-        uint32_t avail = 0;
 #pragma unroll
         for (int i = 0; i < kMaxPerLane; ++i) {
             const int e = lane + 32 * i;
-            const bool in = e < p.Eg;
-            key[i] = in ? order_key(row[e]) : 0u;
-            if (in) avail |= 1u << i;
+            key[i] = (e < p.Eg) ? order_key(row[e]) : 0u;
         }
-        // best untaken entry of this lane (lower index wins ties = lower id)
-        auto lane_best = [&](uint32_t& bk, uint32_t& bid) {
-            bk = 0;
-            bid = kNoId;
-#pragma unroll
-            for (int i = 0; i < kMaxPerLane; ++i)
-                if (((avail >> i) & 1u) && (bid == kNoId || key[i] > bk)) {
-                    bk = key[i];
-                    bid = static_cast<uint32_t>(lane + 32 * i);
-                }
-        };
-        uint32_t bk, bid;
-        lane_best(bk, bid);
+        uint32_t bk;
+        int bi;
+        lane_best(key, bk, bi);
         uint32_t my_key = 0, my_id = 0;
         for (int j = 0; j < p.k; ++j) {
-            // lanes without candidates hold bid = kNoId and never win
-            const uint32_t kmax = __reduce_max_sync(0xffffffffu, bid == kNoId ? 0u : bk);
-            const uint32_t win = __reduce_min_sync(0xffffffffu, (bid != kNoId && bk == kmax) ? bid : kNoId);
+            const uint32_t kmax = __reduce_max_sync(0xffffffffu, bk);
+            const uint32_t cand = (bk == kmax && bk != 0) ? static_cast<uint32_t>(lane + 32 * bi) : 0xFFFFFFFFu;
+            const uint32_t win = __reduce_min_sync(0xffffffffu, cand);
             if (lane == static_cast<int>(win & 31)) {
-                avail &= ~(1u << (win >> 5));
-                lane_best(bk, bid);
+#pragma unroll
+                for (int i = 0; i < kMaxPerLane; ++i)
+                    if (i == static_cast<int>(win >> 5)) key[i] = 0;
+                lane_best(key, bk, bi);
             }
             if (lane == j) {
                 my_key = kmax;
