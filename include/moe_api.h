@@ -195,6 +195,25 @@ int moe_layer_events(const moe_shape* shape, const float* logits, const uint16_t
                      const moe_weights* weights, int32_t* topk_ids, float* topk_w, void* workspace,
                      size_t workspace_bytes, uint16_t* out, void* const* events, moe_stream_t stream);
 
+/* moe_layer for callers that cannot allocate device memory (for example code
+ * running under another framework's allocator with allocation disabled, or a
+ * runtime that must not call cudaMalloc after start-up).  The reference pages
+ * have no counterpart to this call.  The layer's scratch is one 32 MiB
+ * file-scope device array that every GPU loading this library holds until
+ * the process exits; shapes whose moe_workspace_bytes exceeds 32 MiB are
+ * rejected with MOE_ERR_WORKSPACE (decode with T <= 32 at E 896, k 16,
+ * H 3584, I 384 fits).  The caller passes inputs and outputs as for
+ * moe_layer; the call allocates nothing.  The first call on a device looks up
+ * the array's device address (cudaGetSymbolAddress, with that device
+ * current), so make that first call before any stream capture.  Every call on
+ * a device shares the one array and leaves its contents behind: calls whose
+ * executions overlap on the GPU (other streams, other host threads) race and
+ * must be serialised by the caller.  Device-side errors are recorded in that
+ * array's status word, which this entry point does not expose. */
+int moe_layer_noalloc(const moe_shape* shape, const float* logits, const uint16_t* shared_logit, const uint16_t* x,
+                      const moe_weights* weights, int32_t* topk_ids, float* topk_w, uint16_t* out,
+                      moe_stream_t stream);
+
 /* Workspace views (device pointers) for inspection. */
 int moe_get_views(const moe_shape* shape, void* workspace, moe_views* views);
 

@@ -19,8 +19,8 @@ from . import build as _build
 __all__ = [
     "MoeShape", "MoeWeights", "MoeError", "lib", "moe_is_supported", "moe_workspace_bytes",
     "moe_quantize_mxfp4", "moe_pack_weights", "moe_route", "moe_sort", "moe_forward",
-    "moe_layer", "moe_layer_host", "moe_layer_events", "moe_get_views", "moe_get_status", "moe_num_sms", "quantize_expert_weights",
-    "workspace", "MOE_OK", "MOE_ERR_TIMEOUT",
+    "moe_layer", "moe_layer_host", "moe_layer_events", "moe_layer_noalloc", "moe_get_views", "moe_get_status", "moe_num_sms", "quantize_expert_weights",
+    "workspace", "MOE_OK", "MOE_ERR_TIMEOUT", "MOE_ERR_WORKSPACE",
 ]
 
 MOE_OK = 0
@@ -102,6 +102,7 @@ _SIGS = {
     "moe_layer": [ctypes.c_void_p] * 8 + [ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p],
     "moe_layer_host": [ctypes.c_void_p] * 6 + [ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p],
     "moe_layer_events": [ctypes.c_void_p] * 8 + [ctypes.c_size_t] + [ctypes.c_void_p] * 3,
+    "moe_layer_noalloc": [ctypes.c_void_p] * 9,
     "moe_get_views": [ctypes.c_void_p] * 3,
     "moe_get_status": [ctypes.c_void_p] * 3,
     "moe_num_sms": [ctypes.c_void_p],
@@ -277,6 +278,26 @@ def moe_layer_events(shape: MoeShape, logits, shared_logit, x, weights: MoeWeigh
           topk_ids.data_ptr(), topk_w.data_ptr(), ws.data_ptr(), ws.numel(), out.data_ptr(), arr,
           _stream(x.device))
     return out
+
+
+def moe_layer_noalloc(shape: MoeShape, logits, shared_logit, x, weights: MoeWeights, topk_ids=None, topk_w=None,
+                      out=None):
+    """moe_layer without a workspace argument, for callers that cannot
+    allocate device memory: the scratch is the library's fixed 32 MiB device
+    array (shapes needing more raise MoeError(MOE_ERR_WORKSPACE)).  Calls that
+    run concurrently on the GPU share that array and must be serialised."""
+    _check_cuda(logits, shared_logit, x)
+    dev = x.device
+    if topk_ids is None:
+        topk_ids = torch.empty((shape.T, shape.kp), dtype=torch.int32, device=dev)
+    if topk_w is None:
+        topk_w = torch.empty((shape.T, shape.kp), dtype=torch.float32, device=dev)
+    if out is None:
+        out = torch.empty((shape.T, shape.hidden), dtype=torch.bfloat16, device=dev)
+    s, w = shape.c(), weights.c()
+    _call("moe_layer_noalloc", ctypes.byref(s), logits.data_ptr(), _ptr(shared_logit), x.data_ptr(),
+          ctypes.byref(w), topk_ids.data_ptr(), topk_w.data_ptr(), out.data_ptr(), _stream(dev))
+    return out, topk_ids, topk_w
 
 
 def moe_layer_host(shape: MoeShape, logits_h, shared_logit_h, x_h, weights: MoeWeights, ws, out_h):
