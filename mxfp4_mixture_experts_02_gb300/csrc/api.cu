@@ -92,7 +92,7 @@ int run_sort(const moe_shape* s, const int32_t* ids, void* ws, cudaStream_t st, 
     const Layout L = make_layout(d);
     SortParams p{ids, at<int32_t>(ws, L.header), at<int32_t>(ws, L.counts), at<int32_t>(ws, L.offsets),
                  at<int4>(ws, L.vinfo), at<int4>(ws, L.groups), at<int32_t>(ws, L.a_map), at<int32_t>(ws, L.c_map),
-                 d.T, d.kp, d.Eg, d.E, d.off, d.S, d.Et, d.B, d.G};
+                 at<int32_t>(ws, L.sort_hist), d.T, d.kp, d.Eg, d.E, d.off, d.S, d.Et, d.B, d.G};
     return cuda_rc(launch_sort(p, st, pdl));
 }
 
@@ -114,8 +114,10 @@ int run_forward(const moe_shape* s, const uint16_t* x, const moe_weights* wt, co
     if (nsm <= 0) return MOE_ERR_CUDA;
 
     GatherParams gp{x, at<int32_t>(ws, L.header), at<int4>(ws, L.vinfo), at<int32_t>(ws, L.a_map),
-                    at<uint8_t>(ws, L.xq), at<uint8_t>(ws, L.xsf), d.H, d.kp, d.B, L.xsf_tile_bytes, d.V_max,
-                    d.V_max < 4 * nsm ? d.V_max : 4 * nsm};
+                    at<uint8_t>(ws, L.xq), at<uint8_t>(ws, L.xsf),
+                    d.mode == kModePrefill ? at<uint8_t>(ws, L.xq_nat) : nullptr,
+                    d.mode == kModePrefill ? at<uint8_t>(ws, L.xsf_nat) : nullptr, d.H, d.kp, d.B, L.xsf_tile_bytes,
+                    d.V_max, d.V_max < 4 * nsm ? d.V_max : 4 * nsm, d.T};
     cudaError_t e = launch_gather(gp, st, pdl);
     if (e != cudaSuccess || !rec(ev, 3, st)) return MOE_ERR_CUDA;
 

@@ -36,8 +36,8 @@ struct Dims {
 
 // Byte offsets of the workspace regions (256-byte aligned).
 struct Layout {
-    size_t header, counts, offsets, vinfo, groups, a_map, c_map;
-    size_t xq, xsf, act, asf, y;
+    size_t header, counts, offsets, vinfo, groups, a_map, c_map, sort_hist;
+    size_t xq, xsf, act, asf, y, xq_nat, xsf_nat;
     size_t st_logits, st_shared, st_x, st_ids, st_w, st_out;
     size_t total;
     int xsf_tile_bytes, asf_tile_bytes, y_bf16;
@@ -83,6 +83,7 @@ inline Layout make_layout(const Dims& d) {
     L.groups = take(size_t(d.V_max) * 16);
     L.a_map = take(size_t(d.R_max) * 4);
     L.c_map = take(size_t(d.R_max) * 4);
+    L.sort_hist = take(size_t((d.R_max + 4095) / 4096) * d.Et * 4);
     // Tile scale layout: per virtual expert and 128-K chunk one 512-byte
     // block, tile row r / K-block b at (r % 32) * 16 + (r / 32) * 4 + b: one
     // tcgen05.cp .32x128b.warpx4 puts it in 4 TMEM columns, row r at lane
@@ -95,6 +96,9 @@ inline Layout make_layout(const Dims& d) {
     L.act = take(size_t(d.rows_alloc) * d.I);
     L.asf = take(size_t(d.V_max) * L.asf_tile_bytes);
     L.y = take(size_t(d.R_max) * d.H * (L.y_bf16 ? 2 : 4));
+    // natural-order MXFP8 x for the two-pass gather (prefill tiling)
+    L.xq_nat = take(d.mode == kModePrefill ? size_t(d.max_T) * d.H : 0);
+    L.xsf_nat = take(d.mode == kModePrefill ? size_t(d.max_T) * (d.H / 32) : 0);
     L.st_logits = take(size_t(d.max_T) * d.Eg * 4);
     L.st_shared = take(size_t(d.max_T) * (d.S > 0 ? d.S : 1) * 2);
     L.st_x = take(size_t(d.max_T) * d.H * 2);

@@ -44,7 +44,7 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 
-template <int TM, int STAGES>
+template <int TM, int STAGES, bool STAGE_Y>
 struct Cfg {
     static constexpr int kWTile = 256 * 128;           // 256 weight rows x 128 K (16-byte E2M1 chunks)
     static constexpr int kOffSFW = kWTile;             // 2 x 512 B weight scales
@@ -53,7 +53,11 @@ struct Cfg {
     static constexpr int kXTile = TM * 128;            // bytes of the loaded token rows
     static constexpr int kXRegion = STAGES * kXTile + (TM < 128 ? 128 * 128 - kXTile : 0);
     static constexpr int kOffX = STAGES * kStageBytes;
-    static constexpr int kOffBar = kOffX + kXRegion;
+    // bf16 FC2 rows of 128-row tiles are staged per epilogue warp (32 rows x
+    // 256 B) and written back as whole row segments
+    static constexpr int kOffEpi = kOffX + kXRegion;
+    static constexpr int kEpiBytes = STAGE_Y ? 8 * 32 * 256 : 0;
+    static constexpr int kOffBar = kOffEpi + kEpiBytes;
     static constexpr int kSmemBytes = kOffBar + (2 * STAGES + 4) * 8 + 16 + 1024;
     static constexpr int kAccCols = 256;
     static constexpr int kSfCols = 16;                  // per stage: 4 token-scale + 8 weight-scale columns
@@ -103,7 +107,8 @@ template <int TM, bool FC1, bool YBF16, int STAGES>
 __global__ void __launch_bounds__(kThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                     const GemmParams p) {
-    using C = Cfg<TM, STAGES>;
+    constexpr bool kStageY = !FC1 && YBF16 && TM == 128;
+    using C = Cfg<TM, STAGES, kStageY>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
@@ -293,7 +298,35 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(accempty);  // accumulator free for the next item
-            if (valid) {
+            if constexpr (kStageY) {
+                // lane = tile row q*32+lane: its 128 weighted bf16 values go to
+                // its own 256-byte staging row (16-byte chunks XOR-swizzled by
+                // the row), then the warp stores one whole row per instruction.
+                uint8_t* stg = smem + C::kOffEpi + warp * (32 * 256);
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    uint32_t pk[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const __nv_bfloat162 b2 =
+                            __floats2bfloat162_rn(__uint_as_float(r[c >> 2][8 * (c & 3) + 2 * u]) * w_row,
+                                                  __uint_as_float(r[c >> 2][8 * (c & 3) + 2 * u + 1]) * w_row);
+                        pk[u] = *reinterpret_cast<const uint32_t*>(&b2);
+                    }
+                    *reinterpret_cast<uint4*>(stg + lane * 256 + ((c ^ (lane & 15)) << 4)) =
+                        make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                }
+                __syncwarp();
+                const int n0 = nb * 256 + half * 128;
+                for (int rr = 0; rr < 32; ++rr) {
+                    if (q * 32 + rr >= rows) break;  // warp-uniform
+                    const uint2 v2 = *reinterpret_cast<const uint2*>(stg + rr * 256 + (((lane >> 1) ^ (rr & 15)) << 4) +
+                                                                      (lane & 1) * 8);
+                    *reinterpret_cast<uint2*>(p.y_bf16 + static_cast<int64_t>(first + q * 32 + rr) * p.H + n0 +
+                                              lane * 4) = v2;
+                }
+                __syncwarp();
+            } else if (valid) {
                 const int64_t row = first + i;
                 if constexpr (FC1) {
                     const int f0 = nb * 128 + half * 64;  // first intermediate feature of this lane
@@ -359,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int TM, bool FC1, bool YBF16, int STAGES>
 cudaError_t launch_impl(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmParams& p, int grid,
                         cudaStream_t stream, bool pdl) {
-    using C = Cfg<TM, STAGES>;
+    using C = Cfg<TM, STAGES, !FC1 && YBF16 && TM == 128>;
     auto kern = moe_gemm_kernel<TM, FC1, YBF16, STAGES>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (err != cudaSuccess) return err;
@@ -377,7 +410,7 @@ cudaError_t launch_gemm(bool fc1, const CUtensorMap& tmW, const CUtensorMap& tmX
     }
     if (TM == 16) return launch_impl<16, false, false, 5>(tmW, tmX, p, grid, stream, pdl);
     if (TM == 32) return launch_impl<32, false, false, 5>(tmW, tmX, p, grid, stream, pdl);
-    return launch_impl<128, false, true, 4>(tmW, tmX, p, grid, stream, pdl);
+    return launch_impl<128, false, true, 3>(tmW, tmX, p, grid, stream, pdl);
 }
 
 }  // namespace moe

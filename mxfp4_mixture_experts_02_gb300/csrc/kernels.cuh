@@ -44,6 +44,7 @@ struct SortParams {
     int4* groups;
     int32_t* a_map;
     int32_t* c_map;
+    int32_t* cta_hist;  // [ceil(T*k' / 4096)][Et]: large-sort scratch
     int T, kp, Eg, E, off, S, Et, B, G;
 };
 
@@ -54,7 +55,9 @@ struct GatherParams {  // x -> MXFP8 rows in expert order + tile scales
     const int32_t* a_map;
     uint8_t* xq;
     uint8_t* xsf;
-    int H, kp, B, xsf_tile_bytes, max_v, grid;
+    uint8_t* xq_nat;   // NULL: one fused pass; else the two-pass path's natural-order MXFP8 x [T, H]
+    uint8_t* xsf_nat;  // its scales [T, H/32]
+    int H, kp, B, xsf_tile_bytes, max_v, grid, T;
 };
 
 struct GemmParams {

@@ -68,6 +68,71 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(GatherParams p) 
     ptx::pdl_launch_dependents();
 }
 
+// Two-pass path for large token counts.  Pass 1: x -> MXFP8 once per token
+// in natural order (xq_nat [T, H], xsf_nat [T, H/32]); one thread per
+// 32-element block.
+__global__ void __launch_bounds__(kGatherThreads) quant_x_kernel(GatherParams p) {
+    ptx::pdl_wait();
+    const int nb = p.H / 32;
+    const int64_t total = static_cast<int64_t>(p.T) * nb;
+    for (int64_t job = blockIdx.x * static_cast<int64_t>(kGatherThreads) + threadIdx.x; job < total;
+         job += static_cast<int64_t>(gridDim.x) * kGatherThreads) {
+        const int64_t t = job / nb;
+        const int b = static_cast<int>(job - t * nb);
+        const uint4* src = reinterpret_cast<const uint4*>(p.x + t * p.H + b * 32);
+        uint4 raw[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) raw[c] = src[c];
+        const uint16_t* hv = reinterpret_cast<const uint16_t*>(raw);
+        float f[32];
+        float amax = 0.f;
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+            f[e] = bf16_bits_to_float(hv[e]);
+            amax = fmaxf(amax, fabsf(f[e]));
+        }
+        const int ex = mx_shared_exponent(amax, 8);
+        const float inv = exp2_int(-ex);
+        uint32_t packed[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const uint32_t lo = e4m3x2(f[4 * e] * inv, f[4 * e + 1] * inv);
+            const uint32_t hi = e4m3x2(f[4 * e + 2] * inv, f[4 * e + 3] * inv);
+            packed[e] = lo | (hi << 16);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(p.xq_nat + t * p.H + b * 32);
+        dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+        dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+        p.xsf_nat[t * nb + b] = static_cast<uint8_t>(ex + 127);
+    }
+    ptx::pdl_launch_dependents();
+}
+
+// Pass 2: copy each row's MXFP8 bytes from its token's natural-order row and
+// its scales into the tile layout.  One warp per row, 16-byte moves.
+__global__ void __launch_bounds__(kGatherThreads) gather_copy_kernel(GatherParams p) {
+    ptx::pdl_wait();
+    const int nv = p.header[kHdrNumV];
+    const int warps = kGatherThreads / 32;
+    const int lane = threadIdx.x & 31;
+    const int nb = p.H / 32, n16 = p.H / 16;
+    for (int v = blockIdx.x; v < nv; v += gridDim.x) {
+        const int4 vi = p.vinfo[v];
+        const int first = vi.y, rows = vi.z;
+        uint8_t* sf_tile = p.xsf + static_cast<size_t>(v) * p.xsf_tile_bytes;
+        for (int i = threadIdx.x >> 5; i < rows; i += warps) {
+            const int row = first + i;
+            const int64_t t = p.a_map[row] / p.kp;
+            const uint4* src = reinterpret_cast<const uint4*>(p.xq_nat + t * p.H);
+            uint4* dst = reinterpret_cast<uint4*>(p.xq + static_cast<int64_t>(row) * p.H);
+            for (int c = lane; c < n16; c += 32) dst[c] = src[c];
+            for (int b = lane; b < nb; b += 32)
+                sf_tile[(b >> 2) * 512 + (i & 31) * 16 + (i >> 5) * 4 + (b & 3)] = p.xsf_nat[t * nb + b];
+        }
+    }
+    ptx::pdl_launch_dependents();
+}
+
 // One thread per 32-element block of a row.
 __global__ void quantize_mxfp4_kernel(QuantParams p) {
     const int64_t nb = p.K / 32;
@@ -156,7 +221,12 @@ unsigned grid_for(int64_t n, int threads) {
 }  // namespace
 
 cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream, bool pdl) {
-    return launch_kernel(gather_kernel, dim3(p.grid), dim3(kGatherThreads), 0, stream, pdl, p);
+    if (!p.xq_nat) return launch_kernel(gather_kernel, dim3(p.grid), dim3(kGatherThreads), 0, stream, pdl, p);
+    const int64_t blocks = (static_cast<int64_t>(p.T) * (p.H / 32) + kGatherThreads - 1) / kGatherThreads;
+    cudaError_t e = launch_kernel(quant_x_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kGatherThreads), 0,
+                                  stream, pdl, p);
+    if (e != cudaSuccess) return e;
+    return launch_kernel(gather_copy_kernel, dim3(p.grid), dim3(kGatherThreads), 0, stream, true, p);
 }
 
 cudaError_t launch_quantize_mxfp4(const QuantParams& p, cudaStream_t stream) {
