@@ -108,26 +108,32 @@ __global__ void __launch_bounds__(kGatherThreads) quant_x_kernel(GatherParams p)
     ptx::pdl_launch_dependents();
 }
 
-// Pass 2: copy each row's MXFP8 bytes from its token's natural-order row and
-// its scales into the tile layout.  One warp per row, 16-byte moves.
+// Pass 2: copy each row's MXFP8 bytes from its token's natural-order row (one
+// warp per row, 16-byte moves) and build the tile's scale blocks: each thread
+// moves one row's four K-block scales of one 128-K chunk (4 bytes) into its
+// word (i % 32) * 16 + (i / 32) * 4 of the chunk's 512-byte block.
 __global__ void __launch_bounds__(kGatherThreads) gather_copy_kernel(GatherParams p) {
     ptx::pdl_wait();
     const int nv = p.header[kHdrNumV];
     const int warps = kGatherThreads / 32;
     const int lane = threadIdx.x & 31;
-    const int nb = p.H / 32, n16 = p.H / 16;
+    const int nb = p.H / 32, n16 = p.H / 16, kchunks = p.H / 128;
     for (int v = blockIdx.x; v < nv; v += gridDim.x) {
         const int4 vi = p.vinfo[v];
         const int first = vi.y, rows = vi.z;
-        uint8_t* sf_tile = p.xsf + static_cast<size_t>(v) * p.xsf_tile_bytes;
         for (int i = threadIdx.x >> 5; i < rows; i += warps) {
             const int row = first + i;
             const int64_t t = p.a_map[row] / p.kp;
             const uint4* src = reinterpret_cast<const uint4*>(p.xq_nat + t * p.H);
             uint4* dst = reinterpret_cast<uint4*>(p.xq + static_cast<int64_t>(row) * p.H);
             for (int c = lane; c < n16; c += 32) dst[c] = src[c];
-            for (int b = lane; b < nb; b += 32)
-                sf_tile[(b >> 2) * 512 + (i & 31) * 16 + (i >> 5) * 4 + (b & 3)] = p.xsf_nat[t * nb + b];
+        }
+        uint32_t* sf_tile = reinterpret_cast<uint32_t*>(p.xsf + static_cast<size_t>(v) * p.xsf_tile_bytes);
+        for (int j = threadIdx.x; j < kchunks * rows; j += kGatherThreads) {
+            const int kc = j / rows, i = j - kc * rows;
+            const int64_t t = p.a_map[first + i] / p.kp;
+            sf_tile[kc * 128 + (i & 31) * 4 + (i >> 5)] =
+                *reinterpret_cast<const uint32_t*>(p.xsf_nat + t * nb + kc * 4);
         }
     }
     ptx::pdl_launch_dependents();
