@@ -117,7 +117,7 @@ int run_forward(const moe_shape* s, const uint16_t* x, const moe_weights* wt, co
                     at<uint8_t>(ws, L.xq), at<uint8_t>(ws, L.xsf),
                     d.mode == kModePrefill ? at<uint8_t>(ws, L.xq_nat) : nullptr,
                     d.mode == kModePrefill ? at<uint8_t>(ws, L.xsf_nat) : nullptr, d.H, d.kp, d.B, L.xsf_tile_bytes,
-                    d.V_max, d.V_max < 4 * nsm ? d.V_max : 4 * nsm, d.T};
+                    topk_w, at<float>(ws, L.row_w), d.V_max, d.V_max < 8 * nsm ? d.V_max : 8 * nsm, d.T};
     cudaError_t e = launch_gather(gp, st, pdl);
     if (e != cudaSuccess || !rec(ev, 3, st)) return MOE_ERR_CUDA;
 
@@ -142,6 +142,7 @@ int run_forward(const moe_shape* s, const uint16_t* x, const moe_weights* wt, co
     g.vinfo = at<int4>(ws, L.vinfo);
     g.a_map = at<int32_t>(ws, L.a_map);
     g.topk_w = topk_w;
+    g.row_w = at<float>(ws, L.row_w);
     g.act = at<uint8_t>(ws, L.act);
     g.act_sf = at<uint8_t>(ws, L.asf);
     g.y = L.y_bf16 ? nullptr : at<float>(ws, L.y);

@@ -36,7 +36,7 @@ struct Dims {
 
 // Byte offsets of the workspace regions (256-byte aligned).
 struct Layout {
-    size_t header, counts, offsets, vinfo, groups, a_map, c_map, sort_hist;
+    size_t header, counts, offsets, vinfo, groups, a_map, c_map, sort_hist, row_w;
     size_t xq, xsf, act, asf, y, xq_nat, xsf_nat;
     size_t st_logits, st_shared, st_x, st_ids, st_w, st_out;
     size_t total;
@@ -84,6 +84,7 @@ inline Layout make_layout(const Dims& d) {
     L.a_map = take(size_t(d.R_max) * 4);
     L.c_map = take(size_t(d.R_max) * 4);
     L.sort_hist = take(size_t((d.R_max + 4095) / 4096) * d.Et * 4);
+    L.row_w = take(size_t(d.R_max) * 4);
     // Tile scale layout: per virtual expert and 128-K chunk one 512-byte
     // block, tile row r / K-block b at (r % 32) * 16 + (r / 32) * 4 + b: one
     // tcgen05.cp .32x128b.warpx4 puts it in 4 TMEM columns, row r at lane

@@ -179,9 +179,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                                    &full[j]);
                 }
             };
+            int4 vi_next = blockIdx.x < nitems ? p.vinfo[blockIdx.x / NB] : make_int4(0, 0, 0, 0);
             for (int it = blockIdx.x; ok && it < nitems; it += gridDim.x) {
                 const int v = it / NB, nb = it - v * NB;
-                const int4 vi = p.vinfo[v];
+                const int4 vi = vi_next;
+                // next item's descriptor, in flight while this item streams
+                const int itn = it + gridDim.x;
+                if (itn < nitems) vi_next = p.vinfo[itn / NB];
                 const int e = vi.x, first = vi.y;
                 const int64_t tile0 = (static_cast<int64_t>(e) * NB + nb) * KC;
                 for (int kc = 0; kc < KC; ++kc) {
@@ -268,14 +272,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = warp & 3, half = warp >> 2;
         const bool active = (TM > 32) || q == 0;
         uint32_t aphase = 0;
-        for (int it = blockIdx.x; active && it < nitems; it += gridDim.x) {
+        const int i = q * 32 + lane;  // token row of this lane within a tile
+        // Descriptors two items ahead and row weights one item ahead are
+        // loaded early, so no dependent load chain sits between two items.
+        const int4 kNoTile = make_int4(0, 0, 0, 0);
+        const int g = gridDim.x;
+        int4 vi_cur = (active && blockIdx.x < nitems) ? p.vinfo[blockIdx.x / NB] : kNoTile;
+        int4 vi_nxt = (active && blockIdx.x + g < nitems) ? p.vinfo[(blockIdx.x + g) / NB] : kNoTile;
+        float w_cur = (!FC1 && i < vi_cur.z) ? p.row_w[vi_cur.y + i] : 0.f;
+        for (int it = blockIdx.x; active && it < nitems; it += g) {
             const int v = it / NB, nb = it - v * NB;
-            const int4 vi = p.vinfo[v];
+            const int4 vi = vi_cur;
+            const float w_row = w_cur;
+            const int4 vi_n2 = (it + 2 * g < nitems) ? p.vinfo[(it + 2 * g) / NB] : kNoTile;
+            w_cur = (!FC1 && i < vi_nxt.z) ? p.row_w[vi_nxt.y + i] : 0.f;
+            vi_cur = vi_nxt;
+            vi_nxt = vi_n2;
             const int first = vi.y, rows = vi.z;
-            const int i = q * 32 + lane;  // token row of this lane within the tile
             const bool valid = i < rows;
-            float w_row = 0.f;
-            if (!FC1 && valid) w_row = p.topk_w[p.a_map[first + i]];
             if (!wait_or_abort(accfull, aphase, p.wait_ns, abort_flag)) {
                 if (lane == 0 && !*abort_flag) record_timeout(p, abort_flag, kSiteEpiAccFull);
                 break;

@@ -57,6 +57,8 @@ struct GatherParams {  // x -> MXFP8 rows in expert order + tile scales
     uint8_t* xsf;
     uint8_t* xq_nat;   // NULL: one fused pass; else the two-pass path's natural-order MXFP8 x [T, H]
     uint8_t* xsf_nat;  // its scales [T, H/32]
+    const float* topk_w;
+    float* row_w;      // routing weight of each row: topk_w[a_map[row]]
     int H, kp, B, xsf_tile_bytes, max_v, grid, T;
 };
 
@@ -67,6 +69,7 @@ struct GemmParams {
     const int4* vinfo;
     const int32_t* a_map;
     const float* topk_w;
+    const float* row_w;    // routing weight per row (written by the gather)
     const uint8_t* a_sf;   // packed weight scales
     const uint8_t* b_sf;   // tile scales of the activation operand
     uint8_t* act;          // FC1 output codes [rows_alloc, I]

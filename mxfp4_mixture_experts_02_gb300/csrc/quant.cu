@@ -37,7 +37,9 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(GatherParams p) 
         for (int job = threadIdx.x; job < rows * nb; job += kGatherThreads) {
             const int i = job / nb, b = job - i * nb;
             const int row = first + i;
-            const int t = p.a_map[row] / p.kp;
+            const int slot = p.a_map[row];
+            const int t = slot / p.kp;
+            if (b == 0) p.row_w[row] = p.topk_w[slot];
             const uint4* src = reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(t) * p.H + b * 32);
             uint4 raw[4];
 #pragma unroll
@@ -123,7 +125,9 @@ __global__ void __launch_bounds__(kGatherThreads) gather_copy_kernel(GatherParam
         const int first = vi.y, rows = vi.z;
         for (int i = threadIdx.x >> 5; i < rows; i += warps) {
             const int row = first + i;
-            const int64_t t = p.a_map[row] / p.kp;
+            const int slot = p.a_map[row];
+            const int64_t t = slot / p.kp;
+            if (lane == 0) p.row_w[row] = p.topk_w[slot];
             const uint4* src = reinterpret_cast<const uint4*>(p.xq_nat + t * p.H);
             uint4* dst = reinterpret_cast<uint4*>(p.xq + static_cast<int64_t>(row) * p.H);
             for (int c = lane; c < n16; c += 32) dst[c] = src[c];
