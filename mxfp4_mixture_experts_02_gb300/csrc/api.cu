@@ -116,8 +116,8 @@ int run_forward(const moe_shape* s, const uint16_t* x, const moe_weights* wt, co
     GatherParams gp{x, at<int32_t>(ws, L.header), at<int4>(ws, L.vinfo), at<int32_t>(ws, L.a_map),
                     at<uint8_t>(ws, L.xq), at<uint8_t>(ws, L.xsf),
                     d.mode == kModePrefill ? at<uint8_t>(ws, L.xq_nat) : nullptr,
-                    d.mode == kModePrefill ? at<uint8_t>(ws, L.xsf_nat) : nullptr, d.H, d.kp, d.B, L.xsf_tile_bytes,
-                    topk_w, at<float>(ws, L.row_w), d.V_max, d.V_max < 8 * nsm ? d.V_max : 8 * nsm, d.T};
+                    d.mode == kModePrefill ? at<uint8_t>(ws, L.xsf_nat) : nullptr, topk_w, at<float>(ws, L.row_w),
+                    d.H, d.kp, d.B, L.xsf_tile_bytes, d.V_max, d.V_max < 8 * nsm ? d.V_max : 8 * nsm, d.T};
     cudaError_t e = launch_gather(gp, st, pdl);
     if (e != cudaSuccess || !rec(ev, 3, st)) return MOE_ERR_CUDA;
 
