@@ -125,7 +125,7 @@ int run_forward(const moe_shape* s, const uint16_t* x, const moe_weights* wt, co
     // a GEMM stage is one 256-row box, one contiguous 16 KiB run of global
     // memory.  Token operands: boxes of B rows x 128 K of the expert-ordered
     // MXFP8 activations.
-    CUtensorMap mw1, mw2, mx, mact;
+    CUtensorMap mw1, mw2, mx, mact, my;
     const uint64_t Et = static_cast<uint64_t>(d.Et);
     if (!make_map(&mw1, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, wt->w1, 128, Et * 2 * d.I * (d.H / 128),
                   kFp4BytesPer128Row, 128, 256) ||
@@ -134,6 +134,14 @@ int run_forward(const moe_shape* s, const uint16_t* x, const moe_weights* wt, co
         !make_map(&mx, CU_TENSOR_MAP_DATA_TYPE_UINT8, at<uint8_t>(ws, L.xq), d.H, d.rows_alloc, d.H, 128, d.B) ||
         !make_map(&mact, CU_TENSOR_MAP_DATA_TYPE_UINT8, at<uint8_t>(ws, L.act), d.I, d.rows_alloc, d.I, 128, d.B))
         return MOE_ERR_CUDA;
+    // bf16 FC2 rows (128-row tiling): each epilogue warp stores 32 rows x 64
+    // columns per box
+    if (L.y_bf16) {
+        if (!make_map(&my, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, at<uint16_t>(ws, L.y), d.H, d.rows_alloc, d.H * 2, 64, 32))
+            return MOE_ERR_CUDA;
+    } else {
+        my = mact;
+    }
 
     GemmParams g{};
     g.header = at<int32_t>(ws, L.header);
@@ -156,13 +164,13 @@ int run_forward(const moe_shape* s, const uint16_t* x, const moe_weights* wt, co
     g.a_sf = wt->w1_sf;
     g.b_sf = at<uint8_t>(ws, L.xsf);
     g.b_sf_tile_bytes = L.xsf_tile_bytes;
-    e = launch_gemm(true, mw1, mx, g, d.B, nsm, st, pdl);
+    e = launch_gemm(true, mw1, mx, my, g, d.B, nsm, st, pdl);
     if (e != cudaSuccess || !rec(ev, 4, st)) return MOE_ERR_CUDA;
 
     g.a_sf = wt->w2_sf;
     g.b_sf = at<uint8_t>(ws, L.asf);
     g.b_sf_tile_bytes = L.asf_tile_bytes;
-    e = launch_gemm(false, mw2, mact, g, d.B, nsm, st, pdl);
+    e = launch_gemm(false, mw2, mact, my, g, d.B, nsm, st, pdl);
     if (e != cudaSuccess || !rec(ev, 5, st)) return MOE_ERR_CUDA;
 
     CombineParams cp{at<int32_t>(ws, L.c_map), L.y_bf16 ? nullptr : at<float>(ws, L.y),

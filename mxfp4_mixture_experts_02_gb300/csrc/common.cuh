@@ -96,7 +96,9 @@ inline Layout make_layout(const Dims& d) {
     L.xsf = take(size_t(d.V_max) * L.xsf_tile_bytes);
     L.act = take(size_t(d.rows_alloc) * d.I);
     L.asf = take(size_t(d.V_max) * L.asf_tile_bytes);
-    L.y = take(size_t(d.R_max) * d.H * (L.y_bf16 ? 2 : 4));
+    // bf16 rows carry the TMA tail too: the store map's row extent is
+    // rows_alloc (>= 128), so a 32-row box never exceeds it
+    L.y = take(size_t(L.y_bf16 ? d.rows_alloc : d.R_max) * d.H * (L.y_bf16 ? 2 : 4));
     // natural-order MXFP8 x for the two-pass gather (prefill tiling)
     L.xq_nat = take(d.mode == kModePrefill ? size_t(d.max_T) * d.H : 0);
     L.xsf_nat = take(d.mode == kModePrefill ? size_t(d.max_T) * (d.H / 32) : 0);

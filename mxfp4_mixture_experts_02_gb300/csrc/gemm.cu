@@ -39,6 +39,27 @@ namespace moe {
 
 namespace {
 
+// Ring depths (stages of 256 weight rows x 128 K).  The decode GEMMs stream
+// weights at close to the MMA issue rate, so their rings are as deep as the
+// shared memory of a 32-row token tile allows; the prefill rings share shared
+// memory with 128-row token tiles (and FC2's output staging).
+#ifndef MOE_STAGES_DEC_FC1
+#define MOE_STAGES_DEC_FC1 5
+#endif
+#ifndef MOE_STAGES_DEC_FC2
+#define MOE_STAGES_DEC_FC2 5
+#endif
+#ifndef MOE_STAGES_PRE_FC1
+#define MOE_STAGES_PRE_FC1 4
+#endif
+#ifndef MOE_STAGES_PRE_FC2
+#define MOE_STAGES_PRE_FC2 3
+#endif
+constexpr int kStagesDecFc1 = MOE_STAGES_DEC_FC1;
+constexpr int kStagesDecFc2 = MOE_STAGES_DEC_FC2;
+constexpr int kStagesPreFc1 = MOE_STAGES_PRE_FC1;
+constexpr int kStagesPreFc2 = MOE_STAGES_PRE_FC2;
+
 constexpr int kWarps = 10;
 constexpr int kThreads = kWarps * 32;
 constexpr int kProducerWarp = 8;
@@ -53,8 +74,8 @@ struct Cfg {
     static constexpr int kXTile = TM * 128;            // bytes of the loaded token rows
     static constexpr int kXRegion = STAGES * kXTile + (TM < 128 ? 128 * 128 - kXTile : 0);
     static constexpr int kOffX = STAGES * kStageBytes;
-    // bf16 FC2 rows of 128-row tiles are staged per epilogue warp (32 rows x
-    // 256 B) and written back as whole row segments
+    // bf16 FC2 rows of 128-row tiles are staged per epilogue warp (two
+    // 1024-byte-aligned 32-row x 64-column boxes) and leave by TMA stores
     static constexpr int kOffEpi = kOffX + kXRegion;
     static constexpr int kEpiBytes = STAGE_Y ? 8 * 32 * 256 : 0;
     static constexpr int kOffBar = kOffEpi + kEpiBytes;
@@ -106,7 +127,7 @@ __device__ __forceinline__ uint32_t mxfp8_block(const float* v, uint32_t (&w)[8]
 template <int TM, bool FC1, bool YBF16, int STAGES>
 __global__ void __launch_bounds__(kThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                    const GemmParams p) {
+                    const __grid_constant__ CUtensorMap tmY, const GemmParams p) {
     constexpr bool kStageY = !FC1 && YBF16 && TM == 128;
     using C = Cfg<TM, STAGES, kStageY>;
     extern __shared__ uint8_t smem_raw[];
@@ -313,33 +334,52 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(accempty);  // accumulator free for the next item
             if constexpr (kStageY) {
-                // lane = tile row q*32+lane: its 128 weighted bf16 values go to
-                // its own 256-byte staging row (16-byte chunks XOR-swizzled by
-                // the row), then the warp stores one whole row per instruction.
+                // lane = tile row q*32+lane.  Its 128 weighted bf16 values are
+                // staged as two 32-row x 64-column boxes in the 128-byte TMA
+                // swizzle (16-byte chunk j of row r at chunk j ^ (r % 8)); a
+                // slab of 32 valid rows leaves with two tensor stores, a slab
+                // cut by the tile's last row with row stores of its valid rows
+                // (a tensor store would overwrite the next tile's rows).
                 uint8_t* stg = smem + C::kOffEpi + warp * (32 * 256);
+                const int slab_rows = rows - q * 32;
+                if (slab_rows > 0) {
+                    if (lane == 0) ptx::bulk_wait_read_all();  // previous item's stores left the buffer
+                    __syncwarp();
 #pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    uint32_t pk[4];
+                    for (int c = 0; c < 16; ++c) {
+                        uint32_t pk[4];
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const __nv_bfloat162 b2 =
-                            __floats2bfloat162_rn(__uint_as_float(r[c >> 2][8 * (c & 3) + 2 * u]) * w_row,
-                                                  __uint_as_float(r[c >> 2][8 * (c & 3) + 2 * u + 1]) * w_row);
-                        pk[u] = *reinterpret_cast<const uint32_t*>(&b2);
+                        for (int u = 0; u < 4; ++u) {
+                            const __nv_bfloat162 b2 =
+                                __floats2bfloat162_rn(__uint_as_float(r[c >> 2][8 * (c & 3) + 2 * u]) * w_row,
+                                                      __uint_as_float(r[c >> 2][8 * (c & 3) + 2 * u + 1]) * w_row);
+                            pk[u] = *reinterpret_cast<const uint32_t*>(&b2);
+                        }
+                        *reinterpret_cast<uint4*>(stg + (c >> 3) * 4096 + lane * 128 + (((c & 7) ^ (lane & 7)) << 4)) =
+                            make_uint4(pk[0], pk[1], pk[2], pk[3]);
                     }
-                    *reinterpret_cast<uint4*>(stg + lane * 256 + ((c ^ (lane & 15)) << 4)) =
-                        make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    const int n0 = nb * 256 + half * 128;
+                    if (slab_rows >= 32) {
+                        ptx::fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            ptx::tma_store_2d(&tmY, stg, n0, first + q * 32);
+                            ptx::tma_store_2d(&tmY, stg + 4096, n0 + 64, first + q * 32);
+                            ptx::bulk_commit_group();
+                        }
+                    } else {
+                        __syncwarp();
+                        // lane owns columns n0 + 4*lane .. +3: chunk lane/2, half lane%2
+                        const int cb = lane >> 1;
+                        for (int rr = 0; rr < slab_rows; ++rr) {
+                            const uint2 v2 = *reinterpret_cast<const uint2*>(
+                                stg + (cb >> 3) * 4096 + rr * 128 + (((cb & 7) ^ (rr & 7)) << 4) + (lane & 1) * 8);
+                            *reinterpret_cast<uint2*>(p.y_bf16 + static_cast<int64_t>(first + q * 32 + rr) * p.H +
+                                                      n0 + lane * 4) = v2;
+                        }
+                    }
+                    __syncwarp();
                 }
-                __syncwarp();
-                const int n0 = nb * 256 + half * 128;
-                for (int rr = 0; rr < 32; ++rr) {
-                    if (q * 32 + rr >= rows) break;  // warp-uniform
-                    const uint2 v2 = *reinterpret_cast<const uint2*>(stg + rr * 256 + (((lane >> 1) ^ (rr & 15)) << 4) +
-                                                                      (lane & 1) * 8);
-                    *reinterpret_cast<uint2*>(p.y_bf16 + static_cast<int64_t>(first + q * 32 + rr) * p.H + n0 +
-                                              lane * 4) = v2;
-                }
-                __syncwarp();
             } else if (valid) {
                 const int64_t row = first + i;
                 if constexpr (FC1) {
@@ -391,6 +431,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
+        if constexpr (kStageY) {
+            if (lane == 0) ptx::bulk_wait_all();  // tensor stores complete before the CTA exits
+            __syncwarp();
+        }
     }
 
     ptx::pdl_launch_dependents();
@@ -404,27 +448,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int TM, bool FC1, bool YBF16, int STAGES>
-cudaError_t launch_impl(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmParams& p, int grid,
-                        cudaStream_t stream, bool pdl) {
+cudaError_t launch_impl(const CUtensorMap& tmW, const CUtensorMap& tmX, const CUtensorMap& tmY, const GemmParams& p,
+                        int grid, cudaStream_t stream, bool pdl) {
     using C = Cfg<TM, STAGES, !FC1 && YBF16 && TM == 128>;
     auto kern = moe_gemm_kernel<TM, FC1, YBF16, STAGES>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (err != cudaSuccess) return err;
-    return launch_kernel(kern, dim3(grid), dim3(kThreads), C::kSmemBytes, stream, pdl, tmW, tmX, p);
+    return launch_kernel(kern, dim3(grid), dim3(kThreads), C::kSmemBytes, stream, pdl, tmW, tmX, tmY, p);
 }
 
 }  // namespace
 
-cudaError_t launch_gemm(bool fc1, const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmParams& p, int TM,
-                        int grid, cudaStream_t stream, bool pdl) {
+cudaError_t launch_gemm(bool fc1, const CUtensorMap& tmW, const CUtensorMap& tmX, const CUtensorMap& tmY,
+                        const GemmParams& p, int TM, int grid, cudaStream_t stream, bool pdl) {
     if (fc1) {
-        if (TM == 16) return launch_impl<16, true, false, 5>(tmW, tmX, p, grid, stream, pdl);
-        if (TM == 32) return launch_impl<32, true, false, 5>(tmW, tmX, p, grid, stream, pdl);
-        return launch_impl<128, true, true, 4>(tmW, tmX, p, grid, stream, pdl);
+        if (TM == 16) return launch_impl<16, true, false, kStagesDecFc1>(tmW, tmX, tmY, p, grid, stream, pdl);
+        if (TM == 32) return launch_impl<32, true, false, kStagesDecFc1>(tmW, tmX, tmY, p, grid, stream, pdl);
+        return launch_impl<128, true, true, kStagesPreFc1>(tmW, tmX, tmY, p, grid, stream, pdl);
     }
-    if (TM == 16) return launch_impl<16, false, false, 5>(tmW, tmX, p, grid, stream, pdl);
-    if (TM == 32) return launch_impl<32, false, false, 5>(tmW, tmX, p, grid, stream, pdl);
-    return launch_impl<128, false, true, 3>(tmW, tmX, p, grid, stream, pdl);
+    if (TM == 16) return launch_impl<16, false, false, kStagesDecFc2>(tmW, tmX, tmY, p, grid, stream, pdl);
+    if (TM == 32) return launch_impl<32, false, false, kStagesDecFc2>(tmW, tmX, tmY, p, grid, stream, pdl);
+    return launch_impl<128, false, true, kStagesPreFc2>(tmW, tmX, tmY, p, grid, stream, pdl);
 }
 
 }  // namespace moe

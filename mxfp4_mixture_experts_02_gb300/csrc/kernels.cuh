@@ -109,8 +109,10 @@ struct PackParams {
 cudaError_t launch_route(const RouteParams& p, cudaStream_t stream, bool pdl);
 cudaError_t launch_sort(const SortParams& p, cudaStream_t stream, bool pdl);
 cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream, bool pdl);
-cudaError_t launch_gemm(bool fc1, const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmParams& p, int TM,
-                        int grid, cudaStream_t stream, bool pdl);
+// tmY: bf16 FC2 rows as boxes of 64 columns x 32 rows (read only by the
+// 128-row FC2 tiling; any valid map otherwise).
+cudaError_t launch_gemm(bool fc1, const CUtensorMap& tmW, const CUtensorMap& tmX, const CUtensorMap& tmY,
+                        const GemmParams& p, int TM, int grid, cudaStream_t stream, bool pdl);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream, bool pdl);
 cudaError_t launch_quantize_mxfp4(const QuantParams& p, cudaStream_t stream);
 cudaError_t launch_pack_weights(const PackParams& p, cudaStream_t stream);
