@@ -137,7 +137,12 @@ int moe_quantize_mxfp4(const float* w, int64_t rows, int64_t K, uint8_t* codes, 
  *   packed_scales: two 512-byte blocks (block rows 0-127, 128-255), row r /
  *                  K-block j of the chunk at byte (r % 32) * 16 + (r / 32) * 4
  *                  + j (the tensor-memory scale layout, one tcgen05.cp each).
- * Sizes equal the inputs'.  N % 256 == 0, K % 128 == 0. */
+ * N % 256 == 0, K % 128 == 0.  Sizes: moe_packed_weight_bytes. */
+/* Rows per block (256) and the byte sizes of moe_pack_weights' outputs for
+ * one weight matrix per expert [experts, N, K] (equal to the inputs'). */
+int moe_packed_weight_bytes(int64_t experts, int64_t N, int64_t K, int32_t pair_halves, int32_t* block_rows,
+                            size_t* code_bytes, size_t* scale_bytes);
+
 int moe_pack_weights(const uint8_t* codes, const uint8_t* scales, int64_t experts, int64_t N, int64_t K,
                      int32_t pair_halves, uint8_t* packed_codes, uint8_t* packed_scales, moe_stream_t stream);
 

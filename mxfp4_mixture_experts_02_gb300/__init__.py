@@ -18,8 +18,9 @@ from . import build as _build
 
 __all__ = [
     "MoeShape", "MoeWeights", "MoeError", "lib", "moe_is_supported", "moe_workspace_bytes",
-    "moe_quantize_mxfp4", "moe_pack_weights", "moe_route", "moe_sort", "moe_forward",
-    "moe_layer", "moe_layer_host", "moe_layer_events", "moe_layer_noalloc", "moe_get_views", "moe_get_status", "moe_num_sms", "quantize_expert_weights",
+    "moe_quantize_mxfp4", "moe_packed_weight_bytes", "moe_pack_weights", "moe_route", "moe_sort", "moe_forward",
+    "moe_layer", "moe_layer_host", "moe_layer_events", "moe_layer_noalloc", "moe_get_views", "moe_get_status",
+    "moe_num_sms", "quantize_expert_weights",
     "workspace", "MOE_OK", "MOE_ERR_TIMEOUT", "MOE_ERR_WORKSPACE",
 ]
 
@@ -94,6 +95,8 @@ _SIGS = {
     "moe_workspace_bytes": [ctypes.c_void_p, ctypes.c_void_p],
     "moe_quantize_mxfp4": [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
                            ctypes.c_void_p],
+    "moe_packed_weight_bytes": [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p,
+                                ctypes.c_void_p, ctypes.c_void_p],
     "moe_pack_weights": [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                          ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p],
     "moe_route": [ctypes.c_void_p] * 6,
@@ -187,14 +190,26 @@ def moe_quantize_mxfp4(w: torch.Tensor):
     return codes, scales
 
 
+def moe_packed_weight_bytes(experts: int, N: int, K: int, pair_halves: bool):
+    """(rows per block, packed code bytes, packed scale bytes) of one weight
+    matrix per expert [experts, N, K] (see moe_api.h)."""
+    rb = ctypes.c_int32()
+    nc = ctypes.c_size_t()
+    ns = ctypes.c_size_t()
+    _call("moe_packed_weight_bytes", experts, N, K, 1 if pair_halves else 0, ctypes.byref(rb), ctypes.byref(nc),
+          ctypes.byref(ns))
+    return rb.value, nc.value, ns.value
+
+
 def moe_pack_weights(codes: torch.Tensor, scales: torch.Tensor, pair_halves: bool):
     """Row-major MXFP4 of one weight matrix per expert -- codes uint8 [E, N, K/2],
     scales uint8 [E, N, K/32] -- to the tile-major layout the GEMMs stream
     (see moe_api.h).  Returns (packed_codes, packed_scales), flat uint8."""
     _check_cuda(codes, scales)
     E, N, K2 = codes.shape
-    pc = torch.empty(codes.numel(), dtype=torch.uint8, device=codes.device)
-    ps = torch.empty(scales.numel(), dtype=torch.uint8, device=codes.device)
+    _, nc, ns = moe_packed_weight_bytes(E, N, 2 * K2, pair_halves)
+    pc = torch.empty(nc, dtype=torch.uint8, device=codes.device)
+    ps = torch.empty(ns, dtype=torch.uint8, device=codes.device)
     _call("moe_pack_weights", codes.data_ptr(), scales.data_ptr(), E, N, 2 * K2, 1 if pair_halves else 0,
           pc.data_ptr(), ps.data_ptr(), _stream(codes.device))
     return pc, ps

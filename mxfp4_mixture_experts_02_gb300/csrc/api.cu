@@ -226,10 +226,21 @@ int moe_quantize_mxfp4(const float* w, int64_t rows, int64_t K, uint8_t* codes, 
     return cuda_rc(launch_quantize_mxfp4(p, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int moe_packed_weight_bytes(int64_t experts, int64_t N, int64_t K, int32_t pair_halves, int32_t* block_rows,
+                            size_t* code_bytes, size_t* scale_bytes) {
+    (void)pair_halves;
+    if (experts <= 0 || N <= 0 || K <= 0 || K % 128 || N % 256) return MOE_ERR_SHAPE;
+    if (block_rows) *block_rows = 256;
+    if (code_bytes) *code_bytes = static_cast<size_t>(experts) * N * (K / 2);
+    if (scale_bytes) *scale_bytes = static_cast<size_t>(experts) * N * (K / 32);
+    return MOE_OK;
+}
+
 int moe_pack_weights(const uint8_t* codes, const uint8_t* scales, int64_t experts, int64_t N, int64_t K,
                      int32_t pair_halves, uint8_t* packed_codes, uint8_t* packed_scales, moe_stream_t stream) {
     if (!codes || !scales || !packed_codes || !packed_scales) return MOE_ERR_NULL;
-    if (experts <= 0 || N <= 0 || K <= 0 || K % 128 || N % 256) return MOE_ERR_SHAPE;
+    int rc = moe_packed_weight_bytes(experts, N, K, pair_halves, nullptr, nullptr, nullptr);
+    if (rc) return rc;
     if (!aligned(codes, 16) || !aligned(packed_codes, 16)) return MOE_ERR_ALIGN;
     PackParams p{codes, scales, packed_codes, packed_scales, experts, N, K, pair_halves ? 1 : 0};
     return cuda_rc(launch_pack_weights(p, reinterpret_cast<cudaStream_t>(stream)));

@@ -35,6 +35,10 @@ GRID = [
     SMALL.replace(T=256, block_n=32, num_shared=1, zipf_s=1.1, hidden=1536, inter=384),
     SMALL.replace(T=200, block_n=128, top_k=8, num_shared=1, zipf_s=1.1),
     SMALL.replace(T=64, block_n=128, E_local=32, expert_offset=32, hidden=1536, inter=384),
+    # the layer's own hidden size at small E: decode and 128-row tilings with
+    # several items per CTA, full and cut 32-row slabs
+    SMALL.replace(T=40, block_n=32, E_global=16, E_local=16, hidden=3584, inter=256),
+    SMALL.replace(T=1200, block_n=128, E_global=8, E_local=8, top_k=2, hidden=3584, inter=128),
     synth.CONFIGS["tiny"],
 ]
 FULL = [synth.CONFIGS[n] for n in ("decode_t32", "ep_slice_t64", "skewed_shared_t256", "prefill_t32768")]

@@ -76,3 +76,12 @@ def test_host_side_errors_launch_nothing():
     assert L.moe_pack_weights(16, 16, 2, 100, 128, 0, 16, 16, None) == -2
     assert L.moe_pack_weights(16, 16, 2, 128, 128, 1, 16, 16, None) == -2
     assert L.moe_quantize_mxfp4(16, 4, 33, 16, 16, None) == -2
+
+
+def test_packed_weight_sizes():
+    # 256-row blocks; packed sizes equal the row-major inputs'
+    assert moe.moe_packed_weight_bytes(2, 3584, 384, False) == (256, 2 * 3584 * 192, 2 * 3584 * 12)
+    assert moe.moe_packed_weight_bytes(3, 768, 3584, True) == (256, 3 * 768 * 1792, 3 * 768 * 112)
+    for bad in [(2, 100, 384, False), (2, 448, 384, True), (2, 512, 100, False), (0, 512, 384, False)]:
+        with pytest.raises(moe.MoeError):
+            moe.moe_packed_weight_bytes(*bad)
