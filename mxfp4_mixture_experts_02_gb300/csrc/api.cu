@@ -96,9 +96,34 @@ int run_sort(const moe_shape* s, const int32_t* ids, void* ws, cudaStream_t st, 
     return cuda_rc(launch_sort(p, st, pdl));
 }
 
+// Route then sort, fused into one launch when the batch has at most 1024
+// slots.  `ev` (optional) gets events 1 (routed) and 2 (sorted); fused, both
+// are recorded after the one kernel.
+int run_route_sort(const moe_shape* s, const float* logits, const uint16_t* shared_logit, int32_t* ids, float* w,
+                   void* ws, cudaStream_t st, void* const* ev);
+
 // Records events[i] on the stream when an events array is given.
 inline bool rec(void* const* ev, int i, cudaStream_t st) {
     return !ev || cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), st) == cudaSuccess;
+}
+
+int run_route_sort(const moe_shape* s, const float* logits, const uint16_t* shared_logit, int32_t* ids, float* w,
+                   void* ws, cudaStream_t st, void* const* ev) {
+    const Dims d = make_dims(*s);
+    if (route_sort_fusable(d.T, d.kp)) {
+        const Layout L = make_layout(d);
+        RouteParams rp{logits, shared_logit, ids, w, d.T, d.Eg, d.k, d.S, d.kp, d.shared_scale};
+        SortParams sp{ids, at<int32_t>(ws, L.header), at<int32_t>(ws, L.counts), at<int32_t>(ws, L.offsets),
+                      at<int4>(ws, L.vinfo), at<int4>(ws, L.groups), at<int32_t>(ws, L.a_map), at<int32_t>(ws, L.c_map),
+                      at<int32_t>(ws, L.sort_hist), d.T, d.kp, d.Eg, d.E, d.off, d.S, d.Et, d.B, d.G};
+        if (launch_route_sort_small(rp, sp, st, false) != cudaSuccess) return MOE_ERR_CUDA;
+        return (rec(ev, 1, st) && rec(ev, 2, st)) ? MOE_OK : MOE_ERR_CUDA;
+    }
+    int rc = run_route(s, logits, shared_logit, ids, w, st, false);
+    if (rc) return rc;
+    if (!rec(ev, 1, st)) return MOE_ERR_CUDA;
+    if ((rc = run_sort(s, ids, ws, st, ev == nullptr))) return rc;
+    return rec(ev, 2, st) ? MOE_OK : MOE_ERR_CUDA;
 }
 
 int run_forward(const moe_shape* s, const uint16_t* x, const moe_weights* wt, const float* topk_w, void* ws,
@@ -284,8 +309,7 @@ int moe_layer(const moe_shape* s, const float* logits, const uint16_t* shared_lo
     if ((rc = check_weights(w))) return rc;
     if ((rc = check_ws(s, ws, ws_bytes))) return rc;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if ((rc = run_route(s, logits, shared_logit, topk_ids, topk_w, st, false))) return rc;
-    if ((rc = run_sort(s, topk_ids, ws, st, true))) return rc;
+    if ((rc = run_route_sort(s, logits, shared_logit, topk_ids, topk_w, ws, st, nullptr))) return rc;
     return run_forward(s, x, w, topk_w, ws, out, st, true);
 }
 
@@ -304,10 +328,7 @@ int moe_layer_events(const moe_shape* s, const float* logits, const uint16_t* sh
     if ((rc = check_ws(s, ws, ws_bytes))) return rc;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (!rec(events, 0, st)) return MOE_ERR_CUDA;
-    if ((rc = run_route(s, logits, shared_logit, topk_ids, topk_w, st, false))) return rc;
-    if (!rec(events, 1, st)) return MOE_ERR_CUDA;
-    if ((rc = run_sort(s, topk_ids, ws, st, false))) return rc;
-    if (!rec(events, 2, st)) return MOE_ERR_CUDA;
+    if ((rc = run_route_sort(s, logits, shared_logit, topk_ids, topk_w, ws, st, events))) return rc;
     return run_forward(s, x, w, topk_w, ws, out, st, false, events);
 }
 
@@ -336,8 +357,7 @@ int moe_layer_host(const moe_shape* s, const float* logits_host, const uint16_t*
         return MOE_ERR_CUDA;
     int32_t* ids = at<int32_t>(ws, L.st_ids);
     float* tw = at<float>(ws, L.st_w);
-    if ((rc = run_route(s, lg, d.S > 0 ? sl : nullptr, ids, tw, st, false))) return rc;
-    if ((rc = run_sort(s, ids, ws, st, true))) return rc;
+    if ((rc = run_route_sort(s, lg, d.S > 0 ? sl : nullptr, ids, tw, ws, st, nullptr))) return rc;
     if ((rc = run_forward(s, xd, w, tw, ws, od, st, true))) return rc;
     if (cudaMemcpyAsync(out_host, od, size_t(d.T) * d.H * 2, cudaMemcpyDeviceToHost, st) != cudaSuccess)
         return MOE_ERR_CUDA;

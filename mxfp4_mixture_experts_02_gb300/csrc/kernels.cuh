@@ -108,6 +108,9 @@ struct PackParams {
 
 cudaError_t launch_route(const RouteParams& p, cudaStream_t stream, bool pdl);
 cudaError_t launch_sort(const SortParams& p, cudaStream_t stream, bool pdl);
+// Route + sort fused in one CTA, for batches of at most 1024 slots.
+bool route_sort_fusable(int T, int kp);
+cudaError_t launch_route_sort_small(const RouteParams& rp, const SortParams& p, cudaStream_t stream, bool pdl);
 cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream, bool pdl);
 // tmY: bf16 FC2 rows as boxes of 64 columns x 32 rows (read only by the
 // 128-row FC2 tiling; any valid map otherwise).

@@ -18,6 +18,7 @@
 #include "common.cuh"
 #include "kernels.cuh"
 #include "ptx.cuh"
+#include "route_sort.cuh"
 
 namespace moe {
 
@@ -25,91 +26,8 @@ namespace {
 
 constexpr int kSortThreads = 1024;
 constexpr int kSortWarps = kSortThreads / 32;
-
-__device__ __forceinline__ int local_expert(int32_t id, const SortParams& p) {
-    if (id >= p.Eg && id < p.Eg + p.S) return p.E + (id - p.Eg);
-    if (id >= p.off && id < p.off + p.E) return id - p.off;
-    return -1;
-}
-
-// Exclusive scan of three ints across the block (one expert per thread).
-__device__ __forceinline__ void block_scan3(int a, int b, int c, int& ea, int& eb, int& ec, int& ta, int& tb, int& tc,
-                                            int (*s_tot)[kSortWarps]) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int ia = a, ib = b, ic = c;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int xa = __shfl_up_sync(0xffffffffu, ia, o);
-        const int xb = __shfl_up_sync(0xffffffffu, ib, o);
-        const int xc = __shfl_up_sync(0xffffffffu, ic, o);
-        if (lane >= o) {
-            ia += xa;
-            ib += xb;
-            ic += xc;
-        }
-    }
-    if (lane == 31) {
-        s_tot[0][warp] = ia;
-        s_tot[1][warp] = ib;
-        s_tot[2][warp] = ic;
-    }
-    __syncthreads();
-    if (warp == 0) {
-        int va = s_tot[0][lane], vb = s_tot[1][lane], vc = s_tot[2][lane];
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int xa = __shfl_up_sync(0xffffffffu, va, o);
-            const int xb = __shfl_up_sync(0xffffffffu, vb, o);
-            const int xc = __shfl_up_sync(0xffffffffu, vc, o);
-            if (lane >= o) {
-                va += xa;
-                vb += xb;
-                vc += xc;
-            }
-        }
-        s_tot[0][lane] = va;  // inclusive prefix of warp totals
-        s_tot[1][lane] = vb;
-        s_tot[2][lane] = vc;
-    }
-    __syncthreads();
-    const int pa = warp ? s_tot[0][warp - 1] : 0;
-    const int pb = warp ? s_tot[1][warp - 1] : 0;
-    const int pc = warp ? s_tot[2][warp - 1] : 0;
-    ea = pa + ia - a;
-    eb = pb + ib - b;
-    ec = pc + ic - c;
-    ta = s_tot[0][kSortWarps - 1];
-    tb = s_tot[1][kSortWarps - 1];
-    tc = s_tot[2][kSortWarps - 1];
-}
-
-// Expert-level part shared by both paths (one CTA of kSortThreads, thread
-// tid = expert): given each expert's row count, scan (count, tiles, groups),
-// write counts / offsets / virtual experts / work groups and the header, and
-// leave each expert's first row in s_off.
-__device__ __forceinline__ void place_experts(const SortParams& p, int cnt, int* s_off, int (*s_tot)[kSortWarps]) {
-    const int tid = threadIdx.x;
-    const int tiles = (cnt + p.B - 1) / p.B;
-    const int grps = (tiles + p.G - 1) / p.G;
-    int off, vb, gb, R, V, NG;
-    block_scan3(cnt, tiles, grps, off, vb, gb, R, V, NG, s_tot);
-    if (tid < p.Et) {
-        if (s_off) s_off[tid] = off;
-        p.counts[tid] = cnt;
-        p.offsets[tid] = off;
-        for (int c = 0; c < tiles; ++c)
-            p.vinfo[vb + c] = make_int4(tid, off + c * p.B, min(p.B, cnt - c * p.B), c);
-        for (int g = 0; g < grps; ++g) p.groups[gb + g] = make_int4(tid, vb + g * p.G, min(p.G, tiles - g * p.G), 0);
-    }
-    if (tid == 0) {
-        p.offsets[p.Et] = R;
-        p.header[kHdrRows] = R;
-        p.header[kHdrNumV] = V;
-        p.header[kHdrNumGroups] = NG;
-        p.header[kHdrStatus] = 0;
-        p.header[kHdrDetail] = 0;
-    }
-}
+using rs::local_expert;
+using rs::place_experts;
 
 // Per-warp histogram of the slots [s0, s1) into my_hist (rounds of 32).
 __device__ __forceinline__ void warp_count(const SortParams& p, int s0, int s1, int* my_hist) {
@@ -150,7 +68,7 @@ __global__ void __launch_bounds__(kSortThreads, 1) sort_kernel(SortParams p) {
     extern __shared__ int s_dyn[];
     int* hist = s_dyn;                       // [32][Et]: per-warp counts, then per-warp bases
     int* s_off = s_dyn + kSortWarps * p.Et;  // [Et]
-    __shared__ int s_tot[3][kSortWarps];
+    __shared__ int s_tot[3][rs::kScanWarps];
 
     const int tid = threadIdx.x, warp = tid >> 5;
     for (int i = tid; i < kSortWarps * p.Et; i += kSortThreads) hist[i] = 0;
@@ -184,6 +102,79 @@ __global__ void __launch_bounds__(kSortThreads, 1) sort_kernel(SortParams p) {
     ptx::pdl_launch_dependents();
 }
 
+// Route and sort in one CTA when the batch has at most kSmallSlots slots
+// (decode): warps route tokens w, w + 32, ... into shared memory; then the
+// (local expert, slot) keys -- masked or foreign ids as expert 2047 -- are
+// sorted ascending by a block-wide bitonic sort, so position p of a routed
+// key is its row (experts in order, slots ascending inside each expert: the
+// same rows as the counting passes below); an expert's count is the width of
+// its key range, found by binary search.
+constexpr int kSmallSlots = 1024;
+
+__device__ __forceinline__ int lower_bound_u32(const uint32_t* a, int n, uint32_t x) {
+    int lo = 0, hi = n;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (a[mid] < x)
+            lo = mid + 1;
+        else
+            hi = mid;
+    }
+    return lo;
+}
+
+__global__ void __launch_bounds__(kSortThreads, 1) route_sort_small_kernel(RouteParams rp, SortParams p) {
+    __shared__ uint2 s_cand[kSortWarps][rs::kMaxCand];
+    __shared__ int s_ids[kSmallSlots];
+    __shared__ uint32_t s_key[kSmallSlots];
+    __shared__ int s_tot[3][rs::kScanWarps];
+    ptx::pdl_wait();
+    const int tid = threadIdx.x, warp = tid >> 5;
+    for (int t = warp; t < rp.T; t += kSortWarps) rs::route_token(rp, t, s_cand[warp], s_ids);
+    __syncthreads();
+
+    const int n = p.T * p.kp;
+    int npow = 1;
+    while (npow < n) npow <<= 1;
+    if (tid < npow) {
+        uint32_t key = 0xFFFFFFFFu;
+        if (tid < n) {
+            const int e = local_expert(s_ids[tid], p);
+            key = (static_cast<uint32_t>(e < 0 ? 2047 : e) << 10) | static_cast<uint32_t>(tid);
+        }
+        s_key[tid] = key;
+    }
+    __syncthreads();
+    for (int size = 2; size <= npow; size <<= 1)
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            const int partner = tid ^ stride;
+            if (tid < npow && partner > tid) {
+                const uint32_t a = s_key[tid], b = s_key[partner];
+                if ((a > b) == ((tid & size) == 0)) {
+                    s_key[tid] = b;
+                    s_key[partner] = a;
+                }
+            }
+            __syncthreads();
+        }
+    if (tid < n) {
+        const uint32_t key = s_key[tid];
+        const int e = static_cast<int>(key >> 10), slot = static_cast<int>(key & 1023u);
+        if (e < p.Et) {
+            p.a_map[tid] = slot;
+            p.c_map[slot] = tid;
+        } else {
+            p.c_map[slot] = -1;
+        }
+    }
+    int cnt = 0;
+    if (tid < p.Et)
+        cnt = lower_bound_u32(s_key, n, static_cast<uint32_t>(tid + 1) << 10) -
+              lower_bound_u32(s_key, n, static_cast<uint32_t>(tid) << 10);
+    place_experts(p, cnt, nullptr, s_tot);
+    ptx::pdl_launch_dependents();
+}
+
 // Large slot counts: CTA c owns slots [c * kBigChunk, (c + 1) * kBigChunk),
 // warp w of it the w-th sub-run of kBigWarpSlots.
 constexpr int kBigWarps = 8;
@@ -213,7 +204,7 @@ __global__ void __launch_bounds__(kBigWarps * 32) sort_count_kernel(SortParams p
 // Pass 2 (one CTA): per expert, exclusive prefix over CTAs in place and the
 // total; then the expert-level placement.
 __global__ void __launch_bounds__(kSortThreads, 1) sort_scan_kernel(SortParams p, int nctas) {
-    __shared__ int s_tot[3][kSortWarps];
+    __shared__ int s_tot[3][rs::kScanWarps];
     ptx::pdl_wait();
     const int tid = threadIdx.x;
     int cnt = 0;
@@ -278,6 +269,12 @@ cudaError_t launch_sort(const SortParams& p, cudaStream_t stream, bool pdl) {
     err = launch_kernel(sort_scan_kernel, dim3(1), dim3(kSortThreads), 0, stream, true, p, nctas);
     if (err != cudaSuccess) return err;
     return launch_kernel(sort_rank_kernel, dim3(nctas), dim3(kBigWarps * 32), smem, stream, true, p);
+}
+
+bool route_sort_fusable(int T, int kp) { return static_cast<int64_t>(T) * kp <= kSmallSlots; }
+
+cudaError_t launch_route_sort_small(const RouteParams& rp, const SortParams& p, cudaStream_t stream, bool pdl) {
+    return launch_kernel(route_sort_small_kernel, dim3(1), dim3(kSortThreads), 0, stream, pdl, rp, p);
 }
 
 }  // namespace moe

@@ -212,6 +212,69 @@ def test_synth_generators_agree():
     np.testing.assert_array_equal(synth.x_host(cfg), bf16_bits(synth.x_device(cfg)))
 
 
+def _tie_logits(T, Eg, seed, coarse):
+    """Logits on a 0.5 grid (coarse: heavy ties at the top, the selection's
+    fallback path) or plain normal draws (its candidate path)."""
+    rng = np.random.default_rng(seed)
+    lg = rng.normal(0, 1, (T, Eg))
+    if coarse:
+        lg = np.round(lg * 2) / 2
+    return lg.astype(np.float32)
+
+
+def _check_sort_views(shape, ws, ref, T, kp):
+    v = moe.moe_get_views(shape, ws)
+    R = int(ref["offsets"][-1])
+    hdr = v["header"].cpu().numpy()
+    assert hdr[0] == R and hdr[1] == ref["num_v"] and hdr[3] == 0
+    np.testing.assert_array_equal(v["expert_counts"].cpu().numpy(), ref["counts"])
+    np.testing.assert_array_equal(v["expert_offsets"].cpu().numpy(), ref["offsets"])
+    np.testing.assert_array_equal(v["c_map"].cpu().numpy()[:T * kp], ref["c_map"])
+    np.testing.assert_array_equal(v["a_map"].cpu().numpy()[:R], ref["a_map"])
+    np.testing.assert_array_equal(v["vinfo"].cpu().numpy()[:ref["num_v"]], ref["vinfo"])
+
+
+@pytest.mark.parametrize("Eg,k,coarse", [(8, 2, True), (33, 5, False), (896, 16, True), (896, 16, False),
+                                         (1024, 32, True), (1024, 32, False), (640, 1, True)])
+def test_route_kernel_exact_with_and_without_ties(Eg, k, coarse):
+    T = 300
+    lg = _tie_logits(T, Eg, Eg + k, coarse)
+    shape = moe.MoeShape(T=T, max_T=T, E_global=Eg, E_local=Eg, expert_offset=0, top_k=k, num_shared=0,
+                         hidden=512, inter=128, block_n=32)
+    ids, w = moe.moe_route(shape, torch.from_numpy(lg).cuda())
+    torch.cuda.synchronize()
+    oids, ow = oracle.route(lg, k)
+    np.testing.assert_array_equal(ids.cpu().numpy(), oids)
+    wg = w.cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(wg - ow) <= 4e-6 * np.abs(ow) + 1e-7)
+
+
+@pytest.mark.parametrize("T,coarse,S", [(32, True, 0), (64, False, 0), (48, True, 1), (7, False, 1)])
+def test_fused_and_split_route_sort_agree_with_oracle(T, coarse, S):
+    # T * k' <= 1024: moe_layer routes and sorts in one kernel; moe_route +
+    # moe_sort run the split kernels.  Both must give the oracle's maps.
+    cfg = SMALL.replace(T=T, top_k=16, num_shared=S, E_local=64, block_n=32)
+    shape = shape_of(cfg)
+    assert shape.T * shape.kp <= 1024
+    lg = _tie_logits(T, cfg.E_global, T + S, coarse)
+    x, _, sl = device_inputs(cfg)
+    oids, ow = oracle.route(lg, cfg.top_k, S, synth.shared_logit_host(cfg) if S else None, cfg.shared_scale)
+    ref = oracle.sort(oids, cfg.E_global, cfg.E_local, cfg.expert_offset, S, cfg.block_n)
+    lgd = torch.from_numpy(lg).cuda()
+    ws = moe.workspace(shape)
+    _, ids, w = moe.moe_layer(shape, lgd, sl, x, _weights(cfg), ws)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(ids.cpu().numpy(), oids)
+    assert np.all(np.abs(w.cpu().numpy() - ow) <= 4e-6 * np.abs(ow) + 1e-7)
+    _check_sort_views(shape, ws, ref, T, shape.kp)
+    ws2 = moe.workspace(shape)
+    ids2, _ = moe.moe_route(shape, lgd, sl)
+    moe.moe_sort(shape, ids2, ws2)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(ids2.cpu().numpy(), oids)
+    _check_sort_views(shape, ws2, ref, T, shape.kp)
+
+
 def test_deterministic_and_status_ok():
     cfg = GRID[3]
     _, ws, out1, _, _, st = run_layer(cfg)
