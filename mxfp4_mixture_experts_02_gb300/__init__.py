@@ -20,7 +20,7 @@ __all__ = [
     "MoeShape", "MoeWeights", "MoeError", "lib", "moe_is_supported", "moe_workspace_bytes",
     "moe_quantize_mxfp4", "moe_packed_weight_bytes", "moe_pack_weights", "moe_route", "moe_sort", "moe_forward",
     "moe_layer", "moe_layer_host", "moe_layer_events", "moe_layer_noalloc", "moe_get_views", "moe_get_status",
-    "moe_num_sms", "quantize_expert_weights",
+    "moe_num_sms", "moe_layer_launch_count", "quantize_expert_weights",
     "workspace", "MOE_OK", "MOE_ERR_TIMEOUT", "MOE_ERR_WORKSPACE",
 ]
 
@@ -109,6 +109,7 @@ _SIGS = {
     "moe_get_views": [ctypes.c_void_p] * 3,
     "moe_get_status": [ctypes.c_void_p] * 3,
     "moe_num_sms": [ctypes.c_void_p],
+    "moe_layer_launch_count": [ctypes.c_void_p, ctypes.c_void_p],
 }
 
 
@@ -165,6 +166,14 @@ def moe_workspace_bytes(shape: MoeShape) -> int:
     s = shape.c()
     n = ctypes.c_size_t(0)
     _call("moe_workspace_bytes", ctypes.byref(s), ctypes.byref(n))
+    return n.value
+
+
+def moe_layer_launch_count(shape: MoeShape) -> int:
+    """Kernel launches moe_layer issues for this shape."""
+    n = ctypes.c_int32()
+    s = shape.c()
+    _call("moe_layer_launch_count", ctypes.byref(s), ctypes.byref(n))
     return n.value
 
 

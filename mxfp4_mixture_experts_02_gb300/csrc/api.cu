@@ -405,4 +405,15 @@ int moe_num_sms(int32_t* n) {
     return *n > 0 ? MOE_OK : MOE_ERR_CUDA;
 }
 
+int moe_layer_launch_count(const moe_shape* s, int32_t* count) {
+    int rc = check_shape(s);
+    if (rc) return rc;
+    if (!count) return MOE_ERR_NULL;
+    const Dims d = make_dims(*s);
+    int n = route_sort_fusable(d.T, d.kp) ? 1 : 1 + sort_launch_count(static_cast<int64_t>(d.T) * d.kp);
+    if (d.T > 0) n += (d.mode == kModePrefill ? 2 : 1) + 3;
+    *count = n;
+    return MOE_OK;
+}
+
 }  // extern "C"

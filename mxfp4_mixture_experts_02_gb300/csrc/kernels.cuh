@@ -110,6 +110,8 @@ cudaError_t launch_route(const RouteParams& p, cudaStream_t stream, bool pdl);
 cudaError_t launch_sort(const SortParams& p, cudaStream_t stream, bool pdl);
 // Route + sort fused in one CTA, for batches of at most 1024 slots.
 bool route_sort_fusable(int T, int kp);
+// Kernels launch_sort issues for T*k' slots (1, or 3 above one CTA's share).
+int sort_launch_count(int64_t slots);
 cudaError_t launch_route_sort_small(const RouteParams& rp, const SortParams& p, cudaStream_t stream, bool pdl);
 cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream, bool pdl);
 // tmY: bf16 FC2 rows as boxes of 64 columns x 32 rows (read only by the

@@ -271,6 +271,8 @@ cudaError_t launch_sort(const SortParams& p, cudaStream_t stream, bool pdl) {
     return launch_kernel(sort_rank_kernel, dim3(nctas), dim3(kBigWarps * 32), smem, stream, true, p);
 }
 
+int sort_launch_count(int64_t slots) { return slots <= kSortWarps * kBigWarpSlots ? 1 : 3; }
+
 bool route_sort_fusable(int T, int kp) { return static_cast<int64_t>(T) * kp <= kSmallSlots; }
 
 cudaError_t launch_route_sort_small(const RouteParams& rp, const SortParams& p, cudaStream_t stream, bool pdl) {

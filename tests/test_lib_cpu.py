@@ -85,3 +85,14 @@ def test_packed_weight_sizes():
     for bad in [(2, 100, 384, False), (2, 448, 384, True), (2, 512, 100, False), (0, 512, 384, False)]:
         with pytest.raises(moe.MoeError):
             moe.moe_packed_weight_bytes(*bad)
+
+
+def test_layer_launch_count():
+    # decode: fused route+sort, gather, FC1, FC2, combine
+    assert moe.moe_layer_launch_count(_shape()) == 5
+    # 256 tokens x 16 picks > 1024 slots: route, one-CTA sort, then 4
+    assert moe.moe_layer_launch_count(_shape(T=256, max_T=256)) == 6
+    # prefill tiling at 32768 tokens: route, 3-kernel sort, 2-kernel gather, FC1, FC2, combine
+    assert moe.moe_layer_launch_count(_shape(T=32768, max_T=32768, block_n=128)) == 9
+    assert moe.moe_layer_launch_count(_shape(T=0)) == 1
+
