@@ -55,6 +55,10 @@ namespace {
 #ifndef MOE_STAGES_PRE_FC2
 #define MOE_STAGES_PRE_FC2 3
 #endif
+#ifndef MOE_ITEM_CONTIG
+#define MOE_ITEM_CONTIG 0
+#endif
+constexpr bool kItemContig = MOE_ITEM_CONTIG != 0;
 constexpr int kStagesDecFc1 = MOE_STAGES_DEC_FC1;
 constexpr int kStagesDecFc2 = MOE_STAGES_DEC_FC2;
 constexpr int kStagesPreFc1 = MOE_STAGES_PRE_FC1;
@@ -174,6 +178,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int NB = FC1 ? p.I / 128 : p.H / 256;  // 256-row weight blocks per expert
     const int KC = FC1 ? p.H / 128 : p.I / 128;  // 128-wide K chunks
     const int nitems = num_v * NB;
+    // This CTA's items: it0, it0 + istep, ... below iend (round-robin over the
+    // grid, or one contiguous range per CTA).
+    int it0, istep, iend;
+    if (kItemContig) {
+        const int per = (nitems + gridDim.x - 1) / gridDim.x;
+        it0 = blockIdx.x * per;
+        istep = 1;
+        iend = min(nitems, it0 + per);
+    } else {
+        it0 = blockIdx.x;
+        istep = gridDim.x;
+        iend = nitems;
+    }
 
     if (warp == kProducerWarp) {
         if (lane == 0) {
@@ -200,13 +217,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                                    &full[j]);
                 }
             };
-            int4 vi_next = blockIdx.x < nitems ? p.vinfo[blockIdx.x / NB] : make_int4(0, 0, 0, 0);
-            for (int it = blockIdx.x; ok && it < nitems; it += gridDim.x) {
+            // descriptors of the next three items in flight (an FC2 item streams
+            // only I/128 stages, less than an L2 round trip under load)
+            const int g = istep;
+            const int4 kNone = make_int4(0, 0, 0, 0);
+            int4 vq0 = it0 < iend ? p.vinfo[it0 / NB] : kNone;
+            int4 vq1 = it0 + g < iend ? p.vinfo[(it0 + g) / NB] : kNone;
+            int4 vq2 = it0 + 2 * g < iend ? p.vinfo[(it0 + 2 * g) / NB] : kNone;
+            for (int it = it0; ok && it < iend; it += g) {
                 const int v = it / NB, nb = it - v * NB;
-                const int4 vi = vi_next;
-                // next item's descriptor, in flight while this item streams
-                const int itn = it + gridDim.x;
-                if (itn < nitems) vi_next = p.vinfo[itn / NB];
+                const int4 vi = vq0;
+                vq0 = vq1;
+                vq1 = vq2;
+                vq2 = (it + 3 * g < iend) ? p.vinfo[(it + 3 * g) / NB] : kNone;
                 const int e = vi.x, first = vi.y;
                 const int64_t tile0 = (static_cast<int64_t>(e) * NB + nb) * KC;
                 for (int kc = 0; kc < KC; ++kc) {
@@ -251,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t kIdesc = ptx::idesc_mx(ptx::kFmtE4M3, ptx::kFmtE2M1, 128, 256);
             uint32_t stage = 0, phase = 0, aphase = 0;
             bool ok = true;
-            for (int it = blockIdx.x; ok && it < nitems; it += gridDim.x) {
+            for (int it = it0; ok && it < iend; it += istep) {
                 if (!wait_or_abort(accempty, aphase ^ 1, p.wait_ns, abort_flag)) {
                     if (!*abort_flag) record_timeout(p, abort_flag, kSiteMmaAccEmpty);
                     break;
@@ -297,15 +320,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Descriptors two items ahead and row weights one item ahead are
         // loaded early, so no dependent load chain sits between two items.
         const int4 kNoTile = make_int4(0, 0, 0, 0);
-        const int g = gridDim.x;
-        int4 vi_cur = (active && blockIdx.x < nitems) ? p.vinfo[blockIdx.x / NB] : kNoTile;
-        int4 vi_nxt = (active && blockIdx.x + g < nitems) ? p.vinfo[(blockIdx.x + g) / NB] : kNoTile;
+        const int g = istep;
+        int4 vi_cur = (active && it0 < iend) ? p.vinfo[it0 / NB] : kNoTile;
+        int4 vi_nxt = (active && it0 + g < iend) ? p.vinfo[(it0 + g) / NB] : kNoTile;
         float w_cur = (!FC1 && i < vi_cur.z) ? p.row_w[vi_cur.y + i] : 0.f;
-        for (int it = blockIdx.x; active && it < nitems; it += g) {
+        for (int it = it0; active && it < iend; it += g) {
             const int v = it / NB, nb = it - v * NB;
             const int4 vi = vi_cur;
             const float w_row = w_cur;
-            const int4 vi_n2 = (it + 2 * g < nitems) ? p.vinfo[(it + 2 * g) / NB] : kNoTile;
+            const int4 vi_n2 = (it + 2 * g < iend) ? p.vinfo[(it + 2 * g) / NB] : kNoTile;
             w_cur = (!FC1 && i < vi_nxt.z) ? p.row_w[vi_nxt.y + i] : 0.f;
             vi_cur = vi_nxt;
             vi_nxt = vi_n2;

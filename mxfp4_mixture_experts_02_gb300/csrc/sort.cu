@@ -20,6 +20,8 @@
 #include "ptx.cuh"
 #include "route_sort.cuh"
 
+#include <cooperative_groups.h>
+
 namespace moe {
 
 namespace {
@@ -102,14 +104,18 @@ __global__ void __launch_bounds__(kSortThreads, 1) sort_kernel(SortParams p) {
     ptx::pdl_launch_dependents();
 }
 
-// Route and sort in one CTA when the batch has at most kSmallSlots slots
-// (decode): warps route tokens w, w + 32, ... into shared memory; then the
-// (local expert, slot) keys -- masked or foreign ids as expert 2047 -- are
-// sorted ascending by a block-wide bitonic sort, so position p of a routed
-// key is its row (experts in order, slots ascending inside each expert: the
-// same rows as the counting passes below); an expert's count is the width of
-// its key range, found by binary search.
+// Route and sort in one launch when the batch has at most kSmallSlots slots
+// (decode).  A cluster of kRouteCtas CTAs routes the tokens (token t on CTA
+// t % kRouteCtas, so the routing spreads over that many SMs) and stores the
+// picked ids straight into CTA 0's shared memory; after the cluster barrier
+// CTA 0 sorts the (local expert, slot) keys -- masked or foreign ids as
+// expert 2047 -- ascending with a bitonic network (shuffles for strides
+// below 32, shared memory above), so position p of a routed key is its row
+// (experts in order, slots ascending inside each expert: the same rows as
+// the counting passes below); an expert's count is the width of its key
+// range, found by binary search.
 constexpr int kSmallSlots = 1024;
+constexpr int kRouteCtas = 8;
 
 __device__ __forceinline__ int lower_bound_u32(const uint32_t* a, int n, uint32_t x) {
     int lo = 0, hi = n;
@@ -123,42 +129,49 @@ __device__ __forceinline__ int lower_bound_u32(const uint32_t* a, int n, uint32_
     return lo;
 }
 
-__global__ void __launch_bounds__(kSortThreads, 1) route_sort_small_kernel(RouteParams rp, SortParams p) {
+__global__ void __cluster_dims__(kRouteCtas, 1, 1) __launch_bounds__(kSortThreads, 1)
+    route_sort_small_kernel(RouteParams rp, SortParams p) {
     __shared__ uint2 s_cand[kSortWarps][rs::kMaxCand];
     __shared__ int s_ids[kSmallSlots];
     __shared__ uint32_t s_key[kSmallSlots];
     __shared__ int s_tot[3][rs::kScanWarps];
+    namespace cg = cooperative_groups;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int rank = static_cast<int>(cluster.block_rank());
+    int* ids0 = cluster.map_shared_rank(s_ids, 0);  // CTA 0's id table
     ptx::pdl_wait();
     const int tid = threadIdx.x, warp = tid >> 5;
-    for (int t = warp; t < rp.T; t += kSortWarps) rs::route_token(rp, t, s_cand[warp], s_ids);
-    __syncthreads();
+    for (int t = rank + kRouteCtas * warp; t < rp.T; t += kRouteCtas * kSortWarps)
+        rs::route_token(rp, t, s_cand[warp], ids0);
+    cluster.sync();
+    if (rank != 0) return;  // nothing reads the other CTAs' shared memory
 
     const int n = p.T * p.kp;
     int npow = 1;
     while (npow < n) npow <<= 1;
-    if (tid < npow) {
-        uint32_t key = 0xFFFFFFFFu;
-        if (tid < n) {
-            const int e = local_expert(s_ids[tid], p);
-            key = (static_cast<uint32_t>(e < 0 ? 2047 : e) << 10) | static_cast<uint32_t>(tid);
-        }
-        s_key[tid] = key;
+    uint32_t key = 0xFFFFFFFFu;
+    if (tid < n) {
+        const int e = local_expert(s_ids[tid], p);
+        key = (static_cast<uint32_t>(e < 0 ? 2047 : e) << 10) | static_cast<uint32_t>(tid);
     }
-    __syncthreads();
+    // threads >= npow hold the maximum key and only ever meet each other
     for (int size = 2; size <= npow; size <<= 1)
         for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            const int partner = tid ^ stride;
-            if (tid < npow && partner > tid) {
-                const uint32_t a = s_key[tid], b = s_key[partner];
-                if ((a > b) == ((tid & size) == 0)) {
-                    s_key[tid] = b;
-                    s_key[partner] = a;
-                }
+            uint32_t other;
+            if (stride >= 32) {
+                s_key[tid] = key;
+                __syncthreads();
+                other = s_key[tid ^ stride];
+                __syncthreads();
+            } else {
+                other = __shfl_xor_sync(0xffffffffu, key, stride);
             }
-            __syncthreads();
+            const bool ascending = (tid & size) == 0, lower = (tid & stride) == 0;
+            key = (ascending == lower) ? min(key, other) : max(key, other);
         }
+    s_key[tid] = key;
+    __syncthreads();
     if (tid < n) {
-        const uint32_t key = s_key[tid];
         const int e = static_cast<int>(key >> 10), slot = static_cast<int>(key & 1023u);
         if (e < p.Et) {
             p.a_map[tid] = slot;
@@ -276,7 +289,7 @@ int sort_launch_count(int64_t slots) { return slots <= kSortWarps * kBigWarpSlot
 bool route_sort_fusable(int T, int kp) { return static_cast<int64_t>(T) * kp <= kSmallSlots; }
 
 cudaError_t launch_route_sort_small(const RouteParams& rp, const SortParams& p, cudaStream_t stream, bool pdl) {
-    return launch_kernel(route_sort_small_kernel, dim3(1), dim3(kSortThreads), 0, stream, pdl, rp, p);
+    return launch_kernel(route_sort_small_kernel, dim3(kRouteCtas), dim3(kSortThreads), 0, stream, pdl, rp, p);
 }
 
 }  // namespace moe
