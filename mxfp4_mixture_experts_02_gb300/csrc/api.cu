@@ -92,7 +92,8 @@ int run_sort(const moe_shape* s, const int32_t* ids, void* ws, cudaStream_t st, 
     const Layout L = make_layout(d);
     SortParams p{ids, at<int32_t>(ws, L.header), at<int32_t>(ws, L.counts), at<int32_t>(ws, L.offsets),
                  at<int4>(ws, L.vinfo), at<int4>(ws, L.groups), at<int32_t>(ws, L.a_map), at<int32_t>(ws, L.c_map),
-                 at<int32_t>(ws, L.sort_hist), d.T, d.kp, d.Eg, d.E, d.off, d.S, d.Et, d.B, d.G};
+                 at<int32_t>(ws, L.vbase), at<int32_t>(ws, L.sort_hist), d.T, d.kp, d.Eg, d.E, d.off, d.S, d.Et, d.B,
+                 d.G};
     return cuda_rc(launch_sort(p, st, pdl));
 }
 
@@ -115,7 +116,8 @@ int run_route_sort(const moe_shape* s, const float* logits, const uint16_t* shar
         RouteParams rp{logits, shared_logit, ids, w, d.T, d.Eg, d.k, d.S, d.kp, d.shared_scale};
         SortParams sp{ids, at<int32_t>(ws, L.header), at<int32_t>(ws, L.counts), at<int32_t>(ws, L.offsets),
                       at<int4>(ws, L.vinfo), at<int4>(ws, L.groups), at<int32_t>(ws, L.a_map), at<int32_t>(ws, L.c_map),
-                      at<int32_t>(ws, L.sort_hist), d.T, d.kp, d.Eg, d.E, d.off, d.S, d.Et, d.B, d.G};
+                      at<int32_t>(ws, L.vbase), at<int32_t>(ws, L.sort_hist), d.T, d.kp, d.Eg, d.E, d.off, d.S, d.Et,
+                      d.B, d.G};
         if (launch_route_sort_small(rp, sp, st, false) != cudaSuccess) return MOE_ERR_CUDA;
         return (rec(ev, 1, st) && rec(ev, 2, st)) ? MOE_OK : MOE_ERR_CUDA;
     }
@@ -138,11 +140,27 @@ int run_forward(const moe_shape* s, const uint16_t* x, const moe_weights* wt, co
     const int nsm = num_sms_cached();
     if (nsm <= 0) return MOE_ERR_CUDA;
 
-    GatherParams gp{x, at<int32_t>(ws, L.header), at<int4>(ws, L.vinfo), at<int32_t>(ws, L.a_map),
-                    at<uint8_t>(ws, L.xq), at<uint8_t>(ws, L.xsf),
-                    d.mode == kModePrefill ? at<uint8_t>(ws, L.xq_nat) : nullptr,
-                    d.mode == kModePrefill ? at<uint8_t>(ws, L.xsf_nat) : nullptr, topk_w, at<float>(ws, L.row_w),
-                    d.H, d.kp, d.B, L.xsf_tile_bytes, d.V_max, d.V_max < 8 * nsm ? d.V_max : 8 * nsm, d.T};
+    GatherParams gp{};
+    gp.x = x;
+    gp.header = at<int32_t>(ws, L.header);
+    gp.vinfo = at<int4>(ws, L.vinfo);
+    gp.a_map = at<int32_t>(ws, L.a_map);
+    gp.xq = at<uint8_t>(ws, L.xq);
+    gp.xsf = at<uint8_t>(ws, L.xsf);
+    gp.topk_w = topk_w;
+    gp.row_w = at<float>(ws, L.row_w);
+    gp.c_map = at<int32_t>(ws, L.c_map);
+    gp.offsets = at<int32_t>(ws, L.offsets);
+    gp.vbase = at<int32_t>(ws, L.vbase);
+    gp.token_major = d.mode == kModePrefill;
+    gp.H = d.H;
+    gp.kp = d.kp;
+    gp.B = d.B;
+    gp.xsf_tile_bytes = L.xsf_tile_bytes;
+    gp.max_v = d.V_max;
+    gp.grid = d.V_max < 8 * nsm ? d.V_max : 8 * nsm;
+    gp.T = d.T;
+    gp.Et = d.Et;
     cudaError_t e = launch_gather(gp, st, pdl);
     if (e != cudaSuccess || !rec(ev, 3, st)) return MOE_ERR_CUDA;
 

@@ -37,7 +37,7 @@ struct Dims {
 // Byte offsets of the workspace regions (256-byte aligned).
 struct Layout {
     size_t header, counts, offsets, vinfo, groups, a_map, c_map, sort_hist, row_w;
-    size_t xq, xsf, act, asf, y, xq_nat, xsf_nat;
+    size_t xq, xsf, act, asf, y, vbase;
     size_t st_logits, st_shared, st_x, st_ids, st_w, st_out;
     size_t total;
     int xsf_tile_bytes, asf_tile_bytes, y_bf16;
@@ -99,9 +99,7 @@ inline Layout make_layout(const Dims& d) {
     // bf16 rows carry the TMA tail too: the store map's row extent is
     // rows_alloc (>= 128), so a 32-row box never exceeds it
     L.y = take(size_t(L.y_bf16 ? d.rows_alloc : d.R_max) * d.H * (L.y_bf16 ? 2 : 4));
-    // natural-order MXFP8 x for the two-pass gather (prefill tiling)
-    L.xq_nat = take(d.mode == kModePrefill ? size_t(d.max_T) * d.H : 0);
-    L.xsf_nat = take(d.mode == kModePrefill ? size_t(d.max_T) * (d.H / 32) : 0);
+    L.vbase = take(size_t(d.Et) * 4);
     L.st_logits = take(size_t(d.max_T) * d.Eg * 4);
     L.st_shared = take(size_t(d.max_T) * (d.S > 0 ? d.S : 1) * 2);
     L.st_x = take(size_t(d.max_T) * d.H * 2);

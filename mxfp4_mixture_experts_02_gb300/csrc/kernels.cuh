@@ -44,6 +44,7 @@ struct SortParams {
     int4* groups;
     int32_t* a_map;
     int32_t* c_map;
+    int32_t* vbase;     // [Et]: index of each expert's first virtual expert
     int32_t* cta_hist;  // [ceil(T*k' / 4096)][Et]: large-sort scratch
     int T, kp, Eg, E, off, S, Et, B, G;
 };
@@ -55,11 +56,14 @@ struct GatherParams {  // x -> MXFP8 rows in expert order + tile scales
     const int32_t* a_map;
     uint8_t* xq;
     uint8_t* xsf;
-    uint8_t* xq_nat;   // NULL: one fused pass; else the two-pass path's natural-order MXFP8 x [T, H]
-    uint8_t* xsf_nat;  // its scales [T, H/32]
     const float* topk_w;
     float* row_w;      // routing weight of each row: topk_w[a_map[row]]
-    int H, kp, B, xsf_tile_bytes, max_v, grid, T;
+    // token-major pass (128-row tiles): slot -> row map and expert placement
+    const int32_t* c_map;
+    const int32_t* offsets;
+    const int32_t* vbase;
+    int token_major;
+    int H, kp, B, xsf_tile_bytes, max_v, grid, T, Et;
 };
 
 struct GemmParams {

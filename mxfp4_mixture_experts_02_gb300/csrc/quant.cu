@@ -70,74 +70,119 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(GatherParams p) 
     ptx::pdl_launch_dependents();
 }
 
-// Two-pass path for large token counts.  Pass 1: x -> MXFP8 once per token
-// in natural order (xq_nat [T, H], xsf_nat [T, H/32]); one thread per
-// 32-element block.
-__global__ void __launch_bounds__(kGatherThreads) quant_x_kernel(GatherParams p) {
-    ptx::pdl_wait();
-    const int nb = p.H / 32;
-    const int64_t total = static_cast<int64_t>(p.T) * nb;
-    for (int64_t job = blockIdx.x * static_cast<int64_t>(kGatherThreads) + threadIdx.x; job < total;
-         job += static_cast<int64_t>(gridDim.x) * kGatherThreads) {
-        const int64_t t = job / nb;
-        const int b = static_cast<int>(job - t * nb);
-        const uint4* src = reinterpret_cast<const uint4*>(p.x + t * p.H + b * 32);
-        uint4 raw[4];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) raw[c] = src[c];
-        const uint16_t* hv = reinterpret_cast<const uint16_t*>(raw);
-        float f[32];
-        float amax = 0.f;
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-            f[e] = bf16_bits_to_float(hv[e]);
-            amax = fmaxf(amax, fabsf(f[e]));
-        }
-        const int ex = mx_shared_exponent(amax, 8);
-        const float inv = exp2_int(-ex);
-        uint32_t packed[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const uint32_t lo = e4m3x2(f[4 * e] * inv, f[4 * e + 1] * inv);
-            const uint32_t hi = e4m3x2(f[4 * e + 2] * inv, f[4 * e + 3] * inv);
-            packed[e] = lo | (hi << 16);
-        }
-        uint4* dst = reinterpret_cast<uint4*>(p.xq_nat + t * p.H + b * 32);
-        dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-        dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-        p.xsf_nat[t * nb + b] = static_cast<uint8_t>(ex + 127);
+// Token-major pass (128-row tiles, long batches): one warp per token
+// quantises the token's row once and writes it to every row the token's
+// slots occupy (c_map), with the row's routing weight and its scale words.
+// Lane l holds the 16-element half-blocks l, l + 32, ... of each 4096-column
+// slab (lanes 2k, 2k+1 share MX block k: one shuffle gives the block amax),
+// so each store instruction writes 512 contiguous bytes; the four K-block
+// scales of 128-K chunk kc form one word, stored by lane kc at word
+// kc * 128 + (i % 32) * 4 + i / 32 of the tile's scale blocks (tile v, tile
+// row i).  Each x row is read once, so the pass costs the x read plus the
+// expert-ordered write.  A row's expert is the last one whose first row is
+// <= it (binary search over the offsets, cached in shared memory); its tile
+// is vbase[e] + (row - off) / B.
+constexpr int kTokWarps = 8;
+constexpr int kTokMaxExperts = 1024;
+
+__device__ __forceinline__ int last_le(const int* a, int n, int x) {  // largest i < n with a[i] <= x (a[0] <= x)
+    int lo = 0, hi = n;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (a[mid] <= x)
+            lo = mid;
+        else
+            hi = mid;
     }
-    ptx::pdl_launch_dependents();
+    return lo;
 }
 
-// Pass 2: copy each row's MXFP8 bytes from its token's natural-order row (one
-// warp per row, 16-byte moves) and build the tile's scale blocks: each thread
-// moves one row's four K-block scales of one 128-K chunk (4 bytes) into its
-// word (i % 32) * 16 + (i / 32) * 4 of the chunk's 512-byte block.
-__global__ void __launch_bounds__(kGatherThreads) gather_copy_kernel(GatherParams p) {
+__global__ void __launch_bounds__(kTokWarps * 32) gather_token_kernel(GatherParams p) {
+    __shared__ int s_off[kTokMaxExperts + 1];
+    __shared__ int s_vb[kTokMaxExperts];
+    __shared__ uint32_t s_exp[kTokWarps][32];  // a slab's 128 block scales (bytes) per warp
     ptx::pdl_wait();
-    const int nv = p.header[kHdrNumV];
-    const int warps = kGatherThreads / 32;
-    const int lane = threadIdx.x & 31;
-    const int nb = p.H / 32, n16 = p.H / 16, kchunks = p.H / 128;
-    for (int v = blockIdx.x; v < nv; v += gridDim.x) {
-        const int4 vi = p.vinfo[v];
-        const int first = vi.y, rows = vi.z;
-        for (int i = threadIdx.x >> 5; i < rows; i += warps) {
-            const int row = first + i;
-            const int slot = p.a_map[row];
-            const int64_t t = slot / p.kp;
-            if (lane == 0) p.row_w[row] = p.topk_w[slot];
-            const uint4* src = reinterpret_cast<const uint4*>(p.xq_nat + t * p.H);
-            uint4* dst = reinterpret_cast<uint4*>(p.xq + static_cast<int64_t>(row) * p.H);
-            for (int c = lane; c < n16; c += 32) dst[c] = src[c];
-        }
-        uint32_t* sf_tile = reinterpret_cast<uint32_t*>(p.xsf + static_cast<size_t>(v) * p.xsf_tile_bytes);
-        for (int j = threadIdx.x; j < kchunks * rows; j += kGatherThreads) {
-            const int kc = j / rows, i = j - kc * rows;
-            const int64_t t = p.a_map[first + i] / p.kp;
-            sf_tile[kc * 128 + (i & 31) * 4 + (i >> 5)] =
-                *reinterpret_cast<const uint32_t*>(p.xsf_nat + t * nb + kc * 4);
+    for (int e = threadIdx.x; e <= p.Et; e += kTokWarps * 32) {
+        s_off[e] = p.offsets[e];
+        if (e < p.Et) s_vb[e] = p.vbase[e];
+    }
+    __syncthreads();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint8_t* exp_bytes = reinterpret_cast<uint8_t*>(s_exp[warp]);
+    const int nh = p.H / 16;  // half-blocks per row
+    for (int t = blockIdx.x * kTokWarps + warp; t < p.T; t += gridDim.x * kTokWarps) {
+        for (int j0 = 0; j0 < p.kp; j0 += 32) {
+            // slot j0 + lane: its row, tile and tile row
+            const int j = j0 + lane;
+            int row = -1, v = 0, i = 0;
+            if (j < p.kp) {
+                row = p.c_map[static_cast<size_t>(t) * p.kp + j];
+                if (row >= 0) {
+                    const int e = last_le(s_off, p.Et, row);
+                    const int rel = row - s_off[e];
+                    v = s_vb[e] + rel / p.B;
+                    i = rel % p.B;
+                    p.row_w[row] = p.topk_w[static_cast<size_t>(t) * p.kp + j];
+                }
+            }
+            const int nj = min(32, p.kp - j0);
+            for (int h0 = 0; h0 < nh; h0 += 256) {  // 4096-column slabs
+                uint4 q[8];
+#pragma unroll
+                for (int m = 0; m < 8; ++m) {
+                    const int h = h0 + lane + 32 * m;
+                    float f[16];
+                    float amax = 0.f;
+                    if (h < nh) {
+                        const uint4* src = reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(t) * p.H + h * 16);
+                        uint4 raw[2];
+                        raw[0] = __ldg(src);
+                        raw[1] = __ldg(src + 1);
+                        const uint16_t* hv = reinterpret_cast<const uint16_t*>(raw);
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            f[e] = bf16_bits_to_float(hv[e]);
+                            amax = fmaxf(amax, fabsf(f[e]));
+                        }
+                    }
+                    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+                    if (h < nh) {
+                        const int ex = mx_shared_exponent(amax, 8);
+                        const float inv = exp2_int(-ex);
+                        uint32_t packed[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const uint32_t lo = e4m3x2(f[4 * e] * inv, f[4 * e + 1] * inv);
+                            const uint32_t hi = e4m3x2(f[4 * e + 2] * inv, f[4 * e + 3] * inv);
+                            packed[e] = lo | (hi << 16);
+                        }
+                        q[m] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                        if ((lane & 1) == 0) exp_bytes[(h - h0) >> 1] = static_cast<uint8_t>(ex + 127);
+                    }
+                }
+                __syncwarp();
+                const int kc = h0 / 8 + lane;  // this lane's 128-K chunk
+                const bool has_sf = 8 * kc < nh;
+                const uint32_t sfw = has_sf ? s_exp[warp][lane] : 0u;
+                __syncwarp();  // s_exp is rewritten by the next slab
+                for (int jj = 0; jj < nj; ++jj) {
+                    const int r = __shfl_sync(0xffffffffu, row, jj);
+                    const int rv = __shfl_sync(0xffffffffu, v, jj);
+                    const int ri = __shfl_sync(0xffffffffu, i, jj);
+                    if (r < 0) continue;  // warp-uniform
+                    uint4* dst = reinterpret_cast<uint4*>(p.xq + static_cast<size_t>(r) * p.H);
+#pragma unroll
+                    for (int m = 0; m < 8; ++m) {
+                        const int h = h0 + lane + 32 * m;
+                        if (h < nh) dst[h] = q[m];
+                    }
+                    if (has_sf) {
+                        uint32_t* sf_tile =
+                            reinterpret_cast<uint32_t*>(p.xsf + static_cast<size_t>(rv) * p.xsf_tile_bytes);
+                        sf_tile[kc * 128 + (ri & 31) * 4 + (ri >> 5)] = sfw;
+                    }
+                }
+            }
         }
     }
     ptx::pdl_launch_dependents();
@@ -231,12 +276,13 @@ unsigned grid_for(int64_t n, int threads) {
 }  // namespace
 
 cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream, bool pdl) {
-    if (!p.xq_nat) return launch_kernel(gather_kernel, dim3(p.grid), dim3(kGatherThreads), 0, stream, pdl, p);
-    const int64_t blocks = (static_cast<int64_t>(p.T) * (p.H / 32) + kGatherThreads - 1) / kGatherThreads;
-    cudaError_t e = launch_kernel(quant_x_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kGatherThreads), 0,
-                                  stream, pdl, p);
-    if (e != cudaSuccess) return e;
-    return launch_kernel(gather_copy_kernel, dim3(p.grid), dim3(kGatherThreads), 0, stream, true, p);
+    if (!p.token_major) return launch_kernel(gather_kernel, dim3(p.grid), dim3(kGatherThreads), 0, stream, pdl, p);
+    const int64_t warps = p.T, per_sm_ctas = 8;
+    int64_t blocks = (warps + kTokWarps - 1) / kTokWarps;
+    const int64_t cap = static_cast<int64_t>(p.grid) * per_sm_ctas;  // grid = min(V_max, 8 * #SM)
+    if (blocks > cap) blocks = cap;
+    return launch_kernel(gather_token_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kTokWarps * 32), 0, stream, pdl,
+                         p);
 }
 
 cudaError_t launch_quantize_mxfp4(const QuantParams& p, cudaStream_t stream) {

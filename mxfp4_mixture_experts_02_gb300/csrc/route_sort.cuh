@@ -253,6 +253,7 @@ __device__ __forceinline__ void place_experts(const SortParams& p, int cnt, int*
         if (s_off) s_off[tid] = off;
         p.counts[tid] = cnt;
         p.offsets[tid] = off;
+        p.vbase[tid] = vb;
         for (int c = 0; c < tiles; ++c)
             p.vinfo[vb + c] = make_int4(tid, off + c * p.B, min(p.B, cnt - c * p.B), c);
         for (int g = 0; g < grps; ++g) p.groups[gb + g] = make_int4(tid, vb + g * p.G, min(p.G, tiles - g * p.G), 0);
