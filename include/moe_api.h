@@ -233,7 +233,7 @@ int moe_num_sms(int32_t* num_sms);
 /* Number of kernel launches moe_layer (and moe_layer_host, besides its
  * copies) issues for the shape: route + sort (one fused launch up to 1024
  * slots T*k', else route and a one- or three-kernel sort), then for T > 0 the
- * gather (one kernel, two at block_n 128), FC1, FC2 and the combine. */
+ * gather, FC1, FC2 and the combine. */
 int moe_layer_launch_count(const moe_shape* shape, int32_t* count);
 
 #ifdef __cplusplus

@@ -429,7 +429,7 @@ int moe_layer_launch_count(const moe_shape* s, int32_t* count) {
     if (!count) return MOE_ERR_NULL;
     const Dims d = make_dims(*s);
     int n = route_sort_fusable(d.T, d.kp) ? 1 : 1 + sort_launch_count(static_cast<int64_t>(d.T) * d.kp);
-    if (d.T > 0) n += (d.mode == kModePrefill ? 2 : 1) + 3;
+    if (d.T > 0) n += 4;  // gather, FC1, FC2, combine
     *count = n;
     return MOE_OK;
 }

@@ -92,7 +92,7 @@ def test_layer_launch_count():
     assert moe.moe_layer_launch_count(_shape()) == 5
     # 256 tokens x 16 picks > 1024 slots: route, one-CTA sort, then 4
     assert moe.moe_layer_launch_count(_shape(T=256, max_T=256)) == 6
-    # prefill tiling at 32768 tokens: route, 3-kernel sort, 2-kernel gather, FC1, FC2, combine
-    assert moe.moe_layer_launch_count(_shape(T=32768, max_T=32768, block_n=128)) == 9
+    # prefill tiling at 32768 tokens: route, 3-kernel sort, gather, FC1, FC2, combine
+    assert moe.moe_layer_launch_count(_shape(T=32768, max_T=32768, block_n=128)) == 8
     assert moe.moe_layer_launch_count(_shape(T=0)) == 1
 
