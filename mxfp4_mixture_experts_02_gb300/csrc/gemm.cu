@@ -55,10 +55,6 @@ namespace {
 #ifndef MOE_STAGES_PRE_FC2
 #define MOE_STAGES_PRE_FC2 3
 #endif
-#ifndef MOE_ITEM_CONTIG
-#define MOE_ITEM_CONTIG 0
-#endif
-constexpr bool kItemContig = MOE_ITEM_CONTIG != 0;
 constexpr int kStagesDecFc1 = MOE_STAGES_DEC_FC1;
 constexpr int kStagesDecFc2 = MOE_STAGES_DEC_FC2;
 constexpr int kStagesPreFc1 = MOE_STAGES_PRE_FC1;
@@ -179,18 +175,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int KC = FC1 ? p.H / 128 : p.I / 128;  // 128-wide K chunks
     const int nitems = num_v * NB;
     // This CTA's items: it0, it0 + istep, ... below iend (round-robin over the
-    // grid, or one contiguous range per CTA).
-    int it0, istep, iend;
-    if (kItemContig) {
-        const int per = (nitems + gridDim.x - 1) / gridDim.x;
-        it0 = blockIdx.x * per;
-        istep = 1;
-        iend = min(nitems, it0 + per);
-    } else {
-        it0 = blockIdx.x;
-        istep = gridDim.x;
-        iend = nitems;
-    }
+    // grid: the token tiles of one expert run side by side and share its
+    // weights in L2).
+    const int it0 = blockIdx.x, istep = gridDim.x, iend = nitems;
 
     if (warp == kProducerWarp) {
         if (lane == 0) {
