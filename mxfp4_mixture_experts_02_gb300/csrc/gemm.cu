@@ -23,10 +23,11 @@
 // rows, the rest alias the next stages' token tiles (their accumulator lanes
 // are never read).
 //
-// Warp roles (10 warps): 0..7 epilogue (warp w reads TMEM lane quadrant w % 4
+// Warp roles (11 warps): 0..7 epilogue (warp w reads TMEM lane quadrant w % 4
 // and column half w / 4; with TM <= 32 only quadrant 0 holds tokens, so only
-// warps 0 and 4 work), 8 TMA producer (STAGES-deep ring), 9 TMEM allocator and
-// single-thread MMA issuer.  The epilogue releases the accumulator as soon as
+// warps 0 and 4 work), 8 weight producer and 10 token producer (one thread
+// each, filling the same STAGES-deep ring: a single issuing thread could not
+// keep up with the MMAs), 9 TMEM allocator and single-thread MMA issuer.  The epilogue releases the accumulator as soon as
 // its TMEM loads complete, so the next item's MMAs overlap the SwiGLU /
 // quantise / store math.  Every wait is bounded; on expiry the CTA records
 // MOE_ERR_TIMEOUT in the workspace status word, stops, lets its MMAs drain,
@@ -60,10 +61,11 @@ constexpr int kStagesDecFc2 = MOE_STAGES_DEC_FC2;
 constexpr int kStagesPreFc1 = MOE_STAGES_PRE_FC1;
 constexpr int kStagesPreFc2 = MOE_STAGES_PRE_FC2;
 
-constexpr int kWarps = 10;
+constexpr int kWarps = 11;
 constexpr int kThreads = kWarps * 32;
-constexpr int kProducerWarp = 8;
+constexpr int kProducerWarp = 8;  // weight tiles and weight scales
 constexpr int kMmaWarp = 9;
+constexpr int kTokenWarp = 10;    // token tiles and token scales
 
 template <int TM, int STAGES, bool STAGE_Y>
 struct Cfg {
@@ -152,10 +154,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 0;
         ptx::fence_mbarrier_init();
     }
-    if (warp == kProducerWarp && lane == 0) {
-        ptx::tma_prefetch_desc(&tmW);
-        ptx::tma_prefetch_desc(&tmX);
-    }
+    if (warp == kProducerWarp && lane == 0) ptx::tma_prefetch_desc(&tmW);
+    if (warp == kTokenWarp && lane == 0) ptx::tma_prefetch_desc(&tmX);
     if (warp == kMmaWarp) {
         ptx::tmem_alloc(tmem_slot, C::kTmemCols);
         ptx::tmem_relinquish();
@@ -168,8 +168,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The work list comes from the sort, which has completed when this grid
     // launches (the previous kernel's CTAs waited on it before triggering
     // this launch).  Only the token operands -- written by the immediately
-    // preceding kernel -- need griddepcontrol.wait, which the producer issues
-    // after it has started streaming the first weight stages.
+    // preceding kernel -- need griddepcontrol.wait, which the token producer
+    // issues while the weight producer streams the first weight stages.
     const int num_v = p.header[kHdrNumV];
     const int NB = FC1 ? p.I / 128 : p.H / 256;  // 256-row weight blocks per expert
     const int KC = FC1 ? p.H / 128 : p.I / 128;  // 128-wide K chunks
@@ -179,35 +179,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     // weights in L2).
     const int it0 = blockIdx.x, istep = gridDim.x, iend = nitems;
 
+    // Descriptors of the next three items stay in flight in each producer (an
+    // FC2 item streams only I/128 stages, less than an L2 round trip under
+    // load).
+    const int4 kNone = make_int4(0, 0, 0, 0);
+    const int g = istep;
     if (warp == kProducerWarp) {
         if (lane == 0) {
-            // ---------------------------------------------------- TMA producer
-            // Weight tiles and weight scales of the first STAGES stages are
-            // issued before griddepcontrol.wait; their token tiles / token
-            // scales after it.  A stage's full barrier expects all its bytes.
+            // ------------------------------------------------- weight producer
+            // Weight tiles and weight scales need nothing from the preceding
+            // kernel: they stream from the start.  This thread sets each
+            // stage's expected bytes (weights and tokens); the token
+            // producer's copies may land before or after.
             uint32_t stage = 0, phase = 0;
             bool ok = true;
             const uint32_t tx = 256 * 64 + C::kXTile + 1536;
-            int pre_v[STAGES], pre_first[STAGES], pre_kc[STAGES];
-            int npre = 0;
-            bool waited = false;
-            // wait for the preceding kernel, then issue the deferred token loads
-            auto flush_prefetched = [&]() {
-                ptx::pdl_wait();
-                waited = true;
-#pragma unroll
-                for (int j = 0; j < STAGES; ++j) {
-                    if (j >= npre) break;
-                    ptx::tma_load_2d(smem + C::kOffX + j * C::kXTile, &tmX, &full[j], pre_kc[j] * 128, pre_first[j]);
-                    ptx::bulk_load(smem + j * C::kStageBytes + C::kOffSFX,
-                                   p.b_sf + static_cast<size_t>(pre_v[j]) * p.b_sf_tile_bytes + pre_kc[j] * 512, 512,
-                                   &full[j]);
-                }
-            };
-            // descriptors of the next three items in flight (an FC2 item streams
-            // only I/128 stages, less than an L2 round trip under load)
-            const int g = istep;
-            const int4 kNone = make_int4(0, 0, 0, 0);
             int4 vq0 = it0 < iend ? p.vinfo[it0 / NB] : kNone;
             int4 vq1 = it0 + g < iend ? p.vinfo[(it0 + g) / NB] : kNone;
             int4 vq2 = it0 + 2 * g < iend ? p.vinfo[(it0 + 2 * g) / NB] : kNone;
@@ -217,12 +203,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 vq0 = vq1;
                 vq1 = vq2;
                 vq2 = (it + 3 * g < iend) ? p.vinfo[(it + 3 * g) / NB] : kNone;
-                const int e = vi.x, first = vi.y;
-                const int64_t tile0 = (static_cast<int64_t>(e) * NB + nb) * KC;
+                const int64_t tile0 = (static_cast<int64_t>(vi.x) * NB + nb) * KC;
                 for (int kc = 0; kc < KC; ++kc) {
-                    // the ring is full of prefetched stages: their token loads
-                    // must be in flight before waiting for a free stage
-                    if (!waited && npre == STAGES) flush_prefetched();
                     if (!wait_or_abort(&empty[stage], phase ^ 1, p.wait_ns, abort_flag)) {
                         if (!*abort_flag) record_timeout(p, abort_flag, kSiteProducerEmpty);
                         ok = false;
@@ -232,27 +214,49 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::mbar_arrive_expect_tx(&full[stage], tx);
                     ptx::tma_load_2d(st, &tmW, &full[stage], 0, static_cast<int32_t>((tile0 + kc) * 256));
                     ptx::bulk_load(st + C::kOffSFW, p.a_sf + static_cast<size_t>(tile0 + kc) * 1024, 1024, &full[stage]);
-                    if (!waited) {  // first lap: stage == npre
-                        pre_v[npre] = v;
-                        pre_first[npre] = first;
-                        pre_kc[npre] = kc;
-                        ++npre;
-                    } else {
-                        ptx::tma_load_2d(smem + C::kOffX + stage * C::kXTile, &tmX, &full[stage], kc * 128, first);
-                        ptx::bulk_load(st + C::kOffSFX, p.b_sf + static_cast<size_t>(v) * p.b_sf_tile_bytes + kc * 512,
-                                       512, &full[stage]);
-                    }
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1;
                     }
                 }
             }
-            if (!waited) flush_prefetched();  // fewer stages than the ring
             // every issued stage lands before the CTA may exit (bounded)
             for (int s = 0; s < STAGES; ++s) {
                 const uint32_t par = (static_cast<uint32_t>(s) < stage) ? phase : (phase ^ 1);
                 ptx::mbar_wait(&full[s], par, 10ull * 1000 * 1000);
+            }
+        }
+    } else if (warp == kTokenWarp) {
+        if (lane == 0) {
+            // -------------------------------------------------- token producer
+            // The token operands are written by the immediately preceding
+            // kernel: wait for it once, then follow the same stage sequence.
+            ptx::pdl_wait();
+            uint32_t stage = 0, phase = 0;
+            bool ok = true;
+            int4 vq0 = it0 < iend ? p.vinfo[it0 / NB] : kNone;
+            int4 vq1 = it0 + g < iend ? p.vinfo[(it0 + g) / NB] : kNone;
+            int4 vq2 = it0 + 2 * g < iend ? p.vinfo[(it0 + 2 * g) / NB] : kNone;
+            for (int it = it0; ok && it < iend; it += g) {
+                const int v = it / NB;
+                const int4 vi = vq0;
+                vq0 = vq1;
+                vq1 = vq2;
+                vq2 = (it + 3 * g < iend) ? p.vinfo[(it + 3 * g) / NB] : kNone;
+                const uint8_t* sfx = p.b_sf + static_cast<size_t>(v) * p.b_sf_tile_bytes;
+                for (int kc = 0; kc < KC; ++kc) {
+                    if (!wait_or_abort(&empty[stage], phase ^ 1, p.wait_ns, abort_flag)) {
+                        if (!*abort_flag) record_timeout(p, abort_flag, kSiteProducerEmpty);
+                        ok = false;
+                        break;
+                    }
+                    ptx::tma_load_2d(smem + C::kOffX + stage * C::kXTile, &tmX, &full[stage], kc * 128, vi.y);
+                    ptx::bulk_load(smem + stage * C::kStageBytes + C::kOffSFX, sfx + kc * 512, 512, &full[stage]);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
             }
         }
     } else if (warp == kMmaWarp) {
@@ -298,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tc_commit(done);
             ptx::mbar_wait(done, 0, 10ull * 1000 * 1000);
         }
-    } else {
+    } else if (warp < 8) {
         // -------------------------------------------------------- epilogue
         const int q = warp & 3, half = warp >> 2;
         const bool active = (TM > 32) || q == 0;
@@ -306,8 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int i = q * 32 + lane;  // token row of this lane within a tile
         // Descriptors two items ahead and row weights one item ahead are
         // loaded early, so no dependent load chain sits between two items.
-        const int4 kNoTile = make_int4(0, 0, 0, 0);
-        const int g = istep;
+        const int4 kNoTile = kNone;
         int4 vi_cur = (active && it0 < iend) ? p.vinfo[it0 / NB] : kNoTile;
         int4 vi_nxt = (active && it0 + g < iend) ? p.vinfo[(it0 + g) / NB] : kNoTile;
         float w_cur = (!FC1 && i < vi_cur.z) ? p.row_w[vi_cur.y + i] : 0.f;
