@@ -108,83 +108,60 @@ __global__ void __launch_bounds__(kSortThreads, 1) sort_kernel(SortParams p) {
 // (decode).  A cluster of kRouteCtas CTAs routes the tokens (token t on CTA
 // t % kRouteCtas, so the routing spreads over that many SMs) and stores the
 // picked ids straight into CTA 0's shared memory; after the cluster barrier
-// CTA 0 sorts the (local expert, slot) keys -- masked or foreign ids as
-// expert 2047 -- ascending with a bitonic network (shuffles for strides
-// below 32, shared memory above), so position p of a routed key is its row
-// (experts in order, slots ascending inside each expert: the same rows as
-// the counting passes below); an expert's count is the width of its key
-// range, found by binary search.
+// CTA 0 ranks the slots with per-expert bitmasks over the slots (the
+// popcount rank of "[sglang] ... MXFP4 decode MoE ... shape templates",
+// section 5, for up to 1024 slots): slot s sets bit s of its expert's mask;
+// the expert's row count is the popcount of the mask and slot s's row is the
+// expert's first row plus the number of its bits below s -- slot order inside
+// each expert, the same rows as the counting passes below.
 constexpr int kSmallSlots = 1024;
 constexpr int kRouteCtas = 8;
-
-__device__ __forceinline__ int lower_bound_u32(const uint32_t* a, int n, uint32_t x) {
-    int lo = 0, hi = n;
-    while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (a[mid] < x)
-            lo = mid + 1;
-        else
-            hi = mid;
-    }
-    return lo;
-}
 
 __global__ void __cluster_dims__(kRouteCtas, 1, 1) __launch_bounds__(kSortThreads, 1)
     route_sort_small_kernel(RouteParams rp, SortParams p) {
     __shared__ uint2 s_cand[kSortWarps][rs::kMaxCand];
     __shared__ int s_ids[kSmallSlots];
-    __shared__ uint32_t s_key[kSmallSlots];
+    __shared__ int s_off[1024];
     __shared__ int s_tot[3][rs::kScanWarps];
+    extern __shared__ uint32_t s_mask[];  // [Et][nw]: slot bitmask per local expert
     namespace cg = cooperative_groups;
     cg::cluster_group cluster = cg::this_cluster();
     const int rank = static_cast<int>(cluster.block_rank());
     int* ids0 = cluster.map_shared_rank(s_ids, 0);  // CTA 0's id table
     ptx::pdl_wait();
     const int tid = threadIdx.x, warp = tid >> 5;
+    const int n = p.T * p.kp;
+    const int nw = (n + 31) >> 5;  // mask words per expert
+    if (rank == 0)
+        for (int w = tid; w < p.Et * nw; w += kSortThreads) s_mask[w] = 0;
     for (int t = rank + kRouteCtas * warp; t < rp.T; t += kRouteCtas * kSortWarps)
         rs::route_token(rp, t, s_cand[warp], ids0);
     cluster.sync();
     if (rank != 0) return;  // nothing reads the other CTAs' shared memory
 
-    const int n = p.T * p.kp;
-    int npow = 1;
-    while (npow < n) npow <<= 1;
-    uint32_t key = 0xFFFFFFFFu;
+    int e = -1;
     if (tid < n) {
-        const int e = local_expert(s_ids[tid], p);
-        key = (static_cast<uint32_t>(e < 0 ? 2047 : e) << 10) | static_cast<uint32_t>(tid);
+        e = local_expert(s_ids[tid], p);
+        if (e >= 0) atomicOr(&s_mask[e * nw + (tid >> 5)], 1u << (tid & 31));
     }
-    // threads >= npow hold the maximum key and only ever meet each other
-    for (int size = 2; size <= npow; size <<= 1)
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            uint32_t other;
-            if (stride >= 32) {
-                s_key[tid] = key;
-                __syncthreads();
-                other = s_key[tid ^ stride];
-                __syncthreads();
-            } else {
-                other = __shfl_xor_sync(0xffffffffu, key, stride);
-            }
-            const bool ascending = (tid & size) == 0, lower = (tid & stride) == 0;
-            key = (ascending == lower) ? min(key, other) : max(key, other);
-        }
-    s_key[tid] = key;
     __syncthreads();
-    if (tid < n) {
-        const int e = static_cast<int>(key >> 10), slot = static_cast<int>(key & 1023u);
-        if (e < p.Et) {
-            p.a_map[tid] = slot;
-            p.c_map[slot] = tid;
-        } else {
-            p.c_map[slot] = -1;
-        }
-    }
     int cnt = 0;
     if (tid < p.Et)
-        cnt = lower_bound_u32(s_key, n, static_cast<uint32_t>(tid + 1) << 10) -
-              lower_bound_u32(s_key, n, static_cast<uint32_t>(tid) << 10);
-    place_experts(p, cnt, nullptr, s_tot);
+        for (int w = 0; w < nw; ++w) cnt += __popc(s_mask[tid * nw + w]);
+    place_experts(p, cnt, s_off, s_tot);
+    __syncthreads();
+    if (tid < n) {
+        if (e >= 0) {
+            const uint32_t* m = s_mask + e * nw;
+            int r = __popc(m[tid >> 5] & ((1u << (tid & 31)) - 1u));
+            for (int w = 0; w < (tid >> 5); ++w) r += __popc(m[w]);
+            const int row = s_off[e] + r;
+            p.a_map[row] = tid;
+            p.c_map[tid] = row;
+        } else {
+            p.c_map[tid] = -1;
+        }
+    }
     ptx::pdl_launch_dependents();
 }
 
@@ -289,7 +266,11 @@ int sort_launch_count(int64_t slots) { return slots <= kSortWarps * kBigWarpSlot
 bool route_sort_fusable(int T, int kp) { return static_cast<int64_t>(T) * kp <= kSmallSlots; }
 
 cudaError_t launch_route_sort_small(const RouteParams& rp, const SortParams& p, cudaStream_t stream, bool pdl) {
-    return launch_kernel(route_sort_small_kernel, dim3(kRouteCtas), dim3(kSortThreads), 0, stream, pdl, rp, p);
+    const size_t smem = static_cast<size_t>(p.Et) * ((p.T * p.kp + 31) / 32) * sizeof(uint32_t);
+    cudaError_t err = cudaFuncSetAttribute(route_sort_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(smem));
+    if (err != cudaSuccess) return err;
+    return launch_kernel(route_sort_small_kernel, dim3(kRouteCtas), dim3(kSortThreads), smem, stream, pdl, rp, p);
 }
 
 }  // namespace moe
