@@ -17,7 +17,10 @@ constexpr int kMaxSlots = 64;
 
 // Block (chunk of 512 hidden columns, token).  The token's rows are read
 // once into shared memory; each thread sums its float4 over the slots in
-// ascending order, issuing the loads of 4 slots before adding them.
+// ascending order, issuing the loads of up to kBatch slots before adding
+// them (one memory round trip for a decode token's 16 slots).
+constexpr int kBatch = 16;
+
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineParams p) {
     __shared__ int rows[kMaxSlots];
     ptx::pdl_wait();
@@ -28,30 +31,21 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineParams 
     if (c < p.H / 4) {
         const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
         float4 acc = zero;
-        int j = 0;
-        for (; j + 4 <= p.kp; j += 4) {
-            float4 v[4];
+        for (int j0 = 0; j0 < p.kp; j0 += kBatch) {
+            float4 v[kBatch];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int r = rows[j + u];
+            for (int u = 0; u < kBatch; ++u) {
+                const int r = (j0 + u < p.kp) ? rows[j0 + u] : -1;
                 v[u] = r >= 0 ? reinterpret_cast<const float4*>(p.y + static_cast<size_t>(r) * p.H)[c] : zero;
             }
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < kBatch; ++u) {
+                if (j0 + u >= p.kp || rows[j0 + u] < 0) continue;  // skipped slots add nothing
                 acc.x += v[u].x;
                 acc.y += v[u].y;
                 acc.z += v[u].z;
                 acc.w += v[u].w;
             }
-        }
-        for (; j < p.kp; ++j) {
-            const int r = rows[j];
-            if (r < 0) continue;
-            const float4 v = reinterpret_cast<const float4*>(p.y + static_cast<size_t>(r) * p.H)[c];
-            acc.x += v.x;
-            acc.y += v.y;
-            acc.z += v.z;
-            acc.w += v.w;
         }
         const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
         const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
