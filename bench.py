@@ -46,6 +46,7 @@ def parse():
     ap.add_argument("--config", default="decode_t32")
     ap.add_argument("--tokens", type=int, default=0, help="override the workload's token count (profiling cases)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--block-n", type=int, default=0, help="override the workload's virtual-expert rows")
     return ap.parse_args()
 
 
@@ -470,7 +471,9 @@ def main():
     import synth
     cfg = synth.CONFIGS[args.config]
     if args.tokens:
-        cfg = cfg.replace(T=args.tokens, name="%s_T%d" % (args.config, args.tokens))
+        cfg = cfg.replace(T=args.tokens, name="%s_T%d" % (cfg.name, args.tokens))
+    if args.block_n:
+        cfg = cfg.replace(block_n=args.block_n, name="%s_B%d" % (cfg.name, args.block_n))
     if args.impl == "reference":
         run_reference(args, cfg)
     else:

@@ -45,10 +45,10 @@ namespace {
 // shared memory of a 32-row token tile allows; the prefill rings share shared
 // memory with 128-row token tiles (and FC2's output staging).
 #ifndef MOE_STAGES_DEC_FC1
-#define MOE_STAGES_DEC_FC1 5
+#define MOE_STAGES_DEC_FC1 6
 #endif
 #ifndef MOE_STAGES_DEC_FC2
-#define MOE_STAGES_DEC_FC2 5
+#define MOE_STAGES_DEC_FC2 6
 #endif
 #ifndef MOE_STAGES_PRE_FC1
 #define MOE_STAGES_PRE_FC1 4
@@ -58,6 +58,7 @@ namespace {
 #endif
 constexpr int kStagesDecFc1 = MOE_STAGES_DEC_FC1;
 constexpr int kStagesDecFc2 = MOE_STAGES_DEC_FC2;
+
 constexpr int kStagesPreFc1 = MOE_STAGES_PRE_FC1;
 constexpr int kStagesPreFc2 = MOE_STAGES_PRE_FC2;
 
@@ -67,18 +68,22 @@ constexpr int kProducerWarp = 8;  // weight tiles and weight scales
 constexpr int kMmaWarp = 9;
 constexpr int kTokenWarp = 10;    // token tiles and token scales
 
+// Shared memory: token tiles first (TM rows x 128 B per stage; the MMA
+// reads 128 rows, so a short tile's reads run on into the following slots
+// and the weight tiles -- bytes whose accumulator lanes are never read),
+// then the weight tiles (32 KiB per stage: 256 rows x 128 E2M1 codes in
+// 16-byte chunks), then each stage's scales (1 KiB weight + 512 B token).
 template <int TM, int STAGES, bool STAGE_Y>
 struct Cfg {
-    static constexpr int kWTile = 256 * 128;           // 256 weight rows x 128 K (16-byte E2M1 chunks)
-    static constexpr int kOffSFW = kWTile;             // 2 x 512 B weight scales
-    static constexpr int kOffSFX = kWTile + 1024;      // 512 B token scales
-    static constexpr int kStageBytes = ((kWTile + 1536) + 1023) & ~1023;
     static constexpr int kXTile = TM * 128;            // bytes of the loaded token rows
-    static constexpr int kXRegion = STAGES * kXTile + (TM < 128 ? 128 * 128 - kXTile : 0);
-    static constexpr int kOffX = STAGES * kStageBytes;
+    static constexpr int kWTile = 256 * 128;           // 256 weight rows x 128 K
+    static constexpr int kSfStage = 1536;
+    static constexpr int kOffX = 0;
+    static constexpr int kOffW = STAGES * kXTile;      // 1024-byte aligned: TM * 128 is
+    static constexpr int kOffSF = kOffW + STAGES * kWTile;
     // bf16 FC2 rows of 128-row tiles are staged per epilogue warp (two
     // 1024-byte-aligned 32-row x 64-column boxes) and leave by TMA stores
-    static constexpr int kOffEpi = kOffX + kXRegion;
+    static constexpr int kOffEpi = (kOffSF + STAGES * kSfStage + 1023) & ~1023;
     static constexpr int kEpiBytes = STAGE_Y ? 8 * 32 * 256 : 0;
     static constexpr int kOffBar = kOffEpi + kEpiBytes;
     static constexpr int kSmemBytes = kOffBar + (2 * STAGES + 4) * 8 + 16 + 1024;
@@ -86,9 +91,14 @@ struct Cfg {
     static constexpr int kSfCols = 16;                  // per stage: 4 token-scale + 8 weight-scale columns
     static constexpr int kTmemCols = 512;
     static constexpr int kEpiWarps = TM <= 32 ? 2 : 8;  // warps holding token lanes
+    static_assert(kOffX + STAGES * kXTile + 128 * 128 <= kOffSF, "a 128-row read of the last token slot stays inside");
     static_assert(kAccCols + STAGES * kSfCols <= kTmemCols, "TMEM budget");
     static_assert(kSmemBytes <= 232448, "shared memory budget");
     static_assert(TM == 16 || TM == 32 || TM == 128, "token tile rows");
+    static __device__ __forceinline__ int x_off(int s) { return kOffX + s * kXTile; }
+    static __device__ __forceinline__ int w_off(int s) { return kOffW + s * kWTile; }
+    static __device__ __forceinline__ int sfw_off(int s) { return kOffSF + s * kSfStage; }
+    static __device__ __forceinline__ int sfx_off(int s) { return kOffSF + s * kSfStage + 1024; }
 };
 
 __device__ __forceinline__ void record_timeout(const GemmParams& p, volatile int* abort_flag, int site) {
@@ -210,10 +220,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
-                    uint8_t* st = smem + stage * C::kStageBytes;
                     ptx::mbar_arrive_expect_tx(&full[stage], tx);
-                    ptx::tma_load_2d(st, &tmW, &full[stage], 0, static_cast<int32_t>((tile0 + kc) * 256));
-                    ptx::bulk_load(st + C::kOffSFW, p.a_sf + static_cast<size_t>(tile0 + kc) * 1024, 1024, &full[stage]);
+                    ptx::tma_load_2d(smem + C::w_off(stage), &tmW, &full[stage], 0,
+                                     static_cast<int32_t>((tile0 + kc) * 256));
+                    ptx::bulk_load(smem + C::sfw_off(stage), p.a_sf + static_cast<size_t>(tile0 + kc) * 1024, 1024,
+                                   &full[stage]);
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1;
@@ -250,8 +261,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
-                    ptx::tma_load_2d(smem + C::kOffX + stage * C::kXTile, &tmX, &full[stage], kc * 128, vi.y);
-                    ptx::bulk_load(smem + stage * C::kStageBytes + C::kOffSFX, sfx + kc * 512, 512, &full[stage]);
+                    ptx::tma_load_2d(smem + C::x_off(stage), &tmX, &full[stage], kc * 128, vi.y);
+                    ptx::bulk_load(smem + C::sfx_off(stage), sfx + kc * 512, 512, &full[stage]);
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1;
@@ -278,13 +289,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     ptx::tc_fence_after();
-                    const uint8_t* st = smem + stage * C::kStageBytes;
                     const uint32_t sf = tmem + C::kAccCols + stage * C::kSfCols;
-                    ptx::tc_cp_32x128b_warpx4(sf, ptx::sdesc_sf(ptx::smem_u32(st + C::kOffSFX)));
-                    ptx::tc_cp_32x128b_warpx4(sf + 4, ptx::sdesc_sf(ptx::smem_u32(st + C::kOffSFW)));
-                    ptx::tc_cp_32x128b_warpx4(sf + 8, ptx::sdesc_sf(ptx::smem_u32(st + C::kOffSFW + 512)));
-                    const uint32_t xa = ptx::smem_u32(smem + C::kOffX + stage * C::kXTile);
-                    const uint32_t wa = ptx::smem_u32(st);
+                    ptx::tc_cp_32x128b_warpx4(sf, ptx::sdesc_sf(ptx::smem_u32(smem + C::sfx_off(stage))));
+                    ptx::tc_cp_32x128b_warpx4(sf + 4, ptx::sdesc_sf(ptx::smem_u32(smem + C::sfw_off(stage))));
+                    ptx::tc_cp_32x128b_warpx4(sf + 8, ptx::sdesc_sf(ptx::smem_u32(smem + C::sfw_off(stage) + 512)));
+                    const uint32_t xa = ptx::smem_u32(smem + C::x_off(stage));
+                    const uint32_t wa = ptx::smem_u32(smem + C::w_off(stage));
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
                         ptx::mma_mxf8f6f4(tmem, ptx::sdesc_sw128(xa + kk * 32), ptx::sdesc_sw128(wa + kk * 32),
