@@ -14,7 +14,10 @@ Functions and the passages they follow (reference page titles):
                 sections 1 and 5, including the expert_offset slice).
   forward    -- the dataflow of the "[SGLang] CUTLASS MoE" structure diagram
                 with MXFP8 activations, MXFP4 weights, silu_and_mul (section 4)
-                and apply_shuffle_mul_sum (section 5).
+                and apply_shuffle_mul_sum (section 5); the FC1 activation may
+                instead be the clamped SwiGLU or SiTU of "... MXFP4 decode MoE
+                ... shape templates", section 4.
+  activation -- h(gate, up) of one element, fp64.
   quantize_* -- the OCP MX v1.0 conversion rule for E2M1 / E4M3 blocks of 32.
 """
 from __future__ import annotations
@@ -32,6 +35,9 @@ _lib = None
 
 FMT_E2M1 = 0
 FMT_E4M3 = 1
+ACT_SWIGLU = 0
+ACT_SWIGLU_CLAMP = 1
+ACT_SITU = 2
 
 
 def build(force: bool = False) -> str:
@@ -62,6 +68,8 @@ def lib():
         L.oracle_e8m0_value.argtypes = [i32]
         L.oracle_bf16_rne.restype = ctypes.c_uint16
         L.oracle_bf16_rne.argtypes = [dbl]
+        L.oracle_activation.restype = dbl
+        L.oracle_activation.argtypes = [i32, dbl, dbl, dbl, dbl]
         L.oracle_mx_quantize_block.restype = None
         L.oracle_mx_quantize_block.argtypes = [P, i32, i32, P, P]
         L.oracle_quantize_mxfp4.restype = None
@@ -73,7 +81,7 @@ def lib():
         L.oracle_sort.restype = i32
         L.oracle_sort.argtypes = [i32, i32, P, i32, i32, i32, i32, i32, P, P, P, P, P]
         L.oracle_forward.restype = i32
-        L.oracle_forward.argtypes = [i32] * 8 + [P] * 8 + [i32] + [P] * 7
+        L.oracle_forward.argtypes = [i32] * 8 + [P] * 8 + [i32] + [P] * 7 + [i32, dbl, dbl]
         _lib = L
     return _lib
 
@@ -101,6 +109,12 @@ def e8m0_value(code: int) -> float:
 
 def bf16_rne(d: float) -> int:
     return int(lib().oracle_bf16_rne(float(d)))
+
+
+def activation(act: int, params, g: float, u: float) -> float:
+    """h(g, u) of the FC1 epilogue; params = (limit,) or (beta, linear_beta)."""
+    c = (list(params) + [0.0, 0.0])[:2]
+    return lib().oracle_activation(int(act), float(c[0]), float(c[1]), float(g), float(u))
 
 
 def mx_quantize_block(values, fmt: int):
@@ -165,12 +179,14 @@ def sort(ids, E_global: int, E_local: int, expert_offset: int, num_shared: int, 
 
 # ------------------------------------------------------------------ forward
 def forward(x_bits, ids, w, wmap, w1, w1s, w2, w2s, *, H: int, I: int, E_global: int, E_local: int,
-            expert_offset: int, num_shared: int, tokens=None, want_act: bool = False, want_xq: bool = False):
+            expert_offset: int, num_shared: int, tokens=None, want_act: bool = False, want_xq: bool = False,
+            activation: int = ACT_SWIGLU, act_params=(0.0, 0.0)):
     """Layer forward for ``tokens`` (default: all).
 
     x_bits uint16 [T, H] (bf16); ids int32 [T, k']; w float64 [T, k'];
     wmap int32 [E_local + S] -> index into the compact weight arrays
     w1 [n, 2I, H/2], w1s [n, 2I, H/32], w2 [n, H, I/2], w2s [n, H, I/32].
+    activation / act_params select the FC1 activation (see ``activation``).
     Returns dict(out_f64, out_bf16 (uint16 bits), [act, act_sf], [xq, xq_sf]).
     """
     x = _c(x_bits, np.uint16)
@@ -187,9 +203,10 @@ def forward(x_bits, ids, w, wmap, w1, w1s, w2, w2s, *, H: int, I: int, E_global:
     xqs = np.zeros((n, H // 32), np.uint8) if want_xq else None
     arrs = [_c(a, np.uint8) for a in (w1, w1s, w2, w2s)]
     wm = _c(wmap, np.int32)
+    c = (list(act_params) + [0.0, 0.0])[:2]
     rc = lib().oracle_forward(T, H, I, kp, E_global, E_local, expert_offset, num_shared, _p(x), _p(ids), _p(w),
                               _p(wm), *[_p(a) for a in arrs], n, _p(toks), _p(out), _p(outb), _p(act), _p(acts),
-                              _p(xq), _p(xqs))
+                              _p(xq), _p(xqs), int(activation), float(c[0]), float(c[1]))
     if rc != 0:
         raise ValueError("oracle_forward: a routed expert has no weights in wmap")
     res = dict(out_f64=out, out_bf16=outb)

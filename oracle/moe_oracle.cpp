@@ -19,6 +19,9 @@
  *        (silu_and_mul: SiLU of the first half times the second half),
  *        section 5 (apply_shuffle_mul_sum: un-permute, multiply by the routing
  *        weight, sum over top-k).
+ *   [P1] section 4 (the FC1 epilogue's activation as a parameter: SiTU with
+ *        constants beta and linear_beta, whose fixed form at beta 4, lb 25 is
+ *        printed there, and the clamped SwiGLU with a limit).
  *   [P5] "[sglang] SGLang MoE shared expert: fuse 3 kernels into 1" -- the
  *        appended shared expert id N_BASE + s and its weight
  *        sigmoid(fp32(logit)) * scale.
@@ -36,6 +39,11 @@
  *     and local index E_local + s.
  *   - Ranks inside an expert follow ascending slot index t*k' + j, which is
  *     ascending token id when a token picks an expert at most once.
+ *   - SiTU<beta, lb>(g, u) = beta tanh(g/beta) sigmoid(g) * lb tanh(u/lb):
+ *     the printed fixed form 2 tanh(g/4) (1 + tanh(g/2)) * 25 tanh(u/25)
+ *     with 1 + tanh(g/2) = 2 sigmoid(g) and the constants generalised.
+ *   - Clamped SwiGLU<L>(g, u) = silu(min(g, L)) * clamp(u, -L, L): the gate
+ *     is capped above, the up projection on both sides.
  */
 #include <algorithm>
 #include <cmath>
@@ -149,6 +157,22 @@ double bf16_to_double(uint16_t b) {
 
 /* Local expert index of a global id, or -1.  Shared experts sit after the
  * routed ones. */
+enum { ACT_SWIGLU = 0, ACT_SWIGLU_CLAMP = 1, ACT_SITU = 2 };
+
+double sigmoid(double z) { return 1.0 / (1.0 + std::exp(-z)); }
+
+/* The FC1 activation h(gate, up) in fp64 ([P3] section 4 for SwiGLU, [P1]
+ * section 4 for the variants). */
+double activation(int act, double c0, double c1, double g, double u) {
+    if (act == ACT_SWIGLU_CLAMP) {
+        double gc = g < c0 ? g : c0;
+        double uc = u < -c0 ? -c0 : (u > c0 ? c0 : u);
+        return gc * sigmoid(gc) * uc;
+    }
+    if (act == ACT_SITU) return c0 * std::tanh(g / c0) * sigmoid(g) * (c1 * std::tanh(u / c1));
+    return g * sigmoid(g) * u;
+}
+
 int local_expert(int32_t id, int E_global, int E_local, int expert_offset, int S) {
     if (id >= E_global && id < E_global + S) return E_local + (id - E_global);
     if (id >= expert_offset && id < expert_offset + E_local) return id - expert_offset;
@@ -192,6 +216,9 @@ double oracle_e2m1_value(int code) { return e2m1_value(code); }
 double oracle_e4m3_value(int code) { return e4m3_value(code); }
 double oracle_e8m0_value(int code) { return e8m0_value(code); }
 uint16_t oracle_bf16_rne(double d) { return bf16_rne(d); }
+/* The FC1 activation: act 0 SwiGLU, 1 clamped SwiGLU (c0 = limit), 2 SiTU
+ * (c0 = beta, c1 = linear beta). */
+double oracle_activation(int act, double c0, double c1, double g, double u) { return activation(act, c0, c1, g, u); }
 
 /* One MX block; fmt 0 = E2M1, 1 = E4M3.  codes are one byte per element. */
 void oracle_mx_quantize_block(const double* v, int n, int fmt, uint8_t* codes, uint8_t* scale_code) {
@@ -308,7 +335,8 @@ int oracle_sort(int T, int kp, const int32_t* ids, int E_global, int E_local, in
  * For each token t in toks[0..ntok):
  *   xq = MXFP8(x[t]);  for each slot j with a local expert e:
  *     G[r] = sum_h dec(xq[h]) dec(W1[e][r][h]),  U[r] = same with row I + r
- *     h[r] = silu(G[r]) * U[r]           (silu(g) = g / (1 + exp(-g)))
+ *     h[r] = act(G[r], U[r])             (SwiGLU: silu(g) u, silu(g) = g / (1 + exp(-g));
+ *                                         the variants as in activation())
  *     hq = MXFP8(h);  Y[n] = sum_i dec(hq[i]) dec(W2[e][n][i])
  *     acc[n] += w[t,j] * Y[n]             (j ascending)
  *   out_f64[t] = acc, out_bf16[t] = bf16_rne(acc).
@@ -319,7 +347,8 @@ int oracle_forward(int T, int H, int I, int kp, int E_global, int E_local, int e
                    const uint16_t* x, const int32_t* ids, const double* w, const int32_t* wmap,
                    const uint8_t* w1, const uint8_t* w1s, const uint8_t* w2, const uint8_t* w2s, int ntok,
                    const int32_t* toks, double* out_f64, uint16_t* out_bf16, uint8_t* act_codes,
-                   uint8_t* act_scales, uint8_t* xq_codes, uint8_t* xq_scales) {
+                   uint8_t* act_scales, uint8_t* xq_codes, uint8_t* xq_scales, int act, double act_c0,
+                   double act_c1) {
     (void)T;
     std::vector<uint8_t> xq(H), xs(H / 32), hq(I), hs(I / 32);
     std::vector<double> xd(H), G(I), U(I), hv(I), hd(I), acc(H), Y(H), wg(H), wu(H), w2r(I);
@@ -357,7 +386,7 @@ int oracle_forward(int T, int H, int I, int kp, int E_global, int E_local, int e
                 }
                 G[r] = g;
                 U[r] = u;
-                hv[r] = g / (1.0 + std::exp(-g)) * u;
+                hv[r] = activation(act, act_c0, act_c1, g, u);
             }
             for (int b = 0; b < I / 32; ++b) mx_quantize_block(&hv[b * 32], 32, FMT_E4M3, &hq[b * 32], &hs[b]);
             if (ac) std::memcpy(ac, hq.data(), I);

@@ -53,6 +53,8 @@ class MoeConfig:
     zipf_s: float = 0.0             # > 0: logits += -s * ln(e + 1)
     shared_scale: float = 1.0
     weight_sigma: float = 0.02
+    activation: int = 0             # FC1 activation: 0 SwiGLU, 1 clamped SwiGLU, 2 SiTU
+    act_params: tuple = (0.0, 0.0)  # (limit,) or (beta, linear beta)
 
     @property
     def kp(self) -> int:

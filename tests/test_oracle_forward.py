@@ -17,6 +17,7 @@ import torch
 
 import oracle
 import synth
+from conftest import golden_lines
 
 H = I = 32
 
@@ -78,6 +79,66 @@ def test_hand_case_B_structured_weights():
     assert (act[:8] == 0x7E).all() and (act[8:] == 0).all() and r["act_sf"][0, 0, 0] == 119
     # token 1: every element saturates negative: -448 * 2^-4 = -28
     assert (r["act"][1, 0] == 0xFE).all() and r["act_sf"][1, 0, 0] == 123
+
+
+def _run_act(x_rows, ids, w, experts, act, params):
+    w1, w1s, w2, w2s = _weights([e[0] for e in experts], [e[1] for e in experts])
+    E = len(experts)
+    return oracle.forward(_bf16_bits(x_rows), np.asarray(ids, np.int32), np.asarray(w, np.float64),
+                          np.arange(E, dtype=np.int32), w1, w1s, w2, w2s, H=H, I=I, E_global=E, E_local=E,
+                          expert_offset=0, num_shared=0, want_act=True, activation=act, act_params=params)
+
+
+@pytest.mark.parametrize("case,up,act,params,act_code,act_scale,out,out_bits", [
+    ("D", 0.5, oracle.ACT_SWIGLU_CLAMP, (7.0,), 0x7C, 124, 768.0, 0x4440),
+    ("E", -0.125, oracle.ACT_SWIGLU_CLAMP, (7.0,), 0xFE, 123, -448.0, 0xC3E0),
+    ("F", 0.5, oracle.ACT_SITU, (4.0, 25.0), 0x7E, 124, 896.0, 0x4460),
+])
+def test_hand_cases_activation_variants(case, up, act, params, act_code, act_scale, out, out_bits):
+    rows = {ln.split()[0]: ln.split() for ln in golden_lines("forward_hand_cases.txt")}
+    assert rows[case][1] == "all" and float(rows[case][2]) == out and float(rows[case][4]) == out
+    w1 = np.concatenate([np.full((I, H), 0.5), np.full((I, H), up)]).astype(np.float32)
+    ex = (w1, np.full((H, I), 0.5, np.float32))
+    r = _run_act([[1.0] * H], [[0]], [[1.0]], [ex, ex], act, params)
+    assert (r["act"][0, 0] == act_code).all() and (r["act_sf"][0, 0] == act_scale).all()
+    np.testing.assert_array_equal(r["out_f64"], np.full((1, H), out))
+    assert (r["out_bf16"] == out_bits).all()
+
+
+def _printed_situ_4_25(g, u):
+    """The fixed-constant SiTU as the shape-templates page prints it (beta 4, lb 25)."""
+    return 2.0 * math.tanh(g * 0.25) * (1.0 + math.tanh(g * 0.5)) * (25.0 * math.tanh(u * 0.04))
+
+
+def test_situ_4_25_matches_the_printed_fixed_form():
+    rng = np.random.default_rng(3)
+    for g, u in list(rng.normal(0, 6, size=(200, 2))) + [(0.0, 1.0), (40.0, -60.0), (-40.0, 3.0)]:
+        assert oracle.activation(oracle.ACT_SITU, (4.0, 25.0), g, u) == pytest.approx(_printed_situ_4_25(g, u),
+                                                                                       rel=1e-12, abs=1e-12)
+
+
+def test_activation_limits_and_symmetries():
+    rng = np.random.default_rng(4)
+    for g, u in rng.normal(0, 3, size=(200, 2)):
+        sw = oracle.activation(oracle.ACT_SWIGLU, (), g, u)
+        assert sw == pytest.approx(g / (1 + math.exp(-g)) * u, rel=1e-13, abs=1e-15)
+        # unbounded constants reduce both variants to SwiGLU
+        assert oracle.activation(oracle.ACT_SITU, (1e7, 1e7), g, u) == pytest.approx(sw, rel=1e-9, abs=1e-12)
+        assert oracle.activation(oracle.ACT_SWIGLU_CLAMP, (1e9,), g, u) == sw
+        # odd in the up projection
+        assert oracle.activation(oracle.ACT_SITU, (2.0, 3.0), g, -u) == -oracle.activation(oracle.ACT_SITU,
+                                                                                            (2.0, 3.0), g, u)
+        # SiTU's factors are bounded by beta and lb
+        assert abs(oracle.activation(oracle.ACT_SITU, (2.0, 3.0), g, u)) <= 2.0 * 3.0
+    L = 1.5
+    for g, u in [(0.3, -0.7), (-5.0, 1.0)]:  # inside the clamp (the gate is capped above only)
+        assert oracle.activation(oracle.ACT_SWIGLU_CLAMP, (L,), g, u) == oracle.activation(oracle.ACT_SWIGLU, (), g, u)
+    s = oracle.activation(oracle.ACT_SWIGLU, (), L, 1.0)  # silu(L)
+    assert oracle.activation(oracle.ACT_SWIGLU_CLAMP, (L,), 9.0, 1.0) == s
+    assert oracle.activation(oracle.ACT_SWIGLU_CLAMP, (L,), 9.0, 4.0) == pytest.approx(s * L, rel=1e-15)
+    assert oracle.activation(oracle.ACT_SWIGLU_CLAMP, (L,), 9.0, -4.0) == pytest.approx(-s * L, rel=1e-15)
+    assert oracle.activation(oracle.ACT_SWIGLU_CLAMP, (L,), -0.5, 4.0) == pytest.approx(
+        oracle.activation(oracle.ACT_SWIGLU, (), -0.5, L), rel=1e-15)
 
 
 def test_hand_case_C_weighted_sum():
