@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--tokens", type=int, default=0, help="override the workload's token count (profiling cases)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--block-n", type=int, default=0, help="override the workload's virtual-expert rows")
+    ap.add_argument("--act", default="swiglu", choices=["swiglu", "swiglu_clamp", "situ"],
+                    help="FC1 activation: SwiGLU (the workload's), clamped SwiGLU (limit 7) or SiTU (beta 4, lb 25)")
     return ap.parse_args()
 
 
@@ -154,7 +156,8 @@ def setup_layer(cfg, device):
 
     shape = moe.MoeShape(T=cfg.T, max_T=cfg.T, E_global=cfg.E_global, E_local=cfg.E_local,
                          expert_offset=cfg.expert_offset, top_k=cfg.top_k, num_shared=cfg.num_shared,
-                         hidden=cfg.hidden, inter=cfg.inter, block_n=cfg.block_n, shared_scale=cfg.shared_scale)
+                         hidden=cfg.hidden, inter=cfg.inter, block_n=cfg.block_n, shared_scale=cfg.shared_scale,
+                         activation=cfg.activation, act_params=tuple(cfg.act_params))
     gids = cfg.global_ids
     E, H, I = gids.size, cfg.hidden, cfg.inter
     c1 = torch.empty((E, 2 * I, H // 2), dtype=torch.uint8, device=device)
@@ -295,7 +298,8 @@ def run_ours(args, cfg):
         "data": "synthetic (seeded Irwin-Hall normal inputs, random-init weights quantised to MXFP4)",
         "config": {"workload": cfg.name, "T": cfg.T, "E_global": cfg.E_global, "E_local": cfg.E_local,
                    "top_k": cfg.top_k, "num_shared": cfg.num_shared, "hidden": H, "inter": I,
-                   "block_n": cfg.block_n, "seed": cfg.seed, "l2": "flushed before every step (512 MiB memset, then "
+                   "block_n": cfg.block_n, "seed": cfg.seed, "activation": ACT_NAMES[cfg.activation],
+                   "act_params": list(cfg.act_params), "l2": "flushed before every step (512 MiB memset, then "
                    "a 256 MiB read of another buffer; outside the step events)", "graph": "one CUDA graph per step", "parallelism": "replicas"},
         "layer": {"routed_rows": R, "touched_experts": touched, "weight_bytes_touched": layer_weight_bytes,
                   "hbm_frac_layer": layer_weight_bytes / (ms * 1e-3) / 1e9 / hbm,
@@ -401,7 +405,7 @@ def oracle_step(cfg, tokens, cache):
     arrs = [np.stack([wc[e][i] for e in loc]) for i in range(4)]
     oracle.forward(cache["x"], ids, w, wmap, *arrs, H=cfg.hidden, I=cfg.inter, E_global=cfg.E_global,
                    E_local=cfg.E_local, expert_offset=cfg.expert_offset, num_shared=cfg.num_shared,
-                   tokens=np.asarray(tokens, np.int32))
+                   tokens=np.asarray(tokens, np.int32), activation=cfg.activation, act_params=cfg.act_params)
 
 
 def cpu_baseline(cfg, budget_s=12.0):
@@ -466,6 +470,10 @@ def allreduce_max(v, world, device):
     return float(t.item())
 
 
+ACT_NAMES = ["swiglu", "swiglu_clamp", "situ"]
+ACT_DEFAULT_PARAMS = [(0.0, 0.0), (7.0, 0.0), (4.0, 25.0)]
+
+
 def main():
     args = parse()
     import synth
@@ -474,6 +482,9 @@ def main():
         cfg = cfg.replace(T=args.tokens, name="%s_T%d" % (cfg.name, args.tokens))
     if args.block_n:
         cfg = cfg.replace(block_n=args.block_n, name="%s_B%d" % (cfg.name, args.block_n))
+    if args.act != "swiglu":
+        act = ACT_NAMES.index(args.act)
+        cfg = cfg.replace(activation=act, act_params=ACT_DEFAULT_PARAMS[act], name="%s_%s" % (cfg.name, args.act))
     if args.impl == "reference":
         run_reference(args, cfg)
     else:

@@ -10,8 +10,8 @@
  *            optional appended shared expert with weight sigmoid(logit)*scale
  *   sort   : token -> expert rows (expert_offsets, a_map, c_map) and virtual
  *            experts of block_n rows
- *   forward: x -> MXFP8, FC1 = [gate | up] on E2M1 weights, silu(gate)*up ->
- *            MXFP8, FC2, weighted un-permute combine -> bf16 out
+ *   forward: x -> MXFP8, FC1 = [gate | up] on E2M1 weights, activation
+ *            h(gate, up) -> MXFP8, FC2, weighted un-permute combine -> bf16 out
  *
  * Ownership: the caller allocates every buffer (device memory unless stated).
  * The library never allocates device memory, never frees and never
@@ -52,7 +52,18 @@ enum {
     MOE_ERR_TIMEOUT = -6    /* device status: a bounded wait expired */
 };
 
-enum { MOE_ACT_SWIGLU = 0 }; /* silu(gate) * up, gate = W1 rows [0, I), up = rows [I, 2I) */
+/* FC1 epilogue activation h(g, u) of gate g = W1 rows [0, I) and up u =
+ * rows [I, 2I), evaluated in fp32 before the MXFP8 requantisation
+ * ("... MXFP4 decode MoE ... shape templates", section 4: the epilogue's
+ * activation is a parameter, SiTU<beta, linear_beta> or SwiGLU<limit>).
+ *   MOE_ACT_SWIGLU        silu(g) * u,  silu(g) = g / (1 + exp(-g))
+ *   MOE_ACT_SWIGLU_CLAMP  silu(min(g, L)) * clamp(u, -L, L),
+ *                         L = act_params[0] > 0 (the clamped SwiGLU)
+ *   MOE_ACT_SITU          (beta tanh(g / beta)) sigmoid(g) * lb tanh(u / lb),
+ *                         beta = act_params[0] > 0, lb = act_params[1] > 0
+ *                         (beta 4, lb 25 give the section's fixed form
+ *                         2 tanh(g/4) (1 + tanh(g/2)) * 25 tanh(u/25)) */
+enum { MOE_ACT_SWIGLU = 0, MOE_ACT_SWIGLU_CLAMP = 1, MOE_ACT_SITU = 2 };
 
 /* Shape of one layer call.
  *   T            tokens in this call (0 <= T <= max_T)
@@ -69,13 +80,16 @@ enum { MOE_ACT_SWIGLU = 0 }; /* silu(gate) * up, gate = W1 rows [0, I), up = row
  *   block_n      rows per virtual expert = token rows of a GEMM tile: 16 or
  *                32 (decode tiling, fp32 FC2 rows) or 128 (prefill tiling,
  *                bf16 FC2 rows); the layer's value does not depend on it
- *   activation   MOE_ACT_SWIGLU
+ *   activation   MOE_ACT_SWIGLU, MOE_ACT_SWIGLU_CLAMP or MOE_ACT_SITU
  *   shared_scale multiplies the shared expert's sigmoid weight (e.g.
- *                1/ep_size, "... shared expert: fuse 3 kernels into 1") */
+ *                1/ep_size, "... shared expert: fuse 3 kernels into 1")
+ *   act_params   the activation's constants (finite, > 0 where used; unused
+ *                entries are ignored) */
 typedef struct moe_shape {
     int32_t T, max_T, E_global, E_local, expert_offset, top_k, num_shared;
     int32_t hidden, inter, block_n, activation;
     float shared_scale;
+    float act_params[2];
 } moe_shape;
 
 /* Packed expert weights (device, read only), E_tot = E_local + num_shared,
@@ -96,7 +110,7 @@ typedef struct moe_weights {
  *   a_map        int32[R] row -> slot t*k' + j;  c_map int32[T*k'] slot -> row or -1
  *   xq           E4M3 [rows_alloc, H]: row r = MXFP8(x[a_map[r] / k'])
  *   xq_sf        E8M0 of xq in the tile layout (see moe_forward)
- *   act, act_sf  the FC1 output (silu(gate)*up, MXFP8) in the same layouts
+ *   act, act_sf  the FC1 output (the activation h(gate, up), MXFP8) in the same layouts
  *   y            the FC2 output rows [R, H], already multiplied by the routing
  *                weight: fp32 for block_n 16/32, bf16 for block_n 128 */
 typedef struct moe_views {
@@ -167,10 +181,11 @@ int moe_sort(const moe_shape* shape, const int32_t* topk_ids, void* workspace, s
 
 /* Forward after moe_sort: x bf16 [T, H] -> out bf16 [T, H].
  *   out[t] = bf16( sum_{j: c_map[t,j] >= 0, ascending j} topk_w[t,j] *
- *                  Y_j(t) ),  Y_j = FC2(MXFP8(silu(G) * U)), [G | U] =
- *                  FC1(MXFP8(x[t])) with expert topk_ids[t,j]'s weights.
+ *                  Y_j(t) ),  Y_j = FC2(MXFP8(h(G, U))), [G | U] =
+ *                  FC1(MXFP8(x[t])) with expert topk_ids[t,j]'s weights and h
+ *                  the shape's activation.
  * FC1/FC2 run on tcgen05 block-scaled tensor cores (E4M3 x E2M1, fp32
- * accumulation), the SwiGLU + MXFP8 requantisation is fused into the FC1
+ * accumulation), the activation + MXFP8 requantisation is fused into the FC1
  * epilogue and the routing-weight multiply into the FC2 epilogue.
  * x, out 16-byte aligned. */
 int moe_forward(const moe_shape* shape, const uint16_t* x, const moe_weights* weights, const float* topk_w,

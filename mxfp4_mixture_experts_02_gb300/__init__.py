@@ -39,7 +39,13 @@ class MoeError(RuntimeError):
 class _Shape(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("T", "max_T", "E_global", "E_local", "expert_offset", "top_k",
                                                "num_shared", "hidden", "inter", "block_n", "activation")] + \
-               [("shared_scale", ctypes.c_float)]
+               [("shared_scale", ctypes.c_float), ("act_params", ctypes.c_float * 2)]
+
+
+# FC1 epilogue activations (the MOE_ACT_* values of the C header)
+ACT_SWIGLU = 0        # silu(g) * u
+ACT_SWIGLU_CLAMP = 1  # silu(min(g, L)) * clamp(u, -L, L), L = act_params[0]
+ACT_SITU = 2          # beta tanh(g/beta) sigmoid(g) * lb tanh(u/lb), (beta, lb) = act_params
 
 
 class _Weights(ctypes.Structure):
@@ -68,13 +74,16 @@ class MoeShape:
     block_n: int
     activation: int = 0
     shared_scale: float = 1.0
+    act_params: tuple = (0.0, 0.0)
 
     @property
     def kp(self):
         return self.top_k + self.num_shared
 
     def c(self) -> _Shape:
-        return _Shape(**dataclasses.asdict(self))
+        d = dataclasses.asdict(self)
+        d["act_params"] = (ctypes.c_float * 2)(*[float(v) for v in d["act_params"]])
+        return _Shape(**d)
 
 
 @dataclasses.dataclass

@@ -203,6 +203,9 @@ int run_forward(const moe_shape* s, const uint16_t* x, const moe_weights* wt, co
     g.out_sf_tile_bytes = L.asf_tile_bytes;
     g.a_tx_bytes = 256 * kFp4BytesPer128Row;
     g.wait_ns = kWaitLimitNs;
+    g.act_kind = s->activation;
+    g.act_c0 = s->act_params[0];
+    g.act_c1 = s->act_params[1];
 
     g.a_sf = wt->w1_sf;
     g.b_sf = at<uint8_t>(ws, L.xsf);
@@ -249,7 +252,14 @@ int moe_is_supported(const moe_shape* s) {
     if (s->expert_offset < 0 || s->expert_offset + s->E_local > s->E_global) return 0;
     if (s->T < 0 || s->T > s->max_T || s->max_T < 1) return 0;
     if (static_cast<int64_t>(s->max_T) * kp >= (1 << 24)) return 0;
-    if (s->activation != MOE_ACT_SWIGLU) return 0;
+    const auto positive = [](float c) { return c > 0.f && c <= 3.0e38f; };  // finite and > 0
+    if (s->activation == MOE_ACT_SWIGLU_CLAMP) {
+        if (!positive(s->act_params[0])) return 0;
+    } else if (s->activation == MOE_ACT_SITU) {
+        if (!positive(s->act_params[0]) || !positive(s->act_params[1])) return 0;
+    } else if (s->activation != MOE_ACT_SWIGLU) {
+        return 0;
+    }
     return 1;
 }
 

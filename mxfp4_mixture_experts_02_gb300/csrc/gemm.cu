@@ -12,9 +12,11 @@
 // instruction count of a weight-streaming (decode) GEMM against 128 rows.
 //
 //   FC1: B = W1[e] gate rows f0..f0+127 and up rows I+f0.. (packed adjacent),
-//        K = H.  Epilogue: h = silu(gate) * up in fp32 and MXFP8 per token
-//        and 32 features -> act / act_sf ("[SGLang] CUTLASS MoE", section 4
-//        silu_and_mul, fused into the GEMM).
+//        K = H.  Epilogue: the activation h(gate, up) in fp32 and MXFP8 per
+//        token and 32 features -> act / act_sf ("[SGLang] CUTLASS MoE",
+//        section 4 silu_and_mul, fused into the GEMM; the clamped SwiGLU and
+//        SiTU variants of "... MXFP4 decode MoE ... shape templates",
+//        section 4).
 //   FC2: B = W2[e] rows nb*256.., K = I.  Epilogue: times the routing weight
 //        of the row's slot -> Y rows (the multiply of section 5's
 //        apply_shuffle_mul_sum, fused).
@@ -28,7 +30,7 @@
 // warps 0 and 4 work), 8 weight producer and 10 token producer (one thread
 // each, filling the same STAGES-deep ring: a single issuing thread could not
 // keep up with the MMAs), 9 TMEM allocator and single-thread MMA issuer.  The epilogue releases the accumulator as soon as
-// its TMEM loads complete, so the next item's MMAs overlap the SwiGLU /
+// its TMEM loads complete, so the next item's MMAs overlap the activation /
 // quantise / store math.  Every wait is bounded; on expiry the CTA records
 // MOE_ERR_TIMEOUT in the workspace status word, stops, lets its MMAs drain,
 // frees TMEM and exits.
@@ -119,6 +121,32 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, ui
 }
 
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
+
+// FC1 activations h(gate, up) ("... MXFP4 decode MoE ... shape templates",
+// section 4).  c0 / c1 are the constants, i0 / i1 their reciprocals.
+//   SwiGLU         silu(g) * u
+//   clamped SwiGLU silu(min(g, L)) * clamp(u, -L, L), L = c0
+//   SiTU           beta tanh(g / beta) sigmoid(g) * lb tanh(u / lb), beta = c0,
+//                  lb = c1 (beta 4, lb 25: the section's fixed
+//                  2 tanh(g/4) (1 + tanh(g/2)) * 25 tanh(u/25), since
+//                  1 + tanh(g/2) = 2 sigmoid(g))
+template <int ACT>
+__device__ __forceinline__ float activation(float g, float u, float c0, float c1, float i0, float i1) {
+    if constexpr (ACT == MOE_ACT_SWIGLU_CLAMP) {
+        return silu(fminf(g, c0)) * fminf(fmaxf(u, -c0), c0);
+    } else if constexpr (ACT == MOE_ACT_SITU) {
+        return c0 * tanhf(g * i0) / (1.0f + expf(-g)) * (c1 * tanhf(u * i1));
+    } else {
+        return silu(g) * u;
+    }
+}
+
+template <int ACT>
+__device__ __forceinline__ void activation_block(const uint32_t (&g)[32], const uint32_t (&u)[32], float (&h)[32],
+                                                 float c0, float c1, float i0, float i1) {
+#pragma unroll
+    for (int c = 0; c < 32; ++c) h[c] = activation<ACT>(__uint_as_float(g[c]), __uint_as_float(u[c]), c0, c1, i0, i1);
+}
 
 // 32 fp32 -> MXFP8 (E4M3 codes in 8 words, E8M0 code returned).
 __device__ __forceinline__ uint32_t mxfp8_block(const float* v, uint32_t (&w)[8]) {
@@ -318,6 +346,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool active = (TM > 32) || q == 0;
         uint32_t aphase = 0;
         const int i = q * 32 + lane;  // token row of this lane within a tile
+        // reciprocals of the SiTU constants (unused by the other activations)
+        const float act_i0 = p.act_kind == MOE_ACT_SITU ? 1.0f / p.act_c0 : 0.f;
+        const float act_i1 = p.act_kind == MOE_ACT_SITU ? 1.0f / p.act_c1 : 0.f;
         // Descriptors two items ahead and row weights one item ahead are
         // loaded early, so no dependent load chain sits between two items.
         const int4 kNoTile = kNone;
@@ -412,9 +443,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int b = 0; b < 2; ++b) {
                         float h[32];
-#pragma unroll
-                        for (int c = 0; c < 32; ++c)
-                            h[c] = silu(__uint_as_float(r[b][c])) * __uint_as_float(r[2 + b][c]);
+                        if (p.act_kind == MOE_ACT_SITU)
+                            activation_block<MOE_ACT_SITU>(r[b], r[2 + b], h, p.act_c0, p.act_c1, act_i0, act_i1);
+                        else if (p.act_kind == MOE_ACT_SWIGLU_CLAMP)
+                            activation_block<MOE_ACT_SWIGLU_CLAMP>(r[b], r[2 + b], h, p.act_c0, p.act_c1, act_i0,
+                                                                   act_i1);
+                        else
+                            activation_block<MOE_ACT_SWIGLU>(r[b], r[2 + b], h, p.act_c0, p.act_c1, act_i0, act_i1);
                         uint32_t wq[8];
                         const uint32_t sc = mxfp8_block(h, wq);
                         uint4* dst = reinterpret_cast<uint4*>(p.act + row * p.I + f0 + 32 * b);

@@ -22,7 +22,8 @@ def shape_of(cfg: synth.MoeConfig, T: int | None = None) -> moe.MoeShape:
     T = cfg.T if T is None else T
     return moe.MoeShape(T=T, max_T=max(T, 1), E_global=cfg.E_global, E_local=cfg.E_local,
                         expert_offset=cfg.expert_offset, top_k=cfg.top_k, num_shared=cfg.num_shared,
-                        hidden=cfg.hidden, inter=cfg.inter, block_n=cfg.block_n, shared_scale=cfg.shared_scale)
+                        hidden=cfg.hidden, inter=cfg.inter, block_n=cfg.block_n, shared_scale=cfg.shared_scale,
+                        activation=cfg.activation, act_params=tuple(cfg.act_params))
 
 
 def device_weights(cfg: synth.MoeConfig, chunk: int = 64, keep_rowmajor: bool = False):
@@ -114,7 +115,8 @@ class OracleCase:
             arrs = tuple(np.stack([w[i] for w in ws]) for i in range(4))
         return oracle.forward(self.x, self.ids, self.w, wmap, *arrs, H=c.hidden, I=c.inter, E_global=c.E_global,
                               E_local=c.E_local, expert_offset=c.expert_offset, num_shared=c.num_shared,
-                              tokens=tokens, want_act=True, want_xq=True)
+                              tokens=tokens, want_act=True, want_xq=True, activation=c.activation,
+                              act_params=c.act_params)
 
 
 def bf16_bits(t: torch.Tensor) -> np.ndarray:

@@ -40,13 +40,19 @@ GRID = [
     SMALL.replace(T=40, block_n=32, E_global=16, E_local=16, hidden=3584, inter=256),
     SMALL.replace(T=1200, block_n=128, E_global=8, E_local=8, top_k=2, hidden=3584, inter=128),
     synth.CONFIGS["tiny"],
+    # FC1 activation variants (clamped SwiGLU, SiTU) with constants small
+    # enough that the clamps and the tanh soft caps act on most elements
+    SMALL.replace(T=48, block_n=32, activation=1, act_params=(0.75, 0.0)),
+    SMALL.replace(T=96, block_n=16, num_shared=1, activation=2, act_params=(1.0, 0.5)),
+    SMALL.replace(T=200, block_n=128, top_k=8, activation=1, act_params=(0.5, 0.0)),
+    SMALL.replace(T=64, block_n=128, hidden=1536, inter=384, activation=2, act_params=(0.5, 0.25)),
 ]
 FULL = [synth.CONFIGS[n] for n in ("decode_t32", "ep_slice_t64", "skewed_shared_t256", "prefill_t32768")]
 
 
 def _cid(c):
-    return "%s-T%d-B%d-E%d+%d-S%d-H%d-I%d" % (c.name, c.T, c.block_n, c.E_local, c.expert_offset, c.num_shared,
-                                               c.hidden, c.inter)
+    return "%s-T%d-B%d-E%d+%d-S%d-H%d-I%d-A%d" % (c.name, c.T, c.block_n, c.E_local, c.expert_offset,
+                                                   c.num_shared, c.hidden, c.inter, c.activation)
 
 
 _WCACHE = {}
@@ -153,6 +159,13 @@ def test_layer_grid_vs_oracle(cfg):
 @pytest.mark.parametrize("cfg", FULL, ids=_cid)
 def test_layer_full_size_vs_oracle(cfg):
     check_layer(cfg, tokens=sample_tokens(cfg.T, 4))
+
+
+@pytest.mark.parametrize("act,params", [(1, (7.0, 0.0)), (2, (4.0, 25.0))])
+def test_decode_layer_activation_variants_vs_oracle(act, params):
+    # the decode layer with the clamped SwiGLU at the usual limit 7 and SiTU
+    # with the constants the shape-templates page fixes (beta 4, lb 25)
+    check_layer(synth.CONFIGS["decode_t32"].replace(activation=act, act_params=params), tokens=sample_tokens(32, 4))
 
 
 def test_weight_quantiser_bit_exact():

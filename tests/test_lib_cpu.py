@@ -36,10 +36,15 @@ def test_supported_shapes_and_limits():
     assert moe.moe_is_supported(_shape())
     assert moe.moe_is_supported(_shape(block_n=16, E_local=448, expert_offset=448, T=64, max_T=64))
     assert moe.moe_is_supported(_shape(num_shared=1, T=256, max_T=256))
+    assert moe.moe_is_supported(_shape(activation=moe.ACT_SWIGLU_CLAMP, act_params=(7.0, 0.0)))
+    assert moe.moe_is_supported(_shape(activation=moe.ACT_SITU, act_params=(4.0, 25.0)))
     bad = [dict(hidden=3500), dict(hidden=256), dict(inter=192), dict(block_n=64), dict(block_n=8),
            dict(top_k=0), dict(top_k=33), dict(top_k=900, E_global=896), dict(E_global=2048, E_local=2048),
            dict(num_shared=2), dict(E_local=0), dict(expert_offset=448), dict(expert_offset=-1),
-           dict(T=33), dict(T=-1), dict(max_T=1 << 20), dict(activation=1)]
+           dict(T=33), dict(T=-1), dict(max_T=1 << 20), dict(activation=3), dict(activation=-1),
+           dict(activation=1), dict(activation=1, act_params=(-1.0, 0.0)),
+           dict(activation=1, act_params=(float("inf"), 0.0)), dict(activation=1, act_params=(float("nan"), 0.0)),
+           dict(activation=2, act_params=(4.0, 0.0)), dict(activation=2, act_params=(0.0, 25.0))]
     for kw in bad:
         assert not moe.moe_is_supported(_shape(**kw)), kw
 
