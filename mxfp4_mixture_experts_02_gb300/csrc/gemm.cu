@@ -127,15 +127,18 @@ __device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
 //   SwiGLU         silu(g) * u
 //   clamped SwiGLU silu(min(g, L)) * clamp(u, -L, L), L = c0
 //   SiTU           beta tanh(g / beta) sigmoid(g) * lb tanh(u / lb), beta = c0,
-//                  lb = c1 (beta 4, lb 25: the section's fixed
-//                  2 tanh(g/4) (1 + tanh(g/2)) * 25 tanh(u/25), since
-//                  1 + tanh(g/2) = 2 sigmoid(g))
+//                  lb = c1, evaluated as (beta / 2) tanh(g / beta)
+//                  (1 + tanh(g / 2)) * lb tanh(u / lb) with the hardware
+//                  tanh approximation, as the section's kernel does (beta 4,
+//                  lb 25 give its fixed form 2 tanh(g/4) (1 + tanh(g/2)) *
+//                  25 tanh(u/25))
 template <int ACT>
 __device__ __forceinline__ float activation(float g, float u, float c0, float c1, float i0, float i1) {
     if constexpr (ACT == MOE_ACT_SWIGLU_CLAMP) {
         return silu(fminf(g, c0)) * fminf(fmaxf(u, -c0), c0);
     } else if constexpr (ACT == MOE_ACT_SITU) {
-        return c0 * tanhf(g * i0) / (1.0f + expf(-g)) * (c1 * tanhf(u * i1));
+        return (0.5f * c0) * ptx::tanh_approx(g * i0) * (1.0f + ptx::tanh_approx(0.5f * g)) *
+               (c1 * ptx::tanh_approx(u * i1));
     } else {
         return silu(g) * u;
     }
@@ -164,7 +167,9 @@ __device__ __forceinline__ uint32_t mxfp8_block(const float* v, uint32_t (&w)[8]
     return static_cast<uint32_t>(ex + 127);
 }
 
-template <int TM, bool FC1, bool YBF16, int STAGES>
+// ACT: the FC1 activation (MOE_ACT_*), a template parameter so that each
+// epilogue carries only its own arithmetic.
+template <int TM, bool FC1, bool YBF16, int STAGES, int ACT>
 __global__ void __launch_bounds__(kThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                     const __grid_constant__ CUtensorMap tmY, const GemmParams p) {
@@ -347,8 +352,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t aphase = 0;
         const int i = q * 32 + lane;  // token row of this lane within a tile
         // reciprocals of the SiTU constants (unused by the other activations)
-        const float act_i0 = p.act_kind == MOE_ACT_SITU ? 1.0f / p.act_c0 : 0.f;
-        const float act_i1 = p.act_kind == MOE_ACT_SITU ? 1.0f / p.act_c1 : 0.f;
+        const float act_i0 = ACT == MOE_ACT_SITU ? 1.0f / p.act_c0 : 0.f;
+        const float act_i1 = ACT == MOE_ACT_SITU ? 1.0f / p.act_c1 : 0.f;
         // Descriptors two items ahead and row weights one item ahead are
         // loaded early, so no dependent load chain sits between two items.
         const int4 kNoTile = kNone;
@@ -443,13 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int b = 0; b < 2; ++b) {
                         float h[32];
-                        if (p.act_kind == MOE_ACT_SITU)
-                            activation_block<MOE_ACT_SITU>(r[b], r[2 + b], h, p.act_c0, p.act_c1, act_i0, act_i1);
-                        else if (p.act_kind == MOE_ACT_SWIGLU_CLAMP)
-                            activation_block<MOE_ACT_SWIGLU_CLAMP>(r[b], r[2 + b], h, p.act_c0, p.act_c1, act_i0,
-                                                                   act_i1);
-                        else
-                            activation_block<MOE_ACT_SWIGLU>(r[b], r[2 + b], h, p.act_c0, p.act_c1, act_i0, act_i1);
+                        activation_block<ACT>(r[b], r[2 + b], h, p.act_c0, p.act_c1, act_i0, act_i1);
                         uint32_t wq[8];
                         const uint32_t sc = mxfp8_block(h, wq);
                         uint4* dst = reinterpret_cast<uint4*>(p.act + row * p.I + f0 + 32 * b);
@@ -505,14 +504,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int TM, bool FC1, bool YBF16, int STAGES>
+template <int TM, bool FC1, bool YBF16, int STAGES, int ACT = MOE_ACT_SWIGLU>
 cudaError_t launch_impl(const CUtensorMap& tmW, const CUtensorMap& tmX, const CUtensorMap& tmY, const GemmParams& p,
                         int grid, cudaStream_t stream, bool pdl) {
     using C = Cfg<TM, STAGES, !FC1 && YBF16 && TM == 128>;
-    auto kern = moe_gemm_kernel<TM, FC1, YBF16, STAGES>;
+    auto kern = moe_gemm_kernel<TM, FC1, YBF16, STAGES, ACT>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (err != cudaSuccess) return err;
     return launch_kernel(kern, dim3(grid), dim3(kThreads), C::kSmemBytes, stream, pdl, tmW, tmX, tmY, p);
+}
+
+template <int ACT>
+cudaError_t launch_fc1(const CUtensorMap& tmW, const CUtensorMap& tmX, const CUtensorMap& tmY, const GemmParams& p,
+                       int TM, int grid, cudaStream_t stream, bool pdl) {
+    if (TM == 16) return launch_impl<16, true, false, kStagesDecFc1, ACT>(tmW, tmX, tmY, p, grid, stream, pdl);
+    if (TM == 32) return launch_impl<32, true, false, kStagesDecFc1, ACT>(tmW, tmX, tmY, p, grid, stream, pdl);
+    return launch_impl<128, true, true, kStagesPreFc1, ACT>(tmW, tmX, tmY, p, grid, stream, pdl);
 }
 
 }  // namespace
@@ -520,9 +527,9 @@ cudaError_t launch_impl(const CUtensorMap& tmW, const CUtensorMap& tmX, const CU
 cudaError_t launch_gemm(bool fc1, const CUtensorMap& tmW, const CUtensorMap& tmX, const CUtensorMap& tmY,
                         const GemmParams& p, int TM, int grid, cudaStream_t stream, bool pdl) {
     if (fc1) {
-        if (TM == 16) return launch_impl<16, true, false, kStagesDecFc1>(tmW, tmX, tmY, p, grid, stream, pdl);
-        if (TM == 32) return launch_impl<32, true, false, kStagesDecFc1>(tmW, tmX, tmY, p, grid, stream, pdl);
-        return launch_impl<128, true, true, kStagesPreFc1>(tmW, tmX, tmY, p, grid, stream, pdl);
+        if (p.act_kind == MOE_ACT_SWIGLU_CLAMP) return launch_fc1<MOE_ACT_SWIGLU_CLAMP>(tmW, tmX, tmY, p, TM, grid, stream, pdl);
+        if (p.act_kind == MOE_ACT_SITU) return launch_fc1<MOE_ACT_SITU>(tmW, tmX, tmY, p, TM, grid, stream, pdl);
+        return launch_fc1<MOE_ACT_SWIGLU>(tmW, tmX, tmY, p, TM, grid, stream, pdl);
     }
     if (TM == 16) return launch_impl<16, false, false, kStagesDecFc2>(tmW, tmX, tmY, p, grid, stream, pdl);
     if (TM == 32) return launch_impl<32, false, false, kStagesDecFc2>(tmW, tmX, tmY, p, grid, stream, pdl);
