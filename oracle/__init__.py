@@ -5,6 +5,8 @@ leg may import this package.  It wraps ``moe_oracle.cpp`` (plain C++17, fp64,
 brute force), which shares no code with the GPU library.
 
 Functions and the passages they follow (reference page titles):
+  router_logits -- fp32(sum_h x[t,h] * wr[e,h]) of bf16 x and router rows
+                (the router GEMM in front of the routing step).
   route      -- top-k with renormalised softmax weights; the shared expert's
                 weight sigmoid(fp32(logit)) * scale ("[sglang] SGLang MoE
                 shared expert: fuse 3 kernels into 1", kernel change).
@@ -76,6 +78,8 @@ def lib():
         L.oracle_quantize_mxfp4.argtypes = [P, i64, i64, P, P]
         L.oracle_quantize_mxfp8_bf16.restype = None
         L.oracle_quantize_mxfp8_bf16.argtypes = [P, i64, i64, P, P]
+        L.oracle_router_logits.restype = None
+        L.oracle_router_logits.argtypes = [i32, i32, i32, P, P, P]
         L.oracle_route.restype = None
         L.oracle_route.argtypes = [i32, i32, i32, P, i32, P, dbl, P, P]
         L.oracle_sort.restype = i32
@@ -147,6 +151,18 @@ def quantize_mxfp8_bf16(x_bits):
 
 
 # ------------------------------------------------------------------ routing
+def router_logits(x_bits, wr_bits):
+    """bf16 bits x [T, H], router rows wr [Eg, H] -> fp32 logits [T, Eg]."""
+    x = _c(x_bits, np.uint16)
+    wr = _c(wr_bits, np.uint16)
+    T, H = x.shape
+    Eg = wr.shape[0]
+    assert wr.shape[1] == H
+    out = np.zeros((T, Eg), np.float32)
+    lib().oracle_router_logits(T, H, Eg, _p(x), _p(wr), _p(out))
+    return out
+
+
 def route(logits, top_k: int, num_shared: int = 0, shared_logit=None, shared_scale: float = 1.0):
     """logits fp32 [T, Eg] -> (ids int32 [T, k+S], weights float64 [T, k+S])."""
     lg = _c(logits, np.float32)

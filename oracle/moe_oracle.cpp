@@ -250,6 +250,24 @@ void oracle_quantize_mxfp8_bf16(const uint16_t* x, int64_t rows, int64_t K, uint
         }
 }
 
+/* Router logits: logits[t][e] = fp32( sum_h x[t][h] * wr[e][h] ) with x bf16
+ * [T, H] and wr bf16 [E_global, H] (row e holds expert e's router weights).
+ * The bf16 products are exact in fp64; the fp64 sum is rounded to fp32 once.
+ * (The router GEMM ahead of the routing step, whose output the pages' kernels
+ * take as given: "... MXFP4 decode MoE ... shape templates", section 5
+ * starts from the logits' top-k ids.) */
+void oracle_router_logits(int T, int H, int E_global, const uint16_t* x, const uint16_t* wr, float* logits) {
+    std::vector<double> xr(H), wrow(H);
+    for (int t = 0; t < T; ++t) {
+        for (int h = 0; h < H; ++h) xr[h] = bf16_to_double(x[(int64_t)t * H + h]);
+        for (int e = 0; e < E_global; ++e) {
+            double acc = 0.0;
+            for (int h = 0; h < H; ++h) acc += xr[h] * bf16_to_double(wr[(int64_t)e * H + h]);
+            logits[(int64_t)t * E_global + e] = static_cast<float>(acc);
+        }
+    }
+}
+
 /* Top-k routing.  Per token: the k largest fp32 logits in descending order,
  * ties to the lower expert id; weights exp(l_j - m) / sum_sel exp(l_i - m),
  * which is softmax over all experts followed by renormalisation over the
