@@ -21,6 +21,7 @@ from __future__ import annotations
 
 import argparse
 import json
+import math
 import os
 import subprocess
 import sys
@@ -47,6 +48,8 @@ def parse():
     ap.add_argument("--tokens", type=int, default=0, help="override the workload's token count (profiling cases)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--block-n", type=int, default=0, help="override the workload's virtual-expert rows")
+    ap.add_argument("--router", action="store_true",
+                    help="start the layer from x and a bf16 router matrix (router GEMM in the chain)")
     ap.add_argument("--act", default="swiglu", choices=["swiglu", "swiglu_clamp", "situ"],
                     help="FC1 activation: SwiGLU (the workload's), clamped SwiGLU (limit 7) or SiTU (beta 4, lb 25)")
     return ap.parse_args()
@@ -203,8 +206,15 @@ def run_ours(args, cfg):
     stream = torch.cuda.Stream(device)
     flush = L2Flush(device)
 
-    def layer():
-        moe.moe_layer(shape, logits, sl, x, weights, ws, ids, tw, out)
+    wr = None
+    if args.router:
+        wr = router_matrix(cfg, device)
+
+        def layer():
+            moe.moe_layer_router(shape, wr, sl, x, weights, ws, logits, ids, tw, out)
+    else:
+        def layer():
+            moe.moe_layer(shape, logits, sl, x, weights, ws, ids, tw, out)
 
     with torch.cuda.stream(stream):
         layer()  # also loads the kernels before capture
@@ -239,7 +249,10 @@ def run_ours(args, cfg):
     ms = float(np.mean(step_ms))
     ms = allreduce_max(ms, world, device)
 
-    # live per-kernel timing (events between the launches, same stream)
+    router = time_router(moe, shape, x, wr, ws, logits, flush, stream, max(10, min(args.steps, 200))) if wr is not None \
+        else None
+    # live per-kernel timing (events between the launches, same stream; in
+    # --router mode the logits are the router GEMM's, left by the last step)
     kernel_ms = profile_kernels(moe, shape, weights, x, logits, sl, ws, ids, tw, out, flush, stream,
                                 max(10, min(args.steps, 200)))
     # end to end through host buffers
@@ -311,10 +324,12 @@ def run_ours(args, cfg):
                           "tflops": fc2_flops / kernel_ms["fc2"] / 1e9}},
         "roofline": roof,
         "e2e": e2e,
-        "gpu_launches": moe.moe_layer_launch_count(shape) * args.steps,
+        "gpu_launches": (moe.moe_layer_launch_count(shape) + (1 if wr is not None else 0)) * args.steps,
         "clocks": clocks,
         "wall_s_timed_region": t_wall,
     }
+    if router is not None:
+        res["router"] = router
     if rank == 0 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(cfg, budget_s=12.0)
     if world > 1:
@@ -322,6 +337,40 @@ def run_ours(args, cfg):
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(res), flush=True)
+
+
+def router_matrix(cfg, device):
+    """bf16 router matrix [E_global, H] from the seeded generator, sigma 1/sqrt(H) (logits ~ N(0, 1))."""
+    import torch
+
+    import synth
+    c = cfg.replace(router_sigma=1.0 / math.sqrt(cfg.hidden))
+    return torch.from_numpy(np.ascontiguousarray(synth.router_host(c).T)).to(device).to(torch.bfloat16)
+
+
+def time_router(moe, shape, x, wr, ws, logits, flush, stream, reps):
+    """The router GEMM alone (one graph, L2 flushed before each replay): us, bytes, flops."""
+    import torch
+    with torch.cuda.stream(stream):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            moe.moe_router(shape, x, wr, ws, logits)
+        for _ in range(3):
+            flush()
+            g.replay()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for a, b in ev:
+            flush()
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+        torch.cuda.synchronize()
+    us = float(np.mean([a.elapsed_time(b) for a, b in ev])) * 1e3
+    T, H, Eg = shape.T, shape.hidden, shape.E_global
+    nbytes = Eg * H * 2 + T * H * 2 + T * Eg * 4
+    flops = 2.0 * T * H * Eg
+    return {"us": us, "bytes": nbytes, "flops": flops, "gbs": nbytes / us / 1e3, "tflops": flops / us / 1e6,
+            "note": "includes the status-word reset node before the kernel"}
 
 
 def ws_counts(moe, shape, ws):
@@ -482,6 +531,8 @@ def main():
         cfg = cfg.replace(T=args.tokens, name="%s_T%d" % (cfg.name, args.tokens))
     if args.block_n:
         cfg = cfg.replace(block_n=args.block_n, name="%s_B%d" % (cfg.name, args.block_n))
+    if args.router:
+        cfg = cfg.replace(name="%s_router" % cfg.name)
     if args.act != "swiglu":
         act = ACT_NAMES.index(args.act)
         cfg = cfg.replace(activation=act, act_params=ACT_DEFAULT_PARAMS[act], name="%s_%s" % (cfg.name, args.act))

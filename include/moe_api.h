@@ -191,6 +191,28 @@ int moe_sort(const moe_shape* shape, const int32_t* topk_ids, void* workspace, s
 int moe_forward(const moe_shape* shape, const uint16_t* x, const moe_weights* weights, const float* topk_w,
                 void* workspace, size_t workspace_bytes, uint16_t* out, moe_stream_t stream);
 
+/* Router GEMM: logits[t][e] = fp32 sum_h x[t][h] * wr[e][h] for x bf16
+ * [T, H] and the router matrix wr bf16 [E_global, H] (row e = expert e),
+ * written to logits fp32 [T, E_global].  The step in front of routing: the
+ * pages' kernel ("... MXFP4 decode MoE ... shape templates", section 5)
+ * starts from the top-k of these logits.  tcgen05 kind::f16 tensor cores
+ * (bf16 products, fp32 accumulation); for T <= 256 the H reduction is split
+ * over the 8 CTAs of a cluster and summed in a fixed order, so the logits are
+ * bit-reproducible.  The fp32 sums differ from an exactly rounded dot
+ * product by the accumulation order only.  Resets the workspace status word,
+ * then records MOE_ERR_TIMEOUT there if a bounded wait expires.  x, wr,
+ * logits 16-byte aligned. */
+int moe_router(const moe_shape* shape, const uint16_t* x, const uint16_t* wr, float* logits, void* workspace,
+               size_t workspace_bytes, moe_stream_t stream);
+
+/* moe_router + route + sort + forward as one fixed launch chain: the layer
+ * from x and the router matrix (logits written to `logits`, ids and weights
+ * to topk_ids / topk_w).  Graph capturable; the status word covers the
+ * router and the GEMMs. */
+int moe_layer_router(const moe_shape* shape, const uint16_t* wr, const uint16_t* shared_logit, const uint16_t* x,
+                     const moe_weights* weights, float* logits, int32_t* topk_ids, float* topk_w, void* workspace,
+                     size_t workspace_bytes, uint16_t* out, moe_stream_t stream);
+
 /* route + sort + forward as one fixed launch chain (programmatic dependent
  * launch between kernels, no host synchronisation, graph capturable). */
 int moe_layer(const moe_shape* shape, const float* logits, const uint16_t* shared_logit, const uint16_t* x,

@@ -19,7 +19,7 @@ from . import build as _build
 __all__ = [
     "MoeShape", "MoeWeights", "MoeError", "lib", "moe_is_supported", "moe_workspace_bytes",
     "moe_quantize_mxfp4", "moe_packed_weight_bytes", "moe_pack_weights", "moe_route", "moe_sort", "moe_forward",
-    "moe_layer", "moe_layer_host", "moe_layer_events", "moe_layer_noalloc", "moe_get_views", "moe_get_status",
+    "moe_layer", "moe_router", "moe_layer_router", "moe_layer_host", "moe_layer_events", "moe_layer_noalloc", "moe_get_views", "moe_get_status",
     "moe_num_sms", "moe_layer_launch_count", "quantize_expert_weights",
     "workspace", "MOE_OK", "MOE_ERR_TIMEOUT", "MOE_ERR_WORKSPACE",
 ]
@@ -112,6 +112,8 @@ _SIGS = {
     "moe_sort": [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p],
     "moe_forward": [ctypes.c_void_p] * 5 + [ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p],
     "moe_layer": [ctypes.c_void_p] * 8 + [ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p],
+    "moe_router": [ctypes.c_void_p] * 5 + [ctypes.c_size_t, ctypes.c_void_p],
+    "moe_layer_router": [ctypes.c_void_p] * 9 + [ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p],
     "moe_layer_host": [ctypes.c_void_p] * 6 + [ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p],
     "moe_layer_events": [ctypes.c_void_p] * 8 + [ctypes.c_size_t] + [ctypes.c_void_p] * 3,
     "moe_layer_noalloc": [ctypes.c_void_p] * 9,
@@ -278,6 +280,38 @@ def moe_forward(shape: MoeShape, x, weights: MoeWeights, topk_w, ws, out=None):
     _call("moe_forward", ctypes.byref(s), x.data_ptr(), ctypes.byref(w), topk_w.data_ptr(), ws.data_ptr(),
           ws.numel(), out.data_ptr(), _stream(x.device))
     return out
+
+
+def moe_router(shape: MoeShape, x, wr, ws, logits=None):
+    """Router GEMM: bf16 x [T, H] times the bf16 router matrix wr [E_global, H] -> fp32 logits [T, E_global]."""
+    _check_cuda(x, wr, ws)
+    if logits is None:
+        logits = torch.empty((shape.T, shape.E_global), dtype=torch.float32, device=x.device)
+    s = shape.c()
+    _call("moe_router", ctypes.byref(s), x.data_ptr(), wr.data_ptr(), logits.data_ptr(), ws.data_ptr(),
+          ws.numel(), _stream(x.device))
+    return logits
+
+
+def moe_layer_router(shape: MoeShape, wr, shared_logit, x, weights: MoeWeights, ws, logits=None, topk_ids=None,
+                     topk_w=None, out=None):
+    """The layer from x and the router matrix: router GEMM -> route -> sort -> forward, one launch chain.
+    Returns (out, logits, topk_ids, topk_w)."""
+    _check_cuda(wr, shared_logit, x, ws)
+    dev = x.device
+    if logits is None:
+        logits = torch.empty((shape.T, shape.E_global), dtype=torch.float32, device=dev)
+    if topk_ids is None:
+        topk_ids = torch.empty((shape.T, shape.kp), dtype=torch.int32, device=dev)
+    if topk_w is None:
+        topk_w = torch.empty((shape.T, shape.kp), dtype=torch.float32, device=dev)
+    if out is None:
+        out = torch.empty((shape.T, shape.hidden), dtype=torch.bfloat16, device=dev)
+    s, w = shape.c(), weights.c()
+    _call("moe_layer_router", ctypes.byref(s), wr.data_ptr(), _ptr(shared_logit), x.data_ptr(), ctypes.byref(w),
+          logits.data_ptr(), topk_ids.data_ptr(), topk_w.data_ptr(), ws.data_ptr(), ws.numel(), out.data_ptr(),
+          _stream(dev))
+    return out, logits, topk_ids, topk_w
 
 
 def moe_layer(shape: MoeShape, logits, shared_logit, x, weights: MoeWeights, ws, topk_ids=None, topk_w=None,

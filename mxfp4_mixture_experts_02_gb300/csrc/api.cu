@@ -87,21 +87,23 @@ int run_route(const moe_shape* s, const float* logits, const uint16_t* shared_lo
     return cuda_rc(launch_route(p, st, pdl));
 }
 
-int run_sort(const moe_shape* s, const int32_t* ids, void* ws, cudaStream_t st, bool pdl) {
+int run_sort(const moe_shape* s, const int32_t* ids, void* ws, cudaStream_t st, bool pdl, bool keep_status = false) {
     const Dims d = make_dims(*s);
     const Layout L = make_layout(d);
     SortParams p{ids, at<int32_t>(ws, L.header), at<int32_t>(ws, L.counts), at<int32_t>(ws, L.offsets),
                  at<int4>(ws, L.vinfo), at<int4>(ws, L.groups), at<int32_t>(ws, L.a_map), at<int32_t>(ws, L.c_map),
                  at<int32_t>(ws, L.vbase), at<int32_t>(ws, L.sort_hist), d.T, d.kp, d.Eg, d.E, d.off, d.S, d.Et, d.B,
-                 d.G};
+                 d.G, keep_status ? 1 : 0};
     return cuda_rc(launch_sort(p, st, pdl));
 }
 
 // Route then sort, fused into one launch when the batch has at most 1024
 // slots.  `ev` (optional) gets events 1 (routed) and 2 (sorted); fused, both
-// are recorded after the one kernel.
+// are recorded after the one kernel.  after_router: the logits come from the
+// router GEMM launched just before (PDL launch; the status word it may have
+// set survives the sort).
 int run_route_sort(const moe_shape* s, const float* logits, const uint16_t* shared_logit, int32_t* ids, float* w,
-                   void* ws, cudaStream_t st, void* const* ev);
+                   void* ws, cudaStream_t st, void* const* ev, bool after_router = false);
 
 // Records events[i] on the stream when an events array is given.
 inline bool rec(void* const* ev, int i, cudaStream_t st) {
@@ -109,7 +111,7 @@ inline bool rec(void* const* ev, int i, cudaStream_t st) {
 }
 
 int run_route_sort(const moe_shape* s, const float* logits, const uint16_t* shared_logit, int32_t* ids, float* w,
-                   void* ws, cudaStream_t st, void* const* ev) {
+                   void* ws, cudaStream_t st, void* const* ev, bool after_router) {
     const Dims d = make_dims(*s);
     if (route_sort_fusable(d.T, d.kp)) {
         const Layout L = make_layout(d);
@@ -117,14 +119,14 @@ int run_route_sort(const moe_shape* s, const float* logits, const uint16_t* shar
         SortParams sp{ids, at<int32_t>(ws, L.header), at<int32_t>(ws, L.counts), at<int32_t>(ws, L.offsets),
                       at<int4>(ws, L.vinfo), at<int4>(ws, L.groups), at<int32_t>(ws, L.a_map), at<int32_t>(ws, L.c_map),
                       at<int32_t>(ws, L.vbase), at<int32_t>(ws, L.sort_hist), d.T, d.kp, d.Eg, d.E, d.off, d.S, d.Et,
-                      d.B, d.G};
-        if (launch_route_sort_small(rp, sp, st, false) != cudaSuccess) return MOE_ERR_CUDA;
+                      d.B, d.G, after_router ? 1 : 0};
+        if (launch_route_sort_small(rp, sp, st, after_router && ev == nullptr) != cudaSuccess) return MOE_ERR_CUDA;
         return (rec(ev, 1, st) && rec(ev, 2, st)) ? MOE_OK : MOE_ERR_CUDA;
     }
-    int rc = run_route(s, logits, shared_logit, ids, w, st, false);
+    int rc = run_route(s, logits, shared_logit, ids, w, st, after_router && ev == nullptr);
     if (rc) return rc;
     if (!rec(ev, 1, st)) return MOE_ERR_CUDA;
-    if ((rc = run_sort(s, ids, ws, st, ev == nullptr))) return rc;
+    if ((rc = run_sort(s, ids, ws, st, ev == nullptr, after_router))) return rc;
     return rec(ev, 2, st) ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -224,6 +226,23 @@ int run_forward(const moe_shape* s, const uint16_t* x, const moe_weights* wt, co
     e = launch_combine(cp, st, pdl);
     if (e != cudaSuccess || !rec(ev, 6, st)) return MOE_ERR_CUDA;
     return MOE_OK;
+}
+
+// Router GEMM x [T, H] bf16 x wr [Eg, H] bf16 -> logits [T, Eg] fp32.  The
+// status words are reset first (a copy node on the stream), so a timeout the
+// router records survives until the sort that follows (keep_status).
+int run_router(const moe_shape* s, const uint16_t* x, const uint16_t* wr, float* logits, void* ws, cudaStream_t st) {
+    const Dims d = make_dims(*s);
+    int32_t* status = at<int32_t>(ws, make_layout(d).header) + kHdrStatus;
+    if (cudaMemsetAsync(status, 0, 2 * sizeof(int32_t), st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (d.T == 0) return MOE_OK;
+    const RouterTiling t = router_tiling(d.T, d.Eg);
+    CUtensorMap mx, mw;
+    if (!make_map(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, d.H, d.T, size_t(d.H) * 2, 64, 128) ||
+        !make_map(&mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, wr, d.H, d.Eg, size_t(d.H) * 2, 64, t.N))
+        return MOE_ERR_CUDA;
+    RouterParams p{logits, status, d.T, d.Eg, d.H, t.N, t.n_tiles, t.ks, kWaitLimitNs};
+    return cuda_rc(launch_router(mx, mw, p, t.grid, st, false));
 }
 
 int check_weights(const moe_weights* w) {
@@ -338,6 +357,32 @@ int moe_layer(const moe_shape* s, const float* logits, const uint16_t* shared_lo
     if ((rc = check_ws(s, ws, ws_bytes))) return rc;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if ((rc = run_route_sort(s, logits, shared_logit, topk_ids, topk_w, ws, st, nullptr))) return rc;
+    return run_forward(s, x, w, topk_w, ws, out, st, true);
+}
+
+int moe_router(const moe_shape* s, const uint16_t* x, const uint16_t* wr, float* logits, void* ws, size_t ws_bytes,
+               moe_stream_t stream) {
+    int rc = check_shape(s);
+    if (rc) return rc;
+    if (s->T > 0 && (!x || !wr || !logits)) return MOE_ERR_NULL;
+    if (!aligned(x, 16) || !aligned(wr, 16) || !aligned(logits, 16)) return MOE_ERR_ALIGN;
+    if ((rc = check_ws(s, ws, ws_bytes))) return rc;
+    return run_router(s, x, wr, logits, ws, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int moe_layer_router(const moe_shape* s, const uint16_t* wr, const uint16_t* shared_logit, const uint16_t* x,
+                     const moe_weights* w, float* logits, int32_t* topk_ids, float* topk_w, void* ws, size_t ws_bytes,
+                     uint16_t* out, moe_stream_t stream) {
+    int rc = check_shape(s);
+    if (rc) return rc;
+    if (s->T > 0 && (!wr || !logits || !x || !topk_ids || !topk_w || !out || (s->num_shared > 0 && !shared_logit)))
+        return MOE_ERR_NULL;
+    if (!aligned(x, 16) || !aligned(wr, 16) || !aligned(logits, 16) || !aligned(out, 16)) return MOE_ERR_ALIGN;
+    if ((rc = check_weights(w))) return rc;
+    if ((rc = check_ws(s, ws, ws_bytes))) return rc;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if ((rc = run_router(s, x, wr, logits, ws, st))) return rc;
+    if ((rc = run_route_sort(s, logits, shared_logit, topk_ids, topk_w, ws, st, nullptr, true))) return rc;
     return run_forward(s, x, w, topk_w, ws, out, st, true);
 }
 

@@ -47,6 +47,22 @@ struct SortParams {
     int32_t* vbase;     // [Et]: index of each expert's first virtual expert
     int32_t* cta_hist;  // [ceil(T*k' / 4096)][Et]: large-sort scratch
     int T, kp, Eg, E, off, S, Et, B, G;
+    int keep_status;    // 1: leave the status word as the router GEMM left it (it was reset before the router)
+};
+
+// Router GEMM (x bf16 [T, H] times router rows bf16 [Eg, H] -> fp32 logits).
+struct RouterParams {
+    float* logits;    // [T, Eg]
+    int32_t* status;  // status word pair, or nullptr
+    int T, Eg, H;
+    int N;            // router rows per tile (64 or 224)
+    int n_tiles;      // tiles over Eg
+    int ks;           // K splits = cluster size
+    uint64_t wait_ns;
+};
+
+struct RouterTiling {
+    int N, ks, n_tiles, grid;
 };
 
 struct GatherParams {  // x -> MXFP8 rows in expert order + tile scales
@@ -125,6 +141,9 @@ cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream, bool pdl);
 cudaError_t launch_gemm(bool fc1, const CUtensorMap& tmW, const CUtensorMap& tmX, const CUtensorMap& tmY,
                         const GemmParams& p, int TM, int grid, cudaStream_t stream, bool pdl);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream, bool pdl);
+RouterTiling router_tiling(int T, int Eg);
+cudaError_t launch_router(const CUtensorMap& tmX, const CUtensorMap& tmW, const RouterParams& p, int grid,
+                          cudaStream_t stream, bool pdl);
 cudaError_t launch_quantize_mxfp4(const QuantParams& p, cudaStream_t stream);
 cudaError_t launch_pack_weights(const PackParams& p, cudaStream_t stream);
 

@@ -167,6 +167,17 @@ __device__ __forceinline__ void mma_mxf8f6f4(uint32_t d_tmem, uint64_t a_desc, u
         : "memory");
 }
 
+// D[tmem] (+)= A(smem) * B(smem)^T, bf16 x bf16 -> fp32 (kind::f16).
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                        uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Copy 32 rows x 16 bytes of shared memory into TMEM, replicated into the
 // four 32-lane quadrants (4 columns of 32 bit).
 __device__ __forceinline__ void tc_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
@@ -221,6 +232,11 @@ enum : uint32_t { kFmtE4M3 = 0, kFmtE2M1 = 5 };
 
 __host__ __device__ constexpr uint32_t idesc_mx(uint32_t a_fmt, uint32_t b_fmt, uint32_t M, uint32_t N) {
     return (b_fmt << 10) | (a_fmt << 7) | ((N >> 3) << 17) | (1u << 23) | ((M >> 4) << 24);
+}
+
+// kind::f16 with bf16 A and B, fp32 D, both operands K-major.
+__host__ __device__ constexpr uint32_t idesc_f16_bf16(uint32_t M, uint32_t N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
 __device__ __forceinline__ uint32_t idesc_with_sf_id(uint32_t base, uint32_t sfa_id, uint32_t sfb_id) {

@@ -263,8 +263,10 @@ __device__ __forceinline__ void place_experts(const SortParams& p, int cnt, int*
         p.header[kHdrRows] = R;
         p.header[kHdrNumV] = V;
         p.header[kHdrNumGroups] = NG;
-        p.header[kHdrStatus] = 0;
-        p.header[kHdrDetail] = 0;
+        if (!p.keep_status) {
+            p.header[kHdrStatus] = 0;
+            p.header[kHdrDetail] = 0;
+        }
     }
 }
 

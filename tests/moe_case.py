@@ -67,11 +67,12 @@ def device_inputs(cfg: synth.MoeConfig, T: int | None = None):
 class OracleCase:
     """The oracle's computation of a config for a subset of tokens."""
 
-    def __init__(self, cfg: synth.MoeConfig, T: int | None = None):
+    def __init__(self, cfg: synth.MoeConfig, T: int | None = None, logits=None):
         self.cfg = cfg
         self.T = cfg.T if T is None else T
         self.x = synth.x_host(cfg, T=self.T)
-        self.logits = synth.logits_host(cfg, T=self.T)
+        # logits: the oracle's own router logits when the layer starts from the router matrix
+        self.logits = synth.logits_host(cfg, T=self.T) if logits is None else logits
         self.shared = synth.shared_logit_host(cfg, T=self.T)
         self.ids, self.w = oracle.route(self.logits, cfg.top_k, cfg.num_shared, self.shared, cfg.shared_scale)
         self.sort = oracle.sort(self.ids, cfg.E_global, cfg.E_local, cfg.expert_offset, cfg.num_shared, cfg.block_n)
@@ -134,3 +135,11 @@ def rel_l2(a, b) -> float:
 
 
 E4M3_VALUES = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+
+
+def router_matrix_bits(cfg: synth.MoeConfig) -> np.ndarray:
+    """The router matrix as bf16 bits [E_global, H]: the seeded fp32 generator
+    (sigma = cfg.router_sigma) rounded to bf16 (RNE) and laid out one expert per row."""
+    wr = synth.router_host(cfg)  # fp32 [H, Eg]
+    t = torch.from_numpy(np.ascontiguousarray(wr.T)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().astype(np.uint16)
