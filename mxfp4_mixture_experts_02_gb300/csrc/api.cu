@@ -206,6 +206,7 @@ int run_forward(const moe_shape* s, const uint16_t* x, const moe_weights* wt, co
     g.a_tx_bytes = 256 * kFp4BytesPer128Row;
     g.wait_ns = kWaitLimitNs;
     g.act_kind = s->activation;
+    g.max_v = d.V_max;
     g.act_c0 = s->act_params[0];
     g.act_c1 = s->act_params[1];
 

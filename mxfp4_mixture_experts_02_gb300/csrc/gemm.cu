@@ -120,7 +120,18 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, ui
     }
 }
 
-__device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
+// silu(g) = g / (1 + e^-g) with the fast exponential and divide (relative
+// error about 1e-6, far below the E4M3 step the result is quantised to).
+__device__ __forceinline__ float silu(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
+
+// Descriptor of work item `it` (NB weight blocks per virtual expert), or
+// `none` past the item count.  The load does not wait for the count: the
+// index is clamped into the array and the value dropped when the item does
+// not exist, so a CTA's first descriptor loads overlap its header load.
+__device__ __forceinline__ int4 item_desc(const GemmParams& p, int it, int NB, int iend, int4 none) {
+    const int4 d = p.vinfo[min(it / NB, p.max_v - 1)];
+    return it < iend ? d : none;
+}
 
 // FC1 activations h(gate, up) ("... MXFP4 decode MoE ... shape templates",
 // section 4).  c0 / c1 are the constants, i0 / i1 their reciprocals.
@@ -237,15 +248,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t stage = 0, phase = 0;
             bool ok = true;
             const uint32_t tx = 256 * 64 + C::kXTile + 1536;
-            int4 vq0 = it0 < iend ? p.vinfo[it0 / NB] : kNone;
-            int4 vq1 = it0 + g < iend ? p.vinfo[(it0 + g) / NB] : kNone;
-            int4 vq2 = it0 + 2 * g < iend ? p.vinfo[(it0 + 2 * g) / NB] : kNone;
+            int4 vq0 = item_desc(p, it0, NB, iend, kNone);
+            int4 vq1 = item_desc(p, it0 + g, NB, iend, kNone);
+            int4 vq2 = item_desc(p, it0 + 2 * g, NB, iend, kNone);
             for (int it = it0; ok && it < iend; it += g) {
                 const int v = it / NB, nb = it - v * NB;
                 const int4 vi = vq0;
                 vq0 = vq1;
                 vq1 = vq2;
-                vq2 = (it + 3 * g < iend) ? p.vinfo[(it + 3 * g) / NB] : kNone;
+                vq2 = item_desc(p, it + 3 * g, NB, iend, kNone);
                 const int64_t tile0 = (static_cast<int64_t>(vi.x) * NB + nb) * KC;
                 for (int kc = 0; kc < KC; ++kc) {
                     if (!wait_or_abort(&empty[stage], phase ^ 1, p.wait_ns, abort_flag)) {
@@ -278,15 +289,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::pdl_wait();
             uint32_t stage = 0, phase = 0;
             bool ok = true;
-            int4 vq0 = it0 < iend ? p.vinfo[it0 / NB] : kNone;
-            int4 vq1 = it0 + g < iend ? p.vinfo[(it0 + g) / NB] : kNone;
-            int4 vq2 = it0 + 2 * g < iend ? p.vinfo[(it0 + 2 * g) / NB] : kNone;
+            int4 vq0 = item_desc(p, it0, NB, iend, kNone);
+            int4 vq1 = item_desc(p, it0 + g, NB, iend, kNone);
+            int4 vq2 = item_desc(p, it0 + 2 * g, NB, iend, kNone);
             for (int it = it0; ok && it < iend; it += g) {
                 const int v = it / NB;
                 const int4 vi = vq0;
                 vq0 = vq1;
                 vq1 = vq2;
-                vq2 = (it + 3 * g < iend) ? p.vinfo[(it + 3 * g) / NB] : kNone;
+                vq2 = item_desc(p, it + 3 * g, NB, iend, kNone);
                 const uint8_t* sfx = p.b_sf + static_cast<size_t>(v) * p.b_sf_tile_bytes;
                 for (int kc = 0; kc < KC; ++kc) {
                     if (!wait_or_abort(&empty[stage], phase ^ 1, p.wait_ns, abort_flag)) {
@@ -357,14 +368,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Descriptors two items ahead and row weights one item ahead are
         // loaded early, so no dependent load chain sits between two items.
         const int4 kNoTile = kNone;
-        int4 vi_cur = (active && it0 < iend) ? p.vinfo[it0 / NB] : kNoTile;
-        int4 vi_nxt = (active && it0 + g < iend) ? p.vinfo[(it0 + g) / NB] : kNoTile;
+        int4 vi_cur = active ? item_desc(p, it0, NB, iend, kNoTile) : kNoTile;
+        int4 vi_nxt = active ? item_desc(p, it0 + g, NB, iend, kNoTile) : kNoTile;
         float w_cur = (!FC1 && i < vi_cur.z) ? p.row_w[vi_cur.y + i] : 0.f;
         for (int it = it0; active && it < iend; it += g) {
             const int v = it / NB, nb = it - v * NB;
             const int4 vi = vi_cur;
             const float w_row = w_cur;
-            const int4 vi_n2 = (it + 2 * g < iend) ? p.vinfo[(it + 2 * g) / NB] : kNoTile;
+            const int4 vi_n2 = item_desc(p, it + 2 * g, NB, iend, kNoTile);
             w_cur = (!FC1 && i < vi_nxt.z) ? p.row_w[vi_nxt.y + i] : 0.f;
             vi_cur = vi_nxt;
             vi_nxt = vi_n2;

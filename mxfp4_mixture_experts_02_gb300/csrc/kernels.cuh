@@ -101,6 +101,7 @@ struct GemmParams {
     int a_tx_bytes;        // transaction bytes of a stage's weight box (packed E2M1 bytes)
     uint64_t wait_ns;
     int act_kind;          // FC1 epilogue activation (MOE_ACT_*)
+    int max_v;             // entries of vinfo (virtual-expert bound)
     float act_c0, act_c1;  // its constants: clamp limit, or SiTU beta and linear beta
 };
 
