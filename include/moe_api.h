@@ -108,16 +108,26 @@ typedef struct moe_weights {
  *   expert_counts int32[E_tot], expert_offsets int32[E_tot + 1]
  *   vinfo        int32[max_v][4] {local expert, first row, rows, chunk}
  *   a_map        int32[R] row -> slot t*k' + j;  c_map int32[T*k'] slot -> row or -1
- *   xq           E4M3 [rows_alloc, H]: row r = MXFP8(x[a_map[r] / k'])
- *   xq_sf        E8M0 of xq in the tile layout (see moe_forward)
- *   act, act_sf  the FC1 output (the activation h(gate, up), MXFP8) in the same layouts
+ *   xq, xq_sf    x in MXFP8.  x_token_order = 1 (block_n 16 / 32): E4M3
+ *                [max_T, H], row t = MXFP8(x[t]), and E8M0 [max_T, H / 32]
+ *                row-major (the decode FC1 gathers each tile's rows from
+ *                here).  x_token_order = 0 (block_n 128): E4M3 [rows_alloc,
+ *                H] in expert-row order, row r = MXFP8(x[a_map[r] / k']),
+ *                and E8M0 in the tile layout of act_sf (sf_tile_bytes_x per
+ *                virtual expert)
+ *   act          E4M3 [rows_alloc, I]: the FC1 output (the activation
+ *                h(gate, up), MXFP8) in expert-row order
+ *   act_sf       E8M0 of act in the tile layout: per virtual expert v and
+ *                128-K chunk kc a 512-byte block (v * sf_tile_bytes_act +
+ *                kc * 512), tile row i / K-block b at (i % 32) * 16 +
+ *                (i / 32) * 4 + b
  *   y            the FC2 output rows [R, H], already multiplied by the routing
  *                weight: fp32 for block_n 16/32, bf16 for block_n 128 */
 typedef struct moe_views {
     int32_t *header, *expert_counts, *expert_offsets, *vinfo, *a_map, *c_map;
     uint8_t *xq, *xq_sf, *act, *act_sf;
     void* y;
-    int32_t max_v, rows_alloc, y_is_bf16, sf_tile_bytes_x, sf_tile_bytes_act;
+    int32_t max_v, rows_alloc, y_is_bf16, sf_tile_bytes_x, sf_tile_bytes_act, x_token_order;
 } moe_views;
 
 /* 1 if the shape is supported, else 0.  Limits: hidden % 512 == 0,

@@ -57,7 +57,7 @@ class _Views(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("header", "expert_counts", "expert_offsets", "vinfo", "a_map",
                                                 "c_map", "xq", "xq_sf", "act", "act_sf", "y")] + \
                [(n, ctypes.c_int32) for n in ("max_v", "rows_alloc", "y_is_bf16", "sf_tile_bytes_x",
-                                              "sf_tile_bytes_act")]
+                                              "sf_tile_bytes_act", "x_token_order")]
 
 
 @dataclasses.dataclass
@@ -401,8 +401,12 @@ def moe_get_views(shape: MoeShape, ws):
         expert_offsets=sub(v.expert_offsets, (Et + 1) * 4, torch.int32),
         vinfo=sub(v.vinfo, v.max_v * 16, torch.int32).view(v.max_v, 4),
         a_map=sub(v.a_map, R_max * 4, torch.int32), c_map=sub(v.c_map, R_max * 4, torch.int32),
-        xq=sub(v.xq, v.rows_alloc * shape.hidden, torch.uint8).view(v.rows_alloc, shape.hidden),
-        xq_sf=sub(v.xq_sf, v.max_v * v.sf_tile_bytes_x, torch.uint8).view(v.max_v, v.sf_tile_bytes_x),
+        xq=(sub(v.xq, shape.max_T * shape.hidden, torch.uint8).view(shape.max_T, shape.hidden) if v.x_token_order
+            else sub(v.xq, v.rows_alloc * shape.hidden, torch.uint8).view(v.rows_alloc, shape.hidden)),
+        xq_sf=(sub(v.xq_sf, shape.max_T * (shape.hidden // 32), torch.uint8).view(shape.max_T, shape.hidden // 32)
+               if v.x_token_order
+               else sub(v.xq_sf, v.max_v * v.sf_tile_bytes_x, torch.uint8).view(v.max_v, v.sf_tile_bytes_x)),
+        x_token_order=v.x_token_order,
         act=sub(v.act, v.rows_alloc * shape.inter, torch.uint8).view(v.rows_alloc, shape.inter),
         act_sf=sub(v.act_sf, v.max_v * v.sf_tile_bytes_act, torch.uint8).view(v.max_v, v.sf_tile_bytes_act),
         y=(sub(v.y, R_max * shape.hidden * 2, torch.bfloat16) if v.y_is_bf16

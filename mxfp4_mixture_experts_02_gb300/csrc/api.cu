@@ -101,9 +101,11 @@ int run_sort(const moe_shape* s, const int32_t* ids, void* ws, cudaStream_t st, 
 // slots.  `ev` (optional) gets events 1 (routed) and 2 (sorted); fused, both
 // are recorded after the one kernel.  after_router: the logits come from the
 // router GEMM launched just before (PDL launch; the status word it may have
-// set survives the sort).
+// set survives the sort).  x (optional): in the decode tilings the fused
+// launch also quantises x (the gather's work); *gathered says whether it did.
 int run_route_sort(const moe_shape* s, const float* logits, const uint16_t* shared_logit, int32_t* ids, float* w,
-                   void* ws, cudaStream_t st, void* const* ev, bool after_router = false);
+                   void* ws, cudaStream_t st, void* const* ev, bool after_router = false,
+                   const uint16_t* x = nullptr, bool* gathered = nullptr);
 
 // Records events[i] on the stream when an events array is given.
 inline bool rec(void* const* ev, int i, cudaStream_t st) {
@@ -111,8 +113,9 @@ inline bool rec(void* const* ev, int i, cudaStream_t st) {
 }
 
 int run_route_sort(const moe_shape* s, const float* logits, const uint16_t* shared_logit, int32_t* ids, float* w,
-                   void* ws, cudaStream_t st, void* const* ev, bool after_router) {
+                   void* ws, cudaStream_t st, void* const* ev, bool after_router, const uint16_t* x, bool* gathered) {
     const Dims d = make_dims(*s);
+    if (gathered) *gathered = false;
     if (route_sort_fusable(d.T, d.kp)) {
         const Layout L = make_layout(d);
         RouteParams rp{logits, shared_logit, ids, w, d.T, d.Eg, d.k, d.S, d.kp, d.shared_scale};
@@ -120,7 +123,18 @@ int run_route_sort(const moe_shape* s, const float* logits, const uint16_t* shar
                       at<int4>(ws, L.vinfo), at<int4>(ws, L.groups), at<int32_t>(ws, L.a_map), at<int32_t>(ws, L.c_map),
                       at<int32_t>(ws, L.vbase), at<int32_t>(ws, L.sort_hist), d.T, d.kp, d.Eg, d.E, d.off, d.S, d.Et,
                       d.B, d.G, after_router ? 1 : 0};
-        if (launch_route_sort_small(rp, sp, st, after_router && ev == nullptr) != cudaSuccess) return MOE_ERR_CUDA;
+        GatherParams gp{};
+        const bool fuse_x = x != nullptr && L.x_token_order && d.T > 0;
+        if (fuse_x) {
+            gp.x = x;
+            gp.xq = at<uint8_t>(ws, L.xq);
+            gp.xsf = at<uint8_t>(ws, L.xsf);
+            gp.row_w = at<float>(ws, L.row_w);
+            gp.H = d.H;
+        }
+        if (launch_route_sort_small(rp, sp, fuse_x ? &gp : nullptr, st, after_router && ev == nullptr) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        if (gathered) *gathered = fuse_x;
         return (rec(ev, 1, st) && rec(ev, 2, st)) ? MOE_OK : MOE_ERR_CUDA;
     }
     int rc = run_route(s, logits, shared_logit, ids, w, st, after_router && ev == nullptr);
@@ -130,8 +144,9 @@ int run_route_sort(const moe_shape* s, const float* logits, const uint16_t* shar
     return rec(ev, 2, st) ? MOE_OK : MOE_ERR_CUDA;
 }
 
+// gathered: the route + sort launch already quantised x (decode tilings).
 int run_forward(const moe_shape* s, const uint16_t* x, const moe_weights* wt, const float* topk_w, void* ws,
-                uint16_t* out, cudaStream_t st, bool pdl, void* const* ev = nullptr) {
+                uint16_t* out, cudaStream_t st, bool pdl, void* const* ev = nullptr, bool gathered = false) {
     const Dims d = make_dims(*s);
     const Layout L = make_layout(d);
     if (d.T == 0) {
@@ -145,7 +160,6 @@ int run_forward(const moe_shape* s, const uint16_t* x, const moe_weights* wt, co
     GatherParams gp{};
     gp.x = x;
     gp.header = at<int32_t>(ws, L.header);
-    gp.vinfo = at<int4>(ws, L.vinfo);
     gp.a_map = at<int32_t>(ws, L.a_map);
     gp.xq = at<uint8_t>(ws, L.xq);
     gp.xsf = at<uint8_t>(ws, L.xsf);
@@ -154,31 +168,36 @@ int run_forward(const moe_shape* s, const uint16_t* x, const moe_weights* wt, co
     gp.c_map = at<int32_t>(ws, L.c_map);
     gp.offsets = at<int32_t>(ws, L.offsets);
     gp.vbase = at<int32_t>(ws, L.vbase);
-    gp.token_major = d.mode == kModePrefill;
+    gp.token_order = L.x_token_order;
     gp.H = d.H;
+    gp.T = d.T;
+    gp.R_max = d.R_max;
+    gp.max_blocks = L.x_token_order ? 16 * nsm : 8 * nsm * 8;
     gp.kp = d.kp;
     gp.B = d.B;
-    gp.xsf_tile_bytes = L.xsf_tile_bytes;
-    gp.max_v = d.V_max;
-    gp.grid = d.V_max < 8 * nsm ? d.V_max : 8 * nsm;
-    gp.T = d.T;
     gp.Et = d.Et;
-    cudaError_t e = launch_gather(gp, st, pdl);
+    gp.xsf_tile_bytes = L.xsf_tile_bytes;
+    cudaError_t e = gathered ? cudaSuccess : launch_gather(gp, st, pdl);
     if (e != cudaSuccess || !rec(ev, 3, st)) return MOE_ERR_CUDA;
 
     // Tile-major packed weights viewed as rows of 128 E2M1 codes (64 bytes):
     // a GEMM stage is one 256-row box, one contiguous 16 KiB run of global
-    // memory.  Token operands: boxes of B rows x 128 K of the expert-ordered
-    // MXFP8 activations.
+    // memory.  Token operands: boxes of B rows x 128 K of expert-ordered MXFP8
+    // rows (the intermediate; x in the 128-row tiling -- the decode FC1
+    // gathers its x rows itself).
     CUtensorMap mw1, mw2, mx, mact, my;
     const uint64_t Et = static_cast<uint64_t>(d.Et);
     if (!make_map(&mw1, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, wt->w1, 128, Et * 2 * d.I * (d.H / 128),
                   kFp4BytesPer128Row, 128, 256) ||
         !make_map(&mw2, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, wt->w2, 128, Et * d.H * (d.I / 128),
                   kFp4BytesPer128Row, 128, 256) ||
-        !make_map(&mx, CU_TENSOR_MAP_DATA_TYPE_UINT8, at<uint8_t>(ws, L.xq), d.H, d.rows_alloc, d.H, 128, d.B) ||
         !make_map(&mact, CU_TENSOR_MAP_DATA_TYPE_UINT8, at<uint8_t>(ws, L.act), d.I, d.rows_alloc, d.I, 128, d.B))
         return MOE_ERR_CUDA;
+    if (L.x_token_order) {
+        mx = mact;  // decode FC1 gathers its token rows with cp.async; the map is not read
+    } else if (!make_map(&mx, CU_TENSOR_MAP_DATA_TYPE_UINT8, at<uint8_t>(ws, L.xq), d.H, d.rows_alloc, d.H, 128, d.B)) {
+        return MOE_ERR_CUDA;
+    }
     // bf16 FC2 rows (128-row tiling): each epilogue warp stores 32 rows x 64
     // columns per box
     if (L.y_bf16) {
@@ -207,12 +226,15 @@ int run_forward(const moe_shape* s, const uint16_t* x, const moe_weights* wt, co
     g.wait_ns = kWaitLimitNs;
     g.act_kind = s->activation;
     g.max_v = d.V_max;
+    g.xq = at<uint8_t>(ws, L.xq);
+    g.xsf = at<uint8_t>(ws, L.xsf);
+    g.kp = d.kp;
     g.act_c0 = s->act_params[0];
     g.act_c1 = s->act_params[1];
 
     g.a_sf = wt->w1_sf;
-    g.b_sf = at<uint8_t>(ws, L.xsf);
-    g.b_sf_tile_bytes = L.xsf_tile_bytes;
+    g.b_sf = L.x_token_order ? nullptr : at<uint8_t>(ws, L.xsf);
+    g.b_sf_tile_bytes = L.x_token_order ? 0 : L.xsf_tile_bytes;
     e = launch_gemm(true, mw1, mx, my, g, d.B, nsm, st, pdl);
     if (e != cudaSuccess || !rec(ev, 4, st)) return MOE_ERR_CUDA;
 
@@ -357,8 +379,9 @@ int moe_layer(const moe_shape* s, const float* logits, const uint16_t* shared_lo
     if ((rc = check_weights(w))) return rc;
     if ((rc = check_ws(s, ws, ws_bytes))) return rc;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if ((rc = run_route_sort(s, logits, shared_logit, topk_ids, topk_w, ws, st, nullptr))) return rc;
-    return run_forward(s, x, w, topk_w, ws, out, st, true);
+    bool gathered = false;
+    if ((rc = run_route_sort(s, logits, shared_logit, topk_ids, topk_w, ws, st, nullptr, false, x, &gathered))) return rc;
+    return run_forward(s, x, w, topk_w, ws, out, st, true, nullptr, gathered);
 }
 
 int moe_router(const moe_shape* s, const uint16_t* x, const uint16_t* wr, float* logits, void* ws, size_t ws_bytes,
@@ -383,8 +406,9 @@ int moe_layer_router(const moe_shape* s, const uint16_t* wr, const uint16_t* sha
     if ((rc = check_ws(s, ws, ws_bytes))) return rc;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if ((rc = run_router(s, x, wr, logits, ws, st))) return rc;
-    if ((rc = run_route_sort(s, logits, shared_logit, topk_ids, topk_w, ws, st, nullptr, true))) return rc;
-    return run_forward(s, x, w, topk_w, ws, out, st, true);
+    bool gathered = false;
+    if ((rc = run_route_sort(s, logits, shared_logit, topk_ids, topk_w, ws, st, nullptr, true, x, &gathered))) return rc;
+    return run_forward(s, x, w, topk_w, ws, out, st, true, nullptr, gathered);
 }
 
 int moe_layer_events(const moe_shape* s, const float* logits, const uint16_t* shared_logit, const uint16_t* x,
@@ -402,8 +426,9 @@ int moe_layer_events(const moe_shape* s, const float* logits, const uint16_t* sh
     if ((rc = check_ws(s, ws, ws_bytes))) return rc;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (!rec(events, 0, st)) return MOE_ERR_CUDA;
-    if ((rc = run_route_sort(s, logits, shared_logit, topk_ids, topk_w, ws, st, events))) return rc;
-    return run_forward(s, x, w, topk_w, ws, out, st, false, events);
+    bool gathered = false;
+    if ((rc = run_route_sort(s, logits, shared_logit, topk_ids, topk_w, ws, st, events, false, x, &gathered))) return rc;
+    return run_forward(s, x, w, topk_w, ws, out, st, false, events, gathered);
 }
 
 int moe_layer_host(const moe_shape* s, const float* logits_host, const uint16_t* shared_logit_host,
@@ -431,8 +456,9 @@ int moe_layer_host(const moe_shape* s, const float* logits_host, const uint16_t*
         return MOE_ERR_CUDA;
     int32_t* ids = at<int32_t>(ws, L.st_ids);
     float* tw = at<float>(ws, L.st_w);
-    if ((rc = run_route_sort(s, lg, d.S > 0 ? sl : nullptr, ids, tw, ws, st, nullptr))) return rc;
-    if ((rc = run_forward(s, xd, w, tw, ws, od, st, true))) return rc;
+    bool gathered = false;
+    if ((rc = run_route_sort(s, lg, d.S > 0 ? sl : nullptr, ids, tw, ws, st, nullptr, false, xd, &gathered))) return rc;
+    if ((rc = run_forward(s, xd, w, tw, ws, od, st, true, nullptr, gathered))) return rc;
     if (cudaMemcpyAsync(out_host, od, size_t(d.T) * d.H * 2, cudaMemcpyDeviceToHost, st) != cudaSuccess)
         return MOE_ERR_CUDA;
     return MOE_OK;
@@ -459,6 +485,7 @@ int moe_get_views(const moe_shape* s, void* ws, moe_views* v) {
     v->rows_alloc = d.rows_alloc;
     v->y_is_bf16 = L.y_bf16;
     v->sf_tile_bytes_x = L.xsf_tile_bytes;
+    v->x_token_order = L.x_token_order;
     v->sf_tile_bytes_act = L.asf_tile_bytes;
     return MOE_OK;
 }
@@ -484,8 +511,10 @@ int moe_layer_launch_count(const moe_shape* s, int32_t* count) {
     if (rc) return rc;
     if (!count) return MOE_ERR_NULL;
     const Dims d = make_dims(*s);
-    int n = route_sort_fusable(d.T, d.kp) ? 1 : 1 + sort_launch_count(static_cast<int64_t>(d.T) * d.kp);
-    if (d.T > 0) n += 4;  // gather, FC1, FC2, combine
+    const bool fused = route_sort_fusable(d.T, d.kp);
+    int n = fused ? 1 : 1 + sort_launch_count(static_cast<int64_t>(d.T) * d.kp);
+    // [gather,] FC1, FC2, combine; the decode tilings' x quantisation rides on the fused route + sort
+    if (d.T > 0) n += (fused && d.mode == kModeDecode) ? 3 : 4;
     *count = n;
     return MOE_OK;
 }

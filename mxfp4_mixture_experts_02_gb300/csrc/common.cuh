@@ -40,7 +40,7 @@ struct Layout {
     size_t xq, xsf, act, asf, y, vbase;
     size_t st_logits, st_shared, st_x, st_ids, st_w, st_out;
     size_t total;
-    int xsf_tile_bytes, asf_tile_bytes, y_bf16;
+    int xsf_tile_bytes, asf_tile_bytes, y_bf16, x_token_order;
 };
 
 inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -85,15 +85,21 @@ inline Layout make_layout(const Dims& d) {
     L.c_map = take(size_t(d.R_max) * 4);
     L.sort_hist = take(size_t((d.R_max + 4095) / 4096) * d.Et * 4);
     L.row_w = take(size_t(d.R_max) * 4);
-    // Tile scale layout: per virtual expert and 128-K chunk one 512-byte
-    // block, tile row r / K-block b at (r % 32) * 16 + (r / 32) * 4 + b: one
-    // tcgen05.cp .32x128b.warpx4 puts it in 4 TMEM columns, row r at lane
-    // r % 32, column r / 32, byte b.
+    // Tile scale layout (the FC1 output's scales; the FC1 token producer
+    // builds the same layout in shared memory for x): per virtual expert and
+    // 128-K chunk one 512-byte block, tile row r / K-block b at (r % 32) * 16 +
+    // (r / 32) * 4 + b: one tcgen05.cp .32x128b.warpx4 puts it in 4 TMEM
+    // columns, row r at lane r % 32, column r / 32, byte b.
     L.xsf_tile_bytes = (d.H / 128) * 512;
     L.asf_tile_bytes = (d.I / 128) * 512;
     L.y_bf16 = (d.mode == kModeDecode) ? 0 : 1;
-    L.xq = take(size_t(d.rows_alloc) * d.H);
-    L.xsf = take(size_t(d.V_max) * L.xsf_tile_bytes);
+    // x in MXFP8.  Decode tilings: token order, codes [max_T, H] and scales
+    // [max_T, H / 32] (the FC1 token producer gathers each tile's rows).
+    // 128-row tiles: expert-row order [rows_alloc, H] with the tile scale
+    // layout (TMA boxes).
+    L.x_token_order = (d.mode == kModeDecode) ? 1 : 0;
+    L.xq = take(size_t(L.x_token_order ? d.max_T : d.rows_alloc) * d.H);
+    L.xsf = take(L.x_token_order ? size_t(d.max_T) * (d.H / 32) : size_t(d.V_max) * L.xsf_tile_bytes);
     L.act = take(size_t(d.rows_alloc) * d.I);
     L.asf = take(size_t(d.V_max) * L.asf_tile_bytes);
     // bf16 rows carry the TMA tail too: the store map's row extent is

@@ -185,6 +185,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                     const __grid_constant__ CUtensorMap tmY, const GemmParams p) {
     constexpr bool kStageY = !FC1 && YBF16 && TM == 128;
+    // decode FC1: the token producer gathers x rows from the token-order MXFP8
+    // rows with cp.async (128-row tiles read expert-ordered rows by TMA)
+    constexpr bool kGatherX = FC1 && TM <= 32;
     using C = Cfg<TM, STAGES, kStageY>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -199,7 +202,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            ptx::mbar_init(&full[s], 1);
+            // gathered x rows: the weight producer's arrive (with the weight
+            // bytes) and one arrive per token-producer lane when its row copies
+            // have landed
+            ptx::mbar_init(&full[s], kGatherX ? 1 + 32 : 1);
             ptx::mbar_init(&empty[s], 1);
         }
         ptx::mbar_init(accfull, 1);
@@ -247,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // producer's copies may land before or after.
             uint32_t stage = 0, phase = 0;
             bool ok = true;
-            const uint32_t tx = 256 * 64 + C::kXTile + 1536;
+            const uint32_t tx = kGatherX ? 256 * 64 + 1024 : 256 * 64 + C::kXTile + 1536;
             int4 vq0 = item_desc(p, it0, NB, iend, kNone);
             int4 vq1 = item_desc(p, it0 + g, NB, iend, kNone);
             int4 vq2 = item_desc(p, it0 + 2 * g, NB, iend, kNone);
@@ -281,6 +287,68 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::mbar_wait(&full[s], par, 10ull * 1000 * 1000);
             }
         }
+    } else if (warp == kTokenWarp && kGatherX) {
+        // ------------------------------------- decode FC1 token producer
+        // The x rows of each tile are gathered from the token-order MXFP8 rows
+        // (written by the preceding kernel) with cp.async.  Each copy
+        // instruction moves 4 whole 128-byte row segments (lanes 8r..8r+7 take
+        // the 16-byte chunks of one row: full cache lines per request); chunk c
+        // of tile row i lands at chunk c ^ (i % 8), the 128-byte swizzle the
+        // MMA descriptors expect.  Lane l also copies the 4 block scales of
+        // the 128-K chunk of rows l, l + 32, ... to the tile scale layout, then
+        // arrives on the stage's full barrier once its copies have landed.
+        constexpr int kRowsPerLane = TM >= 32 ? TM / 32 : 1;
+        ptx::pdl_wait();
+        uint32_t stage = 0, phase = 0;
+        bool ok = true;
+        const int sf_row = p.H / 32;
+        const int chunk = lane & 7, rsub = lane >> 3;
+        int4 vq0 = item_desc(p, it0, NB, iend, kNone);
+        int4 vq1 = item_desc(p, it0 + g, NB, iend, kNone);
+        int4 vq2 = item_desc(p, it0 + 2 * g, NB, iend, kNone);
+        for (int it = it0; ok && it < iend; it += g) {
+            const int4 vi = vq0;
+            vq0 = vq1;
+            vq1 = vq2;
+            vq2 = item_desc(p, it + 3 * g, NB, iend, kNone);
+            int tok[kRowsPerLane];  // token of tile row lane + 32 q, or -1
+#pragma unroll
+            for (int q = 0; q < kRowsPerLane; ++q) {
+                const int i = lane + 32 * q;
+                tok[q] = (i < TM && i < vi.z) ? p.a_map[vi.y + i] / p.kp : -1;
+            }
+            for (int kc = 0; kc < KC; ++kc) {
+                const bool waited = wait_or_abort(&empty[stage], phase ^ 1, p.wait_ns, abort_flag);
+                if (!__all_sync(0xffffffffu, waited)) {
+                    if (lane == 0 && !*abort_flag) record_timeout(p, abort_flag, kSiteProducerEmpty);
+                    ok = false;
+                    break;
+                }
+                uint8_t* xs = smem + C::x_off(stage);
+                uint8_t* ss = smem + C::sfx_off(stage);
+#pragma unroll
+                for (int k = 0; k < TM / 4; ++k) {
+                    const int i = 4 * k + rsub;  // tile row of this lane's chunk
+                    const int t = __shfl_sync(0xffffffffu, tok[k >> 3], i & 31);
+                    if (t >= 0)
+                        ptx::cp_async_16(xs + i * 128 + ((chunk ^ (i & 7)) << 4),
+                                         p.xq + static_cast<size_t>(t) * p.H + kc * 128 + chunk * 16);
+                }
+#pragma unroll
+                for (int q = 0; q < kRowsPerLane; ++q) {
+                    const int i = lane + 32 * q;
+                    if (tok[q] >= 0)
+                        ptx::cp_async_4(ss + (i & 31) * 16 + (i >> 5) * 4,
+                                        p.xsf + static_cast<size_t>(tok[q]) * sf_row + kc * 4);
+                }
+                ptx::cp_async_mbar_arrive_noinc(&full[stage]);
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+        }
+        ptx::cp_async_wait_all();  // no copy lands after the CTA has moved on
     } else if (warp == kTokenWarp) {
         if (lane == 0) {
             // -------------------------------------------------- token producer
@@ -333,6 +401,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     ptx::tc_fence_after();
+                    // gathered token rows arrive through cp.async (the
+                    // generic proxy): make them visible to the tensor core
+                    if constexpr (kGatherX) ptx::fence_proxy_async_smem();
                     const uint32_t sf = tmem + C::kAccCols + stage * C::kSfCols;
                     ptx::tc_cp_32x128b_warpx4(sf, ptx::sdesc_sf(ptx::smem_u32(smem + C::sfx_off(stage))));
                     ptx::tc_cp_32x128b_warpx4(sf + 4, ptx::sdesc_sf(ptx::smem_u32(smem + C::sfw_off(stage))));

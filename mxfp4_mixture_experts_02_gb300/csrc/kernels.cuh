@@ -65,21 +65,20 @@ struct RouterTiling {
     int N, ks, n_tiles, grid;
 };
 
-struct GatherParams {  // x -> MXFP8 rows in expert order + tile scales
-    const uint16_t* x;
-    const int32_t* header;
-    const int4* vinfo;
+struct GatherParams {  // x -> MXFP8 + the routing weight of each expert row
+    const uint16_t* x;      // [T, H] bf16
+    const int32_t* header;  // rows R
     const int32_t* a_map;
-    uint8_t* xq;
-    uint8_t* xsf;
+    uint8_t* xq;            // token order [T, H], or expert-row order [rows_alloc, H]
+    uint8_t* xsf;           // token order [T, H / 32], or the tile scale layout
     const float* topk_w;
-    float* row_w;      // routing weight of each row: topk_w[a_map[row]]
-    // token-major pass (128-row tiles): slot -> row map and expert placement
+    float* row_w;           // routing weight of each row: topk_w[a_map[row]]
+    // expert-row order (128-row tiles): slot -> row map and expert placement
     const int32_t* c_map;
     const int32_t* offsets;
     const int32_t* vbase;
-    int token_major;
-    int H, kp, B, xsf_tile_bytes, max_v, grid, T, Et;
+    int token_order;        // 1: decode tilings (the FC1 kernel gathers the rows)
+    int H, T, R_max, max_blocks, kp, B, Et, xsf_tile_bytes;
 };
 
 struct GemmParams {
@@ -102,6 +101,10 @@ struct GemmParams {
     uint64_t wait_ns;
     int act_kind;          // FC1 epilogue activation (MOE_ACT_*)
     int max_v;             // entries of vinfo (virtual-expert bound)
+    // FC1 token rows: gathered per tile from the token-order MXFP8 x
+    const uint8_t* xq;     // [T, H] E4M3
+    const uint8_t* xsf;    // [T, H / 32] E8M0
+    int kp;                // slots per token (a_map / kp = token)
     float act_c0, act_c1;  // its constants: clamp limit, or SiTU beta and linear beta
 };
 
@@ -135,7 +138,10 @@ cudaError_t launch_sort(const SortParams& p, cudaStream_t stream, bool pdl);
 bool route_sort_fusable(int T, int kp);
 // Kernels launch_sort issues for T*k' slots (1, or 3 above one CTA's share).
 int sort_launch_count(int64_t slots);
-cudaError_t launch_route_sort_small(const RouteParams& rp, const SortParams& p, cudaStream_t stream, bool pdl);
+// gp (optional, token-order x only): the launch also quantises x and writes
+// each row's routing weight -- the work of launch_gather.
+cudaError_t launch_route_sort_small(const RouteParams& rp, const SortParams& p, const GatherParams* gp,
+                                    cudaStream_t stream, bool pdl);
 cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream, bool pdl);
 // tmY: bf16 FC2 rows as boxes of 64 columns x 32 rows (read only by the
 // 128-row FC2 tiling; any valid map otherwise).

@@ -1,11 +1,16 @@
 // MX quantisers (OCP MX v1.0 conversion: shared exponent floor(log2 amax) -
 // emax, elements rounded to nearest even and saturated by the cvt.satfinite
 // instructions):
-//   gather_kernel        : x bf16 -> MXFP8 (E4M3, emax 8), written directly in
-//                          expert-row order (the "[SGLang] CUTLASS MoE"
-//                          section 2 shuffle_rows folded into the quantiser)
-//                          with the tile scale layout the FC1 kernel copies
-//                          into tensor memory;
+//   quant_x_kernel       : decode tilings (16 / 32-row tiles): x bf16 ->
+//                          MXFP8 (E4M3, emax 8) in token order, row-major
+//                          E8M0 scales, and each expert row's routing weight
+//                          (the "[SGLang] CUTLASS MoE" section 2 shuffle_rows
+//                          is done by the FC1 token producer, which gathers
+//                          each tile's rows);
+//   gather_token_kernel  : 128-row tiles: x quantised once per token and
+//                          written to each of its expert rows (shuffle_rows
+//                          folded into the quantiser), with the tile scale
+//                          layout the FC1 kernel copies into tensor memory;
 //   quantize_mxfp4_kernel: fp32 weights -> MXFP4 (E2M1, emax 2), offline;
 //   pack_codes_kernel,
 //   pack_scales_kernel   : row-major MXFP4 -> tile-major codes (one contiguous
@@ -21,51 +26,48 @@ namespace {
 
 constexpr int kGatherThreads = 256;
 
-// CTAs walk the virtual experts (tiles of up to B rows).  Thread job =
-// (row, 32-block).  Tile scale layout: per 128-K chunk a 512-byte block,
-// tile row i / K-block b at byte (i % 32) * 16 + (i / 32) * 4 + b % 4.
-__global__ void __launch_bounds__(kGatherThreads) gather_kernel(GatherParams p) {
+// x -> MXFP8 in natural token order plus the per-row routing weight.  Job j <
+// T * H/32: token j / (H/32), 32-element block j % (H/32) (consecutive
+// threads take consecutive blocks of a row: 64-byte reads, 32-byte code
+// writes and 1-byte scale writes, all contiguous across the warp); the
+// remaining R jobs copy topk_w[a_map[row]] to row_w[row].  The GEMM's token
+// producer gathers the rows of each tile from here.
+__global__ void __launch_bounds__(kGatherThreads) quant_x_kernel(GatherParams p) {
     ptx::pdl_wait();
-    const int nv = p.header[kHdrNumV];
     const int nb = p.H / 32;
-    // Bytes of rows beyond the tile stay as they are: the MMA reads 128 rows,
-    // but the accumulator lanes of rows past the tile are never read.
-    for (int v = blockIdx.x; v < nv; v += gridDim.x) {
-        const int4 vi = p.vinfo[v];
-        const int first = vi.y, rows = vi.z;
-        uint8_t* sf_tile = p.xsf + static_cast<size_t>(v) * p.xsf_tile_bytes;
-        for (int job = threadIdx.x; job < rows * nb; job += kGatherThreads) {
-            const int i = job / nb, b = job - i * nb;
-            const int row = first + i;
-            const int slot = p.a_map[row];
-            const int t = slot / p.kp;
-            if (b == 0) p.row_w[row] = p.topk_w[slot];
-            const uint4* src = reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(t) * p.H + b * 32);
-            uint4 raw[4];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) raw[c] = src[c];
-            const uint16_t* hv = reinterpret_cast<const uint16_t*>(raw);
-            float f[32];
-            float amax = 0.f;
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                f[e] = bf16_bits_to_float(hv[e]);
-                amax = fmaxf(amax, fabsf(f[e]));
-            }
-            const int ex = mx_shared_exponent(amax, 8);
-            const float inv = exp2_int(-ex);
-            uint32_t packed[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const uint32_t lo = e4m3x2(f[4 * e] * inv, f[4 * e + 1] * inv);
-                const uint32_t hi = e4m3x2(f[4 * e + 2] * inv, f[4 * e + 3] * inv);
-                packed[e] = lo | (hi << 16);
-            }
-            uint4* dst = reinterpret_cast<uint4*>(p.xq + static_cast<size_t>(row) * p.H + b * 32);
-            dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-            dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-            sf_tile[(b >> 2) * 512 + (i & 31) * 16 + (i >> 5) * 4 + (b & 3)] = static_cast<uint8_t>(ex + 127);
+    const int64_t nq = static_cast<int64_t>(p.T) * nb;
+    const int64_t total = nq + p.header[kHdrRows];
+    for (int64_t job = static_cast<int64_t>(blockIdx.x) * kGatherThreads + threadIdx.x; job < total;
+         job += static_cast<int64_t>(gridDim.x) * kGatherThreads) {
+        if (job >= nq) {
+            const int row = static_cast<int>(job - nq);
+            p.row_w[row] = p.topk_w[p.a_map[row]];
+            continue;
         }
+        const uint4* src = reinterpret_cast<const uint4*>(p.x) + job * 4;
+        uint4 raw[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) raw[c] = __ldg(src + c);
+        // word k holds elements 2k (low half) and 2k + 1 (high half)
+        const uint32_t* wd = reinterpret_cast<const uint32_t*>(raw);
+        float amax = 0.f;
+#pragma unroll
+        for (int k = 0; k < 16; ++k)
+            amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(wd[k] << 16)), fabsf(__uint_as_float(wd[k] & 0xFFFF0000u))));
+        const int ex = mx_shared_exponent(amax, 8);
+        const float inv = exp2_int(-ex);
+        uint32_t packed[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const uint32_t w0 = wd[2 * e], w1 = wd[2 * e + 1];
+            const uint32_t lo = e4m3x2(__uint_as_float(w0 << 16) * inv, __uint_as_float(w0 & 0xFFFF0000u) * inv);
+            const uint32_t hi = e4m3x2(__uint_as_float(w1 << 16) * inv, __uint_as_float(w1 & 0xFFFF0000u) * inv);
+            packed[e] = lo | (hi << 16);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(p.xq) + job * 2;
+        dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+        dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+        p.xsf[job] = static_cast<uint8_t>(ex + 127);
     }
     ptx::pdl_launch_dependents();
 }
@@ -276,11 +278,17 @@ unsigned grid_for(int64_t n, int threads) {
 }  // namespace
 
 cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream, bool pdl) {
-    if (!p.token_major) return launch_kernel(gather_kernel, dim3(p.grid), dim3(kGatherThreads), 0, stream, pdl, p);
-    const int64_t warps = p.T, per_sm_ctas = 8;
-    int64_t blocks = (warps + kTokWarps - 1) / kTokWarps;
-    const int64_t cap = static_cast<int64_t>(p.grid) * per_sm_ctas;  // grid = min(V_max, 8 * #SM)
-    if (blocks > cap) blocks = cap;
+    if (p.token_order) {
+        const int64_t jobs = static_cast<int64_t>(p.T) * (p.H / 32) + p.R_max;
+        int64_t blocks = (jobs + kGatherThreads - 1) / kGatherThreads;
+        if (blocks > p.max_blocks) blocks = p.max_blocks;
+        if (blocks < 1) blocks = 1;
+        return launch_kernel(quant_x_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kGatherThreads), 0, stream, pdl,
+                             p);
+    }
+    int64_t blocks = (static_cast<int64_t>(p.T) + kTokWarps - 1) / kTokWarps;
+    if (blocks > p.max_blocks) blocks = p.max_blocks;
+    if (blocks < 1) blocks = 1;
     return launch_kernel(gather_token_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kTokWarps * 32), 0, stream, pdl,
                          p);
 }

@@ -114,11 +114,16 @@ __global__ void __launch_bounds__(kSortThreads, 1) sort_kernel(SortParams p) {
 // the expert's row count is the popcount of the mask and slot s's row is the
 // expert's first row plus the number of its bits below s -- slot order inside
 // each expert, the same rows as the counting passes below.
+//
+// fuse_x (decode tilings, x kept in token order): the warps that route no
+// token quantise the CTA's tokens' x rows to MXFP8 meanwhile (the section's
+// x quantised in the routing kernel), and CTA 0 writes each row's routing
+// weight while ranking -- the launch then also does the gather's work.
 constexpr int kSmallSlots = 1024;
 constexpr int kRouteCtas = 8;
 
 __global__ void __cluster_dims__(kRouteCtas, 1, 1) __launch_bounds__(kSortThreads, 1)
-    route_sort_small_kernel(RouteParams rp, SortParams p) {
+    route_sort_small_kernel(RouteParams rp, SortParams p, GatherParams gp, int fuse_x) {
     __shared__ uint2 s_cand[kSortWarps][rs::kMaxCand];
     __shared__ int s_ids[kSmallSlots];
     __shared__ int s_off[1024];
@@ -136,8 +141,47 @@ __global__ void __cluster_dims__(kRouteCtas, 1, 1) __launch_bounds__(kSortThread
         for (int w = tid; w < p.Et * nw; w += kSortThreads) s_mask[w] = 0;
     for (int t = rank + kRouteCtas * warp; t < rp.T; t += kRouteCtas * kSortWarps)
         rs::route_token(rp, t, s_cand[warp], ids0);
+    if (fuse_x) {
+        // x -> MXFP8 of this CTA's tokens (rank, rank + 8, ...), one
+        // 32-element block per job, starting at the first warp that routes no
+        // token; token order, row-major scales
+        const int nt = (p.T - rank + kRouteCtas - 1) / kRouteCtas;
+        const int nb = gp.H / 32;
+        const int q = (tid + kSortThreads - 32 * min(nt, kSortWarps)) % kSortThreads;
+        for (int job = q; job < nt * nb; job += kSortThreads) {
+            const int j = job / nb, b = job - j * nb;
+            const size_t blk = static_cast<size_t>(rank + kRouteCtas * j) * nb + b;
+            const uint4* src = reinterpret_cast<const uint4*>(gp.x) + blk * 4;
+            uint4 raw[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) raw[c] = src[c];
+            // word k holds elements 2k (low half) and 2k + 1 (high half)
+            const uint32_t* wd = reinterpret_cast<const uint32_t*>(raw);
+            float amax = 0.f;
+#pragma unroll
+            for (int k = 0; k < 16; ++k)
+                amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(wd[k] << 16)), fabsf(__uint_as_float(wd[k] & 0xFFFF0000u))));
+            const int ex = mx_shared_exponent(amax, 8);
+            const float inv = exp2_int(-ex);
+            uint32_t packed[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const uint32_t w0 = wd[2 * e], w1 = wd[2 * e + 1];
+                const uint32_t lo = e4m3x2(__uint_as_float(w0 << 16) * inv, __uint_as_float(w0 & 0xFFFF0000u) * inv);
+                const uint32_t hi = e4m3x2(__uint_as_float(w1 << 16) * inv, __uint_as_float(w1 & 0xFFFF0000u) * inv);
+                packed[e] = lo | (hi << 16);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(gp.xq) + blk * 2;
+            dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+            dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+            gp.xsf[blk] = static_cast<uint8_t>(ex + 127);
+        }
+    }
     cluster.sync();
-    if (rank != 0) return;  // nothing reads the other CTAs' shared memory
+    if (rank != 0) {
+        ptx::pdl_launch_dependents();
+        return;  // nothing reads the other CTAs' shared memory
+    }
 
     int e = -1;
     if (tid < n) {
@@ -158,6 +202,7 @@ __global__ void __cluster_dims__(kRouteCtas, 1, 1) __launch_bounds__(kSortThread
             const int row = s_off[e] + r;
             p.a_map[row] = tid;
             p.c_map[tid] = row;
+            if (fuse_x) gp.row_w[row] = rp.w[tid];
         } else {
             p.c_map[tid] = -1;
         }
@@ -265,12 +310,15 @@ int sort_launch_count(int64_t slots) { return slots <= kSortWarps * kBigWarpSlot
 
 bool route_sort_fusable(int T, int kp) { return static_cast<int64_t>(T) * kp <= kSmallSlots; }
 
-cudaError_t launch_route_sort_small(const RouteParams& rp, const SortParams& p, cudaStream_t stream, bool pdl) {
+cudaError_t launch_route_sort_small(const RouteParams& rp, const SortParams& p, const GatherParams* gp,
+                                    cudaStream_t stream, bool pdl) {
     const size_t smem = static_cast<size_t>(p.Et) * ((p.T * p.kp + 31) / 32) * sizeof(uint32_t);
     cudaError_t err = cudaFuncSetAttribute(route_sort_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(smem));
     if (err != cudaSuccess) return err;
-    return launch_kernel(route_sort_small_kernel, dim3(kRouteCtas), dim3(kSortThreads), smem, stream, pdl, rp, p);
+    const GatherParams g = gp ? *gp : GatherParams{};
+    return launch_kernel(route_sort_small_kernel, dim3(kRouteCtas), dim3(kSortThreads), smem, stream, pdl, rp, p, g,
+                         gp ? 1 : 0);
 }
 
 }  // namespace moe

@@ -122,18 +122,22 @@ def check_layer(cfg, tokens=None):
     toks = sample_tokens(cfg.T) if tokens is None else tokens
     ref = orc.forward(toks)
     xq = v["xq"].cpu().numpy()
-    xsf = tile_scales_to_rows(v["xq_sf"], vinfo, s["num_v"], cfg.hidden)
+    token_order = bool(v["x_token_order"])
+    xsf = v["xq_sf"].cpu().numpy() if token_order else tile_scales_to_rows(v["xq_sf"], vinfo, s["num_v"], cfg.hidden)
     act = v["act"].cpu().numpy()
     asf = tile_scales_to_rows(v["act_sf"], vinfo, s["num_v"], cfg.inter)
     n_act, n_diff = 0, 0
     for k, t in enumerate(toks):
+        if token_order:  # x -> MXFP8: bit-exact
+            np.testing.assert_array_equal(xq[t], ref["xq"][k])
+            np.testing.assert_array_equal(xsf[t], ref["xq_sf"][k])
         for j in range(cfg.kp):
             row = s["c_map"][t * cfg.kp + j]
             if row < 0:
                 continue
-            # x -> MXFP8 in expert order: bit-exact
-            np.testing.assert_array_equal(xq[row], ref["xq"][k])
-            np.testing.assert_array_equal(xsf[row], ref["xq_sf"][k])
+            if not token_order:  # x -> MXFP8 in expert-row order: bit-exact
+                np.testing.assert_array_equal(xq[row], ref["xq"][k])
+                np.testing.assert_array_equal(xsf[row], ref["xq_sf"][k])
             # intermediate: decoded values, mostly identical, else one step apart
             ga = E4M3_VALUES[act[row]] * np.exp2(np.repeat(asf[row].astype(np.float64), 32) - 127)
             oa = E4M3_VALUES[ref["act"][k, j]] * np.exp2(np.repeat(ref["act_sf"][k, j].astype(np.float64), 32) - 127)

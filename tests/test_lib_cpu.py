@@ -93,8 +93,8 @@ def test_packed_weight_sizes():
 
 
 def test_layer_launch_count():
-    # decode: fused route+sort, gather, FC1, FC2, combine
-    assert moe.moe_layer_launch_count(_shape()) == 5
+    # decode: route + sort + x quantisation in one launch, FC1, FC2, combine
+    assert moe.moe_layer_launch_count(_shape()) == 4
     # 256 tokens x 16 picks > 1024 slots: route, one-CTA sort, then 4
     assert moe.moe_layer_launch_count(_shape(T=256, max_T=256)) == 6
     # prefill tiling at 32768 tokens: route, 3-kernel sort, gather, FC1, FC2, combine
