@@ -265,7 +265,11 @@ def run_ours(args, cfg):
     H, I = cfg.hidden, cfg.inter
     prefill = cfg.block_n == 128
     ybytes = 2 if prefill else 4
-    fc1_bytes = touched * W1_BYTES_PER_EXPERT(H, I) + R * H * 33 // 32 + R * I * 33 // 32
+    # FC1's x operand: token-order rows gathered per tile (decode tilings: each
+    # token's MXFP8 row is read once from HBM, re-reads hit L2), or the
+    # expert-ordered rows (128-row tiles: R rows)
+    x_rows = cfg.T if not prefill else R
+    fc1_bytes = touched * W1_BYTES_PER_EXPERT(H, I) + x_rows * H * 33 // 32 + R * I * 33 // 32
     fc2_bytes = touched * W2_BYTES_PER_EXPERT(H, I) + R * I * 33 // 32 + R * H * ybytes
     fc1_flops = 2.0 * R * H * 2 * I
     fc2_flops = 2.0 * R * I * H
