@@ -259,7 +259,9 @@ int run_router(const moe_shape* s, const uint16_t* x, const uint16_t* wr, float*
     int32_t* status = at<int32_t>(ws, make_layout(d).header) + kHdrStatus;
     if (cudaMemsetAsync(status, 0, 2 * sizeof(int32_t), st) != cudaSuccess) return MOE_ERR_CUDA;
     if (d.T == 0) return MOE_OK;
-    const RouterTiling t = router_tiling(d.T, d.Eg);
+    const int nsm = num_sms_cached();
+    if (nsm <= 0) return MOE_ERR_CUDA;
+    const RouterTiling t = router_tiling(d.T, d.Eg, nsm);
     CUtensorMap mx, mw;
     if (!make_map(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, d.H, d.T, size_t(d.H) * 2, 64, 128) ||
         !make_map(&mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, wr, d.H, d.Eg, size_t(d.H) * 2, 64, t.N))

@@ -148,7 +148,7 @@ cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream, bool pdl);
 cudaError_t launch_gemm(bool fc1, const CUtensorMap& tmW, const CUtensorMap& tmX, const CUtensorMap& tmY,
                         const GemmParams& p, int TM, int grid, cudaStream_t stream, bool pdl);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream, bool pdl);
-RouterTiling router_tiling(int T, int Eg);
+RouterTiling router_tiling(int T, int Eg, int num_sms);
 cudaError_t launch_router(const CUtensorMap& tmX, const CUtensorMap& tmW, const RouterParams& p, int grid,
                           cudaStream_t stream, bool pdl);
 cudaError_t launch_quantize_mxfp4(const QuantParams& p, cudaStream_t stream);

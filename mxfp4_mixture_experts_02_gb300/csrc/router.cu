@@ -17,7 +17,8 @@
 // the tile over the KS partials in rank order (distributed shared memory
 // loads, a fixed order: the logits are bit-reproducible), then a second
 // barrier keeps the partials alive until all reads are done.  Long batches
-// use N = 224 (E_global 896 = 4 tiles) and no split.
+// use N = 224 (E_global 896 = 4 tiles), no split, and a persistent grid with
+// two TMEM accumulators (below).
 //
 // Warps: 0..3 epilogue (TMEM lane quadrant = warp), 4 TMA producer, 5 TMEM
 // allocator and single-thread MMA issuer.  Every mbarrier wait is bounded; on
@@ -263,6 +264,171 @@ __global__ void __launch_bounds__(kRtThreads, 1)
     }
 }
 
+// Long batches: a persistent grid (one CTA per SM) takes the 128 x 224 tiles
+// round-robin.  Two accumulators of 224 columns in TMEM (kind::f16 needs no
+// scale columns, so 2 x 224 fit in 512): the MMA issuer fills one while the
+// four epilogue warps drain the other to global memory, so a tile's epilogue
+// overlaps the next tile's MMAs.
+constexpr int kRpWarps = 6;  // 0..3 epilogue, 4 producer, 5 MMA
+constexpr int kRpThreads = kRpWarps * 32;
+constexpr int kRpN = 224;
+constexpr int kRpAccStride = 256;  // TMEM columns between the two accumulators
+// pipeline buffers, 13 mbarriers + TMEM slot + abort flag, 1 KiB alignment slack
+constexpr int kRpSmemBytes = RtCfg<kRpN>::kOffBar + 16 * 8 + 1024;
+static_assert(kRpSmemBytes <= 232448, "shared memory budget");
+
+__global__ void __launch_bounds__(kRpThreads, 1)
+    router_gemm_persistent_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                                  const RouterParams p) {
+    using C = RtCfg<kRpN>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+    uint64_t* empty = full + kRtStages;
+    uint64_t* accfull = empty + kRtStages;  // [2]
+    uint64_t* accempty = accfull + 2;       // [2]
+    uint64_t* done = accempty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ntiles = ((p.T + 127) / 128) * p.n_tiles;
+    const int KC = p.H / kRtKChunk;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kRtStages; ++s) {
+            ptx::mbar_init(&full[s], 1);
+            ptx::mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            ptx::mbar_init(&accfull[a], 1);
+            ptx::mbar_init(&accempty[a], 4);  // the four epilogue warps
+        }
+        ptx::mbar_init(done, 1);
+        *abort_flag = 0;
+        ptx::fence_mbarrier_init();
+    }
+    if (warp == kRtProducerWarp && lane == 0) {
+        ptx::tma_prefetch_desc(&tmX);
+        ptx::tma_prefetch_desc(&tmW);
+    }
+    if (warp == kRtMmaWarp) {
+        ptx::tmem_alloc(tmem_slot, 512);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    ptx::pdl_wait();
+
+    if (warp == kRtProducerWarp) {
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0;
+            int issued = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
+                const int m0 = (tile / p.n_tiles) * 128, n0 = (tile % p.n_tiles) * kRpN;
+                for (int kc = 0; kc < KC; ++kc) {
+                    if (!rt_wait(&empty[stage], phase ^ 1, p.wait_ns, abort_flag)) {
+                        if (!*abort_flag) rt_record_timeout(p, abort_flag, kRtSiteProducer);
+                        ok = false;
+                        break;
+                    }
+                    ptx::mbar_arrive_expect_tx(&full[stage], C::kStageTx);
+                    ptx::tma_load_2d(smem + C::kOffA + stage * C::kATile, &tmX, &full[stage], kc * kRtKChunk, m0);
+                    ptx::tma_load_2d(smem + C::kOffB + stage * C::kBTile, &tmW, &full[stage], kc * kRtKChunk, n0);
+                    ++issued;
+                    if (++stage == kRtStages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            for (int i = issued > kRtStages ? issued - kRtStages : 0; i < issued; ++i)
+                ptx::mbar_wait(&full[i % kRtStages], static_cast<uint32_t>(i / kRtStages) & 1, 10ull * 1000 * 1000);
+        }
+    } else if (warp == kRtMmaWarp) {
+        if (lane == 0) {
+            constexpr uint32_t kIdesc = ptx::idesc_f16_bf16(128, kRpN);
+            uint32_t stage = 0, phase = 0;
+            uint32_t aphase[2] = {0, 0};
+            bool ok = true;
+            int j = 0;  // this CTA's tile count
+            for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x, ++j) {
+                const int a = j & 1;
+                if (!rt_wait(&accempty[a], aphase[a] ^ 1, p.wait_ns, abort_flag)) {
+                    if (!*abort_flag) rt_record_timeout(p, abort_flag, kRtSiteMma);
+                    break;
+                }
+                aphase[a] ^= 1;
+                ptx::tc_fence_after();
+                const uint32_t acc = tmem + a * kRpAccStride;
+                for (int kc = 0; kc < KC; ++kc) {
+                    if (!rt_wait(&full[stage], phase, p.wait_ns, abort_flag)) {
+                        if (!*abort_flag) rt_record_timeout(p, abort_flag, kRtSiteMma);
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint32_t xa = ptx::smem_u32(smem + C::kOffA + stage * C::kATile);
+                    const uint32_t wa = ptx::smem_u32(smem + C::kOffB + stage * C::kBTile);
+#pragma unroll
+                    for (int kk = 0; kk < kRtKChunk / 16; ++kk)
+                        ptx::mma_f16(acc, ptx::sdesc_sw128(xa + kk * 32), ptx::sdesc_sw128(wa + kk * 32), kIdesc,
+                                     (kc | kk) != 0);
+                    ptx::tc_commit(&empty[stage]);
+                    if (++stage == kRtStages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (ok) ptx::tc_commit(&accfull[a]);
+            }
+            ptx::tc_commit(done);
+            ptx::mbar_wait(done, 0, 10ull * 1000 * 1000);
+        }
+    } else {
+        // ---------------------------------------------------------- epilogue
+        const int row = warp * 32 + lane;
+        uint32_t aphase[2] = {0, 0};
+        int j = 0;
+        for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++j) {
+            const int a = j & 1;
+            bool ok = rt_wait(&accfull[a], aphase[a], p.wait_ns, abort_flag);
+            if (!ok && lane == 0 && !*abort_flag) rt_record_timeout(p, abort_flag, kRtSiteEpi);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            aphase[a] ^= 1;
+            ptx::tc_fence_after();
+            const int m0 = (tile / p.n_tiles) * 128, n0 = (tile % p.n_tiles) * kRpN;
+            const bool valid = m0 + row < p.T;
+            float* out = p.logits + static_cast<int64_t>(m0 + row) * p.Eg;
+            const uint32_t tq = tmem + a * kRpAccStride + (static_cast<uint32_t>(warp * 32) << 16);
+#pragma unroll 1
+            for (int c = 0; c < kRpN / 32; ++c) {
+                uint32_t r[32];
+                ptx::tmem_ld32(tq + 32 * c, r);
+                ptx::tmem_wait_ld();
+                if (c == kRpN / 32 - 1) {
+                    // the accumulator is free once its last columns are in registers
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(&accempty[a]);
+                }
+                if (valid) store_logits_32(out, n0 + 32 * c, p.Eg, r);
+            }
+        }
+    }
+
+    ptx::pdl_launch_dependents();
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    if (warp == kRtMmaWarp) {
+        __syncwarp();
+        ptx::tmem_dealloc(tmem, 512);
+    }
+}
+
 template <int N>
 cudaError_t launch_router_impl(const CUtensorMap& tmX, const CUtensorMap& tmW, const RouterParams& p, int grid,
                                cudaStream_t stream, bool pdl) {
@@ -294,24 +460,29 @@ cudaError_t launch_router_impl(const CUtensorMap& tmX, const CUtensorMap& tmW, c
 
 }  // namespace
 
-RouterTiling router_tiling(int T, int Eg) {
+RouterTiling router_tiling(int T, int Eg, int num_sms) {
     RouterTiling t{};
     if (T <= 256) {
         t.N = 64;
         t.ks = 8;
     } else {
-        t.N = 224;
+        t.N = kRpN;
         t.ks = 1;
     }
     t.n_tiles = (Eg + t.N - 1) / t.N;
     t.grid = ((T + 127) / 128) * t.n_tiles * t.ks;
+    if (t.ks == 1 && t.grid > num_sms) t.grid = num_sms;  // persistent: tiles round-robin over one CTA per SM
     return t;
 }
 
 cudaError_t launch_router(const CUtensorMap& tmX, const CUtensorMap& tmW, const RouterParams& p, int grid,
                           cudaStream_t stream, bool pdl) {
     if (p.N == 64) return launch_router_impl<64>(tmX, tmW, p, grid, stream, pdl);
-    return launch_router_impl<224>(tmX, tmW, p, grid, stream, pdl);
+    cudaError_t err = cudaFuncSetAttribute(router_gemm_persistent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           kRpSmemBytes);
+    if (err != cudaSuccess) return err;
+    return launch_kernel(router_gemm_persistent_kernel, dim3(grid), dim3(kRpThreads), kRpSmemBytes, stream, pdl, tmX,
+                         tmW, p);
 }
 
 }  // namespace moe
