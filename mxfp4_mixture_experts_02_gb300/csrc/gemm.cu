@@ -27,9 +27,12 @@
 //
 // Warp roles (11 warps): 0..7 epilogue (warp w reads TMEM lane quadrant w % 4
 // and column half w / 4; with TM <= 32 only quadrant 0 holds tokens, so only
-// warps 0 and 4 work), 8 weight producer and 10 token producer (one thread
-// each, filling the same STAGES-deep ring: a single issuing thread could not
-// keep up with the MMAs), 9 TMEM allocator and single-thread MMA issuer.  The epilogue releases the accumulator as soon as
+// warps 0 and 4 work), 8 weight producer (one thread, TMA) and 10 token
+// producer filling the same STAGES-deep ring (a single issuing thread could
+// not keep up with the MMAs): one thread issuing TMA boxes of expert-ordered
+// rows, except in the decode FC1, where all 32 lanes gather the tile's rows
+// from the token-order MXFP8 x with cp.async; 9 TMEM allocator and
+// single-thread MMA issuer.  The epilogue releases the accumulator as soon as
 // its TMEM loads complete, so the next item's MMAs overlap the activation /
 // quantise / store math.  Every wait is bounded; on expiry the CTA records
 // MOE_ERR_TIMEOUT in the workspace status word, stops, lets its MMAs drain,
