@@ -228,11 +228,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    // The work list comes from the sort, which has completed when this grid
-    // launches (the previous kernel's CTAs waited on it before triggering
-    // this launch).  Only the token operands -- written by the immediately
-    // preceding kernel -- need griddepcontrol.wait, which the token producer
-    // issues while the weight producer streams the first weight stages.
+    // The work list comes from the sort: either that grid has completed when
+    // this grid launches (a kernel in between waited on it before triggering
+    // this launch), or it is the fused route + sort launch just before this
+    // one, which makes its work-list writes visible device-wide before it
+    // triggers this launch.  Only the token operands -- written by the
+    // immediately preceding kernel -- need griddepcontrol.wait, which the
+    // token producer issues while the weight producer streams the first
+    // weight stages.
     const int num_v = p.header[kHdrNumV];
     const int NB = FC1 ? p.I / 128 : p.H / 256;  // 256-row weight blocks per expert
     const int KC = FC1 ? p.H / 128 : p.I / 128;  // 128-wide K chunks

@@ -207,6 +207,10 @@ __global__ void __cluster_dims__(kRouteCtas, 1, 1) __launch_bounds__(kSortThread
             p.c_map[tid] = -1;
         }
     }
+    // The GEMM launched next reads the work list (header, virtual experts)
+    // before its griddepcontrol.wait -- its weight stream starts at once --
+    // so the writes are made visible device-wide before the trigger.
+    __threadfence();
     ptx::pdl_launch_dependents();
 }
 
