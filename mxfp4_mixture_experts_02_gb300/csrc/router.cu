@@ -40,7 +40,7 @@ constexpr int kRtWarps = 6;
 constexpr int kRtThreads = kRtWarps * 32;
 constexpr int kRtProducerWarp = 4;
 constexpr int kRtMmaWarp = 5;
-constexpr int kRtStages = 4;
+constexpr int kRtStages = 5;
 constexpr int kRtKChunk = 64;  // bf16 elements per 128-byte row of a stage
 
 enum { kRtSiteProducer = 11, kRtSiteMma = 12, kRtSiteEpi = 13 };
