@@ -128,7 +128,9 @@ __global__ void __cluster_dims__(kRouteCtas, 1, 1) __launch_bounds__(kSortThread
     __shared__ int s_ids[kSmallSlots];
     __shared__ int s_off[1024];
     __shared__ int s_tot[3][rs::kScanWarps];
-    extern __shared__ uint32_t s_mask[];  // [Et][nw]: slot bitmask per local expert
+    // [nw][Et]: word w of every expert's slot bitmask side by side, so the
+    // per-expert counting pass (thread = expert) reads consecutive words
+    extern __shared__ uint32_t s_mask[];
     namespace cg = cooperative_groups;
     cg::cluster_group cluster = cg::this_cluster();
     const int rank = static_cast<int>(cluster.block_rank());
@@ -186,19 +188,19 @@ __global__ void __cluster_dims__(kRouteCtas, 1, 1) __launch_bounds__(kSortThread
     int e = -1;
     if (tid < n) {
         e = local_expert(s_ids[tid], p);
-        if (e >= 0) atomicOr(&s_mask[e * nw + (tid >> 5)], 1u << (tid & 31));
+        if (e >= 0) atomicOr(&s_mask[(tid >> 5) * p.Et + e], 1u << (tid & 31));
     }
     __syncthreads();
     int cnt = 0;
     if (tid < p.Et)
-        for (int w = 0; w < nw; ++w) cnt += __popc(s_mask[tid * nw + w]);
+        for (int w = 0; w < nw; ++w) cnt += __popc(s_mask[w * p.Et + tid]);
     place_experts(p, cnt, s_off, s_tot);
     __syncthreads();
     if (tid < n) {
         if (e >= 0) {
-            const uint32_t* m = s_mask + e * nw;
-            int r = __popc(m[tid >> 5] & ((1u << (tid & 31)) - 1u));
-            for (int w = 0; w < (tid >> 5); ++w) r += __popc(m[w]);
+            const uint32_t* m = s_mask + e;  // word w at m[w * Et]
+            int r = __popc(m[(tid >> 5) * p.Et] & ((1u << (tid & 31)) - 1u));
+            for (int w = 0; w < (tid >> 5); ++w) r += __popc(m[w * p.Et]);
             const int row = s_off[e] + r;
             p.a_map[row] = tid;
             p.c_map[tid] = row;
