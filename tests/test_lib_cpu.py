@@ -77,6 +77,18 @@ def test_host_side_errors_launch_nothing():
     wt = _Weights(48, 256, 256, 256)  # w1 not 32-byte aligned
     need = moe.moe_workspace_bytes(_shape())
     assert L.moe_forward(ctypes.byref(s), 256, ctypes.byref(wt), 256, 256, need, 256, None) == -3
+    # router entry points: NULL, unsupported shape, misaligned buffers, small workspace
+    need = moe.moe_workspace_bytes(_shape())
+    assert L.moe_router(ctypes.byref(s), None, 256, 256, 256, need, None) == -1
+    assert L.moe_router(ctypes.byref(bad), 256, 256, 256, 256, need, None) == -2
+    assert L.moe_router(ctypes.byref(s), 264, 256, 256, 256, need, None) == -3  # x not 16-byte aligned
+    assert L.moe_router(ctypes.byref(s), 256, 256, 260, 256, need, None) == -3  # logits not 16-byte aligned
+    assert L.moe_router(ctypes.byref(s), 256, 256, 256, 256, 100, None) == -4
+    assert L.moe_layer_router(ctypes.byref(s), None, None, 256, ctypes.byref(wt), 256, 256, 256, 256, need, 256,
+                              None) == -1
+    good = _Weights(256, 256, 256, 256)
+    assert L.moe_layer_router(ctypes.byref(s), 256, None, 256, ctypes.byref(good), 256, 256, 256, 256, 100, 256,
+                              None) == -4
     # packing size rules
     assert L.moe_pack_weights(16, 16, 2, 100, 128, 0, 16, 16, None) == -2
     assert L.moe_pack_weights(16, 16, 2, 128, 128, 1, 16, 16, None) == -2
