@@ -116,9 +116,9 @@ __global__ void __launch_bounds__(kSortThreads, 1) sort_kernel(SortParams p) {
 // each expert, the same rows as the counting passes below.
 //
 // fuse_x (decode tilings, x kept in token order): the warps that route no
-// token quantise the CTA's tokens' x rows to MXFP8 meanwhile (the section's
-// x quantised in the routing kernel), and CTA 0 writes each row's routing
-// weight while ranking -- the launch then also does the gather's work.
+// token quantise the CTA's tokens' x rows to MXFP8 meanwhile, and CTA 0
+// writes each row's routing weight while ranking -- the launch then also
+// does the gather's work, and no launch of its own is spent on it.
 constexpr int kSmallSlots = 1024;
 constexpr int kRouteCtas = 8;
 
