@@ -139,7 +139,15 @@ typedef struct moe_views {
  * section 2, restated as runtime checks.) */
 int moe_is_supported(const moe_shape* shape);
 
-/* Bytes of the single workspace buffer (256-byte aligned carve). */
+/* Bytes of the single workspace buffer that every other call carves, at
+ * 256-byte alignment, into the routing header, expert counts / offsets,
+ * virtual-expert descriptors, a_map / c_map, the MXFP8 x, the intermediate
+ * (codes + tile scales, with block_n rows of padding for the last tile's TMA
+ * box) and the FC2 rows.  ("... MXFP4 decode MoE ... shape templates",
+ * section 3: one byte tensor carved once at 256-byte alignment, so the host
+ * allocates a single buffer; the padded intermediate rows are the same
+ * section's last-virtual-expert box.)  Returns MOE_ERR_SHAPE for an
+ * unsupported shape. */
 int moe_workspace_bytes(const moe_shape* shape, size_t* bytes);
 
 /* fp32 [rows, K] -> MXFP4: codes [rows, K/2] and E8M0 scales [rows, K/32]
@@ -163,7 +171,14 @@ int moe_quantize_mxfp4(const float* w, int64_t rows, int64_t K, uint8_t* codes, 
  *                  + j (the tensor-memory scale layout, one tcgen05.cp each).
  * N % 256 == 0, K % 128 == 0.  Sizes: moe_packed_weight_bytes. */
 /* Rows per block (256) and the byte sizes of moe_pack_weights' outputs for
- * one weight matrix per expert [experts, N, K] (equal to the inputs'). */
+ * one weight matrix per expert [experts, N, K] (equal to the inputs').
+ *
+ * moe_pack_weights: the operand shapes are those of "[SGLang] CUTLASS MoE",
+ * structure diagram (GEMM1 (m*topk, k) x (E, k, 2n), GEMM2 (m*topk, n) x
+ * (E, n, k), E2M1 weights with one E8M0 scale per 32 K as in "... MXFP4
+ * decode MoE ... shape templates", section 1); the tile-major order is this
+ * library's own layout for its TMA stages.  Asynchronous on `stream`; the
+ * outputs must not alias the inputs. */
 int moe_packed_weight_bytes(int64_t experts, int64_t N, int64_t K, int32_t pair_halves, int32_t* block_rows,
                             size_t* code_bytes, size_t* scale_bytes);
 
@@ -189,7 +204,10 @@ int moe_route(const moe_shape* shape, const float* logits, const uint16_t* share
 int moe_sort(const moe_shape* shape, const int32_t* topk_ids, void* workspace, size_t workspace_bytes,
              moe_stream_t stream);
 
-/* Forward after moe_sort: x bf16 [T, H] -> out bf16 [T, H].
+/* Forward after moe_sort ("[SGLang] CUTLASS MoE", structure diagram:
+ * quantise + shuffle_rows (section 2), GEMM1, silu_and_mul (section 4),
+ * GEMM2 and apply_shuffle_mul_sum (section 5)): x bf16 [T, H] -> out bf16
+ * [T, H].
  *   out[t] = bf16( sum_{j: c_map[t,j] >= 0, ascending j} topk_w[t,j] *
  *                  Y_j(t) ),  Y_j = FC2(MXFP8(h(G, U))), [G | U] =
  *                  FC1(MXFP8(x[t])) with expert topk_ids[t,j]'s weights and h
@@ -223,8 +241,14 @@ int moe_layer_router(const moe_shape* shape, const uint16_t* wr, const uint16_t*
                      const moe_weights* weights, float* logits, int32_t* topk_ids, float* topk_w, void* workspace,
                      size_t workspace_bytes, uint16_t* out, moe_stream_t stream);
 
-/* route + sort + forward as one fixed launch chain (programmatic dependent
- * launch between kernels, no host synchronisation, graph capturable). */
+/* route + sort + forward as one fixed launch chain: programmatic dependent
+ * launch between kernels, no host synchronisation, and kernels that find no
+ * work exit at once, so one captured CUDA graph serves every routing of the
+ * shape ("[FlashInfer] Device-side gating for the MoE GEMM2 path", section 2
+ * "fixed launch chain for CUDA Graph"; "... MXFP4 decode MoE ... shape
+ * templates", introduction: routing and the MoE launched from one host
+ * entry with PDL).  Same arguments and layouts as moe_route + moe_sort +
+ * moe_forward; topk_ids / topk_w receive the routing. */
 int moe_layer(const moe_shape* shape, const float* logits, const uint16_t* shared_logit, const uint16_t* x,
               const moe_weights* weights, int32_t* topk_ids, float* topk_w, void* workspace, size_t workspace_bytes,
               uint16_t* out, moe_stream_t stream);
@@ -232,7 +256,10 @@ int moe_layer(const moe_shape* shape, const float* logits, const uint16_t* share
 /* moe_layer from HOST buffers: copies logits, shared_logit and x (host,
  * preferably pinned) into the workspace's staging area, runs the chain and
  * copies out (host) back, all on `stream`; the caller synchronises before
- * reading out.  Weights stay on the device. */
+ * reading out.  Weights stay on the device.  The layer is the one of
+ * "[SGLang] CUTLASS MoE", structure diagram (input a (m, k) -> output
+ * (m, k)); the host copies around it are this library's end-to-end entry
+ * point.  Not capturable (host memory). */
 int moe_layer_host(const moe_shape* shape, const float* logits_host, const uint16_t* shared_logit_host,
                    const uint16_t* x_host, const moe_weights* weights, void* workspace, size_t workspace_bytes,
                    uint16_t* out_host, moe_stream_t stream);
@@ -261,18 +288,46 @@ int moe_layer_events(const moe_shape* shape, const float* logits, const uint16_t
  * a device shares the one array and leaves its contents behind: calls whose
  * executions overlap on the GPU (other streams, other host threads) race and
  * must be serialised by the caller.  Device-side errors are recorded in that
- * array's status word, which this entry point does not expose. */
+ * array's status word: read it with moe_noalloc_get_status.  The array's
+ * device address is looked up again on every call issued outside stream
+ * capture (so a device reset that reloads the library's module is picked
+ * up); a call issued during capture reuses the address of the last call on
+ * that device, so at least one call must precede any capture. */
 int moe_layer_noalloc(const moe_shape* shape, const float* logits, const uint16_t* shared_logit, const uint16_t* x,
                       const moe_weights* weights, int32_t* topk_ids, float* topk_w, uint16_t* out,
                       moe_stream_t stream);
 
+/* moe_get_status for moe_layer_noalloc: reads the status word of the
+ * current device's fixed scratch array (synchronous copy; call after the
+ * stream has finished).  The array starts zeroed, so before the first
+ * moe_layer_noalloc call on a device this reads (MOE_OK, 0). */
+int moe_noalloc_get_status(int32_t* status, int32_t* detail);
+
 /* Workspace views (device pointers) for inspection. */
 int moe_get_views(const moe_shape* shape, void* workspace, moe_views* views);
 
-/* Reads the status word (and its detail) from the workspace with a
+/* Reads the status word (and its detail) from the workspace header with a
  * synchronous device-to-host copy: call after the stream has finished.
- * *status is MOE_OK or MOE_ERR_TIMEOUT. */
+ * *status is MOE_OK or MOE_ERR_TIMEOUT; *detail = site * 65536 + block of the
+ * first expired wait (site 1 producer ring slot, 2 MMA data, 3 MMA
+ * accumulator, 4 epilogue accumulator, 5 the test stall below).  The word
+ * lives in the counters region of the single workspace ("... MXFP4 decode MoE
+ * ... shape templates", section 3); the bounded waits that write it are this
+ * library's guard against a kernel that would otherwise spin forever.  The
+ * sort resets it on every call. */
 int moe_get_status(const void* workspace, int32_t* status, int32_t* detail);
+
+/* Test hook for the device-error path, off (0) by default.  While stall_ns is
+ * nonzero, every later launch of the FC1 GEMM (on any device) makes its MMA
+ * thread first wait stall_ns on a barrier that nothing arrives on; the wait
+ * expires, the CTA records MOE_ERR_TIMEOUT (site 5) in the status word,
+ * stops its producers and epilogue, lets their copies land, frees tensor
+ * memory and exits.  FC2 and the combine still run, on stale data: the
+ * output of such a call is garbage, its status says so.  The value is read
+ * when a call is issued (a captured graph keeps the value of its capture).
+ * Not thread safe against concurrent calls; for tests only.  No counterpart
+ * on the reference pages. */
+int moe_test_set_stall(uint64_t stall_ns);
 
 /* Number of SMs the launches are sized for on the current device. */
 int moe_num_sms(int32_t* num_sms);

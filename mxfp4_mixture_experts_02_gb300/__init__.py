@@ -20,7 +20,8 @@ __all__ = [
     "MoeShape", "MoeWeights", "MoeError", "lib", "moe_is_supported", "moe_workspace_bytes",
     "moe_quantize_mxfp4", "moe_packed_weight_bytes", "moe_pack_weights", "moe_route", "moe_sort", "moe_forward",
     "moe_layer", "moe_router", "moe_layer_router", "moe_layer_host", "moe_layer_events", "moe_layer_noalloc", "moe_get_views", "moe_get_status",
-    "moe_num_sms", "moe_layer_launch_count", "quantize_expert_weights",
+    "moe_num_sms", "moe_layer_launch_count", "quantize_expert_weights", "moe_noalloc_get_status",
+    "moe_test_set_stall",
     "workspace", "MOE_OK", "MOE_ERR_TIMEOUT", "MOE_ERR_WORKSPACE",
 ]
 
@@ -119,6 +120,8 @@ _SIGS = {
     "moe_layer_noalloc": [ctypes.c_void_p] * 9,
     "moe_get_views": [ctypes.c_void_p] * 3,
     "moe_get_status": [ctypes.c_void_p] * 3,
+    "moe_noalloc_get_status": [ctypes.c_void_p] * 2,
+    "moe_test_set_stall": [ctypes.c_uint64],
     "moe_num_sms": [ctypes.c_void_p],
     "moe_layer_launch_count": [ctypes.c_void_p, ctypes.c_void_p],
 }
@@ -380,6 +383,20 @@ def moe_get_status(ws):
     st, det = ctypes.c_int32(0), ctypes.c_int32(0)
     _call("moe_get_status", ws.data_ptr(), ctypes.byref(st), ctypes.byref(det))
     return st.value, det.value
+
+
+def moe_noalloc_get_status():
+    """Status word of moe_layer_noalloc's scratch array on the current device (synchronous)."""
+    st, det = ctypes.c_int32(0), ctypes.c_int32(0)
+    _call("moe_noalloc_get_status", ctypes.byref(st), ctypes.byref(det))
+    return st.value, det.value
+
+
+def moe_test_set_stall(stall_ns: int):
+    """Test hook: while nonzero, every FC1 launch stalls its MMA thread on a
+    barrier nothing arrives on for stall_ns, so the call reports
+    MOE_ERR_TIMEOUT (site 5) in its status word.  0 turns it off."""
+    _call("moe_test_set_stall", int(stall_ns))
 
 
 def moe_get_views(shape: MoeShape, ws):

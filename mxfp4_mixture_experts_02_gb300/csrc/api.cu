@@ -6,6 +6,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -17,6 +18,9 @@ namespace {
 // A 16U4_ALIGN16B box completes its packed global byte count (8 bytes per 16
 // E2M1 elements), not its 16-byte-per-16-element shared-memory footprint.
 constexpr int kFp4BytesPer128Row = 64;
+
+// moe_test_set_stall: read by every FC1 launch that is issued
+std::atomic<uint64_t> g_test_stall_ns{0};
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
@@ -231,6 +235,7 @@ int run_forward(const moe_shape* s, const uint16_t* x, const moe_weights* wt, co
     g.kp = d.kp;
     g.act_c0 = s->act_params[0];
     g.act_c1 = s->act_params[1];
+    g.test_stall_ns = g_test_stall_ns.load();
 
     g.a_sf = wt->w1_sf;
     g.b_sf = L.x_token_order ? nullptr : at<uint8_t>(ws, L.xsf);
@@ -238,6 +243,7 @@ int run_forward(const moe_shape* s, const uint16_t* x, const moe_weights* wt, co
     e = launch_gemm(true, mw1, mx, my, g, d.B, nsm, st, pdl);
     if (e != cudaSuccess || !rec(ev, 4, st)) return MOE_ERR_CUDA;
 
+    g.test_stall_ns = 0;  // the hook stalls FC1 only
     g.a_sf = wt->w2_sf;
     g.b_sf = at<uint8_t>(ws, L.asf);
     g.b_sf_tile_bytes = L.asf_tile_bytes;
@@ -499,6 +505,11 @@ int moe_get_status(const void* ws, int32_t* status, int32_t* detail) {
         return MOE_ERR_CUDA;
     *status = h[0];
     *detail = h[1];
+    return MOE_OK;
+}
+
+int moe_test_set_stall(uint64_t stall_ns) {
+    g_test_stall_ns.store(stall_ns);
     return MOE_OK;
 }
 

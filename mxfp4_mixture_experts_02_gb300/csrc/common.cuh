@@ -17,7 +17,7 @@ constexpr int kHeaderWords = 64;
 enum HeaderWord { kHdrRows = 0, kHdrNumV = 1, kHdrNumGroups = 2, kHdrStatus = 3, kHdrDetail = 4 };
 
 // Where a bounded wait expired (status detail = site * 65536 + block index).
-enum WaitSite { kSiteProducerEmpty = 1, kSiteMmaFull = 2, kSiteMmaAccEmpty = 3, kSiteEpiAccFull = 4 };
+enum WaitSite { kSiteProducerEmpty = 1, kSiteMmaFull = 2, kSiteMmaAccEmpty = 3, kSiteEpiAccFull = 4, kSiteTestStall = 5 };
 
 constexpr uint64_t kWaitLimitNs = 200ull * 1000 * 1000;  // 200 ms per wait
 

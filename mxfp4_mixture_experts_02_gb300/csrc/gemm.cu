@@ -91,7 +91,7 @@ struct Cfg {
     static constexpr int kOffEpi = (kOffSF + STAGES * kSfStage + 1023) & ~1023;
     static constexpr int kEpiBytes = STAGE_Y ? 8 * 32 * 256 : 0;
     static constexpr int kOffBar = kOffEpi + kEpiBytes;
-    static constexpr int kSmemBytes = kOffBar + (2 * STAGES + 4) * 8 + 16 + 1024;
+    static constexpr int kSmemBytes = kOffBar + (2 * STAGES + 6) * 8 + 16 + 1024;
     static constexpr int kAccCols = 256;
     static constexpr int kSfCols = 16;                  // per stage: 4 token-scale + 8 weight-scale columns
     static constexpr int kTmemCols = 512;
@@ -199,7 +199,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* accfull = empty + STAGES;
     uint64_t* accempty = accfull + 1;
     uint64_t* done = accempty + 1;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+    uint64_t* stall = done + 1;  // test hook: nothing ever arrives on it
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(stall + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -214,6 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_init(accfull, 1);
         ptx::mbar_init(accempty, C::kEpiWarps);
         ptx::mbar_init(done, 1);
+        ptx::mbar_init(stall, 1);
         *abort_flag = 0;
         ptx::fence_mbarrier_init();
     }
@@ -228,14 +230,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    // The work list comes from the sort: either that grid has completed when
-    // this grid launches (a kernel in between waited on it before triggering
-    // this launch), or it is the fused route + sort launch just before this
-    // one, which makes its work-list writes visible device-wide before it
-    // triggers this launch.  Only the token operands -- written by the
-    // immediately preceding kernel -- need griddepcontrol.wait, which the
-    // token producer issues while the weight producer streams the first
-    // weight stages.
+    // The work list (header, virtual experts) comes from the sort.  In the
+    // decode FC1 the sort may be the launch just before this one (the fused
+    // route + sort), so every thread waits for that grid's completion, which
+    // makes its writes visible, before reading the list.  Everywhere else a
+    // kernel in between already waited for the sort's grid to complete before
+    // it triggered this launch, so the list is read at once, and only the
+    // token operands -- written by the immediately preceding kernel -- need
+    // griddepcontrol.wait, which the token producer issues while the weight
+    // producer streams the first weight stages.
+    if constexpr (kGatherX) ptx::pdl_wait();
     const int num_v = p.header[kHdrNumV];
     const int NB = FC1 ? p.I / 128 : p.H / 256;  // 256-row weight blocks per expert
     const int KC = FC1 ? p.H / 128 : p.I / 128;  // 128-wide K chunks
@@ -394,6 +398,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t kIdesc = ptx::idesc_mx(ptx::kFmtE4M3, ptx::kFmtE2M1, 128, 256);
             uint32_t stage = 0, phase = 0, aphase = 0;
             bool ok = true;
+            // test hook: a wait that cannot complete, so that the timeout path
+            // (status word, abort of the other roles, drain) runs on demand
+            if (p.test_stall_ns && !wait_or_abort(stall, 0, p.test_stall_ns, abort_flag)) {
+                if (!*abort_flag) record_timeout(p, abort_flag, kSiteTestStall);
+                ok = false;
+            }
             for (int it = it0; ok && it < iend; it += istep) {
                 if (!wait_or_abort(accempty, aphase ^ 1, p.wait_ns, abort_flag)) {
                     if (!*abort_flag) record_timeout(p, abort_flag, kSiteMmaAccEmpty);

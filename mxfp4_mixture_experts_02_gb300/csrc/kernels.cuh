@@ -106,6 +106,7 @@ struct GemmParams {
     const uint8_t* xsf;    // [T, H / 32] E8M0
     int kp;                // slots per token (a_map / kp = token)
     float act_c0, act_c1;  // its constants: clamp limit, or SiTU beta and linear beta
+    uint64_t test_stall_ns;  // test hook: the MMA thread first waits this long on a barrier nothing arrives on (0: off)
 };
 
 struct CombineParams {

@@ -22,20 +22,24 @@ __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
 
 // Device address of g_static_scratch per device.  In host code the array's
 // name only stands in for the symbol; the kernels need the address that
-// cudaGetSymbolAddress returns with that device current.
+// cudaGetSymbolAddress returns with that device current.  Outside stream
+// capture the address is looked up on every call (a device reset that
+// reloads the module moves it); during capture the last address seen on the
+// device is reused, since the lookup itself may have to load the module.
 constexpr int kMaxDevices = 64;
 void* g_scratch_ptr[kMaxDevices] = {};
 std::mutex g_scratch_mu;
 
-int scratch_for_current_device(void** out) {
+int scratch_for_current_device(void** out, bool capturing) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_ptr[dev]) {
+    if (!capturing) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
         g_scratch_ptr[dev] = p;
     }
+    if (!g_scratch_ptr[dev]) return MOE_ERR_CUDA;  // the first call on a device was made during capture
     *out = g_scratch_ptr[dev];
     return MOE_OK;
 }
@@ -52,12 +56,24 @@ extern "C" int moe_layer_noalloc(const moe_shape* shape, const float* logits, co
     int rc = moe_workspace_bytes(shape, &need);
     if (rc != MOE_OK) return rc;
     if (need > moe::kStaticScratchBytes) return MOE_ERR_WORKSPACE;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(reinterpret_cast<cudaStream_t>(stream), &cs) != cudaSuccess) return MOE_ERR_CUDA;
     void* scratch = nullptr;
-    if ((rc = moe::scratch_for_current_device(&scratch)) != MOE_OK) return rc;
+    if ((rc = moe::scratch_for_current_device(&scratch, cs != cudaStreamCaptureStatusNone)) != MOE_OK) return rc;
     // Nothing in the scratch has to start at zero: the sort rewrites the
     // maps, counters and status word on every call, and later kernels read
     // only what this call wrote (rows past a tile reach only accumulator lanes
     // that are never read).
     return moe_layer(shape, logits, shared_logit, x, weights, topk_ids, topk_w, scratch, moe::kStaticScratchBytes,
                      out, stream);
+}
+
+// The status word of the current device's scratch array (the header of the
+// workspace carved from it), read after the caller's stream has finished.
+extern "C" int moe_noalloc_get_status(int32_t* status, int32_t* detail) {
+    if (!status || !detail) return MOE_ERR_NULL;
+    void* scratch = nullptr;
+    int rc = moe::scratch_for_current_device(&scratch, false);
+    if (rc != MOE_OK) return rc;
+    return moe_get_status(scratch, status, detail);
 }

@@ -85,7 +85,7 @@ def lib():
         L.oracle_sort.restype = i32
         L.oracle_sort.argtypes = [i32, i32, P, i32, i32, i32, i32, i32, P, P, P, P, P]
         L.oracle_forward.restype = i32
-        L.oracle_forward.argtypes = [i32] * 8 + [P] * 8 + [i32] + [P] * 7 + [i32, dbl, dbl]
+        L.oracle_forward.argtypes = [i32] * 8 + [P] * 8 + [i32] + [P] * 7 + [i32, dbl, dbl, P]
         _lib = L
     return _lib
 
@@ -196,14 +196,15 @@ def sort(ids, E_global: int, E_local: int, expert_offset: int, num_shared: int, 
 # ------------------------------------------------------------------ forward
 def forward(x_bits, ids, w, wmap, w1, w1s, w2, w2s, *, H: int, I: int, E_global: int, E_local: int,
             expert_offset: int, num_shared: int, tokens=None, want_act: bool = False, want_xq: bool = False,
-            activation: int = ACT_SWIGLU, act_params=(0.0, 0.0)):
+            activation: int = ACT_SWIGLU, act_params=(0.0, 0.0), want_y: bool = False):
     """Layer forward for ``tokens`` (default: all).
 
     x_bits uint16 [T, H] (bf16); ids int32 [T, k']; w float64 [T, k'];
     wmap int32 [E_local + S] -> index into the compact weight arrays
     w1 [n, 2I, H/2], w1s [n, 2I, H/32], w2 [n, H, I/2], w2s [n, H, I/32].
     activation / act_params select the FC1 activation (see ``activation``).
-    Returns dict(out_f64, out_bf16 (uint16 bits), [act, act_sf], [xq, xq_sf]).
+    Returns dict(out_f64, out_bf16 (uint16 bits), [act, act_sf], [xq, xq_sf],
+    [y_slot float64 [n, k', H]: each slot's w * Y, the rows the un-permute sums]).
     """
     x = _c(x_bits, np.uint16)
     ids = _c(ids, np.int32)
@@ -217,12 +218,13 @@ def forward(x_bits, ids, w, wmap, w1, w1s, w2, w2s, *, H: int, I: int, E_global:
     acts = np.zeros((n, kp, I // 32), np.uint8) if want_act else None
     xq = np.zeros((n, H), np.uint8) if want_xq else None
     xqs = np.zeros((n, H // 32), np.uint8) if want_xq else None
+    ys = np.zeros((n, kp, H), np.float64) if want_y else None
     arrs = [_c(a, np.uint8) for a in (w1, w1s, w2, w2s)]
     wm = _c(wmap, np.int32)
     c = (list(act_params) + [0.0, 0.0])[:2]
     rc = lib().oracle_forward(T, H, I, kp, E_global, E_local, expert_offset, num_shared, _p(x), _p(ids), _p(w),
                               _p(wm), *[_p(a) for a in arrs], n, _p(toks), _p(out), _p(outb), _p(act), _p(acts),
-                              _p(xq), _p(xqs), int(activation), float(c[0]), float(c[1]))
+                              _p(xq), _p(xqs), int(activation), float(c[0]), float(c[1]), _p(ys))
     if rc != 0:
         raise ValueError("oracle_forward: a routed expert has no weights in wmap")
     res = dict(out_f64=out, out_bf16=outb)
@@ -230,4 +232,6 @@ def forward(x_bits, ids, w, wmap, w1, w1s, w2, w2s, *, H: int, I: int, E_global:
         res.update(act=act, act_sf=acts)
     if want_xq:
         res.update(xq=xq, xq_sf=xqs)
+    if want_y:
+        res.update(y_slot=ys)
     return res

@@ -360,13 +360,15 @@ int oracle_sort(int T, int kp, const int32_t* ids, int E_global, int E_local, in
  *   out_f64[t] = acc, out_bf16[t] = bf16_rne(acc).
  * Optional outputs (may be NULL): act codes [ntok, k', I] and act scales
  * [ntok, k', I/32] (zero for non-local slots); xq codes [ntok, H], xq scales
- * [ntok, H/32].  Returns 0, or -1 when a needed expert is missing. */
+ * [ntok, H/32]; y_slot [ntok, k', H] = w[t,j] * Y of each slot (the rows the
+ * un-permute step sums; zero for non-local slots).  Returns 0, or -1 when a
+ * needed expert is missing. */
 int oracle_forward(int T, int H, int I, int kp, int E_global, int E_local, int expert_offset, int S,
                    const uint16_t* x, const int32_t* ids, const double* w, const int32_t* wmap,
                    const uint8_t* w1, const uint8_t* w1s, const uint8_t* w2, const uint8_t* w2s, int ntok,
                    const int32_t* toks, double* out_f64, uint16_t* out_bf16, uint8_t* act_codes,
                    uint8_t* act_scales, uint8_t* xq_codes, uint8_t* xq_scales, int act, double act_c0,
-                   double act_c1) {
+                   double act_c1, double* y_slot) {
     (void)T;
     std::vector<uint8_t> xq(H), xs(H / 32), hq(I), hs(I / 32);
     std::vector<double> xd(H), G(I), U(I), hv(I), hd(I), acc(H), Y(H), wg(H), wu(H), w2r(I);
@@ -383,9 +385,11 @@ int oracle_forward(int T, int H, int I, int kp, int E_global, int E_local, int e
             int e = local_expert(ids[slot], E_global, E_local, expert_offset, S);
             uint8_t* ac = act_codes ? act_codes + ((int64_t)it * kp + j) * I : nullptr;
             uint8_t* as = act_scales ? act_scales + ((int64_t)it * kp + j) * (I / 32) : nullptr;
+            double* ys = y_slot ? y_slot + ((int64_t)it * kp + j) * H : nullptr;
             if (e < 0) {
                 if (ac) std::memset(ac, 0, I);
                 if (as) std::memset(as, 0, I / 32);
+                if (ys) std::fill(ys, ys + H, 0.0);
                 continue;
             }
             int wi = wmap[e];
@@ -417,6 +421,8 @@ int oracle_forward(int T, int H, int I, int kp, int E_global, int E_local, int e
                 Y[n] = y;
             }
             for (int n = 0; n < H; ++n) acc[n] += w[slot] * Y[n];
+            if (ys)
+                for (int n = 0; n < H; ++n) ys[n] = w[slot] * Y[n];
         }
         for (int n = 0; n < H; ++n) {
             if (out_f64) out_f64[(int64_t)it * H + n] = acc[n];

@@ -10,6 +10,9 @@ Nothing computed by the GPU library feeds the oracle.
 """
 from __future__ import annotations
 
+import concurrent.futures
+import os
+
 import numpy as np
 import torch
 
@@ -87,20 +90,28 @@ class OracleCase:
         return -1
 
     def expert_weights(self, locals_):
-        """Oracle-quantised weights of the given local experts (cached)."""
+        """Oracle-quantised weights of the given local experts (cached; the
+        experts are generated and quantised on all host cores)."""
         c = self.cfg
         need = [e for e in locals_ if e not in self._wcache]
-        if need:
-            gids = c.global_ids[need]
+
+        def one(chunk):
+            gids = c.global_ids[chunk]
             f1 = synth.w1_host(c, gids)
             f2 = synth.w2_host(c, gids)
-            for k, e in enumerate(need):
-                a, b = oracle.quantize_mxfp4(f1[k])
-                d, f = oracle.quantize_mxfp4(f2[k])
-                self._wcache[e] = (a, b, d, f)
+            return [oracle.quantize_mxfp4(f1[k]) + oracle.quantize_mxfp4(f2[k]) for k in range(len(chunk))]
+
+        if need:
+            chunks = [need[i:i + 4] for i in range(0, len(need), 4)]
+            with concurrent.futures.ThreadPoolExecutor(max_workers=host_threads()) as ex:
+                for chunk, q in zip(chunks, ex.map(one, chunks)):
+                    for e, qe in zip(chunk, q):
+                        self._wcache[e] = qe
         return [self._wcache[e] for e in locals_]
 
-    def forward(self, tokens):
+    def forward(self, tokens, want_y: bool = False):
+        """The oracle's forward of `tokens` (rows of the result follow their
+        order), split over all host cores by token."""
         c = self.cfg
         tokens = np.asarray(tokens, np.int32)
         locs = sorted({self.local_of(int(g)) for t in tokens for g in self.ids[t]} - {-1})
@@ -114,10 +125,25 @@ class OracleCase:
                     np.zeros((1, c.hidden, c.inter // 2), np.uint8), np.zeros((1, c.hidden, c.inter // 32), np.uint8))
         else:
             arrs = tuple(np.stack([w[i] for w in ws]) for i in range(4))
-        return oracle.forward(self.x, self.ids, self.w, wmap, *arrs, H=c.hidden, I=c.inter, E_global=c.E_global,
-                              E_local=c.E_local, expert_offset=c.expert_offset, num_shared=c.num_shared,
-                              tokens=tokens, want_act=True, want_xq=True, activation=c.activation,
-                              act_params=c.act_params)
+
+        def run(part):
+            return oracle.forward(self.x, self.ids, self.w, wmap, *arrs, H=c.hidden, I=c.inter, E_global=c.E_global,
+                                  E_local=c.E_local, expert_offset=c.expert_offset, num_shared=c.num_shared,
+                                  tokens=part, want_act=True, want_xq=True, activation=c.activation,
+                                  act_params=c.act_params, want_y=want_y)
+
+        n = host_threads()
+        parts = [p for p in np.array_split(tokens, min(n, max(1, tokens.size))) if p.size]
+        if len(parts) <= 1:
+            return run(tokens)
+        with concurrent.futures.ThreadPoolExecutor(max_workers=n) as ex:
+            res = list(ex.map(run, parts))
+        return {k: np.concatenate([r[k] for r in res]) for k in res[0]}
+
+
+def host_threads() -> int:
+    """Threads for the oracle (its C calls release the GIL)."""
+    return max(1, os.cpu_count() or 1)
 
 
 def bf16_bits(t: torch.Tensor) -> np.ndarray:

@@ -144,6 +144,16 @@ def test_activation_limits_and_symmetries():
 def test_hand_case_C_weighted_sum():
     r = _run([[0.5] * H], [[0, 1]], [[0.75, 0.25]], [_expert_const(), _expert_structured()])
     np.testing.assert_array_equal(r["out_f64"][0], np.full(H, -83.90625))
+    # each slot's row w * Y: the constant expert's h = silu(4) * -8 saturates
+    # to -448 * 2^-4 = -28, Y = 32 * -28 * 0.125 = -112, times 0.75 -> -84; the
+    # structured expert's Y = 0.375 (its one W2 entry per row picks one
+    # intermediate code), times 0.25 -> 0.09375
+    w = oracle.forward(_bf16_bits([[0.5] * H]), np.asarray([[0, 1]], np.int32), np.asarray([[0.75, 0.25]]),
+                       np.arange(2, dtype=np.int32), *_weights([_expert_const()[0], _expert_structured()[0]],
+                                                               [_expert_const()[1], _expert_structured()[1]]),
+                       H=H, I=I, E_global=2, E_local=2, expert_offset=0, num_shared=0, want_y=True)["y_slot"]
+    np.testing.assert_array_equal(w[0, 0], np.full(H, -84.0))
+    np.testing.assert_array_equal(w[0, 1], np.full(H, 0.09375))
     assert (r["out_bf16"][0] == 0xC2A8).all()  # -84.0
     assert (r["act"][0, 1] == 0x7C).all() and r["act_sf"][0, 1, 0] == 117  # 384 = 1.5 * 2^8 -> 0x7C; * 2^-10 = 0.375
 
@@ -194,6 +204,21 @@ def test_expert_parallel_slices_sum_to_full_layer():
         sl = tuple(a[off:off + 4] for a in wts)
         part += _fwd(c, x, ids, w, sl)["out_f64"]
     np.testing.assert_allclose(part, full, rtol=1e-12, atol=1e-12)
+
+
+def test_slot_rows_sum_to_the_output_and_vanish_off_slice():
+    cfg, x, ids, w, wts = _small_layer(E=8, k=3, T=9)
+    c = cfg.replace(E_local=4, expert_offset=4)
+    sl = tuple(a[4:8] for a in wts)
+    r = oracle.forward(x, ids, w, np.arange(4, dtype=np.int32), *sl, H=c.hidden, I=c.inter, E_global=8, E_local=4,
+                       expert_offset=4, num_shared=0, want_y=True)
+    y = r["y_slot"]
+    local = (ids >= 4) & (ids < 8)
+    assert (y[~local] == 0).all() and (np.abs(y[local]).sum(axis=-1) > 0).all()
+    acc = np.zeros_like(r["out_f64"])
+    for j in range(ids.shape[1]):  # the oracle's own order: ascending j
+        acc += y[:, j]
+    np.testing.assert_array_equal(acc, r["out_f64"])
 
 
 def test_shared_expert_adds_its_weighted_output():

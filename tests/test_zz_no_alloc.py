@@ -1,19 +1,22 @@
 """moe_layer_noalloc: the layer for callers that cannot allocate device memory
 (code running under an allocator that forbids new allocations, runtimes that
 must not call cudaMalloc after start-up).  Its scratch is the library's fixed
-32 MiB device array, so these tests compare it with moe_layer on a caller
-workspace, call it twice in a row (the array keeps the previous call's
-contents), and check that shapes needing more scratch are refused.
+32 MiB device array, shared by every call on a device and left holding the
+previous call's contents.  These tests run it on three shapes in a row (a
+larger one, a smaller one, the larger one again, so stale maps and rows of an
+earlier call are present) and require, after each call, exactly the result
+of moe_layer on a fresh caller workspace -- both run the same kernels on the
+same inputs -- and a clean status word; shapes needing more scratch are
+refused.
 
 This file is collected last so that a run stopping at its first failure has
 already run every other test."""
-import numpy as np
 import pytest
 import torch
 
 import mxfp4_mixture_experts_02_gb300 as moe
 import synth
-from moe_case import bf16_bits, bf16_to_f64, device_inputs, device_weights, rel_l2, shape_of
+from moe_case import device_inputs, device_weights, shape_of
 
 pytestmark = pytest.mark.gpu
 
@@ -21,24 +24,25 @@ SMALL = synth.MoeConfig("small", 7, T=48, E_global=64, E_local=64, expert_offset
                         hidden=1024, inter=256, block_n=16, shared_scale=0.5)
 
 
-@pytest.mark.parametrize("cfg", [SMALL, synth.CONFIGS["tiny"]], ids=["small", "tiny"])
-def test_noalloc_matches_workspace_entry_point_on_two_calls(cfg):
-    shape = shape_of(cfg)
-    wts = device_weights(cfg)
-    x, logits, sl = device_inputs(cfg)
-    ws = moe.workspace(shape)
-    ref, ref_ids, ref_w = moe.moe_layer(shape, logits, sl, x, wts, ws)
-    torch.cuda.synchronize()
-    assert moe.moe_get_status(ws) == (0, 0)
-    ref_f = bf16_to_f64(bf16_bits(ref))
-    for _ in range(2):
+def test_noalloc_matches_workspace_entry_point_across_calls():
+    cases = {}
+    for cfg in (SMALL, synth.CONFIGS["tiny"]):
+        shape = shape_of(cfg)
+        wts = device_weights(cfg)
+        x, logits, sl = device_inputs(cfg)
+        ws = moe.workspace(shape)
+        ref = moe.moe_layer(shape, logits, sl, x, wts, ws)
+        torch.cuda.synchronize()
+        assert moe.moe_get_status(ws) == (0, 0)
+        cases[cfg.name] = (shape, wts, x, logits, sl, ref)
+    for name in ("small", "tiny", "small"):
+        shape, wts, x, logits, sl, (ref_out, ref_ids, ref_w) = cases[name]
         out, ids, w = moe.moe_layer_noalloc(shape, logits, sl, x, wts)
         torch.cuda.synchronize()
-        assert torch.equal(ids, ref_ids)
-        np.testing.assert_allclose(w.cpu().numpy(), ref_w.cpu().numpy(), rtol=4e-6, atol=1e-7)
-        got = bf16_to_f64(bf16_bits(out))
-        assert rel_l2(got, ref_f) <= 1e-2
-        assert np.max(np.abs(got - ref_f)) <= 2e-2
+        assert moe.moe_noalloc_get_status() == (0, 0), name
+        assert torch.equal(ids, ref_ids), name
+        assert torch.equal(w, ref_w), name
+        assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16)), name
 
 
 def test_noalloc_refuses_shapes_beyond_its_scratch():
