@@ -175,7 +175,7 @@ class ClockSampler:
             except ValueError:
                 return None
         sm = [num(r[1]) for r in inside if num(r[1]) is not None]
-        mx = [num(r[2]) for r in self.rows if num(r[2]) is not None]
+        mx = [num(r[2]) for _, r in self.rows if num(r[2]) is not None]
         reasons = sorted({n for r in inside for k, n in enumerate(self.NAMES) if r[5 + k] == "Active"})
         return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
                 "reasons": reasons, "samples": len(sm), "samples_total": len(self.rows),

@@ -29,3 +29,20 @@ def test_reference_arm_prints_one_contract_line():
     e2e = d["e2e"]
     assert e2e["value"] == d["value"] and e2e["unit"] == d["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+
+
+def test_clock_sampler_summary_keeps_the_timed_windows():
+    # fake nvidia-smi rows (host time, fields): only samples inside a timed
+    # window (with 50 ms of slack) count towards the median and the reasons
+    sys.path.insert(0, ROOT)
+    import bench
+    cs = bench.ClockSampler.__new__(bench.ClockSampler)
+    cs.p = object()
+    row = lambda mhz, hw="Not Active", cap="Not Active": ["0", str(mhz), "2070", "900", "0x0", hw, "Not Active",
+                                                          "Not Active", cap]
+    cs.rows = [(0.0, row(1400, hw="Active")), (1.0, row(2070)), (1.2, row(2040, cap="Active")), (3.0, row(1000))]
+    cs.windows = [(0.98, 1.21)]
+    s = cs.summary()
+    assert s["sm_mhz"] == 2055.0 and s["samples"] == 2 and s["sm_max_mhz"] == 2070.0
+    assert s["reasons"] == ["sw_power_cap"]
+    assert cs.summary([(2.9, 3.1)])["sm_mhz"] == 1000.0

