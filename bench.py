@@ -60,6 +60,8 @@ def parse():
     ap.add_argument("--block-n", type=int, default=0, help="override the workload's virtual-expert rows")
     ap.add_argument("--router", action="store_true",
                     help="start the layer from x and a bf16 router matrix (router GEMM in the chain)")
+    ap.add_argument("--gemm2", default="auto", choices=["auto", "split", "dense"],
+                    help="GEMM2 path: the device gate's rule, or one path forced")
     ap.add_argument("--act", default="swiglu", choices=["swiglu", "swiglu_clamp", "situ"],
                     help="FC1 activation: SwiGLU (the workload's), clamped SwiGLU (limit 7) or SiTU (beta 4, lb 25)")
     return ap.parse_args()
@@ -237,6 +239,7 @@ def measure_config(args, cfg, device, stream, flush, sampler, steps, warmup, wor
     import torch
 
     moe, shape, weights, x, logits, sl, ws, ids, tw, out = setup_layer(cfg, device)
+    moe.moe_set_gemm2_path({"auto": moe.GEMM2_AUTO, "split": moe.GEMM2_SPLIT, "dense": moe.GEMM2_DENSE}[args.gemm2])
     wr = None
     if args.router:
         wr = router_matrix(cfg, device)
@@ -286,6 +289,7 @@ def measure_config(args, cfg, device, stream, flush, sampler, steps, warmup, wor
     e2e = run_e2e(moe, shape, weights, cfg, ws, stream, flush, reps)
 
     hdr = ws[:64 * 4].view(torch.int32).cpu().numpy()
+    moe.moe_set_gemm2_path(moe.GEMM2_AUTO)
     counts = ws_counts(moe, shape, ws)
     touched = int((counts[:cfg.E_local] > 0).sum()) + int(cfg.num_shared > 0 and counts[cfg.E_local:].sum() > 0)
     R = int(hdr[0])
@@ -342,6 +346,7 @@ def measure_config(args, cfg, device, stream, flush, sampler, steps, warmup, wor
         "workload": cfg.name, "T": cfg.T, "E_global": cfg.E_global, "E_local": cfg.E_local,
         "expert_offset": cfg.expert_offset, "top_k": cfg.top_k, "num_shared": cfg.num_shared, "hidden": H,
         "inter": I, "block_n": cfg.block_n, "seed": cfg.seed, "activation": ACT_NAMES[cfg.activation],
+        "gemm2_path": "dense" if hdr[5] == 1 else "split",
         "tokens_per_s": world * cfg.T / sec, "us_per_layer": ms * 1e3, "steps": stats,
         "layer": {"routed_rows": R, "touched_experts": touched, "weight_bytes_touched": layer_weight_bytes,
                   "kernel_us": {k: kernel_ms[k] * 1e3 for k in names},
@@ -411,7 +416,8 @@ def run_ours(args, cfg):
         "dtype": "mxfp4 weights x mxfp8 activations, fp32 accumulate, bf16 out",
         "data": "synthetic (seeded Irwin-Hall normal inputs, random-init weights quantised to MXFP4)",
         "config": {k: head[k] for k in ("workload", "T", "E_global", "E_local", "expert_offset", "top_k",
-                                        "num_shared", "hidden", "inter", "block_n", "seed", "activation")},
+                                        "num_shared", "hidden", "inter", "block_n", "seed", "activation",
+                                        "gemm2_path")},
         "layer": head["layer"],
         "roofline": head["roofline"],
         "layer_roofline": head["layer_roofline"],

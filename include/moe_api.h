@@ -104,7 +104,8 @@ typedef struct moe_weights {
 
 /* Device pointers into a workspace, for inspection and parity checks.
  *   header       int32[64]: [0] rows R, [1] virtual experts, [2] groups,
- *                [3] status, [4] status detail
+ *                [3] status, [4] status detail, [5] GEMM2 path (0 split,
+ *                1 dense)
  *   expert_counts int32[E_tot], expert_offsets int32[E_tot + 1]
  *   vinfo        int32[max_v][4] {local expert, first row, rows, chunk}
  *   a_map        int32[R] row -> slot t*k' + j;  c_map int32[T*k'] slot -> row or -1
@@ -317,6 +318,26 @@ int moe_get_views(const moe_shape* shape, void* workspace, moe_views* views);
  * sort resets it on every call. */
 int moe_get_status(const void* workspace, int32_t* status, int32_t* detail);
 
+/* GEMM2 strategy ("[FlashInfer] Device-side gating for the MoE GEMM2
+ * path", sections 1-2).  Every forward launches a one-warp gate kernel right
+ * after the sort, which reads the sorted table and picks, on the device:
+ *   MOE_GEMM2_SPLIT  FC2 writes each routed row w * Y; the combine sums a
+ *                    token's rows in ascending slot order (bit-reproducible);
+ *   MOE_GEMM2_DENSE  FC2's epilogue reduces w * Y into an fp32 [T, H]
+ *                    accumulator in the workspace (the finalize fused into
+ *                    GEMM2, reductions performed at the L2); the combine
+ *                    converts it to bf16.  The reductions' order varies, so
+ *                    the result is within the layer's tolerance but not
+ *                    bit-reproducible.
+ * The gate's own rule (MOE_GEMM2_AUTO, the default) takes dense when rows * H
+ * <= 4 Mi, where the reductions cost less than writing and re-reading the
+ * rows; the chain of launches is the same either way.  moe_set_gemm2_path
+ * forces one path for every later call issued from this process (a captured
+ * graph keeps the value of its capture); MOE_ERR_SHAPE for another value.
+ * The path a call took is header word 5 of its workspace (0 split, 1 dense). */
+enum { MOE_GEMM2_AUTO = 0, MOE_GEMM2_SPLIT = 1, MOE_GEMM2_DENSE = 2 };
+int moe_set_gemm2_path(int32_t path);
+
 /* Test hook for the device-error path, off (0) by default.  While stall_ns is
  * nonzero, every later launch of the FC1 GEMM (on any device) makes its MMA
  * thread first wait stall_ns on a barrier that nothing arrives on; the wait
@@ -335,7 +356,8 @@ int moe_num_sms(int32_t* num_sms);
 /* Number of kernel launches moe_layer (and moe_layer_host, besides its
  * copies) issues for the shape: route + sort (one fused launch up to 1024
  * slots T*k', else route and a one- or three-kernel sort), then for T > 0 the
- * gather, FC1, FC2 and the combine. */
+ * GEMM2 gate, the gather (not in the decode tilings when route and sort are
+ * fused), FC1, FC2 and the combine. */
 int moe_layer_launch_count(const moe_shape* shape, int32_t* count);
 
 #ifdef __cplusplus

@@ -21,11 +21,12 @@ __all__ = [
     "moe_quantize_mxfp4", "moe_packed_weight_bytes", "moe_pack_weights", "moe_route", "moe_sort", "moe_forward",
     "moe_layer", "moe_router", "moe_layer_router", "moe_layer_host", "moe_layer_events", "moe_layer_noalloc", "moe_get_views", "moe_get_status",
     "moe_num_sms", "moe_layer_launch_count", "quantize_expert_weights", "moe_noalloc_get_status",
-    "moe_test_set_stall",
+    "moe_test_set_stall", "moe_set_gemm2_path", "GEMM2_AUTO", "GEMM2_SPLIT", "GEMM2_DENSE",
     "workspace", "MOE_OK", "MOE_ERR_TIMEOUT", "MOE_ERR_WORKSPACE",
 ]
 
 MOE_OK = 0
+GEMM2_AUTO, GEMM2_SPLIT, GEMM2_DENSE = 0, 1, 2  # moe_set_gemm2_path
 MOE_ERR_NULL, MOE_ERR_SHAPE, MOE_ERR_ALIGN, MOE_ERR_WORKSPACE, MOE_ERR_CUDA, MOE_ERR_TIMEOUT = -1, -2, -3, -4, -5, -6
 _ERRNAMES = {-1: "MOE_ERR_NULL", -2: "MOE_ERR_SHAPE", -3: "MOE_ERR_ALIGN", -4: "MOE_ERR_WORKSPACE",
              -5: "MOE_ERR_CUDA", -6: "MOE_ERR_TIMEOUT"}
@@ -122,6 +123,7 @@ _SIGS = {
     "moe_get_status": [ctypes.c_void_p] * 3,
     "moe_noalloc_get_status": [ctypes.c_void_p] * 2,
     "moe_test_set_stall": [ctypes.c_uint64],
+    "moe_set_gemm2_path": [ctypes.c_int32],
     "moe_num_sms": [ctypes.c_void_p],
     "moe_layer_launch_count": [ctypes.c_void_p, ctypes.c_void_p],
 }
@@ -390,6 +392,12 @@ def moe_noalloc_get_status():
     st, det = ctypes.c_int32(0), ctypes.c_int32(0)
     _call("moe_noalloc_get_status", ctypes.byref(st), ctypes.byref(det))
     return st.value, det.value
+
+
+def moe_set_gemm2_path(path: int):
+    """Force the GEMM2 path of later calls: GEMM2_AUTO (the device gate's rule),
+    GEMM2_SPLIT or GEMM2_DENSE (see moe_api.h)."""
+    _call("moe_set_gemm2_path", int(path))
 
 
 def moe_test_set_stall(stall_ns: int):

@@ -21,6 +21,12 @@ constexpr int kFp4BytesPer128Row = 64;
 
 // moe_test_set_stall: read by every FC1 launch that is issued
 std::atomic<uint64_t> g_test_stall_ns{0};
+// moe_set_gemm2_path: read by every gate launch that is issued
+std::atomic<int> g_gemm2_path{MOE_GEMM2_AUTO};
+
+// The gate's rule: the dense GEMM2 path when rows * H <= this many fp32
+// reductions (see gate.cu).
+constexpr int64_t kDenseMaxElems = int64_t(4) << 20;
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
@@ -161,8 +167,13 @@ int run_forward(const moe_shape* s, const uint16_t* x, const moe_weights* wt, co
     const int nsm = num_sms_cached();
     if (nsm <= 0) return MOE_ERR_CUDA;
 
+    // The GEMM2 gate: one warp after the sort chooses split or dense.
+    GateParams gt{at<int32_t>(ws, L.header), d.H, g_gemm2_path.load(), kDenseMaxElems};
+    if (launch_gate(gt, st, pdl) != cudaSuccess) return MOE_ERR_CUDA;
+
     GatherParams gp{};
     gp.x = x;
+    gp.acc = at<float>(ws, L.acc);
     gp.header = at<int32_t>(ws, L.header);
     gp.a_map = at<int32_t>(ws, L.a_map);
     gp.xq = at<uint8_t>(ws, L.xq);
@@ -236,6 +247,8 @@ int run_forward(const moe_shape* s, const uint16_t* x, const moe_weights* wt, co
     g.act_c0 = s->act_params[0];
     g.act_c1 = s->act_params[1];
     g.test_stall_ns = g_test_stall_ns.load();
+    g.acc = at<float>(ws, L.acc);
+    g.T = d.T;
 
     g.a_sf = wt->w1_sf;
     g.b_sf = L.x_token_order ? nullptr : at<uint8_t>(ws, L.xsf);
@@ -250,7 +263,8 @@ int run_forward(const moe_shape* s, const uint16_t* x, const moe_weights* wt, co
     e = launch_gemm(false, mw2, mact, my, g, d.B, nsm, st, pdl);
     if (e != cudaSuccess || !rec(ev, 5, st)) return MOE_ERR_CUDA;
 
-    CombineParams cp{at<int32_t>(ws, L.c_map), L.y_bf16 ? nullptr : at<float>(ws, L.y),
+    CombineParams cp{at<int32_t>(ws, L.header), at<float>(ws, L.acc), at<int32_t>(ws, L.c_map),
+                     L.y_bf16 ? nullptr : at<float>(ws, L.y),
                      L.y_bf16 ? at<uint16_t>(ws, L.y) : nullptr, out, d.T, d.kp, d.H};
     e = launch_combine(cp, st, pdl);
     if (e != cudaSuccess || !rec(ev, 6, st)) return MOE_ERR_CUDA;
@@ -508,6 +522,12 @@ int moe_get_status(const void* ws, int32_t* status, int32_t* detail) {
     return MOE_OK;
 }
 
+int moe_set_gemm2_path(int32_t path) {
+    if (path != MOE_GEMM2_AUTO && path != MOE_GEMM2_SPLIT && path != MOE_GEMM2_DENSE) return MOE_ERR_SHAPE;
+    g_gemm2_path.store(path);
+    return MOE_OK;
+}
+
 int moe_test_set_stall(uint64_t stall_ns) {
     g_test_stall_ns.store(stall_ns);
     return MOE_OK;
@@ -526,8 +546,8 @@ int moe_layer_launch_count(const moe_shape* s, int32_t* count) {
     const Dims d = make_dims(*s);
     const bool fused = route_sort_fusable(d.T, d.kp);
     int n = fused ? 1 : 1 + sort_launch_count(static_cast<int64_t>(d.T) * d.kp);
-    // [gather,] FC1, FC2, combine; the decode tilings' x quantisation rides on the fused route + sort
-    if (d.T > 0) n += (fused && d.mode == kModeDecode) ? 3 : 4;
+    // gate, [gather,] FC1, FC2, combine; the decode tilings' x quantisation rides on the fused route + sort
+    if (d.T > 0) n += (fused && d.mode == kModeDecode) ? 4 : 5;
     *count = n;
     return MOE_OK;
 }

@@ -4,6 +4,11 @@
 // (c_map = -1, "[sglang] ... MXFP4 decode MoE ... shape templates", section
 // 5).  Y rows already carry the routing weight (FC2 epilogue), so this is a
 // gather-sum: no atomics, bitwise deterministic.
+//
+// When the GEMM2 gate chose the dense path ("[FlashInfer] Device-side gating
+// for the MoE GEMM2 path"), FC2 has already summed every token's rows into
+// the fp32 accumulator, and this launch is the finalize's last step: out[t] =
+// bf16(acc[t]).
 #include "common.cuh"
 #include "kernels.cuh"
 #include "ptx.cuh"
@@ -21,10 +26,28 @@ constexpr int kMaxSlots = 64;
 // them (one memory round trip for a decode token's 16 slots).
 constexpr int kBatch = 16;
 
+// Dense GEMM2 path: columns 8 * c8 .. 8 * c8 + 7 of token t's fp32 sums to bf16.
+__device__ __forceinline__ void convert_acc_row8(const CombineParams& p, int t, int c8) {
+    const float4* a = reinterpret_cast<const float4*>(p.acc + static_cast<int64_t>(t) * p.H) + 2 * c8;
+    const float4 u = a[0], v = a[1];
+    const __nv_bfloat162 b0 = __floats2bfloat162_rn(u.x, u.y), b1 = __floats2bfloat162_rn(u.z, u.w);
+    const __nv_bfloat162 b2 = __floats2bfloat162_rn(v.x, v.y), b3 = __floats2bfloat162_rn(v.z, v.w);
+    reinterpret_cast<uint4*>(p.out + static_cast<int64_t>(t) * p.H)[c8] =
+        make_uint4(*reinterpret_cast<const uint32_t*>(&b0), *reinterpret_cast<const uint32_t*>(&b1),
+                   *reinterpret_cast<const uint32_t*>(&b2), *reinterpret_cast<const uint32_t*>(&b3));
+}
+
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineParams p) {
     __shared__ int rows[kMaxSlots];
     ptx::pdl_wait();
     const int t = blockIdx.y;
+    if (p.header[kHdrGemm2Path] == kPathDense) {
+        // this block's 512 columns: 64 groups of 8 on the first 64 threads
+        const int c8 = blockIdx.x * (kCombineThreads / 2) + threadIdx.x;
+        if (threadIdx.x < kCombineThreads / 2 && c8 < p.H / 8) convert_acc_row8(p, t, c8);
+        ptx::pdl_launch_dependents();
+        return;
+    }
     if (threadIdx.x < p.kp) rows[threadIdx.x] = p.c_map[static_cast<size_t>(t) * p.kp + threadIdx.x];
     __syncthreads();
     const int c = blockIdx.x * kCombineThreads + threadIdx.x;  // float4 column
@@ -62,6 +85,12 @@ __global__ void __launch_bounds__(kCombineThreads) combine_bf16_kernel(CombinePa
     __shared__ int rows[kMaxSlots];
     ptx::pdl_wait();
     const int t = blockIdx.y;
+    if (p.header[kHdrGemm2Path] == kPathDense) {
+        const int c8 = blockIdx.x * kCombineThreads + threadIdx.x;  // this block's 1024 columns
+        if (c8 < p.H / 8) convert_acc_row8(p, t, c8);
+        ptx::pdl_launch_dependents();
+        return;
+    }
     if (threadIdx.x < p.kp) rows[threadIdx.x] = p.c_map[static_cast<size_t>(t) * p.kp + threadIdx.x];
     __syncthreads();
     const int c = blockIdx.x * kCombineThreads + threadIdx.x;  // uint4 column (8 bf16)

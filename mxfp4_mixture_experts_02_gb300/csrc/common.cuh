@@ -14,7 +14,13 @@
 namespace moe {
 
 constexpr int kHeaderWords = 64;
-enum HeaderWord { kHdrRows = 0, kHdrNumV = 1, kHdrNumGroups = 2, kHdrStatus = 3, kHdrDetail = 4 };
+enum HeaderWord { kHdrRows = 0, kHdrNumV = 1, kHdrNumGroups = 2, kHdrStatus = 3, kHdrDetail = 4, kHdrGemm2Path = 5 };
+
+// GEMM2 strategies the gate chooses between ("[FlashInfer] Device-side gating
+// for the MoE GEMM2 path"): split = FC2 writes each routed row, the combine
+// sums a token's rows; dense = FC2's epilogue reduces w * Y straight into an
+// fp32 [T, H] accumulator (the finalize fused), the combine converts it.
+enum Gemm2Path { kPathSplit = 0, kPathDense = 1 };
 
 // Where a bounded wait expired (status detail = site * 65536 + block index).
 enum WaitSite { kSiteProducerEmpty = 1, kSiteMmaFull = 2, kSiteMmaAccEmpty = 3, kSiteEpiAccFull = 4, kSiteTestStall = 5 };
@@ -37,7 +43,7 @@ struct Dims {
 // Byte offsets of the workspace regions (256-byte aligned).
 struct Layout {
     size_t header, counts, offsets, vinfo, groups, a_map, c_map, sort_hist, row_w;
-    size_t xq, xsf, act, asf, y, vbase;
+    size_t xq, xsf, act, asf, y, vbase, acc;
     size_t st_logits, st_shared, st_x, st_ids, st_w, st_out;
     size_t total;
     int xsf_tile_bytes, asf_tile_bytes, y_bf16, x_token_order;
@@ -106,6 +112,9 @@ inline Layout make_layout(const Dims& d) {
     // rows_alloc (>= 128), so a 32-row box never exceeds it
     L.y = take(size_t(L.y_bf16 ? d.rows_alloc : d.R_max) * d.H * (L.y_bf16 ? 2 : 4));
     L.vbase = take(size_t(d.Et) * 4);
+    // fp32 [max_T, H]: the dense GEMM2 path's accumulator (zeroed in the call
+    // that uses it, before FC2)
+    L.acc = take(size_t(d.max_T) * d.H * 4);
     L.st_logits = take(size_t(d.max_T) * d.Eg * 4);
     L.st_shared = take(size_t(d.max_T) * (d.S > 0 ? d.S : 1) * 2);
     L.st_x = take(size_t(d.max_T) * d.H * 2);

@@ -452,18 +452,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         // reciprocals of the SiTU constants (unused by the other activations)
         const float act_i0 = ACT == MOE_ACT_SITU ? 1.0f / p.act_c0 : 0.f;
         const float act_i1 = ACT == MOE_ACT_SITU ? 1.0f / p.act_c1 : 0.f;
-        // Descriptors two items ahead and row weights one item ahead are
-        // loaded early, so no dependent load chain sits between two items.
+        // FC2: the GEMM2 path the gate chose (dense: reduce w * Y into the
+        // token's accumulator row instead of writing the routed row).  The gate
+        // ran before FC1, which waited for it, and this grid launched after FC1
+        // finished its work, so the word is final.
+        const bool dense = !FC1 && p.header[kHdrGemm2Path] == kPathDense;
+        // Descriptors two items ahead and row weights (dense: and tokens) one
+        // item ahead are loaded early, so no dependent load chain sits between
+        // two items.
         const int4 kNoTile = kNone;
         int4 vi_cur = active ? item_desc(p, it0, NB, iend, kNoTile) : kNoTile;
         int4 vi_nxt = active ? item_desc(p, it0 + g, NB, iend, kNoTile) : kNoTile;
         float w_cur = (!FC1 && i < vi_cur.z) ? p.row_w[vi_cur.y + i] : 0.f;
+        int t_cur = (dense && i < vi_cur.z) ? p.a_map[vi_cur.y + i] / p.kp : 0;
         for (int it = it0; active && it < iend; it += g) {
             const int v = it / NB, nb = it - v * NB;
             const int4 vi = vi_cur;
             const float w_row = w_cur;
+            const int t_row = t_cur;
             const int4 vi_n2 = item_desc(p, it + 2 * g, NB, iend, kNoTile);
             w_cur = (!FC1 && i < vi_nxt.z) ? p.row_w[vi_nxt.y + i] : 0.f;
+            t_cur = (dense && i < vi_nxt.z) ? p.a_map[vi_nxt.y + i] / p.kp : 0;
             vi_cur = vi_nxt;
             vi_nxt = vi_n2;
             const int first = vi.y, rows = vi.z;
@@ -490,7 +499,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(accempty);  // accumulator free for the next item
-            if constexpr (kStageY) {
+            if (dense) {
+                // finalize fused into GEMM2: out_acc[token] += w * Y, four
+                // columns per reduction, performed at the L2
+                if (valid) {
+                    float* dst = p.acc + static_cast<int64_t>(t_row) * p.H + nb * 256 + half * 128;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+#pragma unroll
+                        for (int q4 = 0; q4 < 8; ++q4)
+                            ptx::red_add_v4(dst + c * 32 + q4 * 4, __uint_as_float(r[c][4 * q4]) * w_row,
+                                            __uint_as_float(r[c][4 * q4 + 1]) * w_row,
+                                            __uint_as_float(r[c][4 * q4 + 2]) * w_row,
+                                            __uint_as_float(r[c][4 * q4 + 3]) * w_row);
+                }
+            } else if constexpr (kStageY) {
                 // lane = tile row q*32+lane.  Its 128 weighted bf16 values are
                 // staged as two 32-row x 64-column boxes in the 128-byte TMA
                 // swizzle (16-byte chunk j of row r at chunk j ^ (r % 8)); a
@@ -589,6 +612,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (kStageY) {
             if (lane == 0) ptx::bulk_wait_all();  // tensor stores complete before the CTA exits
             __syncwarp();
+        }
+        if constexpr (kGatherX) {
+            // Decode FC1: the six epilogue warps that hold no token lane zero
+            // the dense GEMM2 accumulator when the gate chose that path (every
+            // thread of this grid waited for the gate's grid, above), so FC2's
+            // reductions start from zero.
+            if (!active && p.header[kHdrGemm2Path] == kPathDense) {
+                const int wi = (q - 1) + 3 * half;  // 0..5
+                const int64_t n4 = static_cast<int64_t>(p.T) * p.H / 4;
+                const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int64_t k = (static_cast<int64_t>(blockIdx.x) * 6 + wi) * 32 + lane; k < n4;
+                     k += static_cast<int64_t>(gridDim.x) * 6 * 32)
+                    reinterpret_cast<float4*>(p.acc)[k] = z;
+            }
         }
     }
 

@@ -77,6 +77,7 @@ struct GatherParams {  // x -> MXFP8 + the routing weight of each expert row
     const int32_t* c_map;
     const int32_t* offsets;
     const int32_t* vbase;
+    float* acc;             // dense GEMM2 accumulator [T, H] (zeroed here when the gate chose dense)
     int token_order;        // 1: decode tilings (the FC1 kernel gathers the rows)
     int H, T, R_max, max_blocks, kp, B, Et, xsf_tile_bytes;
 };
@@ -107,14 +108,26 @@ struct GemmParams {
     int kp;                // slots per token (a_map / kp = token)
     float act_c0, act_c1;  // its constants: clamp limit, or SiTU beta and linear beta
     uint64_t test_stall_ns;  // test hook: the MMA thread first waits this long on a barrier nothing arrives on (0: off)
+    float* acc;              // dense GEMM2 accumulator [T, H] fp32
+    int T;
 };
 
 struct CombineParams {
+    const int32_t* header;  // the gate's GEMM2 path
+    const float* acc;       // dense path: fp32 [T, H] sums
     const int32_t* c_map;
     const float* y;         // fp32 rows, or NULL when y_bf16 is used
     const uint16_t* y_bf16; // bf16 rows (prefill tiling)
     uint16_t* out;
     int T, kp, H;
+};
+
+// The one-warp GEMM2 gate: reads the sort's table and writes the path.
+struct GateParams {
+    int32_t* header;
+    int H;
+    int force;                // 0 the rule below, 1 split, 2 dense
+    int64_t dense_max_elems;  // dense when rows * H <= this
 };
 
 struct QuantParams {
@@ -149,6 +162,7 @@ cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream, bool pdl);
 cudaError_t launch_gemm(bool fc1, const CUtensorMap& tmW, const CUtensorMap& tmX, const CUtensorMap& tmY,
                         const GemmParams& p, int TM, int grid, cudaStream_t stream, bool pdl);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream, bool pdl);
+cudaError_t launch_gate(const GateParams& p, cudaStream_t stream, bool pdl);
 RouterTiling router_tiling(int T, int Eg, int num_sms);
 cudaError_t launch_router(const CUtensorMap& tmX, const CUtensorMap& tmW, const RouterParams& p, int grid,
                           cudaStream_t stream, bool pdl);

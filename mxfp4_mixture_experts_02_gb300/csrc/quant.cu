@@ -112,7 +112,14 @@ __global__ void __launch_bounds__(kTokWarps * 32) gather_token_kernel(GatherPara
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     uint8_t* exp_bytes = reinterpret_cast<uint8_t*>(s_exp[warp]);
     const int nh = p.H / 16;  // half-blocks per row
+    // the gate ran before this launch: with the dense GEMM2 path, each token's
+    // fp32 accumulator row is zeroed here, before FC2 reduces into it
+    const bool zero_acc = p.header[kHdrGemm2Path] == kPathDense;
     for (int t = blockIdx.x * kTokWarps + warp; t < p.T; t += gridDim.x * kTokWarps) {
+        if (zero_acc) {
+            float4* a = reinterpret_cast<float4*>(p.acc + static_cast<int64_t>(t) * p.H);
+            for (int c = lane; c < p.H / 4; c += 32) a[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
         for (int j0 = 0; j0 < p.kp; j0 += 32) {
             // slot j0 + lane: its row, tile and tile row
             const int j = j0 + lane;

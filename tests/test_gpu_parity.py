@@ -355,7 +355,16 @@ def test_fused_and_split_route_sort_agree_with_oracle(T, coarse, S):
     _check_sort_views(shape, ws2, ref, T, shape.kp)
 
 
-def test_deterministic_and_status_ok():
+@pytest.fixture
+def split_path():
+    """Bit-reproducibility checks run on the split GEMM2 path (the dense path
+    reduces in no fixed order; see test_gpu_gemm2_gate.py)."""
+    moe.moe_set_gemm2_path(moe.GEMM2_SPLIT)
+    yield
+    moe.moe_set_gemm2_path(moe.GEMM2_AUTO)
+
+
+def test_deterministic_and_status_ok(split_path):
     cfg = GRID[3]
     _, ws, out1, _, _, st = run_layer(cfg)
     _, ws2, out2, _, _, st2 = run_layer(cfg)
@@ -392,7 +401,7 @@ def test_zero_tokens_and_single_token():
     assert out.shape == (0, cfg.hidden)
 
 
-def test_graph_capture_replays_the_chain():
+def test_graph_capture_replays_the_chain(split_path):
     cfg = GRID[2]
     shape = shape_of(cfg)
     wts = _weights(cfg)
@@ -415,7 +424,7 @@ def test_graph_capture_replays_the_chain():
     assert moe.moe_get_status(ws) == (0, 0)
 
 
-def test_host_buffer_entry_point_matches_device_path():
+def test_host_buffer_entry_point_matches_device_path(split_path):
     cfg = GRID[2]
     shape = shape_of(cfg)
     wts = _weights(cfg)

@@ -104,12 +104,20 @@ def test_packed_weight_sizes():
             moe.moe_packed_weight_bytes(*bad)
 
 
+def test_gemm2_path_override_checks_its_value():
+    for path in (moe.GEMM2_SPLIT, moe.GEMM2_DENSE, moe.GEMM2_AUTO):
+        moe.moe_set_gemm2_path(path)
+    with pytest.raises(moe.MoeError) as e:
+        moe.moe_set_gemm2_path(3)
+    assert e.value.rc == moe.MOE_ERR_SHAPE
+
+
 def test_layer_launch_count():
-    # decode: route + sort + x quantisation in one launch, FC1, FC2, combine
-    assert moe.moe_layer_launch_count(_shape()) == 4
-    # 256 tokens x 16 picks > 1024 slots: route, one-CTA sort, then 4
-    assert moe.moe_layer_launch_count(_shape(T=256, max_T=256)) == 6
-    # prefill tiling at 32768 tokens: route, 3-kernel sort, gather, FC1, FC2, combine
-    assert moe.moe_layer_launch_count(_shape(T=32768, max_T=32768, block_n=128)) == 8
+    # decode: route + sort + x quantisation in one launch, GEMM2 gate, FC1, FC2, combine
+    assert moe.moe_layer_launch_count(_shape()) == 5
+    # 256 tokens x 16 picks > 1024 slots: route, one-CTA sort, gate, x quantisation, FC1, FC2, combine
+    assert moe.moe_layer_launch_count(_shape(T=256, max_T=256)) == 7
+    # prefill tiling at 32768 tokens: route, 3-kernel sort, gate, gather, FC1, FC2, combine
+    assert moe.moe_layer_launch_count(_shape(T=32768, max_T=32768, block_n=128)) == 9
     assert moe.moe_layer_launch_count(_shape(T=0)) == 1
 

@@ -24,7 +24,16 @@ SMALL = synth.MoeConfig("small", 7, T=48, E_global=64, E_local=64, expert_offset
                         hidden=1024, inter=256, block_n=16, shared_scale=0.5)
 
 
-def test_noalloc_matches_workspace_entry_point_across_calls():
+@pytest.fixture
+def split_path():
+    # exact equality needs the bit-reproducible GEMM2 path (the dense one sums
+    # in no fixed order)
+    moe.moe_set_gemm2_path(moe.GEMM2_SPLIT)
+    yield
+    moe.moe_set_gemm2_path(moe.GEMM2_AUTO)
+
+
+def test_noalloc_matches_workspace_entry_point_across_calls(split_path):
     cases = {}
     for cfg in (SMALL, synth.CONFIGS["tiny"]):
         shape = shape_of(cfg)
