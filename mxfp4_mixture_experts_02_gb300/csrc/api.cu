@@ -25,8 +25,8 @@ std::atomic<uint64_t> g_test_stall_ns{0};
 std::atomic<int> g_gemm2_path{MOE_GEMM2_AUTO};
 
 // The gate's rule: the dense GEMM2 path when rows * H <= this many fp32
-// reductions (see gate.cu).
-constexpr int64_t kDenseMaxElems = int64_t(4) << 20;
+// reductions and the accumulator fits well inside L2 (see gate.cu).
+constexpr int64_t kDenseMaxElems = int64_t(32) << 20;
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
@@ -168,7 +168,7 @@ int run_forward(const moe_shape* s, const uint16_t* x, const moe_weights* wt, co
     if (nsm <= 0) return MOE_ERR_CUDA;
 
     // The GEMM2 gate: one warp after the sort chooses split or dense.
-    GateParams gt{at<int32_t>(ws, L.header), d.H, g_gemm2_path.load(), kDenseMaxElems};
+    GateParams gt{at<int32_t>(ws, L.header), d.T, d.H, g_gemm2_path.load(), kDenseMaxElems};
     if (launch_gate(gt, st, pdl) != cudaSuccess) return MOE_ERR_CUDA;
 
     GatherParams gp{};

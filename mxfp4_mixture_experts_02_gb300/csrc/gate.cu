@@ -9,9 +9,12 @@
 //          only converts it to bf16.  The order of the reductions varies
 //          from run to run, so the last bits of the sums may too.
 // The rule: dense when the rows' reductions are few, rows * H <=
-// dense_max_elems (the accumulator then stays in L2 and the reductions cost
-// less than writing and re-reading the rows); split otherwise.  A caller may
-// force either path.
+// dense_max_elems, and the accumulator is small, T * H * 4 bytes <= 32 MiB
+// (well inside the 126 MiB L2, so the reductions run at the L2 and cost less
+// than writing the rows and reading them back); split otherwise.  Measured on
+// GB300: dense is faster at every decode workload (the 4352-row skewed batch
+// by 10 %), and 2x slower at the 32768-token prefill, whose 470 MB
+// accumulator lives in DRAM.  A caller may force either path.
 #include "common.cuh"
 #include "kernels.cuh"
 #include "ptx.cuh"
@@ -21,6 +24,9 @@ namespace moe {
 namespace {
 
 __global__ void __launch_bounds__(32) gemm2_gate_kernel(GateParams p) {
+    // The next launch may start its prologue now: it waits for this grid
+    // (griddepcontrol.wait) before it reads the path or the sort's table.
+    ptx::pdl_launch_dependents();
     ptx::pdl_wait();  // the sort's table is complete and visible
     if (threadIdx.x == 0) {
         const int R = p.header[kHdrRows];  // routed rows of this call
@@ -30,10 +36,12 @@ __global__ void __launch_bounds__(32) gemm2_gate_kernel(GateParams p) {
         else if (p.force == 2)
             path = kPathDense;
         else
-            path = static_cast<int64_t>(R) * p.H <= p.dense_max_elems ? kPathDense : kPathSplit;
+            path = (static_cast<int64_t>(R) * p.H <= p.dense_max_elems &&
+                    static_cast<int64_t>(p.T) * p.H * 4 <= (int64_t(32) << 20))
+                       ? kPathDense
+                       : kPathSplit;
         p.header[kHdrGemm2Path] = path;
     }
-    ptx::pdl_launch_dependents();
 }
 
 }  // namespace

@@ -125,7 +125,7 @@ struct CombineParams {
 // The one-warp GEMM2 gate: reads the sort's table and writes the path.
 struct GateParams {
     int32_t* header;
-    int H;
+    int T, H;
     int force;                // 0 the rule below, 1 split, 2 dense
     int64_t dense_max_elems;  // dense when rows * H <= this
 };

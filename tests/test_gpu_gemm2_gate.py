@@ -69,9 +69,9 @@ def test_both_gemm2_paths_match_the_oracle(cfg):
 
 
 def test_gate_rule_on_the_workloads():
-    # dense where rows * H <= 4 Mi (the decode workloads), split above (the
-    # skewed batch's 4352 rows and the prefill)
-    want = {"tiny": 1, "decode_t32": 1, "ep_slice_t64": 1, "skewed_shared_t256": 0, "prefill_t32768": 0}
+    # dense where rows * H <= 32 Mi with a [T, H] fp32 accumulator of at most
+    # 32 MiB (every decode workload), split at the 32768-token prefill
+    want = {"tiny": 1, "decode_t32": 1, "ep_slice_t64": 1, "skewed_shared_t256": 1, "prefill_t32768": 0}
     for name, path in want.items():
         cfg = synth.CONFIGS[name]
         shape = shape_of(cfg)

@@ -69,13 +69,20 @@ def _weights(cfg):
     return _WCACHE[key]
 
 
-def run_layer(cfg, T=None):
+def run_layer(cfg, T=None, path=moe.GEMM2_SPLIT):
+    """The layer through moe_layer.  By default on the split GEMM2 path, whose
+    FC2 writes the routed rows these tests compare (the dense path, which
+    reduces them into the output instead, is tested in test_gpu_gemm2_gate.py)."""
     shape = shape_of(cfg, T)
     wts = _weights(cfg)
     x, logits, sl = device_inputs(cfg, T=shape.T)
     ws = moe.workspace(shape)
-    out, ids, w = moe.moe_layer(shape, logits, sl, x, wts, ws)
-    torch.cuda.synchronize()
+    moe.moe_set_gemm2_path(path)
+    try:
+        out, ids, w = moe.moe_layer(shape, logits, sl, x, wts, ws)
+        torch.cuda.synchronize()
+    finally:
+        moe.moe_set_gemm2_path(moe.GEMM2_AUTO)
     status = moe.moe_get_status(ws)
     return shape, ws, out, ids, w, status
 
