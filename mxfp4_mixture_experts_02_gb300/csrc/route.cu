@@ -12,13 +12,23 @@ namespace moe {
 namespace {
 
 constexpr int kRouteWarps = 8;
+constexpr int kRouteCtasPerSm = 2;  // resident CTAs per SM: long batches loop several tokens per warp
 
-__global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(RouteParams p) {
+// Each warp routes tokens t, t + stride, ...; while it routes one, its lanes
+// prefetch the next token's logits row (one 128-byte line per lane) into L2,
+// so the next token's loads do not wait for DRAM.
+__global__ void __launch_bounds__(kRouteWarps * 32, kRouteCtasPerSm) route_kernel(RouteParams p) {
     __shared__ uint2 s_cand[kRouteWarps][rs::kMaxCand];
     ptx::pdl_wait();
-    const int warp = threadIdx.x >> 5;
-    const int t = blockIdx.x * kRouteWarps + warp;
-    if (t < p.T) rs::route_token(p, t, s_cand[warp], nullptr);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int stride = gridDim.x * kRouteWarps;
+    const int lines = (p.Eg * 4 + 127) / 128;  // <= 32 for E_global <= 1024
+    for (int t = blockIdx.x * kRouteWarps + warp; t < p.T; t += stride) {
+        const int tn = t + stride;
+        if (tn < p.T && lane < lines)
+            ptx::prefetch_l2(reinterpret_cast<const char*>(p.logits + static_cast<size_t>(tn) * p.Eg) + 128 * lane);
+        rs::route_token(p, t, s_cand[warp], nullptr);
+    }
     ptx::pdl_launch_dependents();
 }
 
@@ -26,7 +36,12 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(RouteParams p) 
 
 cudaError_t launch_route(const RouteParams& p, cudaStream_t stream, bool pdl) {
     if (p.T == 0) return cudaSuccess;
-    const int blocks = (p.T + kRouteWarps - 1) / kRouteWarps;
+    int dev = 0, nsm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) !=
+                                                  cudaSuccess)
+        return cudaErrorUnknown;
+    int blocks = (p.T + kRouteWarps - 1) / kRouteWarps;
+    blocks = blocks < nsm * kRouteCtasPerSm ? blocks : nsm * kRouteCtasPerSm;
     return launch_kernel(route_kernel, dim3(blocks), dim3(kRouteWarps * 32), 0, stream, pdl, p);
 }
 

@@ -222,6 +222,33 @@ constexpr int kBigWarps = 8;
 constexpr int kBigWarpSlots = 512;
 constexpr int kBigChunk = kBigWarps * kBigWarpSlots;
 
+constexpr int kBigRounds = kBigWarpSlots / 32;
+
+// The local experts of a warp's kBigWarpSlots slots [s0, s1), round r in
+// e[r] (lane = slot within the round; -1 past s1 or without a local row).
+// All loads are issued before any is used.
+__device__ __forceinline__ void load_experts(const SortParams& p, int s0, int s1, int (&e)[kBigRounds]) {
+    const int lane = threadIdx.x & 31;
+    int id[kBigRounds];
+#pragma unroll
+    for (int r = 0; r < kBigRounds; ++r) {
+        const int s = s0 + 32 * r + lane;
+        id[r] = s < s1 ? p.ids[s] : -1;
+    }
+#pragma unroll
+    for (int r = 0; r < kBigRounds; ++r) e[r] = (s0 + 32 * r + lane < s1) ? local_expert(id[r], p) : -1;
+}
+
+// warp_count on experts already in registers.
+__device__ __forceinline__ void warp_count_regs(const int (&e)[kBigRounds], int* my_hist) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int r = 0; r < kBigRounds; ++r) {
+        const uint32_t peers = __match_any_sync(0xffffffffu, e[r]);
+        if (e[r] >= 0 && lane == __ffs(peers) - 1) my_hist[e[r]] += __popc(peers);
+    }
+}
+
 // Pass 1: per-CTA expert counts -> cta_hist[c][e].
 __global__ void __launch_bounds__(kBigWarps * 32) sort_count_kernel(SortParams p) {
     extern __shared__ int s_dyn[];
@@ -232,7 +259,9 @@ __global__ void __launch_bounds__(kBigWarps * 32) sort_count_kernel(SortParams p
     __syncthreads();
     const int n = p.T * p.kp;
     const int s0 = blockIdx.x * kBigChunk + warp * kBigWarpSlots;
-    warp_count(p, s0, min(n, s0 + kBigWarpSlots), hist + warp * p.Et);
+    int e[kBigRounds];
+    load_experts(p, s0, min(n, s0 + kBigWarpSlots), e);
+    warp_count_regs(e, hist + warp * p.Et);
     __syncthreads();
     for (int e = tid; e < p.Et; e += kBigWarps * 32) {
         int c = 0;
@@ -250,11 +279,18 @@ __global__ void __launch_bounds__(kSortThreads, 1) sort_scan_kernel(SortParams p
     const int tid = threadIdx.x;
     int cnt = 0;
     if (tid < p.Et) {
-        for (int c = 0; c < nctas; ++c) {
-            int* h = p.cta_hist + static_cast<size_t>(c) * p.Et + tid;
-            const int v = *h;
-            *h = cnt;
-            cnt += v;
+        // 16 CTAs' counts are loaded together (independent loads), then
+        // replaced by their exclusive prefix
+        int* h = p.cta_hist + tid;
+        for (int c0 = 0; c0 < nctas; c0 += 16) {
+            int v[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] = (c0 + j < nctas) ? h[static_cast<size_t>(c0 + j) * p.Et] : 0;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                if (c0 + j < nctas) h[static_cast<size_t>(c0 + j) * p.Et] = cnt;
+                cnt += v[j];
+            }
         }
     }
     place_experts(p, cnt, nullptr, s_tot);
@@ -273,18 +309,39 @@ __global__ void __launch_bounds__(kBigWarps * 32) sort_rank_kernel(SortParams p)
     const int n = p.T * p.kp;
     const int s0 = blockIdx.x * kBigChunk + warp * kBigWarpSlots;
     const int s1 = min(n, s0 + kBigWarpSlots);
-    warp_count(p, s0, s1, hist + warp * p.Et);
+    int e[kBigRounds];
+    load_experts(p, s0, s1, e);
+    warp_count_regs(e, hist + warp * p.Et);
     __syncthreads();
-    for (int e = tid; e < p.Et; e += kBigWarps * 32) {
-        int run = p.offsets[e] + p.cta_hist[static_cast<size_t>(blockIdx.x) * p.Et + e];
+    for (int x = tid; x < p.Et; x += kBigWarps * 32) {
+        int run = p.offsets[x] + p.cta_hist[static_cast<size_t>(blockIdx.x) * p.Et + x];
         for (int w = 0; w < kBigWarps; ++w) {
-            const int c = hist[w * p.Et + e];
-            hist[w * p.Et + e] = run;
+            const int c = hist[w * p.Et + x];
+            hist[w * p.Et + x] = run;
             run += c;
         }
     }
     __syncthreads();
-    warp_rank(p, s0, s1, hist + warp * p.Et);
+    // ranks as in warp_rank, on the experts held in registers
+    const int lane = tid & 31;
+    int* my_base = hist + warp * p.Et;
+#pragma unroll
+    for (int r = 0; r < kBigRounds; ++r) {
+        const int s = s0 + 32 * r + lane;
+        const uint32_t peers = __match_any_sync(0xffffffffu, e[r]);
+        if (s < s1) {
+            if (e[r] >= 0) {
+                const int row = my_base[e[r]] + __popc(peers & ptx::lanemask_lt());
+                p.c_map[s] = row;
+                p.a_map[row] = s;
+            } else {
+                p.c_map[s] = -1;
+            }
+        }
+        __syncwarp();
+        if (e[r] >= 0 && lane == __ffs(peers) - 1) my_base[e[r]] += __popc(peers);
+        __syncwarp();
+    }
     ptx::pdl_launch_dependents();
 }
 
