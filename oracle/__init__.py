@@ -21,6 +21,11 @@ Functions and the passages they follow (reference page titles):
                 ... shape templates", section 4.
   activation -- h(gate, up) of one element, fp64.
   quantize_* -- the OCP MX v1.0 conversion rule for E2M1 / E4M3 blocks of 32.
+  nvfp4_*, quantize_nvfp4*, forward_nvfp4
+             -- the FP4 variant of "[SGLang] CUTLASS MoE", section 6: E2M1
+                with one E4M3 scale per 16 elements and an fp32 global scale
+                per tensor (value = e2m1 * e4m3 / gs), and the layer forward
+                with NVFP4 activations and weights.
 """
 from __future__ import annotations
 
@@ -86,6 +91,18 @@ def lib():
         L.oracle_sort.argtypes = [i32, i32, P, i32, i32, i32, i32, i32, P, P, P, P, P]
         L.oracle_forward.restype = i32
         L.oracle_forward.argtypes = [i32] * 8 + [P] * 8 + [i32] + [P] * 7 + [i32, dbl, dbl, P]
+        flt = ctypes.c_float
+        L.oracle_nvfp4_quantize_block.restype = None
+        L.oracle_nvfp4_quantize_block.argtypes = [P, flt, P, P]
+        L.oracle_nvfp4_global_scale.restype = flt
+        L.oracle_nvfp4_global_scale.argtypes = [P, i64]
+        L.oracle_quantize_nvfp4.restype = None
+        L.oracle_quantize_nvfp4.argtypes = [P, i64, i64, flt, P, P]
+        L.oracle_quantize_nvfp4_bf16.restype = None
+        L.oracle_quantize_nvfp4_bf16.argtypes = [P, i64, i64, flt, P, P]
+        L.oracle_forward_nvfp4.restype = i32
+        L.oracle_forward_nvfp4.argtypes = ([i32] * 8 + [P] * 4 + [P] * 6 + [flt, flt, i32] + [P] * 7 +
+                                           [i32, dbl, dbl, P])
         _lib = L
     return _lib
 
@@ -227,6 +244,86 @@ def forward(x_bits, ids, w, wmap, w1, w1s, w2, w2s, *, H: int, I: int, E_global:
                               _p(xq), _p(xqs), int(activation), float(c[0]), float(c[1]), _p(ys))
     if rc != 0:
         raise ValueError("oracle_forward: a routed expert has no weights in wmap")
+    res = dict(out_f64=out, out_bf16=outb)
+    if want_act:
+        res.update(act=act, act_sf=acts)
+    if want_xq:
+        res.update(xq=xq, xq_sf=xqs)
+    if want_y:
+        res.update(y_slot=ys)
+    return res
+
+
+# ------------------------------------------------------------------ NVFP4
+def nvfp4_quantize_block(values, gs: float):
+    """One NVFP4 block of 16 fp32 values with global scale gs: (E2M1 codes
+    uint8[16] with the sign in bit 3, E4M3 scale code)."""
+    v = _c(values, np.float32)
+    assert v.size == 16
+    codes = np.zeros(16, np.uint8)
+    sf = np.zeros(1, np.uint8)
+    lib().oracle_nvfp4_quantize_block(_p(v), float(gs), _p(codes), _p(sf))
+    return codes, int(sf[0])
+
+
+def nvfp4_global_scale(w) -> float:
+    """fp32(2688 / amax) of a weight matrix (1 for all zeros)."""
+    w = _c(w, np.float32)
+    return float(lib().oracle_nvfp4_global_scale(_p(w), w.size))
+
+
+def quantize_nvfp4(w, gs: float):
+    """fp32 [rows, K] -> (packed E2M1 codes uint8 [rows, K/2], E4M3 scales uint8 [rows, K/16])."""
+    w = _c(w, np.float32)
+    rows, K = w.shape
+    codes = np.zeros((rows, K // 2), np.uint8)
+    scales = np.zeros((rows, K // 16), np.uint8)
+    lib().oracle_quantize_nvfp4(_p(w), rows, K, float(gs), _p(codes), _p(scales))
+    return codes, scales
+
+
+def quantize_nvfp4_bf16(x_bits, gs: float):
+    """bf16 bits uint16 [rows, K] -> (E2M1 codes uint8 [rows, K], one per element; E4M3 scales uint8 [rows, K/16])."""
+    x = _c(x_bits, np.uint16)
+    rows, K = x.shape
+    codes = np.zeros((rows, K), np.uint8)
+    scales = np.zeros((rows, K // 16), np.uint8)
+    lib().oracle_quantize_nvfp4_bf16(_p(x), rows, K, float(gs), _p(codes), _p(scales))
+    return codes, scales
+
+
+def forward_nvfp4(x_bits, ids, w, wmap, w1, w1s, w1gs, w2, w2s, w2gs, *, x_gscale: float, h_gscale: float, H: int,
+                  I: int, E_global: int, E_local: int, expert_offset: int, num_shared: int, tokens=None,
+                  want_act: bool = False, want_xq: bool = False, activation: int = ACT_SWIGLU, act_params=(0.0, 0.0),
+                  want_y: bool = False):
+    """Layer forward of the NVFP4 variant for ``tokens``: as ``forward`` with
+    NVFP4 weights (w1 / w2 packed codes, E4M3 scales per 16, fp32 global scales
+    w1gs / w2gs per compact expert) and NVFP4 activations (global scales
+    x_gscale for x, h_gscale for the intermediate).  act_sf / xq_sf hold one
+    E4M3 scale per 16 elements."""
+    x = _c(x_bits, np.uint16)
+    ids = _c(ids, np.int32)
+    w = _c(w, np.float64)
+    T, kp = ids.shape
+    toks = _c(np.arange(T) if tokens is None else tokens, np.int32)
+    n = toks.size
+    out = np.zeros((n, H), np.float64)
+    outb = np.zeros((n, H), np.uint16)
+    act = np.zeros((n, kp, I), np.uint8) if want_act else None
+    acts = np.zeros((n, kp, I // 16), np.uint8) if want_act else None
+    xq = np.zeros((n, H), np.uint8) if want_xq else None
+    xqs = np.zeros((n, H // 16), np.uint8) if want_xq else None
+    ys = np.zeros((n, kp, H), np.float64) if want_y else None
+    a1, s1, a2, s2 = (_c(a, np.uint8) for a in (w1, w1s, w2, w2s))
+    g1, g2 = _c(w1gs, np.float32), _c(w2gs, np.float32)
+    wm = _c(wmap, np.int32)
+    c = (list(act_params) + [0.0, 0.0])[:2]
+    rc = lib().oracle_forward_nvfp4(T, H, I, kp, E_global, E_local, expert_offset, num_shared, _p(x), _p(ids), _p(w),
+                                    _p(wm), _p(a1), _p(s1), _p(g1), _p(a2), _p(s2), _p(g2), float(x_gscale),
+                                    float(h_gscale), n, _p(toks), _p(out), _p(outb), _p(act), _p(acts), _p(xq),
+                                    _p(xqs), int(activation), float(c[0]), float(c[1]), _p(ys))
+    if rc != 0:
+        raise ValueError("oracle_forward_nvfp4: a routed expert has no weights in wmap")
     res = dict(out_f64=out, out_bf16=outb)
     if want_act:
         res.update(act=act, act_sf=acts)

@@ -206,6 +206,54 @@ void decode_mxfp4_row(const uint8_t* codes, const uint8_t* scales, int64_t K, do
     for (int64_t k = 0; k < K; ++k) out[k] = tb.e2m1[e2m1_code_at(codes, k)] * tb.e8m0[scales[k / 32]];
 }
 
+/* ---------------------------------------------------------------- NVFP4
+ * The FP4 path of "[SGLang] CUTLASS MoE", section 6 (cutlass_moe_fp4): E2M1
+ * elements scaled in blocks of 16, with a per-tensor scale correcting the
+ * narrow E2M1 range (FLOAT4_E2M1_MAX = 6).  Here: one positive E4M3 block
+ * scale per 16 consecutive K elements and one fp32 global scale gs per
+ * tensor (per expert matrix for the weights); value = e2m1 * e4m3 / gs.
+ * Quantising a block of 16 takes every decision in fp32, the precision the
+ * GPU kernels compute in:
+ *   s  = fp32(fp32(amax * gs) / 6),  sf = E4M3 code nearest to s (ties to
+ *        even, saturating at 448);
+ *   dec(sf) == 0 (s underflows E4M3): every element is +0 or -0 by its sign;
+ *   else r = fp32(gs / dec(sf)), q_i = E2M1 code nearest to fp32(v_i * r)
+ *        (ties to even, saturating at 6), the sign of v_i kept.
+ * A weight matrix's global scale is gs = fp32(2688 / amax) (2688 = 448 * 6:
+ * the largest block scale times the largest element), 1 for a zero matrix. */
+constexpr float kNvfp4Range = 2688.0f;
+
+void nvfp4_quantize_block(const float* v, float gs, uint8_t* codes, uint8_t* sf_code) {
+    float amax = 0.0f;
+    for (int i = 0; i < 16; ++i) amax = std::max(amax, std::fabs(v[i]));
+    const float sv = (amax * gs) / 6.0f;
+    const int sf = nearest_code(FMT_E4M3, (double)sv);
+    *sf_code = (uint8_t)sf;
+    const float dsf = (float)e4m3_value(sf);
+    for (int i = 0; i < 16; ++i) {
+        int c = 0;
+        if (dsf > 0.0f) {
+            const float r = gs / dsf;
+            const float q = v[i] * r;
+            c = nearest_code(FMT_E2M1, std::fabs((double)q));
+        }
+        if (std::signbit(v[i])) c |= 0x8;
+        codes[i] = (uint8_t)c;
+    }
+}
+
+float nvfp4_global_scale(const float* w, int64_t n) {
+    float amax = 0.0f;
+    for (int64_t i = 0; i < n; ++i) amax = std::max(amax, std::fabs(w[i]));
+    return amax > 0.0f ? kNvfp4Range / amax : 1.0f;
+}
+
+/* Decode one NVFP4 row of K elements (packed codes, one E4M3 per 16) into fp64. */
+void decode_nvfp4_row(const uint8_t* codes, const uint8_t* scales, int64_t K, float gs, double* out) {
+    const Tables& tb = tables();
+    for (int64_t k = 0; k < K; ++k) out[k] = tb.e2m1[e2m1_code_at(codes, k)] * tb.e4m3[scales[k / 16]] / (double)gs;
+}
+
 }  // namespace
 
 extern "C" {
@@ -247,6 +295,39 @@ void oracle_quantize_mxfp8_bf16(const uint16_t* x, int64_t rows, int64_t K, uint
         for (int64_t b = 0; b < K / 32; ++b) {
             for (int i = 0; i < 32; ++i) v[i] = bf16_to_double(x[r * K + b * 32 + i]);
             mx_quantize_block(v.data(), 32, FMT_E4M3, &codes[r * K + b * 32], &scales[r * (K / 32) + b]);
+        }
+}
+
+/* NVFP4 (see nvfp4_quantize_block).  One block of 16 fp32 values; codes one
+ * byte per element. */
+void oracle_nvfp4_quantize_block(const float* v, float gs, uint8_t* codes, uint8_t* sf_code) {
+    nvfp4_quantize_block(v, gs, codes, sf_code);
+}
+
+/* Global scale of a weight matrix of n fp32 values: fp32(2688 / amax). */
+float oracle_nvfp4_global_scale(const float* w, int64_t n) { return nvfp4_global_scale(w, n); }
+
+/* Rows of fp32 values [rows, K] to NVFP4 with global scale gs: packed codes
+ * [rows, K/2] (element 2i in the low nibble), E4M3 scales [rows, K/16].
+ * K % 16 == 0. */
+void oracle_quantize_nvfp4(const float* w, int64_t rows, int64_t K, float gs, uint8_t* codes, uint8_t* scales) {
+    uint8_t c[16];
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t b = 0; b < K / 16; ++b) {
+            nvfp4_quantize_block(w + r * K + b * 16, gs, c, &scales[r * (K / 16) + b]);
+            for (int i = 0; i < 16; i += 2) codes[r * (K / 2) + b * 8 + i / 2] = (uint8_t)(c[i] | (c[i + 1] << 4));
+        }
+}
+
+/* bf16 rows [rows, K] to NVFP4 with global scale gs: codes one byte per
+ * element [rows, K], E4M3 scales [rows, K/16]. */
+void oracle_quantize_nvfp4_bf16(const uint16_t* x, int64_t rows, int64_t K, float gs, uint8_t* codes,
+                                uint8_t* scales) {
+    float v[16];
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t b = 0; b < K / 16; ++b) {
+            for (int i = 0; i < 16; ++i) v[i] = (float)bf16_to_double(x[r * K + b * 16 + i]);
+            nvfp4_quantize_block(v, gs, &codes[r * K + b * 16], &scales[r * (K / 16) + b]);
         }
 }
 
@@ -416,6 +497,85 @@ int oracle_forward(int T, int H, int I, int kp, int E_global, int E_local, int e
             for (int i = 0; i < I; ++i) hd[i] = tb.e4m3[hq[i]] * tb.e8m0[hs[i / 32]];
             for (int n = 0; n < H; ++n) {
                 decode_mxfp4_row(W2 + (int64_t)n * (I / 2), W2s + (int64_t)n * (I / 32), I, w2r.data());
+                double y = 0.0;
+                for (int i = 0; i < I; ++i) y += hd[i] * w2r[i];
+                Y[n] = y;
+            }
+            for (int n = 0; n < H; ++n) acc[n] += w[slot] * Y[n];
+            if (ys)
+                for (int n = 0; n < H; ++n) ys[n] = w[slot] * Y[n];
+        }
+        for (int n = 0; n < H; ++n) {
+            if (out_f64) out_f64[(int64_t)it * H + n] = acc[n];
+            if (out_bf16) out_bf16[(int64_t)it * H + n] = bf16_rne(acc[n]);
+        }
+    }
+    return 0;
+}
+
+/* The layer forward of the NVFP4 variant ("[SGLang] CUTLASS MoE", section 6:
+ * the activations quantised with a global scale, grouped FP4 GEMMs, per-expert
+ * alphas).  As oracle_forward, with NVFP4 in place of MXFP8 / MXFP4:
+ *   xq = NVFP4(x[t], gs_x);   W1[e], W2[e] NVFP4 with global scales gs_w1[e],
+ *   gs_w2[e] (packed codes [n, N, K/2], E4M3 scales [n, N, K/16]);
+ *   G, U = sum_h dec(xq) dec(W1) in fp64, dec(v) = e2m1 * e4m3 / gs;
+ *   h = act(G, U), rounded to fp32, hq = NVFP4(h, gs_h);
+ *   Y = sum_i dec(hq) dec(W2);  out = bf16(sum_j w_j Y_j).
+ * Optional outputs as in oracle_forward, with scales per 16 elements (act
+ * scales [ntok, k', I/16], xq scales [ntok, H/16]). */
+int oracle_forward_nvfp4(int T, int H, int I, int kp, int E_global, int E_local, int expert_offset, int S,
+                         const uint16_t* x, const int32_t* ids, const double* w, const int32_t* wmap,
+                         const uint8_t* w1, const uint8_t* w1s, const float* w1gs, const uint8_t* w2,
+                         const uint8_t* w2s, const float* w2gs, float gs_x, float gs_h, int ntok, const int32_t* toks,
+                         double* out_f64, uint16_t* out_bf16, uint8_t* act_codes, uint8_t* act_scales,
+                         uint8_t* xq_codes, uint8_t* xq_scales, int act, double act_c0, double act_c1, double* y_slot) {
+    (void)T;
+    std::vector<uint8_t> xq(H), xs(H / 16), hq(I), hs(I / 16);
+    std::vector<double> xd(H), hd(I), acc(H), Y(H), wg(H), wu(H), w2r(I);
+    std::vector<float> hv(I);
+    const Tables& tb = tables();
+    for (int it = 0; it < ntok; ++it) {
+        int t = toks[it];
+        oracle_quantize_nvfp4_bf16(x + (int64_t)t * H, 1, H, gs_x, xq.data(), xs.data());
+        if (xq_codes) std::memcpy(xq_codes + (int64_t)it * H, xq.data(), H);
+        if (xq_scales) std::memcpy(xq_scales + (int64_t)it * (H / 16), xs.data(), H / 16);
+        for (int h = 0; h < H; ++h) xd[h] = tb.e2m1[xq[h]] * tb.e4m3[xs[h / 16]] / (double)gs_x;
+        std::fill(acc.begin(), acc.end(), 0.0);
+        for (int j = 0; j < kp; ++j) {
+            int64_t slot = (int64_t)t * kp + j;
+            int e = local_expert(ids[slot], E_global, E_local, expert_offset, S);
+            uint8_t* ac = act_codes ? act_codes + ((int64_t)it * kp + j) * I : nullptr;
+            uint8_t* as = act_scales ? act_scales + ((int64_t)it * kp + j) * (I / 16) : nullptr;
+            double* ys = y_slot ? y_slot + ((int64_t)it * kp + j) * H : nullptr;
+            if (e < 0) {
+                if (ac) std::memset(ac, 0, I);
+                if (as) std::memset(as, 0, I / 16);
+                if (ys) std::fill(ys, ys + H, 0.0);
+                continue;
+            }
+            int wi = wmap[e];
+            if (wi < 0) return -1;
+            const uint8_t* W1 = w1 + (int64_t)wi * 2 * I * (H / 2);
+            const uint8_t* W1s = w1s + (int64_t)wi * 2 * I * (H / 16);
+            const uint8_t* W2 = w2 + (int64_t)wi * H * (I / 2);
+            const uint8_t* W2s = w2s + (int64_t)wi * H * (I / 16);
+            for (int r = 0; r < I; ++r) {
+                decode_nvfp4_row(W1 + (int64_t)r * (H / 2), W1s + (int64_t)r * (H / 16), H, w1gs[wi], wg.data());
+                decode_nvfp4_row(W1 + (int64_t)(I + r) * (H / 2), W1s + (int64_t)(I + r) * (H / 16), H, w1gs[wi],
+                                 wu.data());
+                double g = 0.0, u = 0.0;
+                for (int h = 0; h < H; ++h) {
+                    g += xd[h] * wg[h];
+                    u += xd[h] * wu[h];
+                }
+                hv[r] = (float)activation(act, act_c0, act_c1, g, u);
+            }
+            for (int b = 0; b < I / 16; ++b) nvfp4_quantize_block(&hv[b * 16], gs_h, &hq[b * 16], &hs[b]);
+            if (ac) std::memcpy(ac, hq.data(), I);
+            if (as) std::memcpy(as, hs.data(), I / 16);
+            for (int i = 0; i < I; ++i) hd[i] = tb.e2m1[hq[i]] * tb.e4m3[hs[i / 16]] / (double)gs_h;
+            for (int n = 0; n < H; ++n) {
+                decode_nvfp4_row(W2 + (int64_t)n * (I / 2), W2s + (int64_t)n * (I / 16), I, w2gs[wi], w2r.data());
                 double y = 0.0;
                 for (int i = 0; i < I; ++i) y += hd[i] * w2r[i];
                 Y[n] = y;
