@@ -60,6 +60,8 @@ def parse():
     ap.add_argument("--block-n", type=int, default=0, help="override the workload's virtual-expert rows")
     ap.add_argument("--router", action="store_true",
                     help="start the layer from x and a bf16 router matrix (router GEMM in the chain)")
+    ap.add_argument("--fmt", default="mxfp8", choices=["mxfp8", "nvfp4"],
+                    help="number format: the workloads' MXFP8 x MXFP4, or the NVFP4 variant (128-row tiles)")
     ap.add_argument("--gemm2", default="auto", choices=["auto", "split", "dense"],
                     help="GEMM2 path: the device gate's rule, or one path forced")
     ap.add_argument("--act", default="swiglu", choices=["swiglu", "swiglu_clamp", "situ"],
@@ -185,7 +187,34 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------------- ours
-def setup_layer(cfg, device):
+# NVFP4 variant: global scales of x (N(0, 1) within +-6: 2688 / 6) and of the
+# intermediate (within +-64)
+NV_X_GSCALE, NV_H_GSCALE = 448.0, 42.0
+
+
+def setup_weights_nvfp4(moe, synth, cfg, device):
+    """NVFP4 weights of the workload: quantised (per-expert global scales) and packed on the device."""
+    import torch
+    gids = cfg.global_ids
+    E, H, I = gids.size, cfg.hidden, cfg.inter
+    c1 = torch.empty((E, 2 * I, H // 2), dtype=torch.uint8, device=device)
+    c2 = torch.empty((E, H, I // 2), dtype=torch.uint8, device=device)
+    s1 = torch.empty((E, 2 * I, H // 16), dtype=torch.uint8, device=device)
+    s2 = torch.empty((E, H, I // 16), dtype=torch.uint8, device=device)
+    g1 = torch.empty(E, dtype=torch.float32, device=device)
+    g2 = torch.empty(E, dtype=torch.float32, device=device)
+    for c0 in range(0, E, 64):
+        ids = gids[c0:c0 + 64]
+        n = ids.size
+        g1[c0:c0 + n], c1[c0:c0 + n], s1[c0:c0 + n] = moe.moe_quantize_nvfp4(synth.w1_device(cfg, ids, device))
+        g2[c0:c0 + n], c2[c0:c0 + n], s2[c0:c0 + n] = moe.moe_quantize_nvfp4(synth.w2_device(cfg, ids, device))
+    p1, q1 = moe.moe_pack_weights_nvfp4(c1, s1, True)
+    p2, q2 = moe.moe_pack_weights_nvfp4(c2, s2, False)
+    del c1, c2, s1, s2
+    return moe.MoeWeights(p1, q1, p2, q2), moe.MoeNvfp4(NV_X_GSCALE, NV_H_GSCALE, g1, g2)
+
+
+def setup_layer(cfg, device, fmt="mxfp8"):
     import torch
 
     import mxfp4_mixture_experts_02_gb300 as moe
@@ -197,6 +226,19 @@ def setup_layer(cfg, device):
                          activation=cfg.activation, act_params=tuple(cfg.act_params))
     gids = cfg.global_ids
     E, H, I = gids.size, cfg.hidden, cfg.inter
+    if fmt == "nvfp4":
+        weights, nv = setup_weights_nvfp4(moe, synth, cfg, device)
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        x = synth.x_device(cfg, device)
+        logits = synth.logits_device(cfg, device)
+        sl = synth.shared_logit_device(cfg, device).contiguous() if cfg.num_shared else None
+        ws = moe.workspace(shape, device)
+        ids = torch.empty((cfg.T, cfg.kp), dtype=torch.int32, device=device)
+        tw = torch.empty((cfg.T, cfg.kp), dtype=torch.float32, device=device)
+        out = torch.empty((cfg.T, H), dtype=torch.bfloat16, device=device)
+        torch.cuda.synchronize()
+        return moe, shape, (weights, nv), x, logits, sl, ws, ids, tw, out
     c1 = torch.empty((E, 2 * I, H // 2), dtype=torch.uint8, device=device)
     c2 = torch.empty((E, H, I // 2), dtype=torch.uint8, device=device)
     s1 = torch.empty((E, 2 * I, H // 32), dtype=torch.uint8, device=device)
@@ -238,10 +280,16 @@ def measure_config(args, cfg, device, stream, flush, sampler, steps, warmup, wor
     router GEMM (--router), the host-buffer path; returns the result record."""
     import torch
 
-    moe, shape, weights, x, logits, sl, ws, ids, tw, out = setup_layer(cfg, device)
+    nvfp4 = getattr(args, "fmt", "mxfp8") == "nvfp4"
+    moe, shape, weights, x, logits, sl, ws, ids, tw, out = setup_layer(cfg, device, "nvfp4" if nvfp4 else "mxfp8")
     moe.moe_set_gemm2_path({"auto": moe.GEMM2_AUTO, "split": moe.GEMM2_SPLIT, "dense": moe.GEMM2_DENSE}[args.gemm2])
     wr = None
-    if args.router:
+    if nvfp4:
+        weights, nv = weights
+
+        def layer():
+            moe.moe_layer_nvfp4(shape, nv, logits, sl, x, weights, ws, ids, tw, out)
+    elif args.router:
         wr = router_matrix(cfg, device)
 
         def layer():
@@ -285,8 +333,9 @@ def measure_config(args, cfg, device, stream, flush, sampler, steps, warmup, wor
     router = time_router(moe, shape, x, wr, ws, logits, flush, stream, reps) if wr is not None else None
     # live per-kernel timing (events between the launches, same stream; in
     # --router mode the logits are the router GEMM's, left by the last step)
-    kernel_ms = profile_kernels(moe, shape, weights, x, logits, sl, ws, ids, tw, out, flush, stream, reps)
-    e2e = run_e2e(moe, shape, weights, cfg, ws, stream, flush, reps)
+    kernel_ms = profile_kernels(moe, shape, weights, x, logits, sl, ws, ids, tw, out, flush, stream, reps,
+                                nv if nvfp4 else None)
+    e2e = run_e2e(moe, shape, weights, cfg, ws, stream, flush, reps, nv if nvfp4 else None)
 
     hdr = ws[:64 * 4].view(torch.int32).cpu().numpy()
     moe.moe_set_gemm2_path(moe.GEMM2_AUTO)
@@ -316,12 +365,22 @@ def measure_config(args, cfg, device, stream, flush, sampler, steps, warmup, wor
     # reported beside it.
     dom_bytes = fc1_bytes if dom == "fc1" else fc2_bytes
     flops = fc1_flops if dom == "fc1" else fc2_flops
-    tpeak = 2.0 * bf16
+    # kind::mxf4nvf4 (NVFP4) runs at the FP4 rate: measured bf16 x 6 (nominal 13.5 : 2.25)
+    tpeak = (6.0 if nvfp4 else 2.0) * bf16
+    if nvfp4:
+        # NVFP4 operand bytes: codes half a byte, one scale byte per 16 elements
+        wb1 = lambda: 2 * I * H // 2 + 2 * I * H // 16  # noqa: E731
+        wb2 = lambda: H * I // 2 + H * I // 16  # noqa: E731
+        fc1_bytes = touched * wb1() + x_rows * H * 9 // 16 + R * I * 9 // 16
+        fc2_bytes = touched * wb2() + R * I * 9 // 16 + R * H * ybytes
+        dom_bytes = fc1_bytes if dom == "fc1" else fc2_bytes
+        layer_weight_bytes = touched * (wb1() + wb2())
     if flops / (tpeak * 1e12) > dom_bytes / (hbm * 1e9):
         achieved = flops / dt / 1e12
         roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": tpeak, "unit": "TFLOP/s",
                 "frac": achieved / tpeak, "traffic": measured_traffic(cfg.name, dom),
-                "peak_kind": "%s bf16 burst x 2 (mxf8f6f4, FP8-class)" % peak_kind,
+                "peak_kind": ("%s bf16 burst x 6 (mxf4nvf4, FP4-class)" % peak_kind if nvfp4 else
+                              "%s bf16 burst x 2 (mxf8f6f4, FP8-class)" % peak_kind),
                 "frac_of_fp4_peak": achieved / (6.0 * bf16), "algorithmic_flops": flops,
                 "algorithmic_bytes": dom_bytes}
     else:
@@ -334,7 +393,9 @@ def measure_config(args, cfg, device, stream, flush, sampler, steps, warmup, wor
     if prefill:
         achieved = (fc1_flops + fc2_flops) / sec / 1e12
         layer_roof = {"bound": "tensor", "achieved": achieved, "unit": "TFLOP/s", "peak": tpeak,
-                      "frac": achieved / tpeak, "peak_kind": "%s bf16 burst x 2 (FP8-class)" % peak_kind,
+                      "frac": achieved / tpeak,
+                      "peak_kind": "%s bf16 burst x %d (%s-class)" % (peak_kind, 6 if nvfp4 else 2,
+                                                                     "FP4" if nvfp4 else "FP8"),
                       "frac_of_nominal_fp8": achieved / 4500.0, "frac_of_nominal_fp4": achieved / 13500.0,
                       "algorithmic_flops": fc1_flops + fc2_flops}
     else:
@@ -347,6 +408,8 @@ def measure_config(args, cfg, device, stream, flush, sampler, steps, warmup, wor
         "expert_offset": cfg.expert_offset, "top_k": cfg.top_k, "num_shared": cfg.num_shared, "hidden": H,
         "inter": I, "block_n": cfg.block_n, "seed": cfg.seed, "activation": ACT_NAMES[cfg.activation],
         "gemm2_path": "dense" if hdr[5] == 1 else "split",
+        "format": "nvfp4 (E2M1 x E2M1, E4M3 scales per 16, fp32 global scales)" if nvfp4 else
+                  "mxfp8 activations x mxfp4 weights (E8M0 scales per 32)",
         "tokens_per_s": world * cfg.T / sec, "us_per_layer": ms * 1e3, "steps": stats,
         "layer": {"routed_rows": R, "touched_experts": touched, "weight_bytes_touched": layer_weight_bytes,
                   "kernel_us": {k: kernel_ms[k] * 1e3 for k in names},
@@ -386,6 +449,8 @@ def run_ours(args, cfg):
             for name in synth.CONFIG_ORDER:
                 c = synth.CONFIGS[name]
                 if name == cfg.name or (args.tokens and name != cfg.name):
+                    continue
+                if args.fmt == "nvfp4":  # the variant is timed on its headline workload alone
                     continue
                 sub_steps = max(args.steps, 50) if c.T <= 256 else args.steps
                 n0 = len(sampler.windows) if sampler else 0
@@ -480,7 +545,7 @@ def ws_counts(moe, shape, ws):
     return v["expert_counts"].cpu().numpy()
 
 
-def profile_kernels(moe, shape, weights, x, logits, sl, ws, ids, tw, out, flush, stream, reps):
+def profile_kernels(moe, shape, weights, x, logits, sl, ws, ids, tw, out, flush, stream, reps, nv=None):
     import torch
     names = ["route", "sort", "gather", "fc1", "fc2", "combine"]
     acc = {k: 0.0 for k in names}
@@ -488,7 +553,10 @@ def profile_kernels(moe, shape, weights, x, logits, sl, ws, ids, tw, out, flush,
         for r in range(reps + 3):
             ev = [torch.cuda.Event(enable_timing=True) for _ in range(7)]
             flush()
-            moe.moe_layer_events(shape, logits, sl, x, weights, ws, ids, tw, out, ev)
+            if nv is not None:
+                moe.moe_layer_nvfp4_events(shape, nv, logits, sl, x, weights, ws, ids, tw, out, ev)
+            else:
+                moe.moe_layer_events(shape, logits, sl, x, weights, ws, ids, tw, out, ev)
             torch.cuda.synchronize()
             if r >= 3:
                 for k, n in enumerate(names):
@@ -496,7 +564,7 @@ def profile_kernels(moe, shape, weights, x, logits, sl, ws, ids, tw, out, flush,
     return {k: v / reps for k, v in acc.items()}
 
 
-def run_e2e(moe, shape, weights, cfg, ws, stream, flush, reps):
+def run_e2e(moe, shape, weights, cfg, ws, stream, flush, reps, nv=None):
     import torch
 
     import synth
@@ -505,13 +573,27 @@ def run_e2e(moe, shape, weights, cfg, ws, stream, flush, reps):
     xh = synth.x_device(cfg, dev).cpu().pin_memory()
     sh = synth.shared_logit_device(cfg, dev).contiguous().cpu().pin_memory() if cfg.num_shared else None
     oh = torch.empty((cfg.T, cfg.hidden), dtype=torch.bfloat16).pin_memory()
+    if nv is not None:  # the public NVFP4 path: copy in, moe_layer_nvfp4, copy out
+        ld, xd = torch.empty_like(lh, device=dev), torch.empty_like(xh, device=dev)
+        sd = torch.empty_like(sh, device=dev) if sh is not None else None
+        od = torch.empty((cfg.T, cfg.hidden), dtype=torch.bfloat16, device=dev)
+        ids = torch.empty((cfg.T, cfg.kp), dtype=torch.int32, device=dev)
+        tw = torch.empty((cfg.T, cfg.kp), dtype=torch.float32, device=dev)
     times = []
     with torch.cuda.stream(stream):
         for r in range(reps + 3):
             flush()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
-            moe.moe_layer_host(shape, lh, sh, xh, weights, ws, oh)
+            if nv is not None:
+                ld.copy_(lh, non_blocking=True)
+                xd.copy_(xh, non_blocking=True)
+                if sd is not None:
+                    sd.copy_(sh, non_blocking=True)
+                moe.moe_layer_nvfp4(shape, nv, ld, sd, xd, weights, ws, ids, tw, od)
+                oh.copy_(od, non_blocking=True)
+            else:
+                moe.moe_layer_host(shape, lh, sh, xh, weights, ws, oh)
             b.record(stream)
             torch.cuda.synchronize()
             if r >= 3:
@@ -680,6 +762,8 @@ def main():
         cfg = cfg.replace(block_n=args.block_n, name="%s_B%d" % (cfg.name, args.block_n))
     if args.router:
         cfg = cfg.replace(name="%s_router" % cfg.name)
+    if args.fmt == "nvfp4":
+        cfg = cfg.replace(name="%s_nvfp4" % cfg.name)
     if args.act != "swiglu":
         act = ACT_NAMES.index(args.act)
         cfg = cfg.replace(activation=act, act_params=ACT_DEFAULT_PARAMS[act], name="%s_%s" % (cfg.name, args.act))

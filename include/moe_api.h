@@ -102,6 +102,61 @@ typedef struct moe_weights {
     const uint8_t *w1, *w1_sf, *w2, *w2_sf;
 } moe_weights;
 
+/* NVFP4 variant ("[SGLang] CUTLASS MoE", section 6, cutlass_moe_fp4: FP4 in
+ * blocks of 16, with a per-tensor scale for the narrow E2M1 range).  A tensor
+ * holds E2M1 codes (two per byte, element 2i in the low nibble), one E4M3
+ * block scale (sign bit clear) per 16 consecutive K elements and one fp32
+ * global scale gs: value = e2m1 * e4m3 / gs.  A block of 16 is quantised with
+ * every decision in fp32: s = (amax * gs) / 6 rounded to E4M3 (nearest even,
+ * saturating at 448); r = gs / dec(s); each element = E2M1(v * r) (nearest
+ * even, saturating at 6; signed zeros when s underflows).  The FC1 / FC2
+ * products are E2M1 x E2M1 on tcgen05 kind::mxf4nvf4 tensor cores, scaled by
+ * 1 / (gs_in * gs_w[e]) in the epilogue; the activation's output is
+ * requantised to NVFP4 with h_gscale.
+ *   x_gscale, h_gscale  global scales of x and of the FC1 activation output
+ *                       (calibrated by the caller: 2688 / (the largest |value|
+ *                       expected) keeps every block scale in range)
+ *   w1_gscale, w2_gscale device fp32 [E_tot]: each expert matrix's global
+ *                       scale, written by moe_quantize_nvfp4 */
+typedef struct moe_nvfp4 {
+    float x_gscale, h_gscale;
+    const float *w1_gscale, *w2_gscale;
+} moe_nvfp4;
+
+/* fp32 weights of `experts` matrices [experts, rows, K] (device, 16-byte
+ * aligned, K % 16 == 0) -> NVFP4: gscale [experts] (fp32(2688 / amax) of each
+ * matrix, 1 for all zeros), codes [experts * rows, K / 2] and E4M3 scales
+ * [experts * rows, K / 16], row-major. */
+int moe_quantize_nvfp4(const float* w, int64_t experts, int64_t rows, int64_t K, float* gscale, uint8_t* codes,
+                       uint8_t* scales, moe_stream_t stream);
+
+/* moe_pack_weights for NVFP4: the codes are packed exactly as for MXFP4
+ * (per expert, 256-row block and 128-K chunk one contiguous 16 KiB run); the
+ * scales (row-major [experts, N, K / 16]) become one 2 KiB block per tile in
+ * the layout the scale_vec::4X MMA reads from tensor memory: for each 64-K
+ * half kk two 512-byte blocks (block rows 0-127, 128-255), row r's 4-byte
+ * cell at (r % 32) * 16 + (r / 32) * 4, byte b = the half's 16-element block
+ * b.  Sizes: codes experts * N * K / 2, scales experts * N * K / 16 bytes.
+ * N % 256 == 0, K % 128 == 0. */
+int moe_pack_weights_nvfp4(const uint8_t* codes, const uint8_t* scales, int64_t experts, int64_t N, int64_t K,
+                           int32_t pair_halves, uint8_t* packed_codes, uint8_t* packed_scales, moe_stream_t stream);
+
+/* moe_layer in the NVFP4 variant, for 128-row tiles (block_n == 128; other
+ * tilings return MOE_ERR_SHAPE): weights packed by moe_pack_weights_nvfp4,
+ * global scales in `nv`.  Same launch chain, GEMM2 gate and outputs as
+ * moe_layer; in the workspace, x and the intermediate hold NVFP4 codes [rows,
+ * H / 2] / [rows, I / 2] with 1 KiB scale blocks per 128-K chunk of a virtual
+ * expert (the layout above, tile rows for matrix rows). */
+int moe_layer_nvfp4(const moe_shape* shape, const moe_nvfp4* nv, const float* logits, const uint16_t* shared_logit,
+                    const uint16_t* x, const moe_weights* weights, int32_t* topk_ids, float* topk_w, void* workspace,
+                    size_t workspace_bytes, uint16_t* out, moe_stream_t stream);
+
+/* moe_layer_nvfp4 with the timing events of moe_layer_events. */
+int moe_layer_nvfp4_events(const moe_shape* shape, const moe_nvfp4* nv, const float* logits,
+                           const uint16_t* shared_logit, const uint16_t* x, const moe_weights* weights,
+                           int32_t* topk_ids, float* topk_w, void* workspace, size_t workspace_bytes, uint16_t* out,
+                           void* const* events, moe_stream_t stream);
+
 /* Device pointers into a workspace, for inspection and parity checks.
  *   header       int32[64]: [0] rows R, [1] virtual experts, [2] groups,
  *                [3] status, [4] status detail, [5] GEMM2 path (0 split,

@@ -22,6 +22,8 @@ __all__ = [
     "moe_layer", "moe_router", "moe_layer_router", "moe_layer_host", "moe_layer_events", "moe_layer_noalloc", "moe_get_views", "moe_get_status",
     "moe_num_sms", "moe_layer_launch_count", "quantize_expert_weights", "moe_noalloc_get_status",
     "moe_test_set_stall", "moe_set_gemm2_path", "GEMM2_AUTO", "GEMM2_SPLIT", "GEMM2_DENSE",
+    "MoeNvfp4", "moe_quantize_nvfp4", "moe_pack_weights_nvfp4", "moe_layer_nvfp4", "moe_layer_nvfp4_events",
+    "quantize_expert_weights_nvfp4",
     "workspace", "MOE_OK", "MOE_ERR_TIMEOUT", "MOE_ERR_WORKSPACE",
 ]
 
@@ -88,6 +90,25 @@ class MoeShape:
         return _Shape(**d)
 
 
+class _Nvfp4(ctypes.Structure):
+    _fields_ = [("x_gscale", ctypes.c_float), ("h_gscale", ctypes.c_float), ("w1_gscale", ctypes.c_void_p),
+                ("w2_gscale", ctypes.c_void_p)]
+
+
+@dataclasses.dataclass
+class MoeNvfp4:
+    """Global scales of the NVFP4 variant (see moe_api.h): x_gscale and
+    h_gscale for the activations, w1_gscale / w2_gscale device fp32 [E_tot]."""
+    x_gscale: float
+    h_gscale: float
+    w1_gscale: torch.Tensor
+    w2_gscale: torch.Tensor
+
+    def c(self) -> _Nvfp4:
+        return _Nvfp4(float(self.x_gscale), float(self.h_gscale), self.w1_gscale.data_ptr(),
+                      self.w2_gscale.data_ptr())
+
+
 @dataclasses.dataclass
 class MoeWeights:
     """Packed expert weights (device tensors, uint8)."""
@@ -124,6 +145,11 @@ _SIGS = {
     "moe_noalloc_get_status": [ctypes.c_void_p] * 2,
     "moe_test_set_stall": [ctypes.c_uint64],
     "moe_set_gemm2_path": [ctypes.c_int32],
+    "moe_quantize_nvfp4": [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64] + [ctypes.c_void_p] * 4,
+    "moe_pack_weights_nvfp4": [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                               ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p],
+    "moe_layer_nvfp4": [ctypes.c_void_p] * 9 + [ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p],
+    "moe_layer_nvfp4_events": [ctypes.c_void_p] * 9 + [ctypes.c_size_t] + [ctypes.c_void_p] * 3,
     "moe_num_sms": [ctypes.c_void_p],
     "moe_layer_launch_count": [ctypes.c_void_p, ctypes.c_void_p],
 }
@@ -257,6 +283,45 @@ def quantize_expert_weights(w1: torch.Tensor, w2: torch.Tensor, keep_rowmajor: b
     return wts
 
 
+def moe_quantize_nvfp4(w: torch.Tensor):
+    """fp32 [experts, rows, K] (device) -> (gscale fp32 [experts], E2M1 codes uint8
+    [experts, rows, K/2], E4M3 scales uint8 [experts, rows, K/16])."""
+    _check_cuda(w)
+    E, rows, K = w.shape
+    gs = torch.empty(E, dtype=torch.float32, device=w.device)
+    codes = torch.empty((E, rows, K // 2), dtype=torch.uint8, device=w.device)
+    scales = torch.empty((E, rows, K // 16), dtype=torch.uint8, device=w.device)
+    _call("moe_quantize_nvfp4", w.data_ptr(), E, rows, K, gs.data_ptr(), codes.data_ptr(), scales.data_ptr(),
+          _stream(w.device))
+    return gs, codes, scales
+
+
+def moe_pack_weights_nvfp4(codes: torch.Tensor, scales: torch.Tensor, pair_halves: bool):
+    """NVFP4 codes uint8 [E, N, K/2] and scales uint8 [E, N, K/16] to the
+    tile-major layout (see moe_api.h).  Returns (packed_codes, packed_scales), flat uint8."""
+    _check_cuda(codes, scales)
+    E, N, K2 = codes.shape
+    pc = torch.empty(E * N * K2, dtype=torch.uint8, device=codes.device)
+    ps = torch.empty(E * N * (2 * K2 // 16), dtype=torch.uint8, device=codes.device)
+    _call("moe_pack_weights_nvfp4", codes.data_ptr(), scales.data_ptr(), E, N, 2 * K2, 1 if pair_halves else 0,
+          pc.data_ptr(), ps.data_ptr(), _stream(codes.device))
+    return pc, ps
+
+
+def quantize_expert_weights_nvfp4(w1: torch.Tensor, w2: torch.Tensor, x_gscale: float, h_gscale: float,
+                                  keep_rowmajor: bool = False):
+    """fp32 W1 [E, 2I, H] and W2 [E, H, I] (device) -> (packed MoeWeights, MoeNvfp4)
+    (and, if asked, the row-major (c1, s1, c2, s2))."""
+    g1, c1, s1 = moe_quantize_nvfp4(w1)
+    g2, c2, s2 = moe_quantize_nvfp4(w2)
+    p1, q1 = moe_pack_weights_nvfp4(c1, s1, True)
+    p2, q2 = moe_pack_weights_nvfp4(c2, s2, False)
+    res = (MoeWeights(p1, q1, p2, q2), MoeNvfp4(x_gscale, h_gscale, g1, g2))
+    if keep_rowmajor:
+        return res + ((c1, s1, c2, s2),)
+    return res
+
+
 # ------------------------------------------------------------------ the layer
 def moe_route(shape: MoeShape, logits, shared_logit=None, topk_ids=None, topk_w=None):
     _check_cuda(logits, shared_logit)
@@ -333,6 +398,40 @@ def moe_layer(shape: MoeShape, logits, shared_logit, x, weights: MoeWeights, ws,
     _call("moe_layer", ctypes.byref(s), logits.data_ptr(), _ptr(shared_logit), x.data_ptr(), ctypes.byref(w),
           topk_ids.data_ptr(), topk_w.data_ptr(), ws.data_ptr(), ws.numel(), out.data_ptr(), _stream(dev))
     return out, topk_ids, topk_w
+
+
+def moe_layer_nvfp4(shape: MoeShape, nv: MoeNvfp4, logits, shared_logit, x, weights: MoeWeights, ws,
+                    topk_ids=None, topk_w=None, out=None):
+    """moe_layer in the NVFP4 variant (128-row tiles)."""
+    _check_cuda(logits, shared_logit, x, ws)
+    dev = x.device
+    if topk_ids is None:
+        topk_ids = torch.empty((shape.T, shape.kp), dtype=torch.int32, device=dev)
+    if topk_w is None:
+        topk_w = torch.empty((shape.T, shape.kp), dtype=torch.float32, device=dev)
+    if out is None:
+        out = torch.empty((shape.T, shape.hidden), dtype=torch.bfloat16, device=dev)
+    s, w, n = shape.c(), weights.c(), nv.c()
+    _call("moe_layer_nvfp4", ctypes.byref(s), ctypes.byref(n), logits.data_ptr(), _ptr(shared_logit), x.data_ptr(),
+          ctypes.byref(w), topk_ids.data_ptr(), topk_w.data_ptr(), ws.data_ptr(), ws.numel(), out.data_ptr(),
+          _stream(dev))
+    return out, topk_ids, topk_w
+
+
+def moe_layer_nvfp4_events(shape: MoeShape, nv: MoeNvfp4, logits, shared_logit, x, weights: MoeWeights, ws, topk_ids,
+                           topk_w, out, events):
+    """moe_layer_nvfp4 with the 7 stage events of moe_layer_events."""
+    _check_cuda(logits, shared_logit, x, ws)
+    stream = torch.cuda.current_stream(x.device)
+    for ev in events:
+        if not ev.cuda_event:
+            ev.record(stream)
+    arr = (ctypes.c_void_p * 7)(*[ev.cuda_event for ev in events])
+    s, w, n = shape.c(), weights.c(), nv.c()
+    _call("moe_layer_nvfp4_events", ctypes.byref(s), ctypes.byref(n), logits.data_ptr(), _ptr(shared_logit),
+          x.data_ptr(), ctypes.byref(w), topk_ids.data_ptr(), topk_w.data_ptr(), ws.data_ptr(), ws.numel(),
+          out.data_ptr(), arr, _stream(x.device))
+    return out
 
 
 def moe_layer_events(shape: MoeShape, logits, shared_logit, x, weights: MoeWeights, ws, topk_ids, topk_w, out,

@@ -45,15 +45,15 @@ bool get_encode() {
 
 // 2-D K-major tensor map: dim0 = K elements (contiguous), dim1 = rows.
 bool make_map(CUtensorMap* map, CUtensorMapDataType type, const void* base, uint64_t K, uint64_t rows,
-              uint64_t row_bytes, uint32_t box_k, uint32_t box_rows) {
+              uint64_t row_bytes, uint32_t box_k, uint32_t box_rows,
+              CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
     if (!get_encode()) return false;
     cuuint64_t dims[2] = {K, rows};
     cuuint64_t strides[1] = {row_bytes};
     cuuint32_t box[2] = {box_k, box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = g_encode(map, type, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                          swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
@@ -155,8 +155,10 @@ int run_route_sort(const moe_shape* s, const float* logits, const uint16_t* shar
 }
 
 // gathered: the route + sort launch already quantised x (decode tilings).
+// nv: the NVFP4 variant (128-row tiles only; null for MXFP8 x MXFP4).
 int run_forward(const moe_shape* s, const uint16_t* x, const moe_weights* wt, const float* topk_w, void* ws,
-                uint16_t* out, cudaStream_t st, bool pdl, void* const* ev = nullptr, bool gathered = false) {
+                uint16_t* out, cudaStream_t st, bool pdl, void* const* ev = nullptr, bool gathered = false,
+                const moe_nvfp4* nv = nullptr) {
     const Dims d = make_dims(*s);
     const Layout L = make_layout(d);
     if (d.T == 0) {
@@ -192,7 +194,17 @@ int run_forward(const moe_shape* s, const uint16_t* x, const moe_weights* wt, co
     gp.B = d.B;
     gp.Et = d.Et;
     gp.xsf_tile_bytes = L.xsf_tile_bytes;
-    cudaError_t e = gathered ? cudaSuccess : launch_gather(gp, st, pdl);
+    // NVFP4: scale tiles of 1 KB per 128-K chunk (two 64-K halves)
+    const int xsf_tile = nv ? 2 * L.xsf_tile_bytes : L.xsf_tile_bytes;
+    const int asf_tile = nv ? 2 * L.asf_tile_bytes : L.asf_tile_bytes;
+    cudaError_t e;
+    if (nv) {
+        gp.xsf_tile_bytes = xsf_tile;
+        gp.x_gscale = nv->x_gscale;
+        e = launch_gather_nvfp4(gp, st, pdl);
+    } else {
+        e = gathered ? cudaSuccess : launch_gather(gp, st, pdl);
+    }
     if (e != cudaSuccess || !rec(ev, 3, st)) return MOE_ERR_CUDA;
 
     // Tile-major packed weights viewed as rows of 128 E2M1 codes (64 bytes):
@@ -202,13 +214,29 @@ int run_forward(const moe_shape* s, const uint16_t* x, const moe_weights* wt, co
     // gathers its x rows itself).
     CUtensorMap mw1, mw2, mx, mact, my;
     const uint64_t Et = static_cast<uint64_t>(d.Et);
-    if (!make_map(&mw1, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, wt->w1, 128, Et * 2 * d.I * (d.H / 128),
-                  kFp4BytesPer128Row, 128, 256) ||
-        !make_map(&mw2, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, wt->w2, 128, Et * d.H * (d.I / 128),
-                  kFp4BytesPer128Row, 128, 256) ||
-        !make_map(&mact, CU_TENSOR_MAP_DATA_TYPE_UINT8, at<uint8_t>(ws, L.act), d.I, d.rows_alloc, d.I, 128, d.B))
+    if (nv) {
+        // NVFP4: packed E2M1 rows of 64 bytes (128 K) with 64-byte swizzle, in
+        // the weights (tile-major as for MXFP4), x and the intermediate
+        constexpr CUtensorMapSwizzle kSw64 = CU_TENSOR_MAP_SWIZZLE_64B;
+        if (!make_map(&mw1, CU_TENSOR_MAP_DATA_TYPE_UINT8, wt->w1, 64, Et * 2 * d.I * (d.H / 128), 64, 64, 256,
+                      kSw64) ||
+            !make_map(&mw2, CU_TENSOR_MAP_DATA_TYPE_UINT8, wt->w2, 64, Et * d.H * (d.I / 128), 64, 64, 256, kSw64) ||
+            !make_map(&mact, CU_TENSOR_MAP_DATA_TYPE_UINT8, at<uint8_t>(ws, L.act), d.I / 2, d.rows_alloc, d.I / 2,
+                      64, d.B, kSw64) ||
+            !make_map(&mx, CU_TENSOR_MAP_DATA_TYPE_UINT8, at<uint8_t>(ws, L.xq), d.H / 2, d.rows_alloc, d.H / 2, 64,
+                      d.B, kSw64))
+            return MOE_ERR_CUDA;
+    } else if (!make_map(&mw1, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, wt->w1, 128, Et * 2 * d.I * (d.H / 128),
+                         kFp4BytesPer128Row, 128, 256) ||
+               !make_map(&mw2, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, wt->w2, 128, Et * d.H * (d.I / 128),
+                         kFp4BytesPer128Row, 128, 256) ||
+               !make_map(&mact, CU_TENSOR_MAP_DATA_TYPE_UINT8, at<uint8_t>(ws, L.act), d.I, d.rows_alloc, d.I, 128,
+                         d.B)) {
         return MOE_ERR_CUDA;
-    if (L.x_token_order) {
+    }
+    if (nv) {
+        // x map made above
+    } else if (L.x_token_order) {
         mx = mact;  // decode FC1 gathers its token rows with cp.async; the map is not read
     } else if (!make_map(&mx, CU_TENSOR_MAP_DATA_TYPE_UINT8, at<uint8_t>(ws, L.xq), d.H, d.rows_alloc, d.H, 128, d.B)) {
         return MOE_ERR_CUDA;
@@ -236,7 +264,7 @@ int run_forward(const moe_shape* s, const uint16_t* x, const moe_weights* wt, co
     g.y_bf16 = L.y_bf16 ? at<uint16_t>(ws, L.y) : nullptr;
     g.H = d.H;
     g.I = d.I;
-    g.out_sf_tile_bytes = L.asf_tile_bytes;
+    g.out_sf_tile_bytes = asf_tile;
     g.a_tx_bytes = 256 * kFp4BytesPer128Row;
     g.wait_ns = kWaitLimitNs;
     g.act_kind = s->activation;
@@ -249,17 +277,27 @@ int run_forward(const moe_shape* s, const uint16_t* x, const moe_weights* wt, co
     g.test_stall_ns = g_test_stall_ns.load();
     g.acc = at<float>(ws, L.acc);
     g.T = d.T;
+    if (nv) {
+        g.nv = 1;
+        g.nv_w_gs = nv->w1_gscale;
+        g.nv_in_gs = nv->x_gscale;
+        g.nv_out_gs = nv->h_gscale;
+    }
 
     g.a_sf = wt->w1_sf;
     g.b_sf = L.x_token_order ? nullptr : at<uint8_t>(ws, L.xsf);
-    g.b_sf_tile_bytes = L.x_token_order ? 0 : L.xsf_tile_bytes;
+    g.b_sf_tile_bytes = L.x_token_order ? 0 : xsf_tile;
     e = launch_gemm(true, mw1, mx, my, g, d.B, nsm, st, pdl);
     if (e != cudaSuccess || !rec(ev, 4, st)) return MOE_ERR_CUDA;
 
     g.test_stall_ns = 0;  // the hook stalls FC1 only
+    if (nv) {
+        g.nv_w_gs = nv->w2_gscale;
+        g.nv_in_gs = nv->h_gscale;
+    }
     g.a_sf = wt->w2_sf;
     g.b_sf = at<uint8_t>(ws, L.asf);
-    g.b_sf_tile_bytes = L.asf_tile_bytes;
+    g.b_sf_tile_bytes = asf_tile;
     e = launch_gemm(false, mw2, mact, my, g, d.B, nsm, st, pdl);
     if (e != cudaSuccess || !rec(ev, 5, st)) return MOE_ERR_CUDA;
 
@@ -404,6 +442,74 @@ int moe_layer(const moe_shape* s, const float* logits, const uint16_t* shared_lo
     bool gathered = false;
     if ((rc = run_route_sort(s, logits, shared_logit, topk_ids, topk_w, ws, st, nullptr, false, x, &gathered))) return rc;
     return run_forward(s, x, w, topk_w, ws, out, st, true, nullptr, gathered);
+}
+
+int moe_quantize_nvfp4(const float* w, int64_t experts, int64_t rows, int64_t K, float* gscale, uint8_t* codes,
+                       uint8_t* scales, moe_stream_t stream) {
+    if (!w || !gscale || !codes || !scales) return MOE_ERR_NULL;
+    if (experts <= 0 || rows <= 0 || K <= 0 || K % 16) return MOE_ERR_SHAPE;
+    if (!aligned(w, 16) || !aligned(codes, 8)) return MOE_ERR_ALIGN;
+    NvQuantParams p{w, gscale, codes, scales, experts, rows, K};
+    return cuda_rc(launch_quantize_nvfp4(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int moe_pack_weights_nvfp4(const uint8_t* codes, const uint8_t* scales, int64_t experts, int64_t N, int64_t K,
+                           int32_t pair_halves, uint8_t* packed_codes, uint8_t* packed_scales, moe_stream_t stream) {
+    if (!codes || !scales || !packed_codes || !packed_scales) return MOE_ERR_NULL;
+    if (experts <= 0 || N <= 0 || K <= 0 || K % 128 || N % 256) return MOE_ERR_SHAPE;
+    if (!aligned(codes, 16) || !aligned(packed_codes, 16)) return MOE_ERR_ALIGN;
+    PackParams p{codes, scales, packed_codes, packed_scales, experts, N, K, pair_halves ? 1 : 0};
+    return cuda_rc(launch_pack_weights_nvfp4(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+namespace {
+int check_nvfp4(const moe_shape* s, const moe_nvfp4* nv) {
+    if (!nv || !nv->w1_gscale || !nv->w2_gscale) return MOE_ERR_NULL;
+    if (s->block_n != 128) return MOE_ERR_SHAPE;
+    const auto positive = [](float c) { return c > 0.f && c <= 3.0e38f; };
+    if (!positive(nv->x_gscale) || !positive(nv->h_gscale)) return MOE_ERR_SHAPE;
+    if (!aligned(nv->w1_gscale, 4) || !aligned(nv->w2_gscale, 4)) return MOE_ERR_ALIGN;
+    return MOE_OK;
+}
+}  // namespace
+
+int moe_layer_nvfp4(const moe_shape* s, const moe_nvfp4* nv, const float* logits, const uint16_t* shared_logit,
+                    const uint16_t* x, const moe_weights* w, int32_t* topk_ids, float* topk_w, void* ws,
+                    size_t ws_bytes, uint16_t* out, moe_stream_t stream) {
+    int rc = check_shape(s);
+    if (rc) return rc;
+    if ((rc = check_nvfp4(s, nv))) return rc;
+    if (s->T > 0 && (!logits || !x || !topk_ids || !topk_w || !out || (s->num_shared > 0 && !shared_logit)))
+        return MOE_ERR_NULL;
+    if (!aligned(x, 16) || !aligned(out, 16)) return MOE_ERR_ALIGN;
+    if ((rc = check_weights(w))) return rc;
+    if ((rc = check_ws(s, ws, ws_bytes))) return rc;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if ((rc = run_route_sort(s, logits, shared_logit, topk_ids, topk_w, ws, st, nullptr, false, nullptr, nullptr)))
+        return rc;
+    return run_forward(s, x, w, topk_w, ws, out, st, true, nullptr, false, nv);
+}
+
+int moe_layer_nvfp4_events(const moe_shape* s, const moe_nvfp4* nv, const float* logits,
+                           const uint16_t* shared_logit, const uint16_t* x, const moe_weights* w, int32_t* topk_ids,
+                           float* topk_w, void* ws, size_t ws_bytes, uint16_t* out, void* const* events,
+                           moe_stream_t stream) {
+    int rc = check_shape(s);
+    if (rc) return rc;
+    if ((rc = check_nvfp4(s, nv))) return rc;
+    if (!events) return MOE_ERR_NULL;
+    for (int i = 0; i < 7; ++i)
+        if (!events[i]) return MOE_ERR_NULL;
+    if (s->T > 0 && (!logits || !x || !topk_ids || !topk_w || !out || (s->num_shared > 0 && !shared_logit)))
+        return MOE_ERR_NULL;
+    if (!aligned(x, 16) || !aligned(out, 16)) return MOE_ERR_ALIGN;
+    if ((rc = check_weights(w))) return rc;
+    if ((rc = check_ws(s, ws, ws_bytes))) return rc;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (!rec(events, 0, st)) return MOE_ERR_CUDA;
+    if ((rc = run_route_sort(s, logits, shared_logit, topk_ids, topk_w, ws, st, events, false, nullptr, nullptr)))
+        return rc;
+    return run_forward(s, x, w, topk_w, ws, out, st, false, events, false, nv);
 }
 
 int moe_router(const moe_shape* s, const uint16_t* x, const uint16_t* wr, float* logits, void* ws, size_t ws_bytes,

@@ -104,10 +104,12 @@ inline Layout make_layout(const Dims& d) {
     // 128-row tiles: expert-row order [rows_alloc, H] with the tile scale
     // layout (TMA boxes).
     L.x_token_order = (d.mode == kModeDecode) ? 1 : 0;
+    // (The NVFP4 variant of the 128-row tiling stores half the code bytes and
+    // twice the scale bytes -- one E4M3 per 16 -- in the same regions.)
     L.xq = take(size_t(L.x_token_order ? d.max_T : d.rows_alloc) * d.H);
-    L.xsf = take(L.x_token_order ? size_t(d.max_T) * (d.H / 32) : size_t(d.V_max) * L.xsf_tile_bytes);
+    L.xsf = take(L.x_token_order ? size_t(d.max_T) * (d.H / 32) : size_t(d.V_max) * L.xsf_tile_bytes * 2);
     L.act = take(size_t(d.rows_alloc) * d.I);
-    L.asf = take(size_t(d.V_max) * L.asf_tile_bytes);
+    L.asf = take(size_t(d.V_max) * L.asf_tile_bytes * (d.mode == kModePrefill ? 2 : 1));
     // bf16 rows carry the TMA tail too: the store map's row extent is
     // rows_alloc (>= 128), so a 32-row box never exceeds it
     L.y = take(size_t(L.y_bf16 ? d.rows_alloc : d.R_max) * d.H * (L.y_bf16 ? 2 : 4));
@@ -156,6 +158,39 @@ __device__ __forceinline__ uint16_t e4m3x2(float v0, float v1) {
 // Two fp32 -> two E2M1 codes (RNE, saturating); v0 in the low nibble.
 __device__ __forceinline__ uint8_t e2m1x2(float v0, float v1) {
     return static_cast<uint8_t>(__nv_cvt_float2_to_fp4x2(make_float2(v0, v1), __NV_E2M1, cudaRoundNearest));
+}
+
+// A non-negative finite E4M3 code to fp32, exactly: subnormals m * 2^-9,
+// normals (1 + m / 8) * 2^(e - 7).
+__device__ __forceinline__ float e4m3_pos_to_float(uint32_t c) {
+    const uint32_t e = (c >> 3) & 15, m = c & 7;
+    return e == 0 ? static_cast<float>(m) * 0.001953125f : __uint_as_float(((e + 120) << 23) | (m << 20));
+}
+
+// NVFP4 ("[SGLang] CUTLASS MoE", section 6): one block of 16 fp32 values with
+// global scale gs -> the E4M3 block scale code (returned) and the 16 E2M1
+// codes, element 2i in the low nibble of byte i (w0: elements 0-7, w1: 8-15).
+// Every decision in fp32: s = (amax * gs) / 6 rounded to E4M3 (nearest even,
+// saturating), r = gs / dec(s), codes = E2M1(v_i * r) (nearest even,
+// saturating; r = 0 when the scale underflows, giving signed zeros).
+__device__ __forceinline__ uint32_t nvfp4_block(const float* v, float gs, uint32_t& w0, uint32_t& w1) {
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    const float s = __fdiv_rn(__fmul_rn(amax, gs), 6.0f);
+    const uint32_t sf = __nv_cvt_float2_to_fp8x2(make_float2(s, 0.f), __NV_SATFINITE, __NV_E4M3) & 0xFFu;
+    const float d = e4m3_pos_to_float(sf);
+    const float r = d > 0.f ? __fdiv_rn(gs, d) : 0.f;
+    uint32_t w[2] = {0u, 0u};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t b = static_cast<uint32_t>(__nv_cvt_float2_to_fp4x2(
+            make_float2(__fmul_rn(v[2 * i], r), __fmul_rn(v[2 * i + 1], r)), __NV_E2M1, cudaRoundNearest));
+        w[i >> 2] |= b << (8 * (i & 3));
+    }
+    w0 = w[0];
+    w1 = w[1];
+    return sf;
 }
 
 __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {

@@ -66,6 +66,10 @@ constexpr int kStagesDecFc2 = MOE_STAGES_DEC_FC2;
 
 constexpr int kStagesPreFc1 = MOE_STAGES_PRE_FC1;
 constexpr int kStagesPreFc2 = MOE_STAGES_PRE_FC2;
+// NVFP4 (128-row tiles): a 128-K stage is 8 KB of tokens, 16 KB of packed
+// weights and 3 KB of scales, so the rings are deeper in the same memory.
+constexpr int kStagesNvFc1 = 7;
+constexpr int kStagesNvFc2 = 5;
 
 constexpr int kWarps = 11;
 constexpr int kThreads = kWarps * 32;
@@ -78,11 +82,18 @@ constexpr int kTokenWarp = 10;    // token tiles and token scales
 // and the weight tiles -- bytes whose accumulator lanes are never read),
 // then the weight tiles (32 KiB per stage: 256 rows x 128 E2M1 codes in
 // 16-byte chunks), then each stage's scales (1 KiB weight + 512 B token).
-template <int TM, int STAGES, bool STAGE_Y>
+// NV: the NVFP4 variant -- packed E2M1 rows of 64 bytes (128 K) in both
+// operands, 64-byte swizzle, scales per 16 K (3 KB per stage: 2 KB weights,
+// 1 KB tokens; 24 TMEM columns: 4 + 4 token, 8 + 8 weight, one set per 64-K
+// MMA).
+template <int TM, int STAGES, bool STAGE_Y, bool NV = false>
 struct Cfg {
-    static constexpr int kXTile = TM * 128;            // bytes of the loaded token rows
-    static constexpr int kWTile = 256 * 128;           // 256 weight rows x 128 K
-    static constexpr int kSfStage = 1536;
+    static constexpr int kRow = NV ? 64 : 128;         // shared-memory bytes of one 128-K row
+    static constexpr int kXTile = TM * kRow;           // bytes of the loaded token rows
+    static constexpr int kWTile = 256 * kRow;          // 256 weight rows x 128 K
+    static constexpr int kSfStage = NV ? 3072 : 1536;
+    static constexpr int kSfW = NV ? 2048 : 1024;      // weight scales per stage
+    static constexpr int kSfX = NV ? 1024 : 512;       // token scales per stage
     static constexpr int kOffX = 0;
     static constexpr int kOffW = STAGES * kXTile;      // 1024-byte aligned: TM * 128 is
     static constexpr int kOffSF = kOffW + STAGES * kWTile;
@@ -93,17 +104,18 @@ struct Cfg {
     static constexpr int kOffBar = kOffEpi + kEpiBytes;
     static constexpr int kSmemBytes = kOffBar + (2 * STAGES + 6) * 8 + 16 + 1024;
     static constexpr int kAccCols = 256;
-    static constexpr int kSfCols = 16;                  // per stage: 4 token-scale + 8 weight-scale columns
+    static constexpr int kSfCols = NV ? 24 : 16;        // per stage: token-scale + weight-scale columns
     static constexpr int kTmemCols = 512;
     static constexpr int kEpiWarps = TM <= 32 ? 2 : 8;  // warps holding token lanes
-    static_assert(kOffX + STAGES * kXTile + 128 * 128 <= kOffSF, "a 128-row read of the last token slot stays inside");
+    static_assert(!NV || TM == 128, "the NVFP4 variant has 128-row tiles");
+    static_assert(kOffX + STAGES * kXTile + 128 * kRow <= kOffSF, "a 128-row read of the last token slot stays inside");
     static_assert(kAccCols + STAGES * kSfCols <= kTmemCols, "TMEM budget");
     static_assert(kSmemBytes <= 232448, "shared memory budget");
     static_assert(TM == 16 || TM == 32 || TM == 128, "token tile rows");
     static __device__ __forceinline__ int x_off(int s) { return kOffX + s * kXTile; }
     static __device__ __forceinline__ int w_off(int s) { return kOffW + s * kWTile; }
     static __device__ __forceinline__ int sfw_off(int s) { return kOffSF + s * kSfStage; }
-    static __device__ __forceinline__ int sfx_off(int s) { return kOffSF + s * kSfStage + 1024; }
+    static __device__ __forceinline__ int sfx_off(int s) { return kOffSF + s * kSfStage + kSfW; }
 };
 
 __device__ __forceinline__ void record_timeout(const GemmParams& p, volatile int* abort_flag, int site) {
@@ -165,6 +177,13 @@ __device__ __forceinline__ void activation_block(const uint32_t (&g)[32], const 
     for (int c = 0; c < 32; ++c) h[c] = activation<ACT>(__uint_as_float(g[c]), __uint_as_float(u[c]), c0, c1, i0, i1);
 }
 
+// NVFP4: the product's scale 1 / (gs_in * gs_w[e]) of the item's expert (the
+// E2M1 x E2M1 MMA sums e2m1 * e4m3 products; each operand's value is that
+// over its global scale).  0 past the last item.
+__device__ __forceinline__ float nv_alpha(const GemmParams& p, const int4& vi) {
+    return vi.z > 0 ? __frcp_rn(p.nv_in_gs * p.nv_w_gs[vi.x]) : 0.f;
+}
+
 // 32 fp32 -> MXFP8 (E4M3 codes in 8 words, E8M0 code returned).
 __device__ __forceinline__ uint32_t mxfp8_block(const float* v, uint32_t (&w)[8]) {
     float amax = 0.f;
@@ -183,7 +202,7 @@ __device__ __forceinline__ uint32_t mxfp8_block(const float* v, uint32_t (&w)[8]
 
 // ACT: the FC1 activation (MOE_ACT_*), a template parameter so that each
 // epilogue carries only its own arithmetic.
-template <int TM, bool FC1, bool YBF16, int STAGES, int ACT>
+template <int TM, bool FC1, bool YBF16, int STAGES, int ACT, bool NV>
 __global__ void __launch_bounds__(kThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                     const __grid_constant__ CUtensorMap tmY, const GemmParams p) {
@@ -191,7 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // decode FC1: the token producer gathers x rows from the token-order MXFP8
     // rows with cp.async (128-row tiles read expert-ordered rows by TMA)
     constexpr bool kGatherX = FC1 && TM <= 32;
-    using C = Cfg<TM, STAGES, kStageY>;
+    using C = Cfg<TM, STAGES, kStageY, NV>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
@@ -263,7 +282,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             // producer's copies may land before or after.
             uint32_t stage = 0, phase = 0;
             bool ok = true;
-            const uint32_t tx = kGatherX ? 256 * 64 + 1024 : 256 * 64 + C::kXTile + 1536;
+            // global bytes: 256 rows x 64 B of weights (E2M1 either way) plus
+            // the token tile and the scales
+            const uint32_t tx = kGatherX ? 256 * 64 + 1024 : 256 * 64 + C::kXTile + C::kSfStage;
             int4 vq0 = item_desc(p, it0, NB, iend, kNone);
             int4 vq1 = item_desc(p, it0 + g, NB, iend, kNone);
             int4 vq2 = item_desc(p, it0 + 2 * g, NB, iend, kNone);
@@ -283,8 +304,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::mbar_arrive_expect_tx(&full[stage], tx);
                     ptx::tma_load_2d(smem + C::w_off(stage), &tmW, &full[stage], 0,
                                      static_cast<int32_t>((tile0 + kc) * 256));
-                    ptx::bulk_load(smem + C::sfw_off(stage), p.a_sf + static_cast<size_t>(tile0 + kc) * 1024, 1024,
-                                   &full[stage]);
+                    ptx::bulk_load(smem + C::sfw_off(stage), p.a_sf + static_cast<size_t>(tile0 + kc) * C::kSfW,
+                                   C::kSfW, &full[stage]);
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1;
@@ -383,8 +404,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
-                    ptx::tma_load_2d(smem + C::x_off(stage), &tmX, &full[stage], kc * 128, vi.y);
-                    ptx::bulk_load(smem + C::sfx_off(stage), sfx + kc * 512, 512, &full[stage]);
+                    ptx::tma_load_2d(smem + C::x_off(stage), &tmX, &full[stage], kc * C::kRow, vi.y);
+                    ptx::bulk_load(smem + C::sfx_off(stage), sfx + kc * C::kSfX, C::kSfX, &full[stage]);
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1;
@@ -421,15 +442,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // generic proxy): make them visible to the tensor core
                     if constexpr (kGatherX) ptx::fence_proxy_async_smem();
                     const uint32_t sf = tmem + C::kAccCols + stage * C::kSfCols;
-                    ptx::tc_cp_32x128b_warpx4(sf, ptx::sdesc_sf(ptx::smem_u32(smem + C::sfx_off(stage))));
-                    ptx::tc_cp_32x128b_warpx4(sf + 4, ptx::sdesc_sf(ptx::smem_u32(smem + C::sfw_off(stage))));
-                    ptx::tc_cp_32x128b_warpx4(sf + 8, ptx::sdesc_sf(ptx::smem_u32(smem + C::sfw_off(stage) + 512)));
                     const uint32_t xa = ptx::smem_u32(smem + C::x_off(stage));
                     const uint32_t wa = ptx::smem_u32(smem + C::w_off(stage));
+                    if constexpr (NV) {
+                        // two 64-K MMAs; each reads a 32-bit cell of four 16-K
+                        // block scales per row: tokens at sf + 4 kk, weights
+                        // (rows 0-127, 128-255) at sf + 8 + 8 kk
+                        constexpr uint32_t kIdescNv = ptx::idesc_nvf4(128, 256);
+                        const uint32_t sx = ptx::smem_u32(smem + C::sfx_off(stage));
+                        const uint32_t sw = ptx::smem_u32(smem + C::sfw_off(stage));
+                        ptx::tc_cp_32x128b_warpx4(sf, ptx::sdesc_sf(sx));
+                        ptx::tc_cp_32x128b_warpx4(sf + 4, ptx::sdesc_sf(sx + 512));
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        ptx::mma_mxf8f6f4(tmem, ptx::sdesc_sw128(xa + kk * 32), ptx::sdesc_sw128(wa + kk * 32),
-                                          ptx::idesc_with_sf_id(kIdesc, kk, kk), sf, sf + 4, (kc | kk) != 0);
+                        for (int q = 0; q < 4; ++q) ptx::tc_cp_32x128b_warpx4(sf + 8 + 4 * q, ptx::sdesc_sf(sw + 512 * q));
+#pragma unroll
+                        for (int kk = 0; kk < 2; ++kk)
+                            ptx::mma_mxf4nvf4(tmem, ptx::sdesc_sw64(xa + kk * 32), ptx::sdesc_sw64(wa + kk * 32),
+                                              kIdescNv, sf + 4 * kk, sf + 8 + 8 * kk, (kc | kk) != 0);
+                    } else {
+                        ptx::tc_cp_32x128b_warpx4(sf, ptx::sdesc_sf(ptx::smem_u32(smem + C::sfx_off(stage))));
+                        ptx::tc_cp_32x128b_warpx4(sf + 4, ptx::sdesc_sf(ptx::smem_u32(smem + C::sfw_off(stage))));
+                        ptx::tc_cp_32x128b_warpx4(sf + 8,
+                                                  ptx::sdesc_sf(ptx::smem_u32(smem + C::sfw_off(stage) + 512)));
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            ptx::mma_mxf8f6f4(tmem, ptx::sdesc_sw128(xa + kk * 32), ptx::sdesc_sw128(wa + kk * 32),
+                                              ptx::idesc_with_sf_id(kIdesc, kk, kk), sf, sf + 4, (kc | kk) != 0);
+                    }
                     ptx::tc_commit(&empty[stage]);
                     if (++stage == STAGES) {
                         stage = 0;
@@ -465,14 +504,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         int4 vi_nxt = active ? item_desc(p, it0 + g, NB, iend, kNoTile) : kNoTile;
         float w_cur = (!FC1 && i < vi_cur.z) ? p.row_w[vi_cur.y + i] : 0.f;
         int t_cur = (dense && i < vi_cur.z) ? p.a_map[vi_cur.y + i] / p.kp : 0;
+        float a_cur = NV ? nv_alpha(p, vi_cur) : 1.f;
         for (int it = it0; active && it < iend; it += g) {
             const int v = it / NB, nb = it - v * NB;
             const int4 vi = vi_cur;
-            const float w_row = w_cur;
+            // FC2: the row's routing weight, times the NVFP4 product scale
+            const float w_row = NV ? w_cur * a_cur : w_cur;
+            const float alpha = a_cur;
             const int t_row = t_cur;
             const int4 vi_n2 = item_desc(p, it + 2 * g, NB, iend, kNoTile);
             w_cur = (!FC1 && i < vi_nxt.z) ? p.row_w[vi_nxt.y + i] : 0.f;
             t_cur = (dense && i < vi_nxt.z) ? p.a_map[vi_nxt.y + i] / p.kp : 0;
+            if constexpr (NV) a_cur = nv_alpha(p, vi_nxt);
             vi_cur = vi_nxt;
             vi_nxt = vi_n2;
             const int first = vi.y, rows = vi.z;
@@ -562,7 +605,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             } else if (valid) {
                 const int64_t row = first + i;
-                if constexpr (FC1) {
+                if constexpr (FC1 && NV) {
+                    // NVFP4 intermediate: features f0 .. f0 + 63 are the 64-K half
+                    // `half` of 128-feature chunk nb: four blocks of 16, their four
+                    // E4M3 scales one 32-bit cell of the chunk's tile block
+                    const int f0 = nb * 128 + half * 64;
+                    uint32_t cell = 0;
+                    uint32_t wq[8];
+#pragma unroll
+                    for (int b = 0; b < 2; ++b) {
+                        float h[32];
+#pragma unroll
+                        for (int c = 0; c < 32; ++c)
+                            h[c] = activation<ACT>(__uint_as_float(r[b][c]) * alpha, __uint_as_float(r[2 + b][c]) * alpha,
+                                                   p.act_c0, p.act_c1, act_i0, act_i1);
+#pragma unroll
+                        for (int hb = 0; hb < 2; ++hb)
+                            cell |= nvfp4_block(h + 16 * hb, p.nv_out_gs, wq[4 * b + 2 * hb], wq[4 * b + 2 * hb + 1])
+                                    << (8 * (2 * b + hb));
+                    }
+                    uint4* dst = reinterpret_cast<uint4*>(p.act + row * (p.I / 2) + f0 / 2);
+                    dst[0] = make_uint4(wq[0], wq[1], wq[2], wq[3]);
+                    dst[1] = make_uint4(wq[4], wq[5], wq[6], wq[7]);
+                    *reinterpret_cast<uint32_t*>(p.act_sf + static_cast<size_t>(v) * p.out_sf_tile_bytes +
+                                                 nb * 1024 + half * 512 + (i & 31) * 16 + (i >> 5) * 4) = cell;
+                } else if constexpr (FC1) {
                     const int f0 = nb * 128 + half * 64;  // first intermediate feature of this lane
                     uint8_t* sf_tile = p.act_sf + static_cast<size_t>(v) * p.out_sf_tile_bytes + nb * 512 +
                                        (i & 31) * 16 + (i >> 5) * 4 + half * 2;
@@ -639,11 +706,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int TM, bool FC1, bool YBF16, int STAGES, int ACT = MOE_ACT_SWIGLU>
+template <int TM, bool FC1, bool YBF16, int STAGES, int ACT = MOE_ACT_SWIGLU, bool NV = false>
 cudaError_t launch_impl(const CUtensorMap& tmW, const CUtensorMap& tmX, const CUtensorMap& tmY, const GemmParams& p,
                         int grid, cudaStream_t stream, bool pdl) {
-    using C = Cfg<TM, STAGES, !FC1 && YBF16 && TM == 128>;
-    auto kern = moe_gemm_kernel<TM, FC1, YBF16, STAGES, ACT>;
+    using C = Cfg<TM, STAGES, !FC1 && YBF16 && TM == 128, NV>;
+    auto kern = moe_gemm_kernel<TM, FC1, YBF16, STAGES, ACT, NV>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (err != cudaSuccess) return err;
     return launch_kernel(kern, dim3(grid), dim3(kThreads), C::kSmemBytes, stream, pdl, tmW, tmX, tmY, p);
@@ -652,6 +719,7 @@ cudaError_t launch_impl(const CUtensorMap& tmW, const CUtensorMap& tmX, const CU
 template <int ACT>
 cudaError_t launch_fc1(const CUtensorMap& tmW, const CUtensorMap& tmX, const CUtensorMap& tmY, const GemmParams& p,
                        int TM, int grid, cudaStream_t stream, bool pdl) {
+    if (p.nv) return launch_impl<128, true, true, kStagesNvFc1, ACT, true>(tmW, tmX, tmY, p, grid, stream, pdl);
     if (TM == 16) return launch_impl<16, true, false, kStagesDecFc1, ACT>(tmW, tmX, tmY, p, grid, stream, pdl);
     if (TM == 32) return launch_impl<32, true, false, kStagesDecFc1, ACT>(tmW, tmX, tmY, p, grid, stream, pdl);
     return launch_impl<128, true, true, kStagesPreFc1, ACT>(tmW, tmX, tmY, p, grid, stream, pdl);
@@ -666,6 +734,7 @@ cudaError_t launch_gemm(bool fc1, const CUtensorMap& tmW, const CUtensorMap& tmX
         if (p.act_kind == MOE_ACT_SITU) return launch_fc1<MOE_ACT_SITU>(tmW, tmX, tmY, p, TM, grid, stream, pdl);
         return launch_fc1<MOE_ACT_SWIGLU>(tmW, tmX, tmY, p, TM, grid, stream, pdl);
     }
+    if (p.nv) return launch_impl<128, false, true, kStagesNvFc2, MOE_ACT_SWIGLU, true>(tmW, tmX, tmY, p, grid, stream, pdl);
     if (TM == 16) return launch_impl<16, false, false, kStagesDecFc2>(tmW, tmX, tmY, p, grid, stream, pdl);
     if (TM == 32) return launch_impl<32, false, false, kStagesDecFc2>(tmW, tmX, tmY, p, grid, stream, pdl);
     return launch_impl<128, false, true, kStagesPreFc2>(tmW, tmX, tmY, p, grid, stream, pdl);

@@ -78,6 +78,7 @@ struct GatherParams {  // x -> MXFP8 + the routing weight of each expert row
     const int32_t* offsets;
     const int32_t* vbase;
     float* acc;             // dense GEMM2 accumulator [T, H] (zeroed here when the gate chose dense)
+    float x_gscale;         // NVFP4: global scale of x
     int token_order;        // 1: decode tilings (the FC1 kernel gathers the rows)
     int H, T, R_max, max_blocks, kp, B, Et, xsf_tile_bytes;
 };
@@ -110,6 +111,11 @@ struct GemmParams {
     uint64_t test_stall_ns;  // test hook: the MMA thread first waits this long on a barrier nothing arrives on (0: off)
     float* acc;              // dense GEMM2 accumulator [T, H] fp32
     int T;
+    // NVFP4 variant (128-row tiles): operands packed E2M1 with E4M3 scales per 16
+    int nv;
+    const float* nv_w_gs;    // per local expert: global scale of this GEMM's weights
+    float nv_in_gs;          // global scale of this GEMM's token operand (x, or the intermediate)
+    float nv_out_gs;         // FC1: global scale the intermediate is quantised with
 };
 
 struct CombineParams {
@@ -137,6 +143,16 @@ struct QuantParams {
     int64_t rows, K;
 };
 
+// NVFP4 weights: rows of experts x rows_per_expert, each expert with its own
+// global scale.
+struct NvQuantParams {
+    const float* w;
+    float* gscale;   // [experts]
+    uint8_t* codes;  // [rows, K / 2]
+    uint8_t* scales; // [rows, K / 16]
+    int64_t experts, rows_per_expert, K;
+};
+
 struct PackParams {
     const uint8_t* codes;
     const uint8_t* scales;
@@ -157,6 +173,8 @@ int sort_launch_count(int64_t slots);
 cudaError_t launch_route_sort_small(const RouteParams& rp, const SortParams& p, const GatherParams* gp,
                                     cudaStream_t stream, bool pdl);
 cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream, bool pdl);
+// NVFP4 x for 128-row tiles (xsf_tile_bytes: 1024 per 128-K chunk).
+cudaError_t launch_gather_nvfp4(const GatherParams& p, cudaStream_t stream, bool pdl);
 // tmY: bf16 FC2 rows as boxes of 64 columns x 32 rows (read only by the
 // 128-row FC2 tiling; any valid map otherwise).
 cudaError_t launch_gemm(bool fc1, const CUtensorMap& tmW, const CUtensorMap& tmX, const CUtensorMap& tmY,
@@ -168,5 +186,7 @@ cudaError_t launch_router(const CUtensorMap& tmX, const CUtensorMap& tmW, const 
                           cudaStream_t stream, bool pdl);
 cudaError_t launch_quantize_mxfp4(const QuantParams& p, cudaStream_t stream);
 cudaError_t launch_pack_weights(const PackParams& p, cudaStream_t stream);
+cudaError_t launch_quantize_nvfp4(const NvQuantParams& p, cudaStream_t stream);
+cudaError_t launch_pack_weights_nvfp4(const PackParams& p, cudaStream_t stream);
 
 }  // namespace moe

@@ -9,9 +9,13 @@
 //     [46,48) version = 1, [49,52) base offset, [52] LBO mode,
 //     [61,64) layout: 0 none, 2 = 128-byte swizzle.
 //   block-scaled instruction descriptor (32 bit): [4,6) B scale-factor id,
-//     [7,10) A format, [10,13) B format (E4M3 = 0, E2M1 = 5), [13],[14]
-//     negate A/B, [15],[16] A/B MN-major, [17,23) N >> 3,
-//     [23] scale type (1 = UE8M0), [24,29) M >> 4, [29,31) A scale-factor id.
+//     [7,10) A format, [10,13) B format (kind::mxf8f6f4: E4M3 = 0, E2M1 = 5;
+//     kind::mxf4nvf4: E2M1 = 1), [13],[14] negate A/B, [15],[16] A/B
+//     MN-major, [17,23) N >> 3, [23] scale type (0 = UE4M3, 1 = UE8M0),
+//     [24,29) M >> 4, [29,31) A scale-factor id.
+//   swizzle layouts: 128-byte rows (layout 2, 1024-byte atoms) for E4M3 and
+//     the padded E2M1 of kind::mxf8f6f4; 64-byte rows (layout 4, 512-byte
+//     atoms) for the packed E2M1 of kind::mxf4nvf4.
 #pragma once
 #include <cstdint>
 #include <cuda.h>
@@ -194,6 +198,19 @@ __device__ __forceinline__ void mma_mxf8f6f4(uint32_t d_tmem, uint64_t a_desc, u
         : "memory");
 }
 
+// D[tmem] (+)= A(smem) * B(smem)^T with per-16-K E4M3 block scales from TMEM
+// (NVFP4: E2M1 x E2M1, K = 64 per instruction, one 32-bit scale cell of four
+// blocks per row).
+__device__ __forceinline__ void mma_mxf4nvf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n\t}"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+        : "memory");
+}
+
 // D[tmem] (+)= A(smem) * B(smem)^T, bf16 x bf16 -> fp32 (kind::f16).
 __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                         uint32_t accumulate) {
@@ -245,6 +262,17 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
     return d;
 }
 
+// K-major operand tile staged by TMA with 64-byte swizzle (packed FP4 rows of
+// 64 B = 128 elements): 8-row (512 B) swizzle atoms stacked along M/N.
+__device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFF);
+    d |= static_cast<uint64_t>(512 >> 4) << 32;  // stride byte offset: next 8-row group
+    d |= static_cast<uint64_t>(1) << 46;         // descriptor version
+    d |= static_cast<uint64_t>(4) << 61;         // 64-byte swizzle
+    return d;
+}
+
 // Scale-factor block: 32 rows x 16 bytes, contiguous, no swizzle.  Core
 // matrices of 8 rows x 16 B are 128 B apart along the rows.
 __device__ __forceinline__ uint64_t sdesc_sf(uint32_t saddr) {
@@ -256,6 +284,12 @@ __device__ __forceinline__ uint64_t sdesc_sf(uint32_t saddr) {
 }
 
 enum : uint32_t { kFmtE4M3 = 0, kFmtE2M1 = 5 };
+
+// kind::mxf4nvf4 (both operands E2M1, format code 1), E4M3 block scales
+// (scale type bit 23 clear), both operands K-major.
+__host__ __device__ constexpr uint32_t idesc_nvf4(uint32_t M, uint32_t N) {
+    return (1u << 10) | (1u << 7) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
 
 __host__ __device__ constexpr uint32_t idesc_mx(uint32_t a_fmt, uint32_t b_fmt, uint32_t M, uint32_t N) {
     return (b_fmt << 10) | (a_fmt << 7) | ((N >> 3) << 17) | (1u << 23) | ((M >> 4) << 24);

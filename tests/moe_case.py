@@ -59,6 +59,32 @@ def device_weights(cfg: synth.MoeConfig, chunk: int = 64, keep_rowmajor: bool = 
     return wts
 
 
+def device_weights_nvfp4(cfg: synth.MoeConfig, x_gscale: float, h_gscale: float, chunk: int = 64):
+    """NVFP4 weights of all local experts (+shared), generated on the device,
+    quantised (per-expert global scales) and packed by the library:
+    (MoeWeights, MoeNvfp4)."""
+    gids = cfg.global_ids
+    E, H, I = gids.size, cfg.hidden, cfg.inter
+    dev = "cuda"
+    c1 = torch.empty((E, 2 * I, H // 2), dtype=torch.uint8, device=dev)
+    c2 = torch.empty((E, H, I // 2), dtype=torch.uint8, device=dev)
+    s1 = torch.empty((E, 2 * I, H // 16), dtype=torch.uint8, device=dev)
+    s2 = torch.empty((E, H, I // 16), dtype=torch.uint8, device=dev)
+    g1 = torch.empty(E, dtype=torch.float32, device=dev)
+    g2 = torch.empty(E, dtype=torch.float32, device=dev)
+    for c0 in range(0, E, chunk):
+        ids = gids[c0:c0 + chunk]
+        n = ids.size
+        g1[c0:c0 + n], c1[c0:c0 + n], s1[c0:c0 + n] = moe.moe_quantize_nvfp4(synth.w1_device(cfg, ids))
+        g2[c0:c0 + n], c2[c0:c0 + n], s2[c0:c0 + n] = moe.moe_quantize_nvfp4(synth.w2_device(cfg, ids))
+    p1, q1 = moe.moe_pack_weights_nvfp4(c1, s1, True)
+    p2, q2 = moe.moe_pack_weights_nvfp4(c2, s2, False)
+    torch.cuda.synchronize()
+    del c1, c2, s1, s2
+    torch.cuda.empty_cache()
+    return moe.MoeWeights(p1, q1, p2, q2), moe.MoeNvfp4(x_gscale, h_gscale, g1, g2)
+
+
 def device_inputs(cfg: synth.MoeConfig, T: int | None = None):
     T = cfg.T if T is None else T
     x = synth.x_device(cfg, T=T)
@@ -108,6 +134,59 @@ class OracleCase:
                     for e, qe in zip(chunk, q):
                         self._wcache[e] = qe
         return [self._wcache[e] for e in locals_]
+
+    def expert_weights_nvfp4(self, locals_):
+        """Oracle NVFP4 weights (codes, scales, global scale for W1 then W2) of
+        the given local experts (cached; all host cores)."""
+        c = self.cfg
+        cache = self.__dict__.setdefault("_wcache_nv", {})
+        need = [e for e in locals_ if e not in cache]
+
+        def one(chunk):
+            gids = c.global_ids[chunk]
+            f1 = synth.w1_host(c, gids)
+            f2 = synth.w2_host(c, gids)
+            out = []
+            for k in range(len(chunk)):
+                g1, g2 = oracle.nvfp4_global_scale(f1[k]), oracle.nvfp4_global_scale(f2[k])
+                out.append(oracle.quantize_nvfp4(f1[k], g1) + (g1,) + oracle.quantize_nvfp4(f2[k], g2) + (g2,))
+            return out
+
+        if need:
+            chunks = [need[i:i + 4] for i in range(0, len(need), 4)]
+            with concurrent.futures.ThreadPoolExecutor(max_workers=host_threads()) as ex:
+                for chunk, q in zip(chunks, ex.map(one, chunks)):
+                    for e, qe in zip(chunk, q):
+                        cache[e] = qe
+        return [cache[e] for e in locals_]
+
+    def forward_nvfp4(self, tokens, x_gscale: float, h_gscale: float, want_y: bool = False):
+        """The oracle's NVFP4 forward of `tokens` (threaded over tokens)."""
+        c = self.cfg
+        tokens = np.asarray(tokens, np.int32)
+        locs = sorted({self.local_of(int(g)) for t in tokens for g in self.ids[t]} - {-1})
+        ws = self.expert_weights_nvfp4(locs)
+        wmap = np.full(c.E_local + c.num_shared, -1, np.int32)
+        for k, e in enumerate(locs):
+            wmap[e] = k
+        arrs = [np.stack([w[i] for w in ws]) for i in (0, 1, 3, 4)]
+        g1 = np.asarray([w[2] for w in ws], np.float32)
+        g2 = np.asarray([w[5] for w in ws], np.float32)
+
+        def run(part):
+            return oracle.forward_nvfp4(self.x, self.ids, self.w, wmap, arrs[0], arrs[1], g1, arrs[2], arrs[3], g2,
+                                        x_gscale=x_gscale, h_gscale=h_gscale, H=c.hidden, I=c.inter,
+                                        E_global=c.E_global, E_local=c.E_local, expert_offset=c.expert_offset,
+                                        num_shared=c.num_shared, tokens=part, want_act=True, want_xq=True,
+                                        activation=c.activation, act_params=c.act_params, want_y=want_y)
+
+        n = host_threads()
+        parts = [p for p in np.array_split(tokens, min(n, max(1, tokens.size))) if p.size]
+        if len(parts) <= 1:
+            return run(tokens)
+        with concurrent.futures.ThreadPoolExecutor(max_workers=n) as ex:
+            res = list(ex.map(run, parts))
+        return {k: np.concatenate([r[k] for r in res]) for k in res[0]}
 
     def forward(self, tokens, want_y: bool = False):
         """The oracle's forward of `tokens` (rows of the result follow their
