@@ -4,10 +4,11 @@
 // the local slice get -1, ranks in ascending token order).
 //
 // Small slot counts: one CTA of 32 warps; warp w owns a contiguous run of
-// slots.  Large slot counts: the same per-warp passes spread over CTAs of 8
-// warps (4096 slots each) with a one-CTA scan in between.  Two passes
-// over the slots in rounds of 32, each round grouping equal experts with
-// __match_any_sync:
+// slots (the slots' local experts are staged in shared memory first).  Large
+// slot counts: the same per-warp passes spread over CTAs of 8 warps (4096
+// slots each, a warp's 512 ids held in registers) with a one-CTA scan in
+// between.  Two passes over the slots in rounds of 32, each round grouping
+// equal experts with __match_any_sync:
 //   count: the group leader adds the group size to the warp's histogram row;
 //   rank : row = offsets[e] + (slots of e in earlier warps) + (slots of e
 //          earlier in this warp) + (lower lanes of the group this round).
@@ -31,24 +32,78 @@ constexpr int kSortWarps = kSortThreads / 32;
 using rs::local_expert;
 using rs::place_experts;
 
-// Per-warp histogram of the slots [s0, s1) into my_hist (rounds of 32).
-__device__ __forceinline__ void warp_count(const SortParams& p, int s0, int s1, int* my_hist) {
+constexpr int kBigWarps = 8;
+constexpr int kBigWarpSlots = 512;
+constexpr int kBigRounds = kBigWarpSlots / 32;
+
+// The local experts of a warp's kBigWarpSlots slots [s0, s1), round r in
+// e[r] (lane = slot within the round; -1 past s1 or without a local row).
+// All loads are issued before any is used.
+__device__ __forceinline__ void load_experts(const SortParams& p, int s0, int s1, int (&e)[kBigRounds]) {
+    const int lane = threadIdx.x & 31;
+    int id[kBigRounds];
+#pragma unroll
+    for (int r = 0; r < kBigRounds; ++r) {
+        const int s = s0 + 32 * r + lane;
+        id[r] = s < s1 ? p.ids[s] : -1;
+    }
+#pragma unroll
+    for (int r = 0; r < kBigRounds; ++r) e[r] = (s0 + 32 * r + lane < s1) ? local_expert(id[r], p) : -1;
+}
+
+// Per-warp histogram of a warp's slots into my_hist, in rounds of 32: equal
+// experts are grouped with __match_any_sync and the group's leader adds the
+// group size.  Here on experts already in registers.
+__device__ __forceinline__ void warp_count_regs(const int (&e)[kBigRounds], int* my_hist) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int r = 0; r < kBigRounds; ++r) {
+        const uint32_t peers = __match_any_sync(0xffffffffu, e[r]);
+        if (e[r] >= 0 && lane == __ffs(peers) - 1) my_hist[e[r]] += __popc(peers);
+    }
+}
+
+// Ranks of a warp's slots [s0, s1): row = my_base[e] + earlier slots of e in
+// this warp + lower lanes of e in this round; my_base advances in place.
+// Here on experts held in registers (round r in e[r]).
+__device__ __forceinline__ void warp_rank_regs(const SortParams& p, int s0, int s1, const int (&e)[kBigRounds],
+                                               int* my_base) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int r = 0; r < kBigRounds; ++r) {
+        const int s = s0 + 32 * r + lane;
+        const uint32_t peers = __match_any_sync(0xffffffffu, e[r]);
+        if (s < s1) {
+            if (e[r] >= 0) {
+                const int row = my_base[e[r]] + __popc(peers & ptx::lanemask_lt());
+                p.c_map[s] = row;
+                p.a_map[row] = s;
+            } else {
+                p.c_map[s] = -1;
+            }
+        }
+        __syncwarp();
+        if (e[r] >= 0 && lane == __ffs(peers) - 1) my_base[e[r]] += __popc(peers);
+        __syncwarp();
+    }
+}
+
+// The same two passes on the slots' local experts staged in shared memory.
+__device__ __forceinline__ void warp_count_smem(const int* s_e, int s0, int s1, int* my_hist) {
     const int lane = threadIdx.x & 31;
     for (int base = s0; base < s1; base += 32) {
         const int s = base + lane;
-        const int e = (s < s1) ? local_expert(p.ids[s], p) : -1;
+        const int e = s < s1 ? s_e[s] : -1;
         const uint32_t peers = __match_any_sync(0xffffffffu, e);
         if (e >= 0 && lane == __ffs(peers) - 1) my_hist[e] += __popc(peers);
     }
 }
 
-// Ranks of the slots [s0, s1): row = my_base[e] + earlier slots of e in this
-// warp + lower lanes of e in this round.  my_base advances in place.
-__device__ __forceinline__ void warp_rank(const SortParams& p, int s0, int s1, int* my_base) {
+__device__ __forceinline__ void warp_rank_smem(const SortParams& p, const int* s_e, int s0, int s1, int* my_base) {
     const int lane = threadIdx.x & 31;
     for (int base = s0; base < s1; base += 32) {
         const int s = base + lane;
-        const int e = (s < s1) ? local_expert(p.ids[s], p) : -1;
+        const int e = s < s1 ? s_e[s] : -1;
         const uint32_t peers = __match_any_sync(0xffffffffu, e);
         if (s < s1) {
             if (e >= 0) {
@@ -78,12 +133,28 @@ __global__ void __launch_bounds__(kSortThreads, 1) sort_kernel(SortParams p) {
     __syncthreads();
 
     const int n = p.T * p.kp;
+    // every slot's local expert, loaded once (eight loads in flight per
+    // thread) into shared memory; both passes read it from there
+    int* s_e = s_off + p.Et;  // [n]
+    for (int i0 = 0; i0 < n; i0 += 8 * kSortThreads) {
+        int id[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i = i0 + u * kSortThreads + tid;
+            id[u] = i < n ? p.ids[i] : -1;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i = i0 + u * kSortThreads + tid;
+            if (i < n) s_e[i] = local_expert(id[u], p);
+        }
+    }
+    __syncthreads();
     const int per = (((n + kSortWarps - 1) / kSortWarps) + 31) & ~31;
-    const int s0 = warp * per;
+    const int s0 = min(n, warp * per);
     const int s1 = min(n, s0 + per);
     int* my_hist = hist + warp * p.Et;
-
-    warp_count(p, s0, s1, my_hist);
+    warp_count_smem(s_e, s0, s1, my_hist);
     __syncthreads();
 
     // per expert: prefix over warps (in place) and totals
@@ -98,9 +169,10 @@ __global__ void __launch_bounds__(kSortThreads, 1) sort_kernel(SortParams p) {
     place_experts(p, cnt, s_off, s_tot);
     __syncthreads();
     // per-warp bases: expert offset + earlier warps
-    for (int i = tid; i < kSortWarps * p.Et; i += kSortThreads) hist[i] += s_off[i % p.Et];
+    for (int x = tid; x < p.Et; x += kSortThreads)
+        for (int w = 0; w < kSortWarps; ++w) hist[w * p.Et + x] += s_off[x];
     __syncthreads();
-    warp_rank(p, s0, s1, my_hist);
+    warp_rank_smem(p, s_e, s0, s1, my_hist);
     ptx::pdl_launch_dependents();
 }
 
@@ -218,36 +290,7 @@ __global__ void __cluster_dims__(kRouteCtas, 1, 1) __launch_bounds__(kSortThread
 
 // Large slot counts: CTA c owns slots [c * kBigChunk, (c + 1) * kBigChunk),
 // warp w of it the w-th sub-run of kBigWarpSlots.
-constexpr int kBigWarps = 8;
-constexpr int kBigWarpSlots = 512;
 constexpr int kBigChunk = kBigWarps * kBigWarpSlots;
-
-constexpr int kBigRounds = kBigWarpSlots / 32;
-
-// The local experts of a warp's kBigWarpSlots slots [s0, s1), round r in
-// e[r] (lane = slot within the round; -1 past s1 or without a local row).
-// All loads are issued before any is used.
-__device__ __forceinline__ void load_experts(const SortParams& p, int s0, int s1, int (&e)[kBigRounds]) {
-    const int lane = threadIdx.x & 31;
-    int id[kBigRounds];
-#pragma unroll
-    for (int r = 0; r < kBigRounds; ++r) {
-        const int s = s0 + 32 * r + lane;
-        id[r] = s < s1 ? p.ids[s] : -1;
-    }
-#pragma unroll
-    for (int r = 0; r < kBigRounds; ++r) e[r] = (s0 + 32 * r + lane < s1) ? local_expert(id[r], p) : -1;
-}
-
-// warp_count on experts already in registers.
-__device__ __forceinline__ void warp_count_regs(const int (&e)[kBigRounds], int* my_hist) {
-    const int lane = threadIdx.x & 31;
-#pragma unroll
-    for (int r = 0; r < kBigRounds; ++r) {
-        const uint32_t peers = __match_any_sync(0xffffffffu, e[r]);
-        if (e[r] >= 0 && lane == __ffs(peers) - 1) my_hist[e[r]] += __popc(peers);
-    }
-}
 
 // Pass 1: per-CTA expert counts -> cta_hist[c][e].
 __global__ void __launch_bounds__(kBigWarps * 32) sort_count_kernel(SortParams p) {
@@ -322,39 +365,21 @@ __global__ void __launch_bounds__(kBigWarps * 32) sort_rank_kernel(SortParams p)
         }
     }
     __syncthreads();
-    // ranks as in warp_rank, on the experts held in registers
-    const int lane = tid & 31;
-    int* my_base = hist + warp * p.Et;
-#pragma unroll
-    for (int r = 0; r < kBigRounds; ++r) {
-        const int s = s0 + 32 * r + lane;
-        const uint32_t peers = __match_any_sync(0xffffffffu, e[r]);
-        if (s < s1) {
-            if (e[r] >= 0) {
-                const int row = my_base[e[r]] + __popc(peers & ptx::lanemask_lt());
-                p.c_map[s] = row;
-                p.a_map[row] = s;
-            } else {
-                p.c_map[s] = -1;
-            }
-        }
-        __syncwarp();
-        if (e[r] >= 0 && lane == __ffs(peers) - 1) my_base[e[r]] += __popc(peers);
-        __syncwarp();
-    }
+    warp_rank_regs(p, s0, s1, e, hist + warp * p.Et);
     ptx::pdl_launch_dependents();
 }
 
 }  // namespace
 
-size_t sort_smem_bytes(int Et) { return static_cast<size_t>(kSortWarps + 1) * Et * sizeof(int); }
+// per-warp histograms [32][Et], expert offsets [Et] and the slots' experts [n]
+size_t sort_smem_bytes(int Et, int n) { return (static_cast<size_t>(kSortWarps + 1) * Et + n) * sizeof(int); }
 
 int sort_big_ctas(int n) { return (n + kBigChunk - 1) / kBigChunk; }
 
 cudaError_t launch_sort(const SortParams& p, cudaStream_t stream, bool pdl) {
     const int n = p.T * p.kp;
     if (n <= kSortWarps * kBigWarpSlots) {
-        const size_t smem = sort_smem_bytes(p.Et);
+        const size_t smem = sort_smem_bytes(p.Et, n);
         cudaError_t err = cudaFuncSetAttribute(sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                static_cast<int>(smem));
         if (err != cudaSuccess) return err;
