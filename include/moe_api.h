@@ -169,8 +169,10 @@ int moe_layer_nvfp4_events(const moe_shape* shape, const moe_nvfp4* nv, const fl
  *                row-major (the decode FC1 gathers each tile's rows from
  *                here).  x_token_order = 0 (block_n 128): E4M3 [rows_alloc,
  *                H] in expert-row order, row r = MXFP8(x[a_map[r] / k']),
- *                and E8M0 in the tile layout of act_sf (sf_tile_bytes_x per
- *                virtual expert)
+ *                and E8M0 per virtual expert v in sf_tile_bytes_x bytes at
+ *                v * sf_tile_bytes_x, lane-major: tile row i / K-block b at
+ *                ((i % 32) * (H / 128) + b / 4) * 16 + (i / 32) * 4 + b % 4
+ *                (the 16-byte cells of act_sf's layout, chunk-minor)
  *   act          E4M3 [rows_alloc, I]: the FC1 output (the activation
  *                h(gate, up), MXFP8) in expert-row order
  *   act_sf       E8M0 of act in the tile layout: per virtual expert v and

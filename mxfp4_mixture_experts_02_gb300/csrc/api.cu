@@ -57,6 +57,21 @@ bool make_map(CUtensorMap* map, CUtensorMapDataType type, const void* base, uint
     return r == CUDA_SUCCESS;
 }
 
+// Byte tensor [d3][d2][d1][d0], densely packed (strides d0, d0 * d1,
+// d0 * d1 * d2 bytes), no swizzle; boxes of {d0, b1, b2, b3} elements.
+bool make_map_4d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t d3, uint32_t b1,
+                 uint32_t b2, uint32_t b3) {
+    if (!get_encode() || d0 > 256) return false;
+    cuuint64_t dims[4] = {d0, d1, d2, d3};
+    cuuint64_t strides[3] = {d0, d0 * d1, d0 * d1 * d2};
+    cuuint32_t box[4] = {static_cast<cuuint32_t>(d0), b1, b2, b3};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 int num_sms_cached() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -287,7 +302,14 @@ int run_forward(const moe_shape* s, const uint16_t* x, const moe_weights* wt, co
     g.a_sf = wt->w1_sf;
     g.b_sf = L.x_token_order ? nullptr : at<uint8_t>(ws, L.xsf);
     g.b_sf_tile_bytes = L.x_token_order ? 0 : xsf_tile;
-    e = launch_gemm(true, mw1, mx, my, g, d.B, nsm, st, pdl);
+    // MXFP8 x scales at 128-row tiles, lane-major per tile: 16-byte cells
+    // (lane l, chunk kc) at (l * chunks + kc) * 16, viewed as 4-D [tiles][32
+    // lanes][chunks][16 bytes]; a stage reads the box of one chunk
+    CUtensorMap mxs = my;
+    if (!nv && !L.x_token_order &&
+        !make_map_4d(&mxs, at<uint8_t>(ws, L.xsf), 16, d.H / 128, 32, static_cast<uint64_t>(d.V_max), 1, 32, 1))
+        return MOE_ERR_CUDA;
+    e = launch_gemm(true, mw1, mx, mxs, g, d.B, nsm, st, pdl);
     if (e != cudaSuccess || !rec(ev, 4, st)) return MOE_ERR_CUDA;
 
     g.test_stall_ns = 0;  // the hook stalls FC1 only

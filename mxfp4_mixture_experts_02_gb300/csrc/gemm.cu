@@ -201,15 +201,21 @@ __device__ __forceinline__ uint32_t mxfp8_block(const float* v, uint32_t (&w)[8]
 }
 
 // ACT: the FC1 activation (MOE_ACT_*), a template parameter so that each
-// epilogue carries only its own arithmetic.
+// epilogue carries only its own arithmetic.  Tensor maps: tmW the packed
+// weights, tmX the token rows, tmAux the bf16 FC2 rows (TMA stores, 128-row
+// tiling) or, for the MXFP8 FC1 at 128-row tiles, the x scale blocks (one 4-D
+// box per stage, see the token producer).
 template <int TM, bool FC1, bool YBF16, int STAGES, int ACT, bool NV>
 __global__ void __launch_bounds__(kThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                    const __grid_constant__ CUtensorMap tmY, const GemmParams p) {
+                    const __grid_constant__ CUtensorMap tmAux, const GemmParams p) {
     constexpr bool kStageY = !FC1 && YBF16 && TM == 128;
     // decode FC1: the token producer gathers x rows from the token-order MXFP8
     // rows with cp.async (128-row tiles read expert-ordered rows by TMA)
     constexpr bool kGatherX = FC1 && TM <= 32;
+    // MXFP8 FC1 at 128-row tiles: the x scales come by TMA from the lane-major
+    // tile layout the token-major gather writes
+    constexpr bool kXScaleMap = FC1 && TM == 128 && !NV;
     using C = Cfg<TM, STAGES, kStageY, NV>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -239,7 +245,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::fence_mbarrier_init();
     }
     if (warp == kProducerWarp && lane == 0) ptx::tma_prefetch_desc(&tmW);
-    if (warp == kTokenWarp && lane == 0) ptx::tma_prefetch_desc(&tmX);
+    if (warp == kTokenWarp && lane == 0) {
+        ptx::tma_prefetch_desc(&tmX);
+        if constexpr (kXScaleMap) ptx::tma_prefetch_desc(&tmAux);
+    }
     if (warp == kMmaWarp) {
         ptx::tmem_alloc(tmem_slot, C::kTmemCols);
         ptx::tmem_relinquish();
@@ -405,7 +414,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     ptx::tma_load_2d(smem + C::x_off(stage), &tmX, &full[stage], kc * C::kRow, vi.y);
-                    ptx::bulk_load(smem + C::sfx_off(stage), sfx + kc * C::kSfX, C::kSfX, &full[stage]);
+                    if constexpr (kXScaleMap) {
+                        // tile v's x scales are stored lane-major (16-byte cell
+                        // of lane l and chunk kc at (l * chunks + kc) * 16), so
+                        // the gather writes each row's words close together;
+                        // the box {16 B, chunk kc, 32 lanes, tile v} lands as
+                        // the 512-byte block the scale copy reads
+                        ptx::tma_load_4d(smem + C::sfx_off(stage), &tmAux, &full[stage], 0, kc, 0, v);
+                    } else {
+                        ptx::bulk_load(smem + C::sfx_off(stage), sfx + kc * C::kSfX, C::kSfX, &full[stage]);
+                    }
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1;
@@ -586,8 +604,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ptx::fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0) {
-                            ptx::tma_store_2d(&tmY, stg, n0, first + q * 32);
-                            ptx::tma_store_2d(&tmY, stg + 4096, n0 + 64, first + q * 32);
+                            ptx::tma_store_2d(&tmAux, stg, n0, first + q * 32);
+                            ptx::tma_store_2d(&tmAux, stg + 4096, n0 + 64, first + q * 32);
                             ptx::bulk_commit_group();
                         }
                     } else {
@@ -707,37 +725,37 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int TM, bool FC1, bool YBF16, int STAGES, int ACT = MOE_ACT_SWIGLU, bool NV = false>
-cudaError_t launch_impl(const CUtensorMap& tmW, const CUtensorMap& tmX, const CUtensorMap& tmY, const GemmParams& p,
+cudaError_t launch_impl(const CUtensorMap& tmW, const CUtensorMap& tmX, const CUtensorMap& tmAux, const GemmParams& p,
                         int grid, cudaStream_t stream, bool pdl) {
     using C = Cfg<TM, STAGES, !FC1 && YBF16 && TM == 128, NV>;
     auto kern = moe_gemm_kernel<TM, FC1, YBF16, STAGES, ACT, NV>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (err != cudaSuccess) return err;
-    return launch_kernel(kern, dim3(grid), dim3(kThreads), C::kSmemBytes, stream, pdl, tmW, tmX, tmY, p);
+    return launch_kernel(kern, dim3(grid), dim3(kThreads), C::kSmemBytes, stream, pdl, tmW, tmX, tmAux, p);
 }
 
 template <int ACT>
-cudaError_t launch_fc1(const CUtensorMap& tmW, const CUtensorMap& tmX, const CUtensorMap& tmY, const GemmParams& p,
+cudaError_t launch_fc1(const CUtensorMap& tmW, const CUtensorMap& tmX, const CUtensorMap& tmAux, const GemmParams& p,
                        int TM, int grid, cudaStream_t stream, bool pdl) {
-    if (p.nv) return launch_impl<128, true, true, kStagesNvFc1, ACT, true>(tmW, tmX, tmY, p, grid, stream, pdl);
-    if (TM == 16) return launch_impl<16, true, false, kStagesDecFc1, ACT>(tmW, tmX, tmY, p, grid, stream, pdl);
-    if (TM == 32) return launch_impl<32, true, false, kStagesDecFc1, ACT>(tmW, tmX, tmY, p, grid, stream, pdl);
-    return launch_impl<128, true, true, kStagesPreFc1, ACT>(tmW, tmX, tmY, p, grid, stream, pdl);
+    if (p.nv) return launch_impl<128, true, true, kStagesNvFc1, ACT, true>(tmW, tmX, tmAux, p, grid, stream, pdl);
+    if (TM == 16) return launch_impl<16, true, false, kStagesDecFc1, ACT>(tmW, tmX, tmAux, p, grid, stream, pdl);
+    if (TM == 32) return launch_impl<32, true, false, kStagesDecFc1, ACT>(tmW, tmX, tmAux, p, grid, stream, pdl);
+    return launch_impl<128, true, true, kStagesPreFc1, ACT>(tmW, tmX, tmAux, p, grid, stream, pdl);
 }
 
 }  // namespace
 
-cudaError_t launch_gemm(bool fc1, const CUtensorMap& tmW, const CUtensorMap& tmX, const CUtensorMap& tmY,
+cudaError_t launch_gemm(bool fc1, const CUtensorMap& tmW, const CUtensorMap& tmX, const CUtensorMap& tmAux,
                         const GemmParams& p, int TM, int grid, cudaStream_t stream, bool pdl) {
     if (fc1) {
-        if (p.act_kind == MOE_ACT_SWIGLU_CLAMP) return launch_fc1<MOE_ACT_SWIGLU_CLAMP>(tmW, tmX, tmY, p, TM, grid, stream, pdl);
-        if (p.act_kind == MOE_ACT_SITU) return launch_fc1<MOE_ACT_SITU>(tmW, tmX, tmY, p, TM, grid, stream, pdl);
-        return launch_fc1<MOE_ACT_SWIGLU>(tmW, tmX, tmY, p, TM, grid, stream, pdl);
+        if (p.act_kind == MOE_ACT_SWIGLU_CLAMP) return launch_fc1<MOE_ACT_SWIGLU_CLAMP>(tmW, tmX, tmAux, p, TM, grid, stream, pdl);
+        if (p.act_kind == MOE_ACT_SITU) return launch_fc1<MOE_ACT_SITU>(tmW, tmX, tmAux, p, TM, grid, stream, pdl);
+        return launch_fc1<MOE_ACT_SWIGLU>(tmW, tmX, tmAux, p, TM, grid, stream, pdl);
     }
-    if (p.nv) return launch_impl<128, false, true, kStagesNvFc2, MOE_ACT_SWIGLU, true>(tmW, tmX, tmY, p, grid, stream, pdl);
-    if (TM == 16) return launch_impl<16, false, false, kStagesDecFc2>(tmW, tmX, tmY, p, grid, stream, pdl);
-    if (TM == 32) return launch_impl<32, false, false, kStagesDecFc2>(tmW, tmX, tmY, p, grid, stream, pdl);
-    return launch_impl<128, false, true, kStagesPreFc2>(tmW, tmX, tmY, p, grid, stream, pdl);
+    if (p.nv) return launch_impl<128, false, true, kStagesNvFc2, MOE_ACT_SWIGLU, true>(tmW, tmX, tmAux, p, grid, stream, pdl);
+    if (TM == 16) return launch_impl<16, false, false, kStagesDecFc2>(tmW, tmX, tmAux, p, grid, stream, pdl);
+    if (TM == 32) return launch_impl<32, false, false, kStagesDecFc2>(tmW, tmX, tmAux, p, grid, stream, pdl);
+    return launch_impl<128, false, true, kStagesPreFc2>(tmW, tmX, tmAux, p, grid, stream, pdl);
 }
 
 }  // namespace moe

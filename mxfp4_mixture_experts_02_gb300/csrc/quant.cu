@@ -78,10 +78,13 @@ __global__ void __launch_bounds__(kGatherThreads) quant_x_kernel(GatherParams p)
 // Lane l holds the 16-element half-blocks l, l + 32, ... of each 4096-column
 // slab (lanes 2k, 2k+1 share MX block k: one shuffle gives the block amax),
 // so each store instruction writes 512 contiguous bytes; the four K-block
-// scales of 128-K chunk kc form one word, stored by lane kc at word
-// kc * 128 + (i % 32) * 4 + i / 32 of the tile's scale blocks (tile v, tile
-// row i).  Each x row is read once, so the pass costs the x read plus the
-// expert-ordered write.  A row's expert is the last one whose first row is
+// scales of 128-K chunk kc form one word, stored by lane kc.  The tile scales
+// are lane-major: tile row i's word of chunk kc sits at word
+// ((i % 32) * chunks + kc) * 4 + i / 32 of tile v's block, so one store
+// instruction puts a row's words into 448 bytes (4 lines at H 3584) instead
+// of one line per chunk; the FC1 token producer picks a chunk's 512-byte
+// block out of it with a 4-D TMA box.  Each x row is read once, so the pass
+// costs the x read plus the expert-ordered write.  A row's expert is the last one whose first row is
 // <= it (binary search over the offsets, cached in shared memory); its tile
 // is vbase[e] + (row - off) / B.
 constexpr int kTokWarps = 8;
@@ -172,6 +175,7 @@ __global__ void __launch_bounds__(kTokWarps * 32) gather_token_kernel(GatherPara
                 __syncwarp();
                 const int kc = h0 / 8 + lane;  // this lane's 128-K chunk
                 const bool has_sf = 8 * kc < nh;
+                const int chunks = nh / 8;
                 const uint32_t sfw = has_sf ? s_exp[warp][lane] : 0u;
                 __syncwarp();  // s_exp is rewritten by the next slab
                 for (int jj = 0; jj < nj; ++jj) {
@@ -188,7 +192,7 @@ __global__ void __launch_bounds__(kTokWarps * 32) gather_token_kernel(GatherPara
                     if (has_sf) {
                         uint32_t* sf_tile =
                             reinterpret_cast<uint32_t*>(p.xsf + static_cast<size_t>(rv) * p.xsf_tile_bytes);
-                        sf_tile[kc * 128 + (ri & 31) * 4 + (ri >> 5)] = sfw;
+                        sf_tile[((ri & 31) * chunks + kc) * 4 + (ri >> 5)] = sfw;
                     }
                 }
             }

@@ -93,6 +93,19 @@ def device_inputs(cfg: synth.MoeConfig, T: int | None = None):
     return x, logits, sl
 
 
+# Oracle-quantised expert weights, shared by the cases of one weight set
+# (seed and shapes); one set per format is held at a time.
+_ORACLE_WEIGHTS = {}
+
+
+def _shared_weight_cache(cfg, kind):
+    key = (cfg.seed, cfg.E_global, cfg.E_local, cfg.expert_offset, cfg.num_shared, cfg.hidden, cfg.inter)
+    held = _ORACLE_WEIGHTS.get(kind)
+    if held is None or held[0] != key:
+        held = _ORACLE_WEIGHTS[kind] = (key, {})
+    return held[1]
+
+
 class OracleCase:
     """The oracle's computation of a config for a subset of tokens."""
 
@@ -105,7 +118,7 @@ class OracleCase:
         self.shared = synth.shared_logit_host(cfg, T=self.T)
         self.ids, self.w = oracle.route(self.logits, cfg.top_k, cfg.num_shared, self.shared, cfg.shared_scale)
         self.sort = oracle.sort(self.ids, cfg.E_global, cfg.E_local, cfg.expert_offset, cfg.num_shared, cfg.block_n)
-        self._wcache = {}
+        self._wcache = _shared_weight_cache(cfg, "mxfp4")
 
     def local_of(self, gid):
         c = self.cfg
@@ -139,7 +152,9 @@ class OracleCase:
         """Oracle NVFP4 weights (codes, scales, global scale for W1 then W2) of
         the given local experts (cached; all host cores)."""
         c = self.cfg
-        cache = self.__dict__.setdefault("_wcache_nv", {})
+        if "_wcache_nv" not in self.__dict__:
+            self._wcache_nv = _shared_weight_cache(c, "nvfp4")
+        cache = self._wcache_nv
         need = [e for e in locals_ if e not in cache]
 
         def one(chunk):

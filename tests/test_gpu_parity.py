@@ -88,21 +88,26 @@ def run_layer(cfg, T=None, path=moe.GEMM2_SPLIT):
     return shape, ws, out, ids, w, status
 
 
-def tile_scale_index(B, K):
+def tile_scale_index(B, K, lane_major=False):
     """Byte offset inside a virtual expert's tile scale block of tile row i and
-    K-block b: per 128-K chunk a 512-byte block, (i % 32) * 16 + (i / 32) * 4 + b % 4."""
+    K-block b.  Chunk-major (the intermediate's act_sf): per 128-K chunk a
+    512-byte block, (i % 32) * 16 + (i / 32) * 4 + b % 4.  Lane-major (x at
+    128-row tiles): the same 16-byte cells ordered by lane, then chunk:
+    ((i % 32) * (K / 128) + b / 4) * 16 + (i / 32) * 4 + b % 4."""
     i = np.arange(B)[:, None]
     b = np.arange(K // 32)[None, :]
+    if lane_major:
+        return ((i % 32) * (K // 128) + b // 4) * 16 + (i // 32) * 4 + (b % 4)
     return (b // 4) * 512 + (i % 32) * 16 + (i // 32) * 4 + (b % 4)
 
 
-def tile_scales_of_rows(sf_view, vinfo, num_v, K, rows):
+def tile_scales_of_rows(sf_view, vinfo, num_v, K, rows, lane_major=False):
     """E8M0 scales [len(rows), K/32] of the given expert rows, read from the
     tile layout (only the virtual experts holding those rows leave the GPU)."""
     rows = np.asarray(rows, np.int64)
     firsts = vinfo[:num_v, 1].astype(np.int64)
     vs = np.searchsorted(firsts, rows, side="right") - 1  # first rows ascend with v
-    idx = tile_scale_index(128, K)  # a tile has at most 128 rows
+    idx = tile_scale_index(128, K, lane_major)  # a tile has at most 128 rows
     blocks = sf_view[torch.from_numpy(vs).to(sf_view.device)].cpu().numpy()
     i = rows - firsts[vs]
     return blocks[np.arange(rows.size)[:, None], idx[i]]
@@ -200,7 +205,7 @@ def check_layer(cfg, tokens=None, y_rows=True):
     elif rows.size:  # x -> MXFP8 in expert-row order: bit-exact
         ks = np.array([k for k, _, _ in slots])
         np.testing.assert_array_equal(v["xq"][rows_t].cpu().numpy(), ref["xq"][ks])
-        np.testing.assert_array_equal(tile_scales_of_rows(v["xq_sf"], vinfo, num_v, cfg.hidden, rows),
+        np.testing.assert_array_equal(tile_scales_of_rows(v["xq_sf"], vinfo, num_v, cfg.hidden, rows, True),
                                       ref["xq_sf"][ks])
     n_act, n_diff, y_worst, n_y = 0, 0, 0.0, 0
     for m, (k, j, row) in enumerate(slots):
@@ -229,6 +234,17 @@ def check_layer(cfg, tokens=None, y_rows=True):
 @pytest.mark.parametrize("cfg", GRID, ids=_cid)
 def test_layer_grid_vs_oracle(cfg):
     check_layer(cfg)
+
+
+# The decode verification points of the shape-template page ("correctness":
+# T in {1, 7, 48, 96, 256} x BlockN in {16, 32}) on the decode layer's own
+# shape: 896 experts, top-16, H 3584, I 384.  Every token is checked.
+SWEEP = [synth.CONFIGS["decode_t32"].replace(T=T, block_n=B) for T in (1, 7, 48, 96, 256) for B in (16, 32)]
+
+
+@pytest.mark.parametrize("cfg", SWEEP, ids=_cid)
+def test_decode_shape_sweep_vs_oracle(cfg):
+    check_layer(cfg, tokens=np.arange(cfg.T))
 
 
 @pytest.mark.parametrize("cfg", FULL, ids=_cid)
@@ -538,7 +554,8 @@ def test_x_quantiser_edge_values_all_paths(T, block_n, path):
         vinfo = v["vinfo"].cpu().numpy()
         np.testing.assert_array_equal(v["xq"][:R].cpu().numpy(), oq[tok])
         np.testing.assert_array_equal(
-            tile_scales_of_rows(v["xq_sf"], vinfo, int(v["header"][1].item()), cfg.hidden, np.arange(R)), osf[tok])
+            tile_scales_of_rows(v["xq_sf"], vinfo, int(v["header"][1].item()), cfg.hidden, np.arange(R), True),
+            osf[tok])
     # the cases are really there: zero, negative-zero and saturated codes
     assert (oq == 0x80).any() and (oq == 0x7E).any() and (osf == 0).any()
 
