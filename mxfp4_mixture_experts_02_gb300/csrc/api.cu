@@ -302,12 +302,14 @@ int run_forward(const moe_shape* s, const uint16_t* x, const moe_weights* wt, co
     g.a_sf = wt->w1_sf;
     g.b_sf = L.x_token_order ? nullptr : at<uint8_t>(ws, L.xsf);
     g.b_sf_tile_bytes = L.x_token_order ? 0 : xsf_tile;
-    // MXFP8 x scales at 128-row tiles, lane-major per tile: 16-byte cells
-    // (lane l, chunk kc) at (l * chunks + kc) * 16, viewed as 4-D [tiles][32
-    // lanes][chunks][16 bytes]; a stage reads the box of one chunk
+    // x scales at 128-row tiles, lane-major per tile: 16-byte cells (lane l,
+    // chunk kc) at (l * chunks + kc) * 16 (NVFP4: the second 64-K half as
+    // lanes 32..63), viewed as 4-D [tiles][32 or 64 lanes][chunks][16 bytes];
+    // a stage reads the box of one chunk
     CUtensorMap mxs = my;
-    if (!nv && !L.x_token_order &&
-        !make_map_4d(&mxs, at<uint8_t>(ws, L.xsf), 16, d.H / 128, 32, static_cast<uint64_t>(d.V_max), 1, 32, 1))
+    const uint32_t sf_lanes = nv ? 64 : 32;
+    if (!L.x_token_order && !make_map_4d(&mxs, at<uint8_t>(ws, L.xsf), 16, d.H / 128, sf_lanes,
+                                         static_cast<uint64_t>(d.V_max), 1, sf_lanes, 1))
         return MOE_ERR_CUDA;
     e = launch_gemm(true, mw1, mx, mxs, g, d.B, nsm, st, pdl);
     if (e != cudaSuccess || !rec(ev, 4, st)) return MOE_ERR_CUDA;

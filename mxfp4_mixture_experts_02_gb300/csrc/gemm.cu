@@ -213,9 +213,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // decode FC1: the token producer gathers x rows from the token-order MXFP8
     // rows with cp.async (128-row tiles read expert-ordered rows by TMA)
     constexpr bool kGatherX = FC1 && TM <= 32;
-    // MXFP8 FC1 at 128-row tiles: the x scales come by TMA from the lane-major
-    // tile layout the token-major gather writes
-    constexpr bool kXScaleMap = FC1 && TM == 128 && !NV;
+    // FC1 at 128-row tiles: the x scales come by TMA from the lane-major tile
+    // layout the token-major gathers write
+    constexpr bool kXScaleMap = FC1 && TM == 128;
     using C = Cfg<TM, STAGES, kStageY, NV>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -416,10 +416,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::tma_load_2d(smem + C::x_off(stage), &tmX, &full[stage], kc * C::kRow, vi.y);
                     if constexpr (kXScaleMap) {
                         // tile v's x scales are stored lane-major (16-byte cell
-                        // of lane l and chunk kc at (l * chunks + kc) * 16), so
-                        // the gather writes each row's words close together;
-                        // the box {16 B, chunk kc, 32 lanes, tile v} lands as
-                        // the 512-byte block the scale copy reads
+                        // of lane l and chunk kc at (l * chunks + kc) * 16; the
+                        // NVFP4 halves as 32 further lanes), so the gather
+                        // writes each row's words close together; the box
+                        // {16 B, chunk kc, 32 (NVFP4: 64) lanes, tile v} lands
+                        // as the block(s) the scale copies read
                         ptx::tma_load_4d(smem + C::sfx_off(stage), &tmAux, &full[stage], 0, kc, 0, v);
                     } else {
                         ptx::bulk_load(smem + C::sfx_off(stage), sfx + kc * C::kSfX, C::kSfX, &full[stage]);

@@ -176,8 +176,8 @@ cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream, bool pdl);
 // NVFP4 x for 128-row tiles (xsf_tile_bytes: 1024 per 128-K chunk).
 cudaError_t launch_gather_nvfp4(const GatherParams& p, cudaStream_t stream, bool pdl);
 // tmAux: for FC2 at 128-row tiles the bf16 rows as boxes of 64 columns x 32
-// rows; for the MXFP8 FC1 at 128-row tiles the x scale blocks as 4-D boxes
-// {16 bytes, 1 chunk, 32 lanes, 1 tile} over the lane-major tile layout; any
+// rows; for FC1 at 128-row tiles the x scale blocks as 4-D boxes {16 bytes,
+// 1 chunk, 32 lanes (NVFP4: 64), 1 tile} over the lane-major tile layout; any
 // valid map otherwise (not read).
 cudaError_t launch_gemm(bool fc1, const CUtensorMap& tmW, const CUtensorMap& tmX, const CUtensorMap& tmAux,
                         const GemmParams& p, int TM, int grid, cudaStream_t stream, bool pdl);

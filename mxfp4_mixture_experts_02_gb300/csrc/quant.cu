@@ -206,10 +206,12 @@ __global__ void __launch_bounds__(kTokWarps * 32) gather_token_kernel(GatherPara
 // 32, ... of each 4096-column slab: one NVFP4 block each, global scale
 // x_gscale) and writes it to every row its slots occupy: packed E2M1 codes
 // [rows, H / 2] (each store instruction writes 256 contiguous bytes) and the
-// block scales in the tile layout the scale_vec::4X MMA reads -- per virtual
-// expert and 128-K chunk two 512-byte blocks, one per 64-K half; tile row i's
-// 4-byte cell at (i % 32) * 16 + (i / 32) * 4 + half * 512, byte b = the
-// half's 16-element block b.
+// block scales of each virtual expert lane-major: 16-byte cells (64-K half,
+// tile lane l, 128-K chunk kc) at ((half * 32 + l) * chunks + kc) * 16, tile
+// row i's word at (i / 32) * 4 of cell (half, i % 32, kc), byte b = the
+// half's 16-element block b.  A chunk's cells of both halves are the two
+// 512-byte blocks the scale_vec::4X MMA reads, fetched by FC1 as one 4-D
+// TMA box.
 __global__ void __launch_bounds__(kTokWarps * 32) gather_token_nvfp4_kernel(GatherParams p) {
     __shared__ int s_off[kTokMaxExperts + 1];
     __shared__ int s_vb[kTokMaxExperts];
@@ -265,6 +267,7 @@ __global__ void __launch_bounds__(kTokWarps * 32) gather_token_nvfp4_kernel(Gath
                 __syncwarp();
                 const int kc = h0 / 8 + lane;  // this lane's 128-K chunk (8 blocks)
                 const bool has_sf = 8 * kc < nh;
+                const int chunks = nh / 8;
                 const uint32_t sf_lo = has_sf ? s_sf[warp][2 * lane] : 0u;      // blocks 0-3 of the chunk
                 const uint32_t sf_hi = has_sf ? s_sf[warp][2 * lane + 1] : 0u;  // blocks 4-7
                 __syncwarp();  // s_sf is rewritten by the next slab
@@ -280,10 +283,13 @@ __global__ void __launch_bounds__(kTokWarps * 32) gather_token_nvfp4_kernel(Gath
                         if (h < nh) dst[h] = q[m];
                     }
                     if (has_sf) {
-                        uint8_t* tile = p.xsf + static_cast<size_t>(rv) * p.xsf_tile_bytes + kc * 1024 +
-                                        (ri & 31) * 16 + (ri >> 5) * 4;
-                        *reinterpret_cast<uint32_t*>(tile) = sf_lo;
-                        *reinterpret_cast<uint32_t*>(tile + 512) = sf_hi;
+                        // lane-major cells (half, tile lane, chunk): half 0 at
+                        // ((i % 32) * chunks + kc) * 16, half 1 32 * chunks
+                        // cells further
+                        uint32_t* tile = reinterpret_cast<uint32_t*>(p.xsf + static_cast<size_t>(rv) * p.xsf_tile_bytes);
+                        const int w = ((ri & 31) * chunks + kc) * 4 + (ri >> 5);
+                        tile[w] = sf_lo;
+                        tile[w + 32 * chunks * 4] = sf_hi;
                     }
                 }
             }

@@ -87,16 +87,21 @@ def test_weight_quantiser_and_packer_bit_exact():
                                 assert ts[pos] == ss[e, row, kc * 8 + kk * 4 + bb]
 
 
-def nv_scales_of_rows(ws_view, vinfo, num_v, K, rows):
-    """E4M3 scales [len(rows), K/16] of expert rows from the NVFP4 tile layout:
-    per virtual expert and 128-K chunk 1 KiB, 64-K half kk at kk * 512, tile
-    row i's cell at (i % 32) * 16 + (i / 32) * 4, byte = the half's block."""
+def nv_scales_of_rows(ws_view, vinfo, num_v, K, rows, lane_major=False):
+    """E4M3 scales [len(rows), K/16] of expert rows from the NVFP4 tile layout.
+    Chunk-major (the intermediate): per virtual expert and 128-K chunk 1 KiB,
+    64-K half kk at kk * 512, tile row i's cell at (i % 32) * 16 + (i / 32) * 4,
+    byte = the half's block.  Lane-major (x): the same 16-byte cells ordered
+    (half, lane, chunk): cell ((kk * 32 + i % 32) * (K / 128) + chunk) * 16."""
     rows = np.asarray(rows, np.int64)
     firsts = vinfo[:num_v, 1].astype(np.int64)
     vs = np.searchsorted(firsts, rows, side="right") - 1
     i = (rows - firsts[vs])[:, None]
     blk = np.arange(K // 16)[None, :]
-    idx = (blk // 8) * 1024 + ((blk // 4) % 2) * 512 + (i % 32) * 16 + (i // 32) * 4 + (blk % 4)
+    if lane_major:
+        idx = ((((blk // 4) % 2) * 32 + i % 32) * (K // 128) + blk // 8) * 16 + (i // 32) * 4 + (blk % 4)
+    else:
+        idx = (blk // 8) * 1024 + ((blk // 4) % 2) * 512 + (i % 32) * 16 + (i // 32) * 4 + (blk % 4)
     tiles = ws_view[torch.from_numpy(vs).to(ws_view.device)].cpu().numpy()
     return tiles[np.arange(rows.size)[:, None], idx]
 
@@ -148,7 +153,7 @@ def check_layer_nvfp4(cfg, tokens, path=moe.GEMM2_SPLIT):
     ks = np.array([k for k, _, _ in slots])
     # x -> NVFP4 in expert-row order: bit-exact
     np.testing.assert_array_equal(unpack(xq[rt].cpu().numpy()), ref["xq"][ks])
-    np.testing.assert_array_equal(nv_scales_of_rows(xsf, vinfo, s["num_v"], H, rows), ref["xq_sf"][ks])
+    np.testing.assert_array_equal(nv_scales_of_rows(xsf, vinfo, s["num_v"], H, rows, True), ref["xq_sf"][ks])
     # intermediate: decoded values mostly identical, else one E2M1 step apart
     ga_c = unpack(act[rt].cpu().numpy())
     ga_s = nv_scales_of_rows(asf, vinfo, s["num_v"], I, rows)
