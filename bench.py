@@ -97,14 +97,15 @@ def gemm_source_hash():
     return h.hexdigest()[:16]
 
 
-def measured_traffic(workload, kernel):
-    """DRAM bytes per launch from the committed ncu capture of this kernel and
-    workload, or None when the GEMM sources changed since the capture."""
+def measured_traffic(workload, T, kernel):
+    """DRAM bytes per launch from the committed ncu capture of this kernel,
+    workload and token count, or None when there is none or the GEMM sources
+    changed since the capture."""
     p = os.path.join(ROOT, "profiles", "roofline_traffic.json")
     if not os.path.exists(p):
         return None
     rec = json.load(open(p)).get("%s/%s" % (workload, kernel))
-    if not rec or rec.get("gemm_source_hash") != gemm_source_hash():
+    if not rec or rec.get("T") != T or rec.get("gemm_source_hash") != gemm_source_hash():
         return None
     return rec["dram_bytes_per_launch"]
 
@@ -378,7 +379,7 @@ def measure_config(args, cfg, device, stream, flush, sampler, steps, warmup, wor
     if flops / (tpeak * 1e12) > dom_bytes / (hbm * 1e9):
         achieved = flops / dt / 1e12
         roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": tpeak, "unit": "TFLOP/s",
-                "frac": achieved / tpeak, "traffic": measured_traffic(cfg.name, dom),
+                "frac": achieved / tpeak, "traffic": measured_traffic(cfg.name, cfg.T, dom),
                 "peak_kind": ("%s bf16 burst x 6 (mxf4nvf4, FP4-class)" % peak_kind if nvfp4 else
                               "%s bf16 burst x 2 (mxf8f6f4, FP8-class)" % peak_kind),
                 "frac_of_fp4_peak": achieved / (6.0 * bf16), "algorithmic_flops": flops,
@@ -386,7 +387,7 @@ def measure_config(args, cfg, device, stream, flush, sampler, steps, warmup, wor
     else:
         achieved = dom_bytes / dt / 1e9
         roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                "frac": achieved / hbm, "traffic": measured_traffic(cfg.name, dom), "peak_kind": peak_kind,
+                "frac": achieved / hbm, "traffic": measured_traffic(cfg.name, cfg.T, dom), "peak_kind": peak_kind,
                 "algorithmic_bytes": dom_bytes, "algorithmic_flops": flops,
                 "tensor_frac": flops / dt / 1e12 / tpeak}
     sec = ms * 1e-3
