@@ -340,17 +340,13 @@ int moe_layer_events(const moe_shape* shape, const float* logits, const uint16_t
  * the process exits; shapes whose moe_workspace_bytes exceeds 32 MiB are
  * rejected with MOE_ERR_WORKSPACE (decode with T <= 32 at E 896, k 16,
  * H 3584, I 384 fits).  The caller passes inputs and outputs as for
- * moe_layer; the call allocates nothing.  The first call on a device looks up
- * the array's device address (cudaGetSymbolAddress, with that device
- * current), so make that first call before any stream capture.  Every call on
- * a device shares the one array and leaves its contents behind: calls whose
- * executions overlap on the GPU (other streams, other host threads) race and
- * must be serialised by the caller.  Device-side errors are recorded in that
- * array's status word: read it with moe_noalloc_get_status.  The array's
- * device address is looked up again on every call issued outside stream
- * capture (so a device reset that reloads the library's module is picked
- * up); a call issued during capture reuses the address of the last call on
- * that device, so at least one call must precede any capture. */
+ * moe_layer; the call allocates nothing.  Each call looks up the array's
+ * device address (cudaGetSymbolAddress, with the call's device current), so
+ * a device reset that reloads the library's module is picked up.  Every call
+ * on a device shares the one array and leaves its contents behind: calls
+ * whose executions overlap on the GPU (other streams, other host threads)
+ * race and must be serialised by the caller.  Device-side errors are recorded
+ * in that array's status word: read it with moe_noalloc_get_status. */
 int moe_layer_noalloc(const moe_shape* shape, const float* logits, const uint16_t* shared_logit, const uint16_t* x,
                       const moe_weights* weights, int32_t* topk_ids, float* topk_w, uint16_t* out,
                       moe_stream_t stream);

@@ -22,10 +22,10 @@ __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
 
 // Device address of g_static_scratch per device.  In host code the array's
 // name only stands in for the symbol; the kernels need the address that
-// cudaGetSymbolAddress returns with that device current.  Outside stream
-// capture the address is looked up on every call (a device reset that
-// reloads the module moves it); during capture the last address seen on the
-// device is reused, since the lookup itself may have to load the module.
+// cudaGetSymbolAddress returns with that device current.  It is looked up on
+// each call (a device reset that reloads the module moves it), except while
+// the stream is capturing, when the lookup, which may load the module, is
+// skipped and the last address seen on the device is used.
 constexpr int kMaxDevices = 64;
 void* g_scratch_ptr[kMaxDevices] = {};
 std::mutex g_scratch_mu;
