@@ -101,8 +101,11 @@ inline Layout make_layout(const Dims& d) {
     L.y_bf16 = (d.mode == kModeDecode) ? 0 : 1;
     // x in MXFP8.  Decode tilings: token order, codes [max_T, H] and scales
     // [max_T, H / 32] (the FC1 token producer gathers each tile's rows).
-    // 128-row tiles: expert-row order [rows_alloc, H] with the tile scale
-    // layout (TMA boxes).
+    // 128-row tiles: expert-row order [rows_alloc, H] (TMA boxes), scales per
+    // tile in the 16-byte cells of the tile scale layout ordered lane-major,
+    // cell (lane l, chunk kc) at (l * H / 128 + kc) * 16, so the token-major
+    // gather writes a row's words close together and a 4-D TMA box fetches a
+    // chunk's 512-byte block.
     L.x_token_order = (d.mode == kModeDecode) ? 1 : 0;
     // (The NVFP4 variant of the 128-row tiling stores half the code bytes and
     // twice the scale bytes -- one E4M3 per 16 -- in the same regions.)

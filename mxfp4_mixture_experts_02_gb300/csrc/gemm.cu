@@ -285,15 +285,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kProducerWarp) {
         if (lane == 0) {
             // ------------------------------------------------- weight producer
-            // Weight tiles and weight scales need nothing from the preceding
-            // kernel: they stream from the start.  This thread sets each
+            // Weight tiles and weight scales need nothing the immediately
+            // preceding kernel writes: once the work list is read (above)
+            // they stream without griddepcontrol.wait.  This thread sets each
             // stage's expected bytes (weights and tokens); the token
             // producer's copies may land before or after.
             uint32_t stage = 0, phase = 0;
             bool ok = true;
             // global bytes: 256 rows x 64 B of weights (E2M1 either way) plus
-            // the token tile and the scales
-            const uint32_t tx = kGatherX ? 256 * 64 + 1024 : 256 * 64 + C::kXTile + C::kSfStage;
+            // the weight scales, and the token tile and its scales where they
+            // come by TMA (the decode FC1's gathered rows arrive by cp.async)
+            const uint32_t tx = kGatherX ? 256 * 64 + C::kSfW : 256 * 64 + C::kXTile + C::kSfStage;
             int4 vq0 = item_desc(p, it0, NB, iend, kNone);
             int4 vq1 = item_desc(p, it0 + g, NB, iend, kNone);
             int4 vq2 = item_desc(p, it0 + 2 * g, NB, iend, kNone);

@@ -70,7 +70,7 @@ struct GatherParams {  // x -> MXFP8 + the routing weight of each expert row
     const int32_t* header;  // rows R
     const int32_t* a_map;
     uint8_t* xq;            // token order [T, H], or expert-row order [rows_alloc, H]
-    uint8_t* xsf;           // token order [T, H / 32], or the tile scale layout
+    uint8_t* xsf;           // token order [T, H / 32], or per 128-row tile the lane-major scale cells
     const float* topk_w;
     float* row_w;           // routing weight of each row: topk_w[a_map[row]]
     // expert-row order (128-row tiles): slot -> row map and expert placement
