@@ -171,9 +171,23 @@ int run_route_sort(const moe_shape* s, const float* logits, const uint16_t* shar
 
 // gathered: the route + sort launch already quantised x (decode tilings).
 // nv: the NVFP4 variant (128-row tiles only; null for MXFP8 x MXFP4).
+// moe_layer_host at 128-row tiles: the host copies run on a second stream in
+// token chunks, so the x gather of each chunk starts as soon as its rows
+// land and the output of each chunk leaves as soon as it is combined.
+constexpr int kHostChunks = 8;
+
+struct HostPipe {
+    cudaStream_t cs;                      // copy stream
+    cudaEvent_t x_in[kHostChunks];        // chunk c of x has landed (recorded on cs)
+    cudaEvent_t out_ready[kHostChunks];   // chunk c of the output is combined (recorded on the compute stream)
+    uint16_t* out_host;
+};
+
+inline int chunk_begin(int T, int c) { return static_cast<int>(static_cast<int64_t>(T) * c / kHostChunks); }
+
 int run_forward(const moe_shape* s, const uint16_t* x, const moe_weights* wt, const float* topk_w, void* ws,
                 uint16_t* out, cudaStream_t st, bool pdl, void* const* ev = nullptr, bool gathered = false,
-                const moe_nvfp4* nv = nullptr) {
+                const moe_nvfp4* nv = nullptr, const HostPipe* hp = nullptr) {
     const Dims d = make_dims(*s);
     const Layout L = make_layout(d);
     if (d.T == 0) {
@@ -218,7 +232,23 @@ int run_forward(const moe_shape* s, const uint16_t* x, const moe_weights* wt, co
         gp.x_gscale = nv->x_gscale;
         e = launch_gather_nvfp4(gp, st, pdl);
     } else {
-        e = gathered ? cudaSuccess : launch_gather(gp, st, pdl);
+        if (gathered) {
+            e = cudaSuccess;
+        } else if (hp && !L.x_token_order) {
+            // token chunk c after its rows have landed
+            e = cudaSuccess;
+            for (int c = 0; c < kHostChunks && e == cudaSuccess; ++c) {
+                gp.t0 = chunk_begin(d.T, c);
+                gp.T = chunk_begin(d.T, c + 1);
+                if (gp.T == gp.t0) continue;
+                e = cudaStreamWaitEvent(st, hp->x_in[c], 0);
+                if (e == cudaSuccess) e = launch_gather(gp, st, pdl);
+            }
+            gp.t0 = 0;
+            gp.T = d.T;
+        } else {
+            e = launch_gather(gp, st, pdl);
+        }
     }
     if (e != cudaSuccess || !rec(ev, 3, st)) return MOE_ERR_CUDA;
 
@@ -328,7 +358,23 @@ int run_forward(const moe_shape* s, const uint16_t* x, const moe_weights* wt, co
     CombineParams cp{at<int32_t>(ws, L.header), at<float>(ws, L.acc), at<int32_t>(ws, L.c_map),
                      L.y_bf16 ? nullptr : at<float>(ws, L.y),
                      L.y_bf16 ? at<uint16_t>(ws, L.y) : nullptr, out, d.T, d.kp, d.H};
-    e = launch_combine(cp, st, pdl);
+    if (hp) {
+        // token chunk c, then its output rows back to the host on the copy stream
+        e = cudaSuccess;
+        for (int c = 0; c < kHostChunks && e == cudaSuccess; ++c) {
+            cp.t0 = chunk_begin(d.T, c);
+            cp.T = chunk_begin(d.T, c + 1);
+            if (cp.T == cp.t0) continue;
+            e = launch_combine(cp, st, pdl);
+            if (e == cudaSuccess) e = cudaEventRecord(hp->out_ready[c], st);
+            if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->cs, hp->out_ready[c], 0);
+            if (e == cudaSuccess)
+                e = cudaMemcpyAsync(hp->out_host + static_cast<size_t>(cp.t0) * d.H, out + static_cast<size_t>(cp.t0) * d.H,
+                                    static_cast<size_t>(cp.T - cp.t0) * d.H * 2, cudaMemcpyDeviceToHost, hp->cs);
+        }
+    } else {
+        e = launch_combine(cp, st, pdl);
+    }
     if (e != cudaSuccess || !rec(ev, 6, st)) return MOE_ERR_CUDA;
     return MOE_OK;
 }
@@ -583,6 +629,36 @@ int moe_layer_events(const moe_shape* s, const float* logits, const uint16_t* sh
     return run_forward(s, x, w, topk_w, ws, out, st, false, events, gathered);
 }
 
+// The copy stream and events of moe_layer_host's pipelined form, one set per
+// device, created on first use; calls enqueue under the mutex, so each wait
+// refers to the record its own call just made.
+struct HostPipeRes {
+    cudaStream_t cs = nullptr;
+    cudaEvent_t start = nullptr, logits_in = nullptr, done = nullptr;
+    cudaEvent_t x_in[kHostChunks] = {}, out_ready[kHostChunks] = {};
+};
+constexpr int kMaxPipeDevices = 64;
+HostPipeRes g_pipe[kMaxPipeDevices];
+std::mutex g_pipe_mu;
+
+int pipe_resources(HostPipeRes** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxPipeDevices) return MOE_ERR_CUDA;
+    HostPipeRes& r = g_pipe[dev];
+    if (!r.cs) {
+        auto mk = [](cudaEvent_t* e) { return cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess; };
+        bool ok = cudaStreamCreateWithFlags(&r.cs, cudaStreamNonBlocking) == cudaSuccess && mk(&r.start) &&
+                  mk(&r.logits_in) && mk(&r.done);
+        for (int c = 0; ok && c < kHostChunks; ++c) ok = mk(&r.x_in[c]) && mk(&r.out_ready[c]);
+        if (!ok) {
+            r.cs = nullptr;
+            return MOE_ERR_CUDA;
+        }
+    }
+    *out = &r;
+    return MOE_OK;
+}
+
 int moe_layer_host(const moe_shape* s, const float* logits_host, const uint16_t* shared_logit_host,
                    const uint16_t* x_host, const moe_weights* w, void* ws, size_t ws_bytes, uint16_t* out_host,
                    moe_stream_t stream) {
@@ -599,19 +675,55 @@ int moe_layer_host(const moe_shape* s, const float* logits_host, const uint16_t*
     uint16_t* sl = at<uint16_t>(ws, L.st_shared);
     uint16_t* xd = at<uint16_t>(ws, L.st_x);
     uint16_t* od = at<uint16_t>(ws, L.st_out);
+    int32_t* ids = at<int32_t>(ws, L.st_ids);
+    float* tw = at<float>(ws, L.st_w);
+    bool gathered = false;
+    const size_t row_bytes = size_t(d.H) * 2;
+    if (d.mode == kModePrefill && d.T > 0) {
+        // Long batches: logits, then x in token chunks, on the copy stream
+        // (after the caller's stream reaches this call); routing starts when
+        // the logits land, each chunk's gather when its rows land; each
+        // chunk's output leaves when it is combined.  The caller's stream
+        // waits for the last copy.
+        std::lock_guard<std::mutex> lock(g_pipe_mu);
+        HostPipeRes* r = nullptr;
+        if ((rc = pipe_resources(&r))) return rc;
+        HostPipe hp{r->cs, {}, {}, out_host};
+        for (int c = 0; c < kHostChunks; ++c) {
+            hp.x_in[c] = r->x_in[c];
+            hp.out_ready[c] = r->out_ready[c];
+        }
+        bool ok = cudaEventRecord(r->start, st) == cudaSuccess && cudaStreamWaitEvent(r->cs, r->start, 0) == cudaSuccess &&
+                  cudaMemcpyAsync(lg, logits_host, size_t(d.T) * d.Eg * 4, cudaMemcpyHostToDevice, r->cs) ==
+                      cudaSuccess &&
+                  (d.S == 0 || cudaMemcpyAsync(sl, shared_logit_host, size_t(d.T) * d.S * 2, cudaMemcpyHostToDevice,
+                                               r->cs) == cudaSuccess) &&
+                  cudaEventRecord(r->logits_in, r->cs) == cudaSuccess;
+        for (int c = 0; ok && c < kHostChunks; ++c) {
+            const int t0 = chunk_begin(d.T, c), t1 = chunk_begin(d.T, c + 1);
+            if (t1 > t0)
+                ok = cudaMemcpyAsync(xd + size_t(t0) * d.H, x_host + size_t(t0) * d.H, size_t(t1 - t0) * row_bytes,
+                                     cudaMemcpyHostToDevice, r->cs) == cudaSuccess;
+            ok = ok && cudaEventRecord(r->x_in[c], r->cs) == cudaSuccess;
+        }
+        if (!ok || cudaStreamWaitEvent(st, r->logits_in, 0) != cudaSuccess) return MOE_ERR_CUDA;
+        if ((rc = run_route_sort(s, lg, d.S > 0 ? sl : nullptr, ids, tw, ws, st, nullptr, false, nullptr, &gathered)))
+            return rc;
+        if ((rc = run_forward(s, xd, w, tw, ws, od, st, true, nullptr, false, nullptr, &hp))) return rc;
+        if (cudaEventRecord(r->done, r->cs) != cudaSuccess || cudaStreamWaitEvent(st, r->done, 0) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        return MOE_OK;
+    }
     if (cudaMemcpyAsync(lg, logits_host, size_t(d.T) * d.Eg * 4, cudaMemcpyHostToDevice, st) != cudaSuccess)
         return MOE_ERR_CUDA;
     if (d.S > 0 &&
         cudaMemcpyAsync(sl, shared_logit_host, size_t(d.T) * d.S * 2, cudaMemcpyHostToDevice, st) != cudaSuccess)
         return MOE_ERR_CUDA;
-    if (cudaMemcpyAsync(xd, x_host, size_t(d.T) * d.H * 2, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    if (cudaMemcpyAsync(xd, x_host, size_t(d.T) * row_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
         return MOE_ERR_CUDA;
-    int32_t* ids = at<int32_t>(ws, L.st_ids);
-    float* tw = at<float>(ws, L.st_w);
-    bool gathered = false;
     if ((rc = run_route_sort(s, lg, d.S > 0 ? sl : nullptr, ids, tw, ws, st, nullptr, false, xd, &gathered))) return rc;
     if ((rc = run_forward(s, xd, w, tw, ws, od, st, true, nullptr, gathered))) return rc;
-    if (cudaMemcpyAsync(out_host, od, size_t(d.T) * d.H * 2, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    if (cudaMemcpyAsync(out_host, od, size_t(d.T) * row_bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
         return MOE_ERR_CUDA;
     return MOE_OK;
 }

@@ -40,7 +40,7 @@ __device__ __forceinline__ void convert_acc_row8(const CombineParams& p, int t, 
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineParams p) {
     __shared__ int rows[kMaxSlots];
     ptx::pdl_wait();
-    const int t = blockIdx.y;
+    const int t = p.t0 + static_cast<int>(blockIdx.y);
     if (p.header[kHdrGemm2Path] == kPathDense) {
         // this block's 512 columns: 64 groups of 8 on the first 64 threads
         const int c8 = blockIdx.x * (kCombineThreads / 2) + threadIdx.x;
@@ -84,7 +84,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineParams 
 __global__ void __launch_bounds__(kCombineThreads) combine_bf16_kernel(CombineParams p) {
     __shared__ int rows[kMaxSlots];
     ptx::pdl_wait();
-    const int t = blockIdx.y;
+    const int t = p.t0 + static_cast<int>(blockIdx.y);
     if (p.header[kHdrGemm2Path] == kPathDense) {
         const int c8 = blockIdx.x * kCombineThreads + threadIdx.x;  // this block's 1024 columns
         if (c8 < p.H / 8) convert_acc_row8(p, t, c8);
@@ -142,12 +142,12 @@ __global__ void __launch_bounds__(kCombineThreads) combine_bf16_kernel(CombinePa
 }  // namespace
 
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream, bool pdl) {
-    if (p.T == 0) return cudaSuccess;
+    if (p.T <= p.t0) return cudaSuccess;
     if (p.y_bf16) {
-        const dim3 grid((p.H / 8 + kCombineThreads - 1) / kCombineThreads, p.T);
+        const dim3 grid((p.H / 8 + kCombineThreads - 1) / kCombineThreads, p.T - p.t0);
         return launch_kernel(combine_bf16_kernel, grid, dim3(kCombineThreads), 0, stream, pdl, p);
     }
-    const dim3 grid((p.H / 4 + kCombineThreads - 1) / kCombineThreads, p.T);
+    const dim3 grid((p.H / 4 + kCombineThreads - 1) / kCombineThreads, p.T - p.t0);
     return launch_kernel(combine_kernel, grid, dim3(kCombineThreads), 0, stream, pdl, p);
 }
 

@@ -81,6 +81,7 @@ struct GatherParams {  // x -> MXFP8 + the routing weight of each expert row
     float x_gscale;         // NVFP4: global scale of x
     int token_order;        // 1: decode tilings (the FC1 kernel gathers the rows)
     int H, T, R_max, max_blocks, kp, B, Et, xsf_tile_bytes;
+    int t0;                 // token-major gathers: first token (tokens t0 .. T - 1)
 };
 
 struct GemmParams {
@@ -126,6 +127,7 @@ struct CombineParams {
     const uint16_t* y_bf16; // bf16 rows (prefill tiling)
     uint16_t* out;
     int T, kp, H;
+    int t0;  // first token (tokens t0 .. T - 1; 0 for the whole batch)
 };
 
 // The one-warp GEMM2 gate: reads the sort's table and writes the path.

@@ -118,7 +118,7 @@ __global__ void __launch_bounds__(kTokWarps * 32) gather_token_kernel(GatherPara
     // the gate ran before this launch: with the dense GEMM2 path, each token's
     // fp32 accumulator row is zeroed here, before FC2 reduces into it
     const bool zero_acc = p.header[kHdrGemm2Path] == kPathDense;
-    for (int t = blockIdx.x * kTokWarps + warp; t < p.T; t += gridDim.x * kTokWarps) {
+    for (int t = p.t0 + blockIdx.x * kTokWarps + warp; t < p.T; t += gridDim.x * kTokWarps) {
         if (zero_acc) {
             float4* a = reinterpret_cast<float4*>(p.acc + static_cast<int64_t>(t) * p.H);
             for (int c = lane; c < p.H / 4; c += 32) a[c] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -226,7 +226,7 @@ __global__ void __launch_bounds__(kTokWarps * 32) gather_token_nvfp4_kernel(Gath
     uint8_t* sf_bytes = reinterpret_cast<uint8_t*>(s_sf[warp]);
     const int nh = p.H / 16;  // NVFP4 blocks per row
     const bool zero_acc = p.header[kHdrGemm2Path] == kPathDense;
-    for (int t = blockIdx.x * kTokWarps + warp; t < p.T; t += gridDim.x * kTokWarps) {
+    for (int t = p.t0 + blockIdx.x * kTokWarps + warp; t < p.T; t += gridDim.x * kTokWarps) {
         if (zero_acc) {
             float4* a = reinterpret_cast<float4*>(p.acc + static_cast<int64_t>(t) * p.H);
             for (int c = lane; c < p.H / 4; c += 32) a[c] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -465,7 +465,7 @@ cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream, bool pdl) 
         return launch_kernel(quant_x_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kGatherThreads), 0, stream, pdl,
                              p);
     }
-    int64_t blocks = (static_cast<int64_t>(p.T) + kTokWarps - 1) / kTokWarps;
+    int64_t blocks = (static_cast<int64_t>(p.T - p.t0) + kTokWarps - 1) / kTokWarps;
     if (blocks > p.max_blocks) blocks = p.max_blocks;
     if (blocks < 1) blocks = 1;
     return launch_kernel(gather_token_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kTokWarps * 32), 0, stream, pdl,
@@ -473,7 +473,7 @@ cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream, bool pdl) 
 }
 
 cudaError_t launch_gather_nvfp4(const GatherParams& p, cudaStream_t stream, bool pdl) {
-    int64_t blocks = (static_cast<int64_t>(p.T) + kTokWarps - 1) / kTokWarps;
+    int64_t blocks = (static_cast<int64_t>(p.T - p.t0) + kTokWarps - 1) / kTokWarps;
     if (blocks > p.max_blocks) blocks = p.max_blocks;
     if (blocks < 1) blocks = 1;
     return launch_kernel(gather_token_nvfp4_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kTokWarps * 32), 0,

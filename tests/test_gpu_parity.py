@@ -450,8 +450,12 @@ def test_graph_capture_replays_the_chain(split_path):
     assert moe.moe_get_status(ws) == (0, 0)
 
 
-def test_host_buffer_entry_point_matches_device_path(split_path):
-    cfg = GRID[2]
+@pytest.mark.parametrize("cfg", [GRID[2], GRID[6], GRID[9], SMALL.replace(T=5, block_n=128, num_shared=1)],
+                         ids=_cid)
+def test_host_buffer_entry_point_matches_device_path(split_path, cfg):
+    # 128-row tilings take the pipelined form (copies in token chunks on a
+    # second stream, overlapped with the gather and the combine; at T 5 most
+    # chunks are empty); two calls in a row on one workspace reuse its staging
     shape = shape_of(cfg)
     wts = _weights(cfg)
     x, logits, sl = device_inputs(cfg)
@@ -459,11 +463,13 @@ def test_host_buffer_entry_point_matches_device_path(split_path):
     ref, _, _ = moe.moe_layer(shape, logits, sl, x, wts, ws)
     xh, lh = x.cpu().pin_memory(), logits.cpu().pin_memory()
     sh = sl.cpu().pin_memory() if sl is not None else None
-    oh = torch.empty((shape.T, shape.hidden), dtype=torch.bfloat16).pin_memory()
     ws2 = moe.workspace(shape)
-    moe.moe_layer_host(shape, lh, sh, xh, wts, ws2, oh)
-    torch.cuda.synchronize()
-    assert torch.equal(oh.view(torch.int16), ref.cpu().view(torch.int16))
+    for _ in range(2):
+        oh = torch.full((shape.T, shape.hidden), float("nan"), dtype=torch.bfloat16).pin_memory()
+        moe.moe_layer_host(shape, lh, sh, xh, wts, ws2, oh)
+        torch.cuda.synchronize()
+        assert moe.moe_get_status(ws2) == (0, 0)
+        assert torch.equal(oh.view(torch.int16), ref.cpu().view(torch.int16))
 
 
 # ----------------------------------------------------------------- edge values
