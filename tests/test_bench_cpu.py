@@ -46,3 +46,21 @@ def test_clock_sampler_summary_keeps_the_timed_windows():
     assert s["sm_mhz"] == 2055.0 and s["samples"] == 2 and s["sm_max_mhz"] == 2070.0
     assert s["reasons"] == ["sw_power_cap"]
     assert cs.summary([(2.9, 3.1)])["sm_mhz"] == 1000.0
+
+
+def test_recorded_traffic_matches_workload_token_count_and_sources():
+    # the roofline's `traffic` is the committed ncu capture of that kernel and
+    # workload, dropped when the token count differs or the GEMM sources changed
+    sys.path.insert(0, ROOT)
+    import bench
+    rec = json.load(open(os.path.join(ROOT, "profiles", "roofline_traffic.json")))
+    key = "decode_t32/fc1"
+    assert key in rec and rec[key]["T"] == 32
+    got = bench.measured_traffic("decode_t32", 32, "fc1")
+    if rec[key]["gemm_source_hash"] == bench.gemm_source_hash():
+        assert got == rec[key]["dram_bytes_per_launch"]
+    else:
+        assert got is None
+    assert bench.measured_traffic("decode_t32", 31, "fc1") is None
+    assert bench.measured_traffic("decode_t32_T31", 31, "fc1") is None
+    assert bench.measured_traffic("no_such_workload", 32, "fc1") is None
