@@ -116,7 +116,10 @@ __device__ __forceinline__ void warp_count_smem(const int* s_e, int s0, int s1, 
     }
 }
 
-__device__ __forceinline__ void warp_rank_smem(const SortParams& p, const int* s_e, int s0, int s1, int* my_base) {
+// my_base[e]: this warp's first rank inside expert e; e_off[e]: the expert's
+// first row.
+__device__ __forceinline__ void warp_rank_smem(const SortParams& p, const int* s_e, int s0, int s1, int* my_base,
+                                               const int* e_off) {
     const int lane = threadIdx.x & 31;
     for (int base = s0; base < s1; base += 32) {
         const int s = base + lane;
@@ -124,7 +127,7 @@ __device__ __forceinline__ void warp_rank_smem(const SortParams& p, const int* s
         const uint32_t peers = same_expert_lanes(e);
         if (s < s1) {
             if (e >= 0) {
-                const int row = my_base[e] + __popc(peers & ptx::lanemask_lt());
+                const int row = e_off[e] + my_base[e] + __popc(peers & ptx::lanemask_lt());
                 p.c_map[s] = row;
                 p.a_map[row] = s;
             } else {
@@ -174,22 +177,26 @@ __global__ void __launch_bounds__(kSortThreads, 1) sort_kernel(SortParams p) {
     warp_count_smem(s_e, s0, s1, my_hist);
     __syncthreads();
 
-    // per expert: prefix over warps (in place) and totals
+    // per expert: exclusive prefix over the warps (in place), in batches of 8
+    // loads so that they overlap, and the total
     int cnt = 0;
     if (tid < p.Et) {
-        for (int w = 0; w < kSortWarps; ++w) {
-            const int c = hist[w * p.Et + tid];
-            hist[w * p.Et + tid] = cnt;
-            cnt += c;
+#pragma unroll
+        for (int w0 = 0; w0 < kSortWarps; w0 += 8) {
+            int c[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) c[u] = hist[(w0 + u) * p.Et + tid];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                hist[(w0 + u) * p.Et + tid] = cnt;
+                cnt += c[u];
+            }
         }
     }
     place_experts(p, cnt, s_off, s_tot);
     __syncthreads();
-    // per-warp bases: expert offset + earlier warps
-    for (int x = tid; x < p.Et; x += kSortThreads)
-        for (int w = 0; w < kSortWarps; ++w) hist[w * p.Et + x] += s_off[x];
-    __syncthreads();
-    warp_rank_smem(p, s_e, s0, s1, my_hist);
+    // ranks: the expert's first row (s_off) + earlier warps + this warp's
+    warp_rank_smem(p, s_e, s0, s1, my_hist, s_off);
     ptx::pdl_launch_dependents();
 }
 
