@@ -241,12 +241,16 @@ __global__ void __cluster_dims__(kRouteCtas, 1, 1) __launch_bounds__(kSortThread
         rs::route_token(rp, t, s_cand[warp], ids0);
     if (fuse_x) {
         // x -> MXFP8 of this CTA's tokens (rank, rank + 8, ...), one
-        // 32-element block per job, starting at the first warp that routes no
-        // token; token order, row-major scales
+        // 32-element block per job, on the warps that route no token while
+        // the others route (on every warp, after routing, when all route);
+        // token order, row-major scales
         const int nt = (p.T - rank + kRouteCtas - 1) / kRouteCtas;
         const int nb = gp.H / 32;
-        const int q = (tid + kSortThreads - 32 * min(nt, kSortWarps)) % kSortThreads;
-        for (int job = q; job < nt * nb; job += kSortThreads) {
+        const int nr = 32 * min(nt, kSortWarps);  // routing threads
+        const bool all_route = nr == kSortThreads;
+        const int first = all_route ? tid : tid - nr;
+        const int stride = all_route ? kSortThreads : kSortThreads - nr;
+        for (int job = first; first >= 0 && job < nt * nb; job += stride) {
             const int j = job / nb, b = job - j * nb;
             const size_t blk = static_cast<size_t>(rank + kRouteCtas * j) * nb + b;
             const uint4* src = reinterpret_cast<const uint4*>(gp.x) + blk * 4;
@@ -288,14 +292,17 @@ __global__ void __cluster_dims__(kRouteCtas, 1, 1) __launch_bounds__(kSortThread
     }
     __syncthreads();
     int cnt = 0;
-    if (tid < p.Et)
+    if (tid < p.Et) {
+#pragma unroll 8
         for (int w = 0; w < nw; ++w) cnt += __popc(s_mask[w * p.Et + tid]);
+    }
     place_experts(p, cnt, s_off, s_tot);
     __syncthreads();
     if (tid < n) {
         if (e >= 0) {
             const uint32_t* m = s_mask + e;  // word w at m[w * Et]
             int r = __popc(m[(tid >> 5) * p.Et] & ((1u << (tid & 31)) - 1u));
+#pragma unroll 8
             for (int w = 0; w < (tid >> 5); ++w) r += __popc(m[w * p.Et]);
             const int row = s_off[e] + r;
             p.a_map[row] = tid;
@@ -305,10 +312,8 @@ __global__ void __cluster_dims__(kRouteCtas, 1, 1) __launch_bounds__(kSortThread
             p.c_map[tid] = -1;
         }
     }
-    // The GEMM launched next reads the work list (header, virtual experts)
-    // before its griddepcontrol.wait -- its weight stream starts at once --
-    // so the writes are made visible device-wide before the trigger.
-    __threadfence();
+    // The launches that follow read the work list only after their
+    // griddepcontrol.wait (the gate) or after a launch that waited (FC1).
     ptx::pdl_launch_dependents();
 }
 
