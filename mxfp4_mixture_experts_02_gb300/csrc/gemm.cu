@@ -447,11 +447,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = false;
             }
             for (int it = it0; ok && it < iend; it += istep) {
-                if (!wait_or_abort(accempty, aphase ^ 1, p.wait_ns, abort_flag)) {
-                    if (!*abort_flag) record_timeout(p, abort_flag, kSiteMmaAccEmpty);
-                    break;
+                // FC2 at the decode tilings and in NVFP4 (items of I / 128 = 3
+                // stages): an item's first stage copies its scales (scale
+                // columns, not the accumulator) before the wait for the
+                // epilogue to free the accumulator, overlapping that hand-off.
+                // Elsewhere the wait comes first: FC1's items are H / 128
+                // stages long and rarely wait, and the extra fence between
+                // the copies and the MMAs measured slower there and in the
+                // MXFP8 FC2 at 128-row tiles.
+                constexpr bool kCopyFirst = !FC1 && (TM <= 32 || NV);
+                auto acc_free = [&]() -> bool {
+                    if (!wait_or_abort(accempty, aphase ^ 1, p.wait_ns, abort_flag)) {
+                        if (!*abort_flag) record_timeout(p, abort_flag, kSiteMmaAccEmpty);
+                        return false;
+                    }
+                    ptx::tc_fence_after();
+                    return true;
+                };
+                if constexpr (!kCopyFirst) {
+                    if (!acc_free()) break;
                 }
-                ptx::tc_fence_after();
                 for (int kc = 0; kc < KC; ++kc) {
                     if (!wait_or_abort(&full[stage], phase, p.wait_ns, abort_flag)) {
                         if (!*abort_flag) record_timeout(p, abort_flag, kSiteMmaFull);
@@ -476,6 +491,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ptx::tc_cp_32x128b_warpx4(sf + 4, ptx::sdesc_sf(sx + 512));
 #pragma unroll
                         for (int q = 0; q < 4; ++q) ptx::tc_cp_32x128b_warpx4(sf + 8 + 4 * q, ptx::sdesc_sf(sw + 512 * q));
+                        if (kCopyFirst && kc == 0 && !acc_free()) {
+                            ok = false;
+                            break;
+                        }
 #pragma unroll
                         for (int kk = 0; kk < 2; ++kk)
                             ptx::mma_mxf4nvf4(tmem, ptx::sdesc_sw64(xa + kk * 32), ptx::sdesc_sw64(wa + kk * 32),
@@ -485,6 +504,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ptx::tc_cp_32x128b_warpx4(sf + 4, ptx::sdesc_sf(ptx::smem_u32(smem + C::sfw_off(stage))));
                         ptx::tc_cp_32x128b_warpx4(sf + 8,
                                                   ptx::sdesc_sf(ptx::smem_u32(smem + C::sfw_off(stage) + 512)));
+                        if (kCopyFirst && kc == 0 && !acc_free()) {
+                            ok = false;
+                            break;
+                        }
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
                             ptx::mma_mxf8f6f4(tmem, ptx::sdesc_sw128(xa + kk * 32), ptx::sdesc_sw128(wa + kk * 32),
