@@ -318,14 +318,18 @@ int moe_layer(const moe_shape* shape, const float* logits, const uint16_t* share
  * device.  The layer is the one of "[SGLang] CUTLASS MoE", structure diagram
  * (input a (m, k) -> output (m, k)); the host copies around it are this
  * library's end-to-end entry point.  Decode tilings: every copy on `stream`.
- * 128-row tilings (long batches): the copies run on a stream the library
- * creates once per device -- logits first, then x and out in 8 token chunks
- * -- so routing starts when the logits have landed, each chunk's x gather
- * when its rows have landed, and each chunk's output leaves once combined,
- * overlapping the copies with the gather and the combine; that stream waits
- * for `stream` at the call and `stream` waits for its last copy, so the
- * call is ordered on `stream` like any other.  Calls on one device enqueue
- * one at a time (a mutex).  Not capturable (host memory). */
+ * 128-row tilings (long batches): the copies run on two streams the library
+ * creates once per device, one per direction -- logits first, then x in 8
+ * token chunks host-to-device; out in 8 token chunks device-to-host -- so
+ * routing starts when the logits have landed, each chunk's x gather when its
+ * rows have landed, and each chunk's output leaves once combined,
+ * overlapping the copies with the gather and the combine.  The input copies
+ * wait for `stream` at the call and `stream` waits for the last output copy,
+ * so the call is ordered on `stream` like any other.  Calls issued on two
+ * streams, each with its own workspace and output buffer, overlap: one
+ * call's output copies share the full-duplex host link with the other's
+ * input copies while the GPU computes.  Calls on one device enqueue one at a
+ * time (a mutex).  Not capturable (host memory). */
 int moe_layer_host(const moe_shape* shape, const float* logits_host, const uint16_t* shared_logit_host,
                    const uint16_t* x_host, const moe_weights* weights, void* workspace, size_t workspace_bytes,
                    uint16_t* out_host, moe_stream_t stream);

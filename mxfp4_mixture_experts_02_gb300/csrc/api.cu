@@ -171,13 +171,15 @@ int run_route_sort(const moe_shape* s, const float* logits, const uint16_t* shar
 
 // gathered: the route + sort launch already quantised x (decode tilings).
 // nv: the NVFP4 variant (128-row tiles only; null for MXFP8 x MXFP4).
-// moe_layer_host at 128-row tiles: the host copies run on a second stream in
-// token chunks, so the x gather of each chunk starts as soon as its rows
-// land and the output of each chunk leaves as soon as it is combined.
+// moe_layer_host at 128-row tiles: the host copies run on two more streams
+// (one per direction: the host link is full duplex) in token chunks, so the
+// x gather of each chunk starts as soon as its rows land and the output of
+// each chunk leaves as soon as it is combined.
 constexpr int kHostChunks = 8;
 
 struct HostPipe {
-    cudaStream_t cs;                      // copy stream
+    cudaStream_t cs;                      // host-to-device copies
+    cudaStream_t ds;                      // device-to-host copies
     cudaEvent_t x_in[kHostChunks];        // chunk c of x has landed (recorded on cs)
     cudaEvent_t out_ready[kHostChunks];   // chunk c of the output is combined (recorded on the compute stream)
     uint16_t* out_host;
@@ -359,7 +361,8 @@ int run_forward(const moe_shape* s, const uint16_t* x, const moe_weights* wt, co
                      L.y_bf16 ? nullptr : at<float>(ws, L.y),
                      L.y_bf16 ? at<uint16_t>(ws, L.y) : nullptr, out, d.T, d.kp, d.H};
     if (hp) {
-        // token chunk c, then its output rows back to the host on the copy stream
+        // token chunk c, then its output rows back to the host on the
+        // device-to-host stream
         e = cudaSuccess;
         for (int c = 0; c < kHostChunks && e == cudaSuccess; ++c) {
             cp.t0 = chunk_begin(d.T, c);
@@ -367,10 +370,10 @@ int run_forward(const moe_shape* s, const uint16_t* x, const moe_weights* wt, co
             if (cp.T == cp.t0) continue;
             e = launch_combine(cp, st, pdl);
             if (e == cudaSuccess) e = cudaEventRecord(hp->out_ready[c], st);
-            if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->cs, hp->out_ready[c], 0);
+            if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->ds, hp->out_ready[c], 0);
             if (e == cudaSuccess)
                 e = cudaMemcpyAsync(hp->out_host + static_cast<size_t>(cp.t0) * d.H, out + static_cast<size_t>(cp.t0) * d.H,
-                                    static_cast<size_t>(cp.T - cp.t0) * d.H * 2, cudaMemcpyDeviceToHost, hp->cs);
+                                    static_cast<size_t>(cp.T - cp.t0) * d.H * 2, cudaMemcpyDeviceToHost, hp->ds);
         }
     } else {
         e = launch_combine(cp, st, pdl);
@@ -629,11 +632,14 @@ int moe_layer_events(const moe_shape* s, const float* logits, const uint16_t* sh
     return run_forward(s, x, w, topk_w, ws, out, st, false, events, gathered);
 }
 
-// The copy stream and events of moe_layer_host's pipelined form, one set per
+// The copy streams and events of moe_layer_host's pipelined form, one set per
 // device, created on first use; calls enqueue under the mutex, so each wait
-// refers to the record its own call just made.
+// refers to the record its own call just made.  With one stream per
+// direction, a call's output copies and the input copies of a call on
+// another caller stream (with its own workspace) share the link instead of
+// queueing behind each other.
 struct HostPipeRes {
-    cudaStream_t cs = nullptr;
+    cudaStream_t cs = nullptr, ds = nullptr;
     cudaEvent_t start = nullptr, logits_in = nullptr, done = nullptr;
     cudaEvent_t x_in[kHostChunks] = {}, out_ready[kHostChunks] = {};
 };
@@ -647,11 +653,12 @@ int pipe_resources(HostPipeRes** out) {
     HostPipeRes& r = g_pipe[dev];
     if (!r.cs) {
         auto mk = [](cudaEvent_t* e) { return cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess; };
-        bool ok = cudaStreamCreateWithFlags(&r.cs, cudaStreamNonBlocking) == cudaSuccess && mk(&r.start) &&
+        bool ok = cudaStreamCreateWithFlags(&r.cs, cudaStreamNonBlocking) == cudaSuccess &&
+                  cudaStreamCreateWithFlags(&r.ds, cudaStreamNonBlocking) == cudaSuccess && mk(&r.start) &&
                   mk(&r.logits_in) && mk(&r.done);
         for (int c = 0; ok && c < kHostChunks; ++c) ok = mk(&r.x_in[c]) && mk(&r.out_ready[c]);
         if (!ok) {
-            r.cs = nullptr;
+            r.cs = r.ds = nullptr;
             return MOE_ERR_CUDA;
         }
     }
@@ -680,15 +687,16 @@ int moe_layer_host(const moe_shape* s, const float* logits_host, const uint16_t*
     bool gathered = false;
     const size_t row_bytes = size_t(d.H) * 2;
     if (d.mode == kModePrefill && d.T > 0) {
-        // Long batches: logits, then x in token chunks, on the copy stream
-        // (after the caller's stream reaches this call); routing starts when
-        // the logits land, each chunk's gather when its rows land; each
-        // chunk's output leaves when it is combined.  The caller's stream
-        // waits for the last copy.
+        // Long batches: logits, then x in token chunks, on the host-to-device
+        // stream (after the caller's stream reaches this call); routing
+        // starts when the logits land, each chunk's gather when its rows
+        // land; each chunk's output leaves on the device-to-host stream when
+        // it is combined.  The caller's stream waits for the last output
+        // copy.
         std::lock_guard<std::mutex> lock(g_pipe_mu);
         HostPipeRes* r = nullptr;
         if ((rc = pipe_resources(&r))) return rc;
-        HostPipe hp{r->cs, {}, {}, out_host};
+        HostPipe hp{r->cs, r->ds, {}, {}, out_host};
         for (int c = 0; c < kHostChunks; ++c) {
             hp.x_in[c] = r->x_in[c];
             hp.out_ready[c] = r->out_ready[c];
@@ -710,7 +718,7 @@ int moe_layer_host(const moe_shape* s, const float* logits_host, const uint16_t*
         if ((rc = run_route_sort(s, lg, d.S > 0 ? sl : nullptr, ids, tw, ws, st, nullptr, false, nullptr, &gathered)))
             return rc;
         if ((rc = run_forward(s, xd, w, tw, ws, od, st, true, nullptr, false, nullptr, &hp))) return rc;
-        if (cudaEventRecord(r->done, r->cs) != cudaSuccess || cudaStreamWaitEvent(st, r->done, 0) != cudaSuccess)
+        if (cudaEventRecord(r->done, r->ds) != cudaSuccess || cudaStreamWaitEvent(st, r->done, 0) != cudaSuccess)
             return MOE_ERR_CUDA;
         return MOE_OK;
     }

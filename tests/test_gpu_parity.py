@@ -472,6 +472,38 @@ def test_host_buffer_entry_point_matches_device_path(split_path, cfg):
         assert torch.equal(oh.view(torch.int16), ref.cpu().view(torch.int16))
 
 
+def test_host_buffer_calls_on_two_streams(split_path):
+    # consecutive moe_layer_host calls alternating over two caller streams,
+    # each stream with its own workspace, different inputs per stream and no
+    # host synchronisation between calls: one call's output copies overlap
+    # the next call's input copies and compute, and each output must still be
+    # its own call's, bit for bit
+    cfg = GRID[9]
+    shape = shape_of(cfg)
+    wts = _weights(cfg)
+    x, logits, sl = device_inputs(cfg)
+    flip = lambda t: t.flip(0).contiguous() if t is not None else None  # noqa: E731
+    inputs = [(x, logits, sl), (flip(x), flip(logits), flip(sl))]
+    ws0 = moe.workspace(shape)
+    refs = [moe.moe_layer(shape, lg, s_, xx, wts, ws0)[0].cpu() for xx, lg, s_ in inputs]
+    assert not torch.equal(refs[0], refs[1])
+    pin = lambda t: t.cpu().pin_memory() if t is not None else None  # noqa: E731
+    host = [(pin(xx), pin(lg), pin(s_)) for xx, lg, s_ in inputs]
+    wss = [moe.workspace(shape), moe.workspace(shape)]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = [torch.full((shape.T, shape.hidden), float("nan"), dtype=torch.bfloat16).pin_memory() for _ in range(6)]
+    torch.cuda.synchronize()
+    for i, oh in enumerate(outs):
+        xh, lh, sh = host[i % 2]
+        with torch.cuda.stream(streams[i % 2]):
+            moe.moe_layer_host(shape, lh, sh, xh, wts, wss[i % 2], oh)
+    torch.cuda.synchronize()
+    for i, oh in enumerate(outs):
+        assert torch.equal(oh.view(torch.int16), refs[i % 2].view(torch.int16)), i
+    for w in wss:
+        assert moe.moe_get_status(w) == (0, 0)
+
+
 # ----------------------------------------------------------------- edge values
 def _e4m3_midpoints(rng, n):
     """Values half-way between two adjacent positive normal E4M3 codes (exact
