@@ -12,7 +12,7 @@ namespace moe {
 namespace {
 
 constexpr int kRouteWarps = 8;
-constexpr int kRouteCtasPerSm = 2;  // resident CTAs per SM: long batches loop several tokens per warp
+constexpr int kRouteCtasPerSm = 3;  // resident CTAs per SM: long batches loop several tokens per warp
 
 // Each warp routes tokens t, t + stride, ...; while it routes one, its lanes
 // prefetch the next token's logits row (one 128-byte line per lane) into L2,
