@@ -122,12 +122,13 @@ int run_sort(const moe_shape* s, const int32_t* ids, void* ws, cudaStream_t st, 
     return cuda_rc(launch_sort(p, st, pdl));
 }
 
-// Route then sort, fused into one launch when the batch has at most 1024
-// slots.  `ev` (optional) gets events 1 (routed) and 2 (sorted); fused, both
+// Route then sort, fused into one launch when the batch has at most 128
+// tokens.  `ev` (optional) gets events 1 (routed) and 2 (sorted); fused, both
 // are recorded after the one kernel.  after_router: the logits come from the
 // router GEMM launched just before (PDL launch; the status word it may have
 // set survives the sort).  x (optional): in the decode tilings the fused
-// launch also quantises x (the gather's work); *gathered says whether it did.
+// launch also quantises x (the gather's work) up to 64 tokens; *gathered
+// says whether it did.
 int run_route_sort(const moe_shape* s, const float* logits, const uint16_t* shared_logit, int32_t* ids, float* w,
                    void* ws, cudaStream_t st, void* const* ev, bool after_router = false,
                    const uint16_t* x = nullptr, bool* gathered = nullptr);
@@ -149,7 +150,7 @@ int run_route_sort(const moe_shape* s, const float* logits, const uint16_t* shar
                       at<int32_t>(ws, L.vbase), at<int32_t>(ws, L.sort_hist), d.T, d.kp, d.Eg, d.E, d.off, d.S, d.Et,
                       d.B, d.G, after_router ? 1 : 0};
         GatherParams gp{};
-        const bool fuse_x = x != nullptr && L.x_token_order && d.T > 0;
+        const bool fuse_x = x != nullptr && L.x_token_order && route_sort_fuses_x(d.T);
         if (fuse_x) {
             gp.x = x;
             gp.xq = at<uint8_t>(ws, L.xq);
@@ -796,8 +797,9 @@ int moe_layer_launch_count(const moe_shape* s, int32_t* count) {
     const Dims d = make_dims(*s);
     const bool fused = route_sort_fusable(d.T, d.kp);
     int n = fused ? 1 : 1 + sort_launch_count(static_cast<int64_t>(d.T) * d.kp);
-    // gate, [gather,] FC1, FC2, combine; the decode tilings' x quantisation rides on the fused route + sort
-    if (d.T > 0) n += (fused && d.mode == kModeDecode) ? 4 : 5;
+    // gate, [gather,] FC1, FC2, combine; the decode tilings' x quantisation
+    // rides on the fused route + sort up to 64 tokens
+    if (d.T > 0) n += (fused && d.mode == kModeDecode && route_sort_fuses_x(d.T)) ? 4 : 5;
     *count = n;
     return MOE_OK;
 }

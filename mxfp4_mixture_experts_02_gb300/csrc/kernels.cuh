@@ -166,8 +166,10 @@ struct PackParams {
 
 cudaError_t launch_route(const RouteParams& p, cudaStream_t stream, bool pdl);
 cudaError_t launch_sort(const SortParams& p, cudaStream_t stream, bool pdl);
-// Route + sort fused in one CTA, for batches of at most 1024 slots.
+// Route + sort fused in one cluster launch, for batches of at most 128 tokens.
 bool route_sort_fusable(int T, int kp);
+// Whether that launch also quantises token-order x (batches of at most 64 tokens).
+bool route_sort_fuses_x(int T);
 // Kernels launch_sort issues for T*k' slots (1, or 3 above one CTA's share).
 int sort_launch_count(int64_t slots);
 // gp (optional, token-order x only): the launch also quantises x and writes

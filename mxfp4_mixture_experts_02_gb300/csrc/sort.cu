@@ -200,41 +200,53 @@ __global__ void __launch_bounds__(kSortThreads, 1) sort_kernel(SortParams p) {
     ptx::pdl_launch_dependents();
 }
 
-// Route and sort in one launch when the batch has at most kSmallSlots slots
+// Route and sort in one launch when the batch has at most kFusedMaxT tokens
 // (decode).  A cluster of kRouteCtas CTAs routes the tokens (token t on CTA
 // t % kRouteCtas, so the routing spreads over that many SMs) and stores the
 // picked ids straight into CTA 0's shared memory; after the cluster barrier
-// CTA 0 ranks the slots with per-expert bitmasks over the slots (the
+// CTA 0 ranks the slots with per-expert bitmasks over the tokens (the
 // popcount rank of "[sglang] ... MXFP4 decode MoE ... shape templates",
-// section 5, for up to 1024 slots): slot s sets bit s of its expert's mask;
-// the expert's row count is the popcount of the mask and slot s's row is the
-// expert's first row plus the number of its bits below s -- slot order inside
-// each expert, the same rows as the counting passes below.
+// section 5).  A token picks an expert at most once -- the top-k are
+// distinct experts and the shared experts are distinct from them -- so
+// token t sets bit t of each picked expert's mask; the expert's row count is
+// the popcount of the mask and slot (t, j)'s row is the expert's first row
+// plus the number of its bits below t: ascending token inside each expert,
+// the same rows as the counting passes below.
 //
-// fuse_x (decode tilings, x kept in token order): the warps that route no
-// token quantise the CTA's tokens' x rows to MXFP8 meanwhile, and CTA 0
-// writes each row's routing weight while ranking -- the launch then also
-// does the gather's work, and no launch of its own is spent on it.
-constexpr int kSmallSlots = 1024;
+// Measured on GB300 with the decode tilings: fused, T 72 / 96 / 128 take
+// 1.5 - 2 us less per layer than route + sort launches; at T 192 / 256 the
+// layer is the same or slower (skewed T 256: +1.6 us) although the fused
+// launch alone is shorter, so kFusedMaxT is 128.
+//
+// fuse_x (decode tilings, x kept in token order, at most kFuseXMaxT tokens):
+// the warps that route no token quantise the CTA's tokens' x rows to MXFP8
+// meanwhile, and CTA 0 writes each row's routing weight while ranking -- the
+// launch then also does the gather's work, and no launch of its own is spent
+// on it.  Past kFuseXMaxT tokens every warp routes, and x on 8 SMs would run
+// after the routing at those SMs' bandwidth: the quantiser's own launch over
+// the whole GPU is faster there.
+constexpr int kFusedMaxT = 128;
+constexpr int kFuseXMaxT = 64;
 constexpr int kRouteCtas = 8;
 
 __global__ void __cluster_dims__(kRouteCtas, 1, 1) __launch_bounds__(kSortThreads, 1)
     route_sort_small_kernel(RouteParams rp, SortParams p, GatherParams gp, int fuse_x) {
     __shared__ uint2 s_cand[kSortWarps][rs::kMaxCand];
-    __shared__ int s_ids[kSmallSlots];
     __shared__ int s_off[1024];
     __shared__ int s_tot[3][rs::kScanWarps];
-    // [nw][Et]: word w of every expert's slot bitmask side by side, so the
-    // per-expert counting pass (thread = expert) reads consecutive words
+    // dynamic: [nw][Et] token bitmasks (word w of every expert side by side,
+    // so the per-expert counting pass -- thread = expert -- reads consecutive
+    // words), then the slots' picked ids [T * k']
     extern __shared__ uint32_t s_mask[];
     namespace cg = cooperative_groups;
     cg::cluster_group cluster = cg::this_cluster();
     const int rank = static_cast<int>(cluster.block_rank());
+    const int nw = (p.T + 31) >> 5;  // mask words per expert
+    int* s_ids = reinterpret_cast<int*>(s_mask + p.Et * nw);
     int* ids0 = cluster.map_shared_rank(s_ids, 0);  // CTA 0's id table
     ptx::pdl_wait();
     const int tid = threadIdx.x, warp = tid >> 5;
     const int n = p.T * p.kp;
-    const int nw = (n + 31) >> 5;  // mask words per expert
     if (rank == 0)
         for (int w = tid; w < p.Et * nw; w += kSortThreads) s_mask[w] = 0;
     for (int t = rank + kRouteCtas * warp; t < rp.T; t += kRouteCtas * kSortWarps)
@@ -285,10 +297,10 @@ __global__ void __cluster_dims__(kRouteCtas, 1, 1) __launch_bounds__(kSortThread
         return;  // nothing reads the other CTAs' shared memory
     }
 
-    int e = -1;
-    if (tid < n) {
-        e = local_expert(s_ids[tid], p);
-        if (e >= 0) atomicOr(&s_mask[(tid >> 5) * p.Et + e], 1u << (tid & 31));
+    for (int sl = tid; sl < n; sl += kSortThreads) {
+        const int e = local_expert(s_ids[sl], p);
+        const int t = sl / p.kp;
+        if (e >= 0) atomicOr(&s_mask[(t >> 5) * p.Et + e], 1u << (t & 31));
     }
     __syncthreads();
     int cnt = 0;
@@ -298,18 +310,20 @@ __global__ void __cluster_dims__(kRouteCtas, 1, 1) __launch_bounds__(kSortThread
     }
     place_experts(p, cnt, s_off, s_tot);
     __syncthreads();
-    if (tid < n) {
+    for (int sl = tid; sl < n; sl += kSortThreads) {
+        const int e = local_expert(s_ids[sl], p);
         if (e >= 0) {
+            const int t = sl / p.kp;
             const uint32_t* m = s_mask + e;  // word w at m[w * Et]
-            int r = __popc(m[(tid >> 5) * p.Et] & ((1u << (tid & 31)) - 1u));
+            int r = __popc(m[(t >> 5) * p.Et] & ((1u << (t & 31)) - 1u));
 #pragma unroll 8
-            for (int w = 0; w < (tid >> 5); ++w) r += __popc(m[w * p.Et]);
+            for (int w = 0; w < (t >> 5); ++w) r += __popc(m[w * p.Et]);
             const int row = s_off[e] + r;
-            p.a_map[row] = tid;
-            p.c_map[tid] = row;
-            if (fuse_x) gp.row_w[row] = rp.w[tid];
+            p.a_map[row] = sl;
+            p.c_map[sl] = row;
+            if (fuse_x) gp.row_w[row] = rp.w[sl];
         } else {
-            p.c_map[tid] = -1;
+            p.c_map[sl] = -1;
         }
     }
     // The launches that follow read the work list only after their
@@ -425,11 +439,13 @@ cudaError_t launch_sort(const SortParams& p, cudaStream_t stream, bool pdl) {
 
 int sort_launch_count(int64_t slots) { return slots <= kSortWarps * kBigWarpSlots ? 1 : 3; }
 
-bool route_sort_fusable(int T, int kp) { return static_cast<int64_t>(T) * kp <= kSmallSlots; }
+bool route_sort_fusable(int T, int kp) { return T <= kFusedMaxT && kp <= 33; }
+
+bool route_sort_fuses_x(int T) { return T > 0 && T <= kFuseXMaxT; }
 
 cudaError_t launch_route_sort_small(const RouteParams& rp, const SortParams& p, const GatherParams* gp,
                                     cudaStream_t stream, bool pdl) {
-    const size_t smem = static_cast<size_t>(p.Et) * ((p.T * p.kp + 31) / 32) * sizeof(uint32_t);
+    const size_t smem = (static_cast<size_t>(p.Et) * ((p.T + 31) / 32) + static_cast<size_t>(p.T) * p.kp) * 4;
     cudaError_t err = cudaFuncSetAttribute(route_sort_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(smem));
     if (err != cudaSuccess) return err;

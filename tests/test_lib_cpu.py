@@ -115,7 +115,13 @@ def test_gemm2_path_override_checks_its_value():
 def test_layer_launch_count():
     # decode: route + sort + x quantisation in one launch, GEMM2 gate, FC1, FC2, combine
     assert moe.moe_layer_launch_count(_shape()) == 5
-    # 256 tokens x 16 picks > 1024 slots: route, one-CTA sort, gate, x quantisation, FC1, FC2, combine
+    # up to 64 tokens the decode tilings route, sort and quantise x in one cluster launch;
+    # up to 128 route and sort, and x has a launch of its own
+    assert moe.moe_layer_launch_count(_shape(T=64, max_T=64)) == 5
+    assert moe.moe_layer_launch_count(_shape(T=65, max_T=65)) == 6
+    assert moe.moe_layer_launch_count(_shape(T=128, max_T=128)) == 6
+    # 129 tokens: route, one-CTA sort, gate, x quantisation, FC1, FC2, combine
+    assert moe.moe_layer_launch_count(_shape(T=129, max_T=129)) == 7
     assert moe.moe_layer_launch_count(_shape(T=256, max_T=256)) == 7
     # prefill tiling at 32768 tokens: route, 3-kernel sort, gate, gather, FC1, FC2, combine
     assert moe.moe_layer_launch_count(_shape(T=32768, max_T=32768, block_n=128)) == 9
