@@ -112,13 +112,17 @@ int run_route(const moe_shape* s, const float* logits, const uint16_t* shared_lo
     return cuda_rc(launch_route(p, st, pdl));
 }
 
-int run_sort(const moe_shape* s, const int32_t* ids, void* ws, cudaStream_t st, bool pdl, bool keep_status = false) {
+// routed: the ids are the layer's own routing (each token's picks distinct),
+// so batches of up to 512 tokens take the one-CTA token-bitmask sort.
+int run_sort(const moe_shape* s, const int32_t* ids, void* ws, cudaStream_t st, bool pdl, bool keep_status = false,
+             bool routed = false) {
     const Dims d = make_dims(*s);
     const Layout L = make_layout(d);
     SortParams p{ids, at<int32_t>(ws, L.header), at<int32_t>(ws, L.counts), at<int32_t>(ws, L.offsets),
                  at<int4>(ws, L.vinfo), at<int4>(ws, L.groups), at<int32_t>(ws, L.a_map), at<int32_t>(ws, L.c_map),
                  at<int32_t>(ws, L.vbase), at<int32_t>(ws, L.sort_hist), d.T, d.kp, d.Eg, d.E, d.off, d.S, d.Et, d.B,
                  d.G, keep_status ? 1 : 0};
+    if (routed && sort_tokens_ok(d.T, d.kp)) return cuda_rc(launch_sort_tokens(p, st, pdl));
     return cuda_rc(launch_sort(p, st, pdl));
 }
 
@@ -166,7 +170,7 @@ int run_route_sort(const moe_shape* s, const float* logits, const uint16_t* shar
     int rc = run_route(s, logits, shared_logit, ids, w, st, after_router && ev == nullptr);
     if (rc) return rc;
     if (!rec(ev, 1, st)) return MOE_ERR_CUDA;
-    if ((rc = run_sort(s, ids, ws, st, ev == nullptr, after_router))) return rc;
+    if ((rc = run_sort(s, ids, ws, st, ev == nullptr, after_router, true))) return rc;
     return rec(ev, 2, st) ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -796,7 +800,7 @@ int moe_layer_launch_count(const moe_shape* s, int32_t* count) {
     if (!count) return MOE_ERR_NULL;
     const Dims d = make_dims(*s);
     const bool fused = route_sort_fusable(d.T, d.kp);
-    int n = fused ? 1 : 1 + sort_launch_count(static_cast<int64_t>(d.T) * d.kp);
+    int n = fused ? 1 : 1 + (sort_tokens_ok(d.T, d.kp) ? 1 : sort_launch_count(static_cast<int64_t>(d.T) * d.kp));
     // gate, [gather,] FC1, FC2, combine; the decode tilings' x quantisation
     // rides on the fused route + sort up to 64 tokens
     if (d.T > 0) n += (fused && d.mode == kModeDecode && route_sort_fuses_x(d.T)) ? 4 : 5;

@@ -170,6 +170,10 @@ cudaError_t launch_sort(const SortParams& p, cudaStream_t stream, bool pdl);
 bool route_sort_fusable(int T, int kp);
 // Whether that launch also quantises token-order x (batches of at most 64 tokens).
 bool route_sort_fuses_x(int T);
+// One-CTA sort of the layer's own routing (ids distinct per token) by token
+// bitmasks, for batches of at most 512 tokens.
+bool sort_tokens_ok(int T, int kp);
+cudaError_t launch_sort_tokens(const SortParams& p, cudaStream_t stream, bool pdl);
 // Kernels launch_sort issues for T*k' slots (1, or 3 above one CTA's share).
 int sort_launch_count(int64_t slots);
 // gp (optional, token-order x only): the launch also quantises x and writes

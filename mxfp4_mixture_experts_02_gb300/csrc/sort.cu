@@ -200,18 +200,81 @@ __global__ void __launch_bounds__(kSortThreads, 1) sort_kernel(SortParams p) {
     ptx::pdl_launch_dependents();
 }
 
+// Ranks the T * k' slots whose picked ids sit in s_ids, in one CTA of
+// kSortThreads threads, with per-expert bitmasks over the tokens (s_mask:
+// [nw][Et] words, word w of every expert side by side so that the counting
+// pass -- thread = expert -- reads consecutive words; zeroed by the caller).
+// Valid when a token picks an expert at most once, as the routing's picks do
+// (the top-k are distinct experts and the shared experts are distinct from
+// them): token t sets bit t of each picked expert's mask; the expert's row
+// count is the popcount of its mask and slot (t, j)'s row is the expert's
+// first row plus the number of its bits below t -- ascending token inside
+// each expert, the rows of the ballot-grouped passes (the popcount rank of
+// "[sglang] ... MXFP4 decode MoE ... shape templates", section 5, over the
+// whole batch).  row_w (optional) receives each row's routing weight w[slot].
+__device__ __forceinline__ void rank_by_token_masks(const SortParams& p, const int* s_ids, uint32_t* s_mask,
+                                                    int* s_off, int (*s_tot)[rs::kScanWarps], const float* w,
+                                                    float* row_w) {
+    const int tid = threadIdx.x;
+    const int n = p.T * p.kp;
+    const int nw = (p.T + 31) >> 5;
+    for (int sl = tid; sl < n; sl += kSortThreads) {
+        const int e = local_expert(s_ids[sl], p);
+        const int t = sl / p.kp;
+        if (e >= 0) atomicOr(&s_mask[(t >> 5) * p.Et + e], 1u << (t & 31));
+    }
+    __syncthreads();
+    int cnt = 0;
+    if (tid < p.Et) {
+#pragma unroll 8
+        for (int wd = 0; wd < nw; ++wd) cnt += __popc(s_mask[wd * p.Et + tid]);
+    }
+    place_experts(p, cnt, s_off, s_tot);
+    __syncthreads();
+    for (int sl = tid; sl < n; sl += kSortThreads) {
+        const int e = local_expert(s_ids[sl], p);
+        if (e >= 0) {
+            const int t = sl / p.kp;
+            const uint32_t* m = s_mask + e;  // word w at m[w * Et]
+            int r = __popc(m[(t >> 5) * p.Et] & ((1u << (t & 31)) - 1u));
+#pragma unroll 8
+            for (int wd = 0; wd < (t >> 5); ++wd) r += __popc(m[wd * p.Et]);
+            const int row = s_off[e] + r;
+            p.a_map[row] = sl;
+            p.c_map[sl] = row;
+            if (row_w) row_w[row] = w[sl];
+        } else {
+            p.c_map[sl] = -1;
+        }
+    }
+}
+
+// The layer's own routing past the fused range: the ids are the routing's,
+// so one CTA ranks them with token bitmasks (rank_by_token_masks) instead of
+// the ballot-grouped passes that arbitrary ids (duplicates, masked -1) need.
+constexpr int kSortTokensMaxT = 512;
+
+__global__ void __launch_bounds__(kSortThreads, 1) sort_tokens_kernel(SortParams p) {
+    __shared__ int s_off[1024];
+    __shared__ int s_tot[3][rs::kScanWarps];
+    extern __shared__ uint32_t s_mask[];  // [nw][Et] token bitmasks, then the ids [T * k']
+    const int tid = threadIdx.x;
+    const int nw = (p.T + 31) >> 5;
+    int* s_ids = reinterpret_cast<int*>(s_mask + p.Et * nw);
+    for (int wd = tid; wd < p.Et * nw; wd += kSortThreads) s_mask[wd] = 0;
+    ptx::pdl_wait();
+    const int n = p.T * p.kp;
+    for (int sl = tid; sl < n; sl += kSortThreads) s_ids[sl] = p.ids[sl];
+    __syncthreads();
+    rank_by_token_masks(p, s_ids, s_mask, s_off, s_tot, nullptr, nullptr);
+    ptx::pdl_launch_dependents();
+}
+
 // Route and sort in one launch when the batch has at most kFusedMaxT tokens
 // (decode).  A cluster of kRouteCtas CTAs routes the tokens (token t on CTA
 // t % kRouteCtas, so the routing spreads over that many SMs) and stores the
 // picked ids straight into CTA 0's shared memory; after the cluster barrier
-// CTA 0 ranks the slots with per-expert bitmasks over the tokens (the
-// popcount rank of "[sglang] ... MXFP4 decode MoE ... shape templates",
-// section 5).  A token picks an expert at most once -- the top-k are
-// distinct experts and the shared experts are distinct from them -- so
-// token t sets bit t of each picked expert's mask; the expert's row count is
-// the popcount of the mask and slot (t, j)'s row is the expert's first row
-// plus the number of its bits below t: ascending token inside each expert,
-// the same rows as the counting passes below.
+// CTA 0 ranks the slots with per-expert token bitmasks (rank_by_token_masks).
 //
 // Measured on GB300 with the decode tilings: fused, T 72 / 96 / 128 take
 // 1.5 - 2 us less per layer than route + sort launches; at T 192 / 256 the
@@ -246,7 +309,6 @@ __global__ void __cluster_dims__(kRouteCtas, 1, 1) __launch_bounds__(kSortThread
     int* ids0 = cluster.map_shared_rank(s_ids, 0);  // CTA 0's id table
     ptx::pdl_wait();
     const int tid = threadIdx.x, warp = tid >> 5;
-    const int n = p.T * p.kp;
     if (rank == 0)
         for (int w = tid; w < p.Et * nw; w += kSortThreads) s_mask[w] = 0;
     for (int t = rank + kRouteCtas * warp; t < rp.T; t += kRouteCtas * kSortWarps)
@@ -297,35 +359,7 @@ __global__ void __cluster_dims__(kRouteCtas, 1, 1) __launch_bounds__(kSortThread
         return;  // nothing reads the other CTAs' shared memory
     }
 
-    for (int sl = tid; sl < n; sl += kSortThreads) {
-        const int e = local_expert(s_ids[sl], p);
-        const int t = sl / p.kp;
-        if (e >= 0) atomicOr(&s_mask[(t >> 5) * p.Et + e], 1u << (t & 31));
-    }
-    __syncthreads();
-    int cnt = 0;
-    if (tid < p.Et) {
-#pragma unroll 8
-        for (int w = 0; w < nw; ++w) cnt += __popc(s_mask[w * p.Et + tid]);
-    }
-    place_experts(p, cnt, s_off, s_tot);
-    __syncthreads();
-    for (int sl = tid; sl < n; sl += kSortThreads) {
-        const int e = local_expert(s_ids[sl], p);
-        if (e >= 0) {
-            const int t = sl / p.kp;
-            const uint32_t* m = s_mask + e;  // word w at m[w * Et]
-            int r = __popc(m[(t >> 5) * p.Et] & ((1u << (t & 31)) - 1u));
-#pragma unroll 8
-            for (int w = 0; w < (t >> 5); ++w) r += __popc(m[w * p.Et]);
-            const int row = s_off[e] + r;
-            p.a_map[row] = sl;
-            p.c_map[sl] = row;
-            if (fuse_x) gp.row_w[row] = rp.w[sl];
-        } else {
-            p.c_map[sl] = -1;
-        }
-    }
+    rank_by_token_masks(p, s_ids, s_mask, s_off, s_tot, rp.w, fuse_x ? gp.row_w : nullptr);
     // The launches that follow read the work list only after their
     // griddepcontrol.wait (the gate) or after a launch that waited (FC1).
     ptx::pdl_launch_dependents();
@@ -442,6 +476,16 @@ int sort_launch_count(int64_t slots) { return slots <= kSortWarps * kBigWarpSlot
 bool route_sort_fusable(int T, int kp) { return T <= kFusedMaxT && kp <= 33; }
 
 bool route_sort_fuses_x(int T) { return T > 0 && T <= kFuseXMaxT; }
+
+bool sort_tokens_ok(int T, int kp) { return T <= kSortTokensMaxT && kp <= 33; }
+
+cudaError_t launch_sort_tokens(const SortParams& p, cudaStream_t stream, bool pdl) {
+    const size_t smem = (static_cast<size_t>(p.Et) * ((p.T + 31) / 32) + static_cast<size_t>(p.T) * p.kp) * 4;
+    cudaError_t err = cudaFuncSetAttribute(sort_tokens_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(smem));
+    if (err != cudaSuccess) return err;
+    return launch_kernel(sort_tokens_kernel, dim3(1), dim3(kSortThreads), smem, stream, pdl, p);
+}
 
 cudaError_t launch_route_sort_small(const RouteParams& rp, const SortParams& p, const GatherParams* gp,
                                     cudaStream_t stream, bool pdl) {
