@@ -105,28 +105,30 @@ T* at(void* ws, size_t off) {
 
 int cuda_rc(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
+// gp (optional): the launch also quantises token-order x.
 int run_route(const moe_shape* s, const float* logits, const uint16_t* shared_logit, int32_t* ids, float* w,
-              cudaStream_t st, bool pdl) {
+              cudaStream_t st, bool pdl, const GatherParams* gp = nullptr) {
     const Dims d = make_dims(*s);
     RouteParams p{logits, shared_logit, ids, w, d.T, d.Eg, d.k, d.S, d.kp, d.shared_scale};
-    return cuda_rc(launch_route(p, st, pdl));
+    return cuda_rc(launch_route(p, st, pdl, gp));
 }
 
 // routed: the ids are the layer's own routing (each token's picks distinct),
-// so batches of up to 512 tokens take the one-CTA token-bitmask sort.
+// so batches of up to 512 tokens take the one-CTA token-bitmask sort, which
+// also writes each row's routing weight w[slot] to row_w when given.
 int run_sort(const moe_shape* s, const int32_t* ids, void* ws, cudaStream_t st, bool pdl, bool keep_status = false,
-             bool routed = false) {
+             bool routed = false, const float* w = nullptr, float* row_w = nullptr) {
     const Dims d = make_dims(*s);
     const Layout L = make_layout(d);
     SortParams p{ids, at<int32_t>(ws, L.header), at<int32_t>(ws, L.counts), at<int32_t>(ws, L.offsets),
                  at<int4>(ws, L.vinfo), at<int4>(ws, L.groups), at<int32_t>(ws, L.a_map), at<int32_t>(ws, L.c_map),
                  at<int32_t>(ws, L.vbase), at<int32_t>(ws, L.sort_hist), d.T, d.kp, d.Eg, d.E, d.off, d.S, d.Et, d.B,
                  d.G, keep_status ? 1 : 0};
-    if (routed && sort_tokens_ok(d.T, d.kp)) return cuda_rc(launch_sort_tokens(p, st, pdl));
+    if (routed && sort_tokens_ok(d.T, d.kp)) return cuda_rc(launch_sort_tokens(p, st, pdl, w, row_w));
     return cuda_rc(launch_sort(p, st, pdl));
 }
 
-// Route then sort, fused into one launch when the batch has at most 128
+// Route then sort, fused into one launch when the batch has at most 64
 // tokens.  `ev` (optional) gets events 1 (routed) and 2 (sorted); fused, both
 // are recorded after the one kernel.  after_router: the logits come from the
 // router GEMM launched just before (PDL launch; the status word it may have
@@ -167,10 +169,25 @@ int run_route_sort(const moe_shape* s, const float* logits, const uint16_t* shar
         if (gathered) *gathered = fuse_x;
         return (rec(ev, 1, st) && rec(ev, 2, st)) ? MOE_OK : MOE_ERR_CUDA;
     }
-    int rc = run_route(s, logits, shared_logit, ids, w, st, after_router && ev == nullptr);
+    // Past the fused range the decode tilings quantise x in the route launch
+    // (over the whole grid) and the token-bitmask sort writes each row's
+    // routing weight: the gather's work, with no launch of its own.
+    const Layout L = make_layout(d);
+    const bool x_in_route = x != nullptr && L.x_token_order && d.T > 0 && sort_tokens_ok(d.T, d.kp);
+    GatherParams gp{};
+    if (x_in_route) {
+        gp.x = x;
+        gp.xq = at<uint8_t>(ws, L.xq);
+        gp.xsf = at<uint8_t>(ws, L.xsf);
+        gp.H = d.H;
+    }
+    int rc = run_route(s, logits, shared_logit, ids, w, st, after_router && ev == nullptr, x_in_route ? &gp : nullptr);
     if (rc) return rc;
     if (!rec(ev, 1, st)) return MOE_ERR_CUDA;
-    if ((rc = run_sort(s, ids, ws, st, ev == nullptr, after_router, true))) return rc;
+    if ((rc = run_sort(s, ids, ws, st, ev == nullptr, after_router, true, w,
+                       x_in_route ? at<float>(ws, L.row_w) : nullptr)))
+        return rc;
+    if (gathered) *gathered = x_in_route;
     return rec(ev, 2, st) ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -802,8 +819,10 @@ int moe_layer_launch_count(const moe_shape* s, int32_t* count) {
     const bool fused = route_sort_fusable(d.T, d.kp);
     int n = fused ? 1 : 1 + (sort_tokens_ok(d.T, d.kp) ? 1 : sort_launch_count(static_cast<int64_t>(d.T) * d.kp));
     // gate, [gather,] FC1, FC2, combine; the decode tilings' x quantisation
-    // rides on the fused route + sort up to 64 tokens
-    if (d.T > 0) n += (fused && d.mode == kModeDecode && route_sort_fuses_x(d.T)) ? 4 : 5;
+    // rides on the fused route + sort up to 64 tokens, on the route launch up
+    // to 512
+    const bool x_done = d.mode == kModeDecode && (fused ? route_sort_fuses_x(d.T) : sort_tokens_ok(d.T, d.kp));
+    if (d.T > 0) n += x_done ? 4 : 5;
     *count = n;
     return MOE_OK;
 }

@@ -164,7 +164,8 @@ struct PackParams {
     int pair;
 };
 
-cudaError_t launch_route(const RouteParams& p, cudaStream_t stream, bool pdl);
+// gp (optional, token-order x only): the launch also quantises x.
+cudaError_t launch_route(const RouteParams& p, cudaStream_t stream, bool pdl, const GatherParams* gp = nullptr);
 cudaError_t launch_sort(const SortParams& p, cudaStream_t stream, bool pdl);
 // Route + sort fused in one cluster launch, for batches of at most 128 tokens.
 bool route_sort_fusable(int T, int kp);
@@ -173,7 +174,9 @@ bool route_sort_fuses_x(int T);
 // One-CTA sort of the layer's own routing (ids distinct per token) by token
 // bitmasks, for batches of at most 512 tokens.
 bool sort_tokens_ok(int T, int kp);
-cudaError_t launch_sort_tokens(const SortParams& p, cudaStream_t stream, bool pdl);
+// row_w (optional): each row's routing weight w[slot] is written too.
+cudaError_t launch_sort_tokens(const SortParams& p, cudaStream_t stream, bool pdl, const float* w = nullptr,
+                               float* row_w = nullptr);
 // Kernels launch_sort issues for T*k' slots (1, or 3 above one CTA's share).
 int sort_launch_count(int64_t slots);
 // gp (optional, token-order x only): the launch also quantises x and writes

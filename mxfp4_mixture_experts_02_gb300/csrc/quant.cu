@@ -44,30 +44,7 @@ __global__ void __launch_bounds__(kGatherThreads) quant_x_kernel(GatherParams p)
             p.row_w[row] = p.topk_w[p.a_map[row]];
             continue;
         }
-        const uint4* src = reinterpret_cast<const uint4*>(p.x) + job * 4;
-        uint4 raw[4];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) raw[c] = __ldg(src + c);
-        // word k holds elements 2k (low half) and 2k + 1 (high half)
-        const uint32_t* wd = reinterpret_cast<const uint32_t*>(raw);
-        float amax = 0.f;
-#pragma unroll
-        for (int k = 0; k < 16; ++k)
-            amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(wd[k] << 16)), fabsf(__uint_as_float(wd[k] & 0xFFFF0000u))));
-        const int ex = mx_shared_exponent(amax, 8);
-        const float inv = exp2_int(-ex);
-        uint32_t packed[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const uint32_t w0 = wd[2 * e], w1 = wd[2 * e + 1];
-            const uint32_t lo = e4m3x2(__uint_as_float(w0 << 16) * inv, __uint_as_float(w0 & 0xFFFF0000u) * inv);
-            const uint32_t hi = e4m3x2(__uint_as_float(w1 << 16) * inv, __uint_as_float(w1 & 0xFFFF0000u) * inv);
-            packed[e] = lo | (hi << 16);
-        }
-        uint4* dst = reinterpret_cast<uint4*>(p.xq) + job * 2;
-        dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-        dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-        p.xsf[job] = static_cast<uint8_t>(ex + 127);
+        quant_x_block(p.x, p.xq, p.xsf, static_cast<size_t>(job));
     }
     ptx::pdl_launch_dependents();
 }

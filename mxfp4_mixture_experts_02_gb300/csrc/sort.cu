@@ -212,9 +212,12 @@ __global__ void __launch_bounds__(kSortThreads, 1) sort_kernel(SortParams p) {
 // each expert, the rows of the ballot-grouped passes (the popcount rank of
 // "[sglang] ... MXFP4 decode MoE ... shape templates", section 5, over the
 // whole batch).  row_w (optional) receives each row's routing weight w[slot].
+// s_rows (optional, R ints of shared memory): the rank pass records each
+// row's slot there, and a second pass writes a_map and row_w in row order
+// (coalesced) instead of one scattered store per slot.
 __device__ __forceinline__ void rank_by_token_masks(const SortParams& p, const int* s_ids, uint32_t* s_mask,
                                                     int* s_off, int (*s_tot)[rs::kScanWarps], const float* w,
-                                                    float* row_w) {
+                                                    float* row_w, int* s_rows = nullptr) {
     const int tid = threadIdx.x;
     const int n = p.T * p.kp;
     const int nw = (p.T + 31) >> 5;
@@ -240,11 +243,24 @@ __device__ __forceinline__ void rank_by_token_masks(const SortParams& p, const i
 #pragma unroll 8
             for (int wd = 0; wd < (t >> 5); ++wd) r += __popc(m[wd * p.Et]);
             const int row = s_off[e] + r;
-            p.a_map[row] = sl;
             p.c_map[sl] = row;
-            if (row_w) row_w[row] = w[sl];
+            if (s_rows) {
+                s_rows[row] = sl;
+            } else {
+                p.a_map[row] = sl;
+                if (row_w) row_w[row] = w[sl];
+            }
         } else {
             p.c_map[sl] = -1;
+        }
+    }
+    if (s_rows) {
+        __syncthreads();
+        const int R = p.offsets[p.Et];  // written by place_experts before the barrier above
+        for (int row = tid; row < R; row += kSortThreads) {
+            const int sl = s_rows[row];
+            p.a_map[row] = sl;
+            if (row_w) row_w[row] = w[sl];
         }
     }
 }
@@ -253,20 +269,31 @@ __device__ __forceinline__ void rank_by_token_masks(const SortParams& p, const i
 // so one CTA ranks them with token bitmasks (rank_by_token_masks) instead of
 // the ballot-grouped passes that arbitrary ids (duplicates, masked -1) need.
 constexpr int kSortTokensMaxT = 512;
+constexpr size_t kSortTokensRowsSmem = 200 * 1024;  // dynamic shared memory with the row -> slot table
 
-__global__ void __launch_bounds__(kSortThreads, 1) sort_tokens_kernel(SortParams p) {
+__global__ void __launch_bounds__(kSortThreads, 1)
+    sort_tokens_kernel(SortParams p, const float* w, float* row_w, int use_rows) {
     __shared__ int s_off[1024];
     __shared__ int s_tot[3][rs::kScanWarps];
-    extern __shared__ uint32_t s_mask[];  // [nw][Et] token bitmasks, then the ids [T * k']
+    // dynamic: [nw][Et] token bitmasks, the ids [T * k'], (row_w given) the
+    // slots' routing weights [T * k'] staged with the ids so that their loads
+    // are in flight together, then (use_rows) each row's slot [T * k']
+    extern __shared__ uint32_t s_mask[];
     const int tid = threadIdx.x;
     const int nw = (p.T + 31) >> 5;
+    const int n = p.T * p.kp;
     int* s_ids = reinterpret_cast<int*>(s_mask + p.Et * nw);
+    float* s_w = reinterpret_cast<float*>(s_ids + n);
+    int* s_rows = use_rows ? reinterpret_cast<int*>(s_w + (row_w ? n : 0)) : nullptr;
     for (int wd = tid; wd < p.Et * nw; wd += kSortThreads) s_mask[wd] = 0;
     ptx::pdl_wait();
-    const int n = p.T * p.kp;
-    for (int sl = tid; sl < n; sl += kSortThreads) s_ids[sl] = p.ids[sl];
+#pragma unroll 4
+    for (int sl = tid; sl < n; sl += kSortThreads) {
+        s_ids[sl] = p.ids[sl];
+        if (row_w) s_w[sl] = w[sl];
+    }
     __syncthreads();
-    rank_by_token_masks(p, s_ids, s_mask, s_off, s_tot, nullptr, nullptr);
+    rank_by_token_masks(p, s_ids, s_mask, s_off, s_tot, s_w, row_w, s_rows);
     ptx::pdl_launch_dependents();
 }
 
@@ -276,19 +303,15 @@ __global__ void __launch_bounds__(kSortThreads, 1) sort_tokens_kernel(SortParams
 // picked ids straight into CTA 0's shared memory; after the cluster barrier
 // CTA 0 ranks the slots with per-expert token bitmasks (rank_by_token_masks).
 //
-// Measured on GB300 with the decode tilings: fused, T 72 / 96 / 128 take
-// 1.5 - 2 us less per layer than route + sort launches; at T 192 / 256 the
-// layer is the same or slower (skewed T 256: +1.6 us) although the fused
-// launch alone is shorter, so kFusedMaxT is 128.
-//
-// fuse_x (decode tilings, x kept in token order, at most kFuseXMaxT tokens):
-// the warps that route no token quantise the CTA's tokens' x rows to MXFP8
-// meanwhile, and CTA 0 writes each row's routing weight while ranking -- the
-// launch then also does the gather's work, and no launch of its own is spent
-// on it.  Past kFuseXMaxT tokens every warp routes, and x on 8 SMs would run
-// after the routing at those SMs' bandwidth: the quantiser's own launch over
-// the whole GPU is faster there.
-constexpr int kFusedMaxT = 128;
+// fuse_x (decode tilings, x kept in token order): the warps that route no
+// token quantise the CTA's tokens' x rows to MXFP8 meanwhile, and CTA 0
+// writes each row's routing weight while ranking -- the launch then also
+// does the gather's work, and no launch of its own is spent on it.  Past 64
+// tokens every warp routes, and x on 8 SMs would run after the routing at
+// those SMs' bandwidth: the route kernel over the whole GPU (quantising x on
+// its grid) followed by sort_tokens_kernel is faster there (measured on
+// GB300 at T 72 to 256).
+constexpr int kFusedMaxT = 64;
 constexpr int kFuseXMaxT = 64;
 constexpr int kRouteCtas = 8;
 
@@ -327,30 +350,7 @@ __global__ void __cluster_dims__(kRouteCtas, 1, 1) __launch_bounds__(kSortThread
         for (int job = first; first >= 0 && job < nt * nb; job += stride) {
             const int j = job / nb, b = job - j * nb;
             const size_t blk = static_cast<size_t>(rank + kRouteCtas * j) * nb + b;
-            const uint4* src = reinterpret_cast<const uint4*>(gp.x) + blk * 4;
-            uint4 raw[4];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) raw[c] = src[c];
-            // word k holds elements 2k (low half) and 2k + 1 (high half)
-            const uint32_t* wd = reinterpret_cast<const uint32_t*>(raw);
-            float amax = 0.f;
-#pragma unroll
-            for (int k = 0; k < 16; ++k)
-                amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(wd[k] << 16)), fabsf(__uint_as_float(wd[k] & 0xFFFF0000u))));
-            const int ex = mx_shared_exponent(amax, 8);
-            const float inv = exp2_int(-ex);
-            uint32_t packed[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const uint32_t w0 = wd[2 * e], w1 = wd[2 * e + 1];
-                const uint32_t lo = e4m3x2(__uint_as_float(w0 << 16) * inv, __uint_as_float(w0 & 0xFFFF0000u) * inv);
-                const uint32_t hi = e4m3x2(__uint_as_float(w1 << 16) * inv, __uint_as_float(w1 & 0xFFFF0000u) * inv);
-                packed[e] = lo | (hi << 16);
-            }
-            uint4* dst = reinterpret_cast<uint4*>(gp.xq) + blk * 2;
-            dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-            dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-            gp.xsf[blk] = static_cast<uint8_t>(ex + 127);
+            quant_x_block(gp.x, gp.xq, gp.xsf, blk);
         }
     }
     cluster.sync();
@@ -479,12 +479,16 @@ bool route_sort_fuses_x(int T) { return T > 0 && T <= kFuseXMaxT; }
 
 bool sort_tokens_ok(int T, int kp) { return T <= kSortTokensMaxT && kp <= 33; }
 
-cudaError_t launch_sort_tokens(const SortParams& p, cudaStream_t stream, bool pdl) {
-    const size_t smem = (static_cast<size_t>(p.Et) * ((p.T + 31) / 32) + static_cast<size_t>(p.T) * p.kp) * 4;
+cudaError_t launch_sort_tokens(const SortParams& p, cudaStream_t stream, bool pdl, const float* w, float* row_w) {
+    const size_t n = static_cast<size_t>(p.T) * p.kp;
+    size_t smem = (static_cast<size_t>(p.Et) * ((p.T + 31) / 32) + n * (row_w ? 2 : 1)) * 4;
+    const bool use_rows = smem + n * 4 <= kSortTokensRowsSmem;  // room for the row -> slot table
+    if (use_rows) smem += n * 4;
     cudaError_t err = cudaFuncSetAttribute(sort_tokens_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(smem));
     if (err != cudaSuccess) return err;
-    return launch_kernel(sort_tokens_kernel, dim3(1), dim3(kSortThreads), smem, stream, pdl, p);
+    return launch_kernel(sort_tokens_kernel, dim3(1), dim3(kSortThreads), smem, stream, pdl, p, w, row_w,
+                         use_rows ? 1 : 0);
 }
 
 cudaError_t launch_route_sort_small(const RouteParams& rp, const SortParams& p, const GatherParams* gp,

@@ -25,7 +25,7 @@ SMALL = synth.MoeConfig("small", 7, T=48, E_global=64, E_local=64, expert_offset
 CASES = [
     SMALL.replace(T=7, block_n=16),
     SMALL.replace(T=96, block_n=32, num_shared=1, zipf_s=1.1),
-    SMALL.replace(T=300, block_n=32, num_shared=1, zipf_s=1.1),  # route and sort as separate launches
+    SMALL.replace(T=600, block_n=32, num_shared=1, zipf_s=1.1),  # route, sort and x as separate launches
     SMALL.replace(T=200, block_n=128, top_k=8, num_shared=1),
     SMALL.replace(T=256, block_n=16, E_local=32, expert_offset=16),  # EP slice: tokens without local rows
     synth.CONFIGS["tiny"],

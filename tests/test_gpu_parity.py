@@ -50,9 +50,9 @@ GRID = [
     SMALL.replace(T=96, block_n=16, num_shared=1, activation=2, act_params=(1.0, 0.5)),
     SMALL.replace(T=200, block_n=128, top_k=8, activation=1, act_params=(0.5, 0.0)),
     SMALL.replace(T=64, block_n=128, hidden=1536, inter=384, activation=2, act_params=(0.5, 0.25)),
-    # past 256 tokens the decode tilings route, sort and quantise x in
+    # past 512 tokens the decode tilings route, sort and quantise x in
     # separate launches
-    SMALL.replace(T=300, block_n=32, num_shared=1, zipf_s=1.1),
+    SMALL.replace(T=600, block_n=32, num_shared=1, zipf_s=1.1),
 ]
 FULL = [synth.CONFIGS[n] for n in ("decode_t32", "ep_slice_t64", "skewed_shared_t256", "prefill_t32768")]
 
@@ -361,12 +361,13 @@ def test_route_kernel_exact_with_and_without_ties(Eg, k, coarse):
 @pytest.mark.parametrize("T,coarse,S", [(32, True, 0), (64, False, 0), (48, True, 1), (7, False, 1), (100, True, 1),
                                          (128, False, 0), (128, True, 1)])
 def test_fused_and_split_route_sort_agree_with_oracle(T, coarse, S):
-    # T <= 128: moe_layer routes and sorts in one kernel (token bitmasks over
-    # up to 4 words per expert); moe_route + moe_sort run the split kernels.
-    # Both must give the oracle's maps.
+    # moe_layer ranks its own routing with token bitmasks: in the fused route
+    # + sort kernel up to 64 tokens, in a one-CTA sort after the route launch
+    # up to 512; moe_route + moe_sort run the general kernels.  Both must give
+    # the oracle's maps.
     cfg = SMALL.replace(T=T, top_k=16, num_shared=S, E_local=64, block_n=32)
     shape = shape_of(cfg)
-    assert shape.T <= 128
+    assert shape.T <= 512
     lg = _tie_logits(T, cfg.E_global, T + S, coarse)
     x, _, sl = device_inputs(cfg)
     oids, ow = oracle.route(lg, cfg.top_k, S, synth.shared_logit_host(cfg) if S else None, cfg.shared_scale)
@@ -567,18 +568,20 @@ def edge_x_bits(T, H, seed):
     return bits
 
 
-@pytest.mark.parametrize("T,block_n,path", [(16, 32, "fused route+sort"), (128, 32, "quant_x launch"),
-                                            (300, 16, "quant_x launch"), (64, 128, "token-major gather")])
+@pytest.mark.parametrize("T,block_n,path", [(16, 32, "fused route+sort"), (128, 32, "route launch"),
+                                            (600, 16, "quant_x launch"), (64, 128, "token-major gather")])
 def test_x_quantiser_edge_values_all_paths(T, block_n, path):
-    # x -> MXFP8 is computed by three launches depending on the tiling and
-    # batch: inside the fused route + sort (decode tilings, T <= 64),
-    # by its own launch (decode tilings, larger batches) and by the token-major
-    # gather into expert rows (128-row tiles).  All must equal the oracle's
+    # x -> MXFP8 is computed by four launches depending on the tiling and
+    # batch: inside the fused route + sort (decode tilings, T <= 64), in the
+    # route launch (decode tilings, T <= 512), by its own launch (decode
+    # tilings, larger batches) and by the token-major gather into expert rows
+    # (128-row tiles).  All must equal the oracle's
     # quantiser bit for bit on edge values.
     cfg = SMALL.replace(T=T, block_n=block_n, top_k=4)
     shape = shape_of(cfg)
     if block_n < 128:  # 128-row tiles quantise x in the gather even when route and sort are fused
-        assert (shape.T <= 64) == (path == "fused route+sort")
+        expect = "fused route+sort" if shape.T <= 64 else ("route launch" if shape.T <= 512 else "quant_x launch")
+        assert path == expect
     bits = edge_x_bits(T, cfg.hidden, T + block_n)
     x = torch.from_numpy(bits.view(np.int16)).cuda().view(torch.bfloat16)
     _, logits, sl = device_inputs(cfg)

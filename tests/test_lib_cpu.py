@@ -116,13 +116,12 @@ def test_layer_launch_count():
     # decode: route + sort + x quantisation in one launch, GEMM2 gate, FC1, FC2, combine
     assert moe.moe_layer_launch_count(_shape()) == 5
     # up to 64 tokens the decode tilings route, sort and quantise x in one cluster launch;
-    # up to 128 route and sort, and x has a launch of its own
+    # up to 512 x rides on the route launch and a one-CTA sort follows
     assert moe.moe_layer_launch_count(_shape(T=64, max_T=64)) == 5
     assert moe.moe_layer_launch_count(_shape(T=65, max_T=65)) == 6
-    assert moe.moe_layer_launch_count(_shape(T=128, max_T=128)) == 6
-    # 129 tokens: route, one-CTA sort, gate, x quantisation, FC1, FC2, combine
-    assert moe.moe_layer_launch_count(_shape(T=129, max_T=129)) == 7
-    assert moe.moe_layer_launch_count(_shape(T=256, max_T=256)) == 7
+    assert moe.moe_layer_launch_count(_shape(T=512, max_T=512)) == 6
+    # 513 tokens: route, one-CTA sort, gate, x quantisation, FC1, FC2, combine
+    assert moe.moe_layer_launch_count(_shape(T=513, max_T=513)) == 7
     # prefill tiling at 32768 tokens: route, 3-kernel sort, gate, gather, FC1, FC2, combine
     assert moe.moe_layer_launch_count(_shape(T=32768, max_T=32768, block_n=128)) == 9
     assert moe.moe_layer_launch_count(_shape(T=0)) == 1
