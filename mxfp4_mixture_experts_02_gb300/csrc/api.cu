@@ -124,7 +124,7 @@ int run_sort(const moe_shape* s, const int32_t* ids, void* ws, cudaStream_t st, 
                  at<int4>(ws, L.vinfo), at<int4>(ws, L.groups), at<int32_t>(ws, L.a_map), at<int32_t>(ws, L.c_map),
                  at<int32_t>(ws, L.vbase), at<int32_t>(ws, L.sort_hist), d.T, d.kp, d.Eg, d.E, d.off, d.S, d.Et, d.B,
                  d.G, keep_status ? 1 : 0};
-    if (routed && sort_tokens_ok(d.T, d.kp)) return cuda_rc(launch_sort_tokens(p, st, pdl, w, row_w));
+    if (routed && sort_tokens_ok(d.T, d.kp, d.Et)) return cuda_rc(launch_sort_tokens(p, st, pdl, w, row_w));
     return cuda_rc(launch_sort(p, st, pdl));
 }
 
@@ -173,7 +173,7 @@ int run_route_sort(const moe_shape* s, const float* logits, const uint16_t* shar
     // (over the whole grid) and the token-bitmask sort writes each row's
     // routing weight: the gather's work, with no launch of its own.
     const Layout L = make_layout(d);
-    const bool x_in_route = x != nullptr && L.x_token_order && d.T > 0 && sort_tokens_ok(d.T, d.kp);
+    const bool x_in_route = x != nullptr && L.x_token_order && d.T > 0 && sort_tokens_ok(d.T, d.kp, d.Et);
     GatherParams gp{};
     if (x_in_route) {
         gp.x = x;
@@ -817,11 +817,11 @@ int moe_layer_launch_count(const moe_shape* s, int32_t* count) {
     if (!count) return MOE_ERR_NULL;
     const Dims d = make_dims(*s);
     const bool fused = route_sort_fusable(d.T, d.kp);
-    int n = fused ? 1 : 1 + (sort_tokens_ok(d.T, d.kp) ? 1 : sort_launch_count(static_cast<int64_t>(d.T) * d.kp));
+    int n = fused ? 1 : 1 + (sort_tokens_ok(d.T, d.kp, d.Et) ? 1 : sort_launch_count(static_cast<int64_t>(d.T) * d.kp));
     // gate, [gather,] FC1, FC2, combine; the decode tilings' x quantisation
     // rides on the fused route + sort up to 64 tokens, on the route launch up
     // to 512
-    const bool x_done = d.mode == kModeDecode && (fused ? route_sort_fuses_x(d.T) : sort_tokens_ok(d.T, d.kp));
+    const bool x_done = d.mode == kModeDecode && (fused ? route_sort_fuses_x(d.T) : sort_tokens_ok(d.T, d.kp, d.Et));
     if (d.T > 0) n += x_done ? 4 : 5;
     *count = n;
     return MOE_OK;

@@ -172,8 +172,8 @@ bool route_sort_fusable(int T, int kp);
 // Whether that launch also quantises token-order x (batches of at most 64 tokens).
 bool route_sort_fuses_x(int T);
 // One-CTA sort of the layer's own routing (ids distinct per token) by token
-// bitmasks, for batches of at most 512 tokens.
-bool sort_tokens_ok(int T, int kp);
+// bitmasks, for batches of at most 512 tokens whose tables fit in shared memory.
+bool sort_tokens_ok(int T, int kp, int Et);
 // row_w (optional): each row's routing weight w[slot] is written too.
 cudaError_t launch_sort_tokens(const SortParams& p, cudaStream_t stream, bool pdl, const float* w = nullptr,
                                float* row_w = nullptr);

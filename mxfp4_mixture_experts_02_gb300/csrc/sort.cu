@@ -212,36 +212,57 @@ __global__ void __launch_bounds__(kSortThreads, 1) sort_kernel(SortParams p) {
 // each expert, the rows of the ballot-grouped passes (the popcount rank of
 // "[sglang] ... MXFP4 decode MoE ... shape templates", section 5, over the
 // whole batch).  row_w (optional) receives each row's routing weight w[slot].
-// s_rows (optional, R ints of shared memory): the rank pass records each
-// row's slot there, and a second pass writes a_map and row_w in row order
-// (coalesced) instead of one scattered store per slot.
-__device__ __forceinline__ void rank_by_token_masks(const SortParams& p, const int* s_ids, uint32_t* s_mask,
-                                                    int* s_off, int (*s_tot)[rs::kScanWarps], const float* w,
-                                                    float* row_w, int* s_rows = nullptr) {
+// s_ids is overwritten with each slot's local expert (-1: not local).
+// s_pref (optional, [nw][Et] 16-bit): the popcount of each expert's mask
+// words below word w, so a slot's rank takes one masked popcount instead of
+// one per earlier word.  s_rows (optional, R ints of shared memory): the
+// rank pass records each row's slot there, and a second pass writes a_map
+// and row_w in row order (coalesced) instead of one scattered store per
+// slot.  One CTA of kSortThreads threads: the passes are bound by its
+// instruction issue, so a thread steps its slots' token index by addition
+// rather than dividing by k'.
+__device__ __forceinline__ void rank_by_token_masks(const SortParams& p, int* s_ids, uint32_t* s_mask,
+                                                    uint16_t* s_pref, int* s_off, int (*s_tot)[rs::kScanWarps],
+                                                    const float* w, float* row_w, int* s_rows) {
     const int tid = threadIdx.x;
     const int n = p.T * p.kp;
     const int nw = (p.T + 31) >> 5;
-    for (int sl = tid; sl < n; sl += kSortThreads) {
+    const int t0 = tid / p.kp;                             // token of this thread's first slot
+    const int dt = kSortThreads / p.kp, dj = kSortThreads - dt * p.kp;
+    const int j0 = tid - t0 * p.kp;
+    for (int sl = tid, t = t0, j = j0; sl < n; sl += kSortThreads) {
         const int e = local_expert(s_ids[sl], p);
-        const int t = sl / p.kp;
+        s_ids[sl] = e;
         if (e >= 0) atomicOr(&s_mask[(t >> 5) * p.Et + e], 1u << (t & 31));
+        t += dt;
+        j += dj;
+        if (j >= p.kp) {
+            j -= p.kp;
+            ++t;
+        }
     }
     __syncthreads();
     int cnt = 0;
     if (tid < p.Et) {
 #pragma unroll 8
-        for (int wd = 0; wd < nw; ++wd) cnt += __popc(s_mask[wd * p.Et + tid]);
+        for (int wd = 0; wd < nw; ++wd) {
+            if (s_pref) s_pref[wd * p.Et + tid] = static_cast<uint16_t>(cnt);
+            cnt += __popc(s_mask[wd * p.Et + tid]);
+        }
     }
     place_experts(p, cnt, s_off, s_tot);
     __syncthreads();
-    for (int sl = tid; sl < n; sl += kSortThreads) {
-        const int e = local_expert(s_ids[sl], p);
+    for (int sl = tid, t = t0, j = j0; sl < n; sl += kSortThreads) {
+        const int e = s_ids[sl];
         if (e >= 0) {
-            const int t = sl / p.kp;
+            const int wt = t >> 5;
             const uint32_t* m = s_mask + e;  // word w at m[w * Et]
-            int r = __popc(m[(t >> 5) * p.Et] & ((1u << (t & 31)) - 1u));
-#pragma unroll 8
-            for (int wd = 0; wd < (t >> 5); ++wd) r += __popc(m[wd * p.Et]);
+            int r = __popc(m[wt * p.Et] & ((1u << (t & 31)) - 1u));
+            if (s_pref) {
+                r += s_pref[wt * p.Et + e];
+            } else {
+                for (int wd = 0; wd < wt; ++wd) r += __popc(m[wd * p.Et]);
+            }
             const int row = s_off[e] + r;
             p.c_map[sl] = row;
             if (s_rows) {
@@ -252,6 +273,12 @@ __device__ __forceinline__ void rank_by_token_masks(const SortParams& p, const i
             }
         } else {
             p.c_map[sl] = -1;
+        }
+        t += dt;
+        j += dj;
+        if (j >= p.kp) {
+            j -= p.kp;
+            ++t;
         }
     }
     if (s_rows) {
@@ -268,23 +295,35 @@ __device__ __forceinline__ void rank_by_token_masks(const SortParams& p, const i
 // The layer's own routing past the fused range: the ids are the routing's,
 // so one CTA ranks them with token bitmasks (rank_by_token_masks) instead of
 // the ballot-grouped passes that arbitrary ids (duplicates, masked -1) need.
+// Shared memory holds the masks and prefixes (Et * T/32 words and
+// half-words), then the slots' experts, their routing weights (row_w given)
+// and the row -> slot table (T * k' each): up to kSortTokensMaxT tokens when
+// that fits (T 512 at k' 17 and 896 experts does).
 constexpr int kSortTokensMaxT = 512;
-constexpr size_t kSortTokensRowsSmem = 200 * 1024;  // dynamic shared memory with the row -> slot table
+constexpr size_t kSortTokensMaxSmem = 220 * 1024;
 
-__global__ void __launch_bounds__(kSortThreads, 1)
-    sort_tokens_kernel(SortParams p, const float* w, float* row_w, int use_rows) {
+size_t sort_tokens_smem(int T, int kp, int Et, bool with_w) {
+    const size_t n = static_cast<size_t>(T) * kp;
+    const size_t nw = (static_cast<size_t>(T) + 31) / 32;
+    const size_t pref = ((static_cast<size_t>(Et) * nw * 2 + 3) / 4) * 4;
+    return static_cast<size_t>(Et) * nw * 4 + pref + n * 4 * (with_w ? 3 : 2);
+}
+
+__device__ __forceinline__ size_t sort_tokens_pref_bytes(int Et, int T) {
+    return ((static_cast<size_t>(Et) * ((T + 31) / 32) * 2 + 3) / 4) * 4;
+}
+
+__global__ void __launch_bounds__(kSortThreads, 1) sort_tokens_kernel(SortParams p, const float* w, float* row_w) {
     __shared__ int s_off[1024];
     __shared__ int s_tot[3][rs::kScanWarps];
-    // dynamic: [nw][Et] token bitmasks, the ids [T * k'], (row_w given) the
-    // slots' routing weights [T * k'] staged with the ids so that their loads
-    // are in flight together, then (use_rows) each row's slot [T * k']
     extern __shared__ uint32_t s_mask[];
     const int tid = threadIdx.x;
     const int nw = (p.T + 31) >> 5;
     const int n = p.T * p.kp;
-    int* s_ids = reinterpret_cast<int*>(s_mask + p.Et * nw);
+    uint16_t* s_pref = reinterpret_cast<uint16_t*>(s_mask + p.Et * nw);
+    int* s_ids = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(s_pref) + sort_tokens_pref_bytes(p.Et, p.T));
     float* s_w = reinterpret_cast<float*>(s_ids + n);
-    int* s_rows = use_rows ? reinterpret_cast<int*>(s_w + (row_w ? n : 0)) : nullptr;
+    int* s_rows = reinterpret_cast<int*>(s_w + (row_w ? n : 0));
     for (int wd = tid; wd < p.Et * nw; wd += kSortThreads) s_mask[wd] = 0;
     ptx::pdl_wait();
 #pragma unroll 4
@@ -293,7 +332,7 @@ __global__ void __launch_bounds__(kSortThreads, 1)
         if (row_w) s_w[sl] = w[sl];
     }
     __syncthreads();
-    rank_by_token_masks(p, s_ids, s_mask, s_off, s_tot, s_w, row_w, s_rows);
+    rank_by_token_masks(p, s_ids, s_mask, s_pref, s_off, s_tot, s_w, row_w, s_rows);
     ptx::pdl_launch_dependents();
 }
 
@@ -359,7 +398,7 @@ __global__ void __cluster_dims__(kRouteCtas, 1, 1) __launch_bounds__(kSortThread
         return;  // nothing reads the other CTAs' shared memory
     }
 
-    rank_by_token_masks(p, s_ids, s_mask, s_off, s_tot, rp.w, fuse_x ? gp.row_w : nullptr);
+    rank_by_token_masks(p, s_ids, s_mask, nullptr, s_off, s_tot, rp.w, fuse_x ? gp.row_w : nullptr, nullptr);
     // The launches that follow read the work list only after their
     // griddepcontrol.wait (the gate) or after a launch that waited (FC1).
     ptx::pdl_launch_dependents();
@@ -477,18 +516,16 @@ bool route_sort_fusable(int T, int kp) { return T <= kFusedMaxT && kp <= 33; }
 
 bool route_sort_fuses_x(int T) { return T > 0 && T <= kFuseXMaxT; }
 
-bool sort_tokens_ok(int T, int kp) { return T <= kSortTokensMaxT && kp <= 33; }
+bool sort_tokens_ok(int T, int kp, int Et) {
+    return T <= kSortTokensMaxT && sort_tokens_smem(T, kp, Et, true) <= kSortTokensMaxSmem;
+}
 
 cudaError_t launch_sort_tokens(const SortParams& p, cudaStream_t stream, bool pdl, const float* w, float* row_w) {
-    const size_t n = static_cast<size_t>(p.T) * p.kp;
-    size_t smem = (static_cast<size_t>(p.Et) * ((p.T + 31) / 32) + n * (row_w ? 2 : 1)) * 4;
-    const bool use_rows = smem + n * 4 <= kSortTokensRowsSmem;  // room for the row -> slot table
-    if (use_rows) smem += n * 4;
+    const size_t smem = sort_tokens_smem(p.T, p.kp, p.Et, row_w != nullptr);
     cudaError_t err = cudaFuncSetAttribute(sort_tokens_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(smem));
     if (err != cudaSuccess) return err;
-    return launch_kernel(sort_tokens_kernel, dim3(1), dim3(kSortThreads), smem, stream, pdl, p, w, row_w,
-                         use_rows ? 1 : 0);
+    return launch_kernel(sort_tokens_kernel, dim3(1), dim3(kSortThreads), smem, stream, pdl, p, w, row_w);
 }
 
 cudaError_t launch_route_sort_small(const RouteParams& rp, const SortParams& p, const GatherParams* gp,
