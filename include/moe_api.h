@@ -384,8 +384,9 @@ int moe_get_views(const moe_shape* shape, void* workspace, moe_views* views);
 int moe_get_status(const void* workspace, int32_t* status, int32_t* detail);
 
 /* GEMM2 strategy ("[FlashInfer] Device-side gating for the MoE GEMM2
- * path", sections 1-2).  Every forward launches a one-warp gate kernel right
- * after the sort, which reads the sorted table and picks, on the device:
+ * path", sections 1-2).  Every sort decides it on the device: the thread
+ * that places the experts and writes the sorted table's header (rows R)
+ * also picks:
  *   MOE_GEMM2_SPLIT  FC2 writes each routed row w * Y; the combine sums a
  *                    token's rows in ascending slot order (bit-reproducible);
  *   MOE_GEMM2_DENSE  FC2's epilogue reduces w * Y into an fp32 [T, H]
@@ -398,10 +399,10 @@ int moe_get_status(const void* workspace, int32_t* status, int32_t* detail);
  * <= 32 Mi and T * H * 4 bytes <= 32 MiB (the accumulator stays in L2, where
  * the reductions cost less than writing and re-reading the rows: the decode
  * batches), split otherwise (the long prefill); the chain of launches is the
- * same either way.  moe_set_gemm2_path
- * forces one path for every later call issued from this process (a captured
- * graph keeps the value of its capture); MOE_ERR_SHAPE for another value.
- * The path a call took is header word 5 of its workspace (0 split, 1 dense). */
+ * same either way.  moe_set_gemm2_path forces one path for every later sort
+ * (moe_sort, moe_layer*) issued from this process (a captured graph keeps
+ * the value of its capture); MOE_ERR_SHAPE for another value.  The path a
+ * call took is header word 5 of its workspace (0 split, 1 dense). */
 enum { MOE_GEMM2_AUTO = 0, MOE_GEMM2_SPLIT = 1, MOE_GEMM2_DENSE = 2 };
 int moe_set_gemm2_path(int32_t path);
 
@@ -421,10 +422,10 @@ int moe_test_set_stall(uint64_t stall_ns);
 int moe_num_sms(int32_t* num_sms);
 
 /* Number of kernel launches moe_layer (and moe_layer_host, besides its
- * copies) issues for the shape: route + sort (one fused launch up to 1024
- * slots T*k', else route and a one- or three-kernel sort), then for T > 0 the
- * GEMM2 gate, the gather (not in the decode tilings when route and sort are
- * fused), FC1, FC2 and the combine. */
+ * copies) issues for the shape: route + sort (one fused launch up to 64
+ * tokens, else route and a one- or three-kernel sort), then for T > 0 the x
+ * gather (not in the decode tilings up to 512 tokens, where the route launch
+ * quantises x), FC1, FC2 and the combine. */
 int moe_layer_launch_count(const moe_shape* shape, int32_t* count);
 
 #ifdef __cplusplus

@@ -21,11 +21,12 @@ constexpr int kFp4BytesPer128Row = 64;
 
 // moe_test_set_stall: read by every FC1 launch that is issued
 std::atomic<uint64_t> g_test_stall_ns{0};
-// moe_set_gemm2_path: read by every gate launch that is issued
+// moe_set_gemm2_path: read by every sort launch that is issued (the sort's
+// placement thread decides the GEMM2 path)
 std::atomic<int> g_gemm2_path{MOE_GEMM2_AUTO};
 
 // The gate's rule: the dense GEMM2 path when rows * H <= this many fp32
-// reductions and the accumulator fits well inside L2 (see gate.cu).
+// reductions and the accumulator fits well inside L2 (rs::gemm2_path).
 constexpr int64_t kDenseMaxElems = int64_t(32) << 20;
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -123,7 +124,7 @@ int run_sort(const moe_shape* s, const int32_t* ids, void* ws, cudaStream_t st, 
     SortParams p{ids, at<int32_t>(ws, L.header), at<int32_t>(ws, L.counts), at<int32_t>(ws, L.offsets),
                  at<int4>(ws, L.vinfo), at<int4>(ws, L.groups), at<int32_t>(ws, L.a_map), at<int32_t>(ws, L.c_map),
                  at<int32_t>(ws, L.vbase), at<int32_t>(ws, L.sort_hist), d.T, d.kp, d.Eg, d.E, d.off, d.S, d.Et, d.B,
-                 d.G, keep_status ? 1 : 0};
+                 d.G, keep_status ? 1 : 0, d.H, g_gemm2_path.load(), kDenseMaxElems};
     if (routed && sort_tokens_ok(d.T, d.kp, d.Et)) return cuda_rc(launch_sort_tokens(p, st, pdl, w, row_w));
     return cuda_rc(launch_sort(p, st, pdl));
 }
@@ -154,7 +155,7 @@ int run_route_sort(const moe_shape* s, const float* logits, const uint16_t* shar
         SortParams sp{ids, at<int32_t>(ws, L.header), at<int32_t>(ws, L.counts), at<int32_t>(ws, L.offsets),
                       at<int4>(ws, L.vinfo), at<int4>(ws, L.groups), at<int32_t>(ws, L.a_map), at<int32_t>(ws, L.c_map),
                       at<int32_t>(ws, L.vbase), at<int32_t>(ws, L.sort_hist), d.T, d.kp, d.Eg, d.E, d.off, d.S, d.Et,
-                      d.B, d.G, after_router ? 1 : 0};
+                      d.B, d.G, after_router ? 1 : 0, d.H, g_gemm2_path.load(), kDenseMaxElems};
         GatherParams gp{};
         const bool fuse_x = x != nullptr && L.x_token_order && route_sort_fuses_x(d.T);
         if (fuse_x) {
@@ -221,10 +222,6 @@ int run_forward(const moe_shape* s, const uint16_t* x, const moe_weights* wt, co
     }
     const int nsm = num_sms_cached();
     if (nsm <= 0) return MOE_ERR_CUDA;
-
-    // The GEMM2 gate: one warp after the sort chooses split or dense.
-    GateParams gt{at<int32_t>(ws, L.header), d.T, d.H, g_gemm2_path.load(), kDenseMaxElems};
-    if (launch_gate(gt, st, pdl) != cudaSuccess) return MOE_ERR_CUDA;
 
     GatherParams gp{};
     gp.x = x;
@@ -818,11 +815,11 @@ int moe_layer_launch_count(const moe_shape* s, int32_t* count) {
     const Dims d = make_dims(*s);
     const bool fused = route_sort_fusable(d.T, d.kp);
     int n = fused ? 1 : 1 + (sort_tokens_ok(d.T, d.kp, d.Et) ? 1 : sort_launch_count(static_cast<int64_t>(d.T) * d.kp));
-    // gate, [gather,] FC1, FC2, combine; the decode tilings' x quantisation
-    // rides on the fused route + sort up to 64 tokens, on the route launch up
-    // to 512
+    // [gather,] FC1, FC2, combine (the GEMM2 gate is decided inside the
+    // sort); the decode tilings' x quantisation rides on the fused route +
+    // sort up to 64 tokens, on the route launch up to 512
     const bool x_done = d.mode == kModeDecode && (fused ? route_sort_fuses_x(d.T) : sort_tokens_ok(d.T, d.kp, d.Et));
-    if (d.T > 0) n += x_done ? 4 : 5;
+    if (d.T > 0) n += x_done ? 3 : 4;
     *count = n;
     return MOE_OK;
 }

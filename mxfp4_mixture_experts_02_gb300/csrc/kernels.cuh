@@ -48,6 +48,10 @@ struct SortParams {
     int32_t* cta_hist;  // [ceil(T*k' / 4096)][Et]: large-sort scratch
     int T, kp, Eg, E, off, S, Et, B, G;
     int keep_status;    // 1: leave the status word as the router GEMM left it (it was reset before the router)
+    // the GEMM2 gate, decided where the expert placement writes the header
+    int H;
+    int gemm2_force;    // 0 the rule (rs::gemm2_path), 1 split, 2 dense
+    int64_t dense_max_elems;  // dense when rows * H <= this (and the accumulator fits)
 };
 
 // Router GEMM (x bf16 [T, H] times router rows bf16 [Eg, H] -> fp32 logits).
@@ -130,14 +134,6 @@ struct CombineParams {
     int t0;  // first token (tokens t0 .. T - 1; 0 for the whole batch)
 };
 
-// The one-warp GEMM2 gate: reads the sort's table and writes the path.
-struct GateParams {
-    int32_t* header;
-    int T, H;
-    int force;                // 0 the rule below, 1 split, 2 dense
-    int64_t dense_max_elems;  // dense when rows * H <= this
-};
-
 struct QuantParams {
     const float* w;
     uint8_t* codes;
@@ -193,7 +189,6 @@ cudaError_t launch_gather_nvfp4(const GatherParams& p, cudaStream_t stream, bool
 cudaError_t launch_gemm(bool fc1, const CUtensorMap& tmW, const CUtensorMap& tmX, const CUtensorMap& tmAux,
                         const GemmParams& p, int TM, int grid, cudaStream_t stream, bool pdl);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream, bool pdl);
-cudaError_t launch_gate(const GateParams& p, cudaStream_t stream, bool pdl);
 RouterTiling router_tiling(int T, int Eg, int num_sms);
 cudaError_t launch_router(const CUtensorMap& tmX, const CUtensorMap& tmW, const RouterParams& p, int grid,
                           cudaStream_t stream, bool pdl);

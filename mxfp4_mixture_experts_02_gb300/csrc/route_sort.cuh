@@ -239,10 +239,36 @@ __device__ __forceinline__ void block_scan3(int a, int b, int c, int& ea, int& e
     tc = s_tot[2][kScanWarps - 1];
 }
 
+// The GEMM2 gate ("[FlashInfer] Device-side gating for the MoE GEMM2 path",
+// sections 1 and 2): chosen on the device once the sorted table's row count
+// R is known, so one fixed launch chain (one CUDA graph) serves every
+// routing:
+//   split: FC2 writes each routed row (w * Y); the combine sums a token's rows
+//          in slot order (bit-reproducible);
+//   dense: FC2's epilogue reduces w * Y straight into an fp32 [T, H]
+//          accumulator at the L2 (the finalize fused into GEMM2); the combine
+//          only converts it to bf16.  The order of the reductions varies from
+//          run to run, so the last bits of the sums may too.
+// The rule: dense when the rows' reductions are few, R * H <= dense_max, and
+// the accumulator is small, T * H * 4 bytes <= 32 MiB (well inside the
+// 126 MiB L2, so the reductions run at the L2 and cost less than writing the
+// rows and reading them back); split otherwise.  Measured on GB300: dense is
+// faster at every decode workload, and 2x slower at the 32768-token prefill,
+// whose 470 MB accumulator lives in DRAM.  A caller may force either path.
+// The pages give the gate a one-warp launch after the sort; here the thread
+// that writes the sort's header decides, and the chain has no launch for it.
+__device__ __forceinline__ int gemm2_path(int R, int T, int H, int force, int64_t dense_max) {
+    if (force == 1) return kPathSplit;
+    if (force == 2) return kPathDense;
+    return (static_cast<int64_t>(R) * H <= dense_max && static_cast<int64_t>(T) * H * 4 <= (int64_t(32) << 20))
+               ? kPathDense
+               : kPathSplit;
+}
+
 // Expert-level placement (one CTA of 1024 threads, thread tid = expert):
 // given each expert's row count, scan (count, tiles, groups), write counts /
-// offsets / virtual experts / work groups and the header, and leave each
-// expert's first row in s_off (when given).
+// offsets / virtual experts / work groups and the header (with the GEMM2
+// gate's path), and leave each expert's first row in s_off (when given).
 __device__ __forceinline__ void place_experts(const SortParams& p, int cnt, int* s_off, int (*s_tot)[kScanWarps]) {
     const int tid = threadIdx.x;
     const int tiles = (cnt + p.B - 1) / p.B;
@@ -263,6 +289,7 @@ __device__ __forceinline__ void place_experts(const SortParams& p, int cnt, int*
         p.header[kHdrRows] = R;
         p.header[kHdrNumV] = V;
         p.header[kHdrNumGroups] = NG;
+        p.header[kHdrGemm2Path] = gemm2_path(R, p.T, p.H, p.gemm2_force, p.dense_max_elems);
         if (!p.keep_status) {
             p.header[kHdrStatus] = 0;
             p.header[kHdrDetail] = 0;

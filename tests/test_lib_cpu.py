@@ -113,16 +113,17 @@ def test_gemm2_path_override_checks_its_value():
 
 
 def test_layer_launch_count():
-    # decode: route + sort + x quantisation in one launch, GEMM2 gate, FC1, FC2, combine
-    assert moe.moe_layer_launch_count(_shape()) == 5
+    # decode: route + sort + x quantisation in one launch (the GEMM2 gate decided
+    # in it), FC1, FC2, combine
+    assert moe.moe_layer_launch_count(_shape()) == 4
     # up to 64 tokens the decode tilings route, sort and quantise x in one cluster launch;
     # up to 512 x rides on the route launch and a one-CTA sort follows
-    assert moe.moe_layer_launch_count(_shape(T=64, max_T=64)) == 5
-    assert moe.moe_layer_launch_count(_shape(T=65, max_T=65)) == 6
-    assert moe.moe_layer_launch_count(_shape(T=512, max_T=512)) == 6
-    # 513 tokens: route, one-CTA sort, gate, x quantisation, FC1, FC2, combine
-    assert moe.moe_layer_launch_count(_shape(T=513, max_T=513)) == 7
-    # prefill tiling at 32768 tokens: route, 3-kernel sort, gate, gather, FC1, FC2, combine
-    assert moe.moe_layer_launch_count(_shape(T=32768, max_T=32768, block_n=128)) == 9
+    assert moe.moe_layer_launch_count(_shape(T=64, max_T=64)) == 4
+    assert moe.moe_layer_launch_count(_shape(T=65, max_T=65)) == 5
+    assert moe.moe_layer_launch_count(_shape(T=512, max_T=512)) == 5
+    # 513 tokens: route, one-CTA sort, x quantisation, FC1, FC2, combine
+    assert moe.moe_layer_launch_count(_shape(T=513, max_T=513)) == 6
+    # prefill tiling at 32768 tokens: route, 3-kernel sort, gather, FC1, FC2, combine
+    assert moe.moe_layer_launch_count(_shape(T=32768, max_T=32768, block_n=128)) == 8
     assert moe.moe_layer_launch_count(_shape(T=0)) == 1
 
