@@ -250,6 +250,20 @@ def test_decode_shape_sweep_vs_oracle(cfg):
     check_layer(cfg, tokens=np.arange(cfg.T))
 
 
+# Longer decode batches on the same shape: at T 512 the one-CTA token-bitmask
+# sort runs with its largest tables (896 experts, k' 16 and 17: 180 and 186 KB
+# of shared memory); past 512 tokens the general sort and the x quantiser's
+# own launch.  The sorted maps are checked in full, the forward on 32 tokens
+# spread over the batch.
+LONG_DECODE = [synth.CONFIGS["decode_t32"].replace(T=512), synth.CONFIGS["skewed_shared_t256"].replace(T=512),
+               synth.CONFIGS["decode_t32"].replace(T=600)]
+
+
+@pytest.mark.parametrize("cfg", LONG_DECODE, ids=_cid)
+def test_decode_long_batches_vs_oracle(cfg):
+    check_layer(cfg, tokens=spread_tokens(cfg.T, 32))
+
+
 @pytest.mark.parametrize("cfg", FULL, ids=_cid)
 def test_layer_full_size_vs_oracle(cfg):
     # every token of the decode workloads; 64 tokens spread over the prefill
