@@ -536,9 +536,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float act_i0 = ACT == MOE_ACT_SITU ? 1.0f / p.act_c0 : 0.f;
         const float act_i1 = ACT == MOE_ACT_SITU ? 1.0f / p.act_c1 : 0.f;
         // FC2: the GEMM2 path the gate chose (dense: reduce w * Y into the
-        // token's accumulator row instead of writing the routed row).  The gate
-        // ran before FC1, which waited for it, and this grid launched after FC1
-        // finished its work, so the word is final.
+        // token's accumulator row instead of writing the routed row).  The
+        // sort decided it before FC1, which waited for the sort's grid (itself
+        // or through the gather), and this grid launched after FC1 finished its
+        // work, so the word is final.
         const bool dense = !FC1 && p.header[kHdrGemm2Path] == kPathDense;
         // Descriptors two items ahead and row weights (dense: and tokens) one
         // item ahead are loaded early, so no dependent load chain sits between
@@ -727,8 +728,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (kGatherX) {
             // Decode FC1: the six epilogue warps that hold no token lane zero
             // the dense GEMM2 accumulator when the gate chose that path (every
-            // thread of this grid waited for the gate's grid, above), so FC2's
-            // reductions start from zero.
+            // thread of this grid waited for the sort's grid, which decided
+            // it, above), so FC2's reductions start from zero.
             if (!active && p.header[kHdrGemm2Path] == kPathDense) {
                 const int wi = (q - 1) + 3 * half;  // 0..5
                 const int64_t n4 = static_cast<int64_t>(p.T) * p.H / 4;

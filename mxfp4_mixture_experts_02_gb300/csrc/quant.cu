@@ -92,8 +92,9 @@ __global__ void __launch_bounds__(kTokWarps * 32) gather_token_kernel(GatherPara
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     uint8_t* exp_bytes = reinterpret_cast<uint8_t*>(s_exp[warp]);
     const int nh = p.H / 16;  // half-blocks per row
-    // the gate ran before this launch: with the dense GEMM2 path, each token's
-    // fp32 accumulator row is zeroed here, before FC2 reduces into it
+    // the sort, which decided the GEMM2 path, ran before this launch: with the
+    // dense path, each token's fp32 accumulator row is zeroed here, before FC2
+    // reduces into it
     const bool zero_acc = p.header[kHdrGemm2Path] == kPathDense;
     for (int t = p.t0 + blockIdx.x * kTokWarps + warp; t < p.T; t += gridDim.x * kTokWarps) {
         if (zero_acc) {
