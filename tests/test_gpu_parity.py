@@ -492,6 +492,40 @@ def test_host_buffer_entry_point_matches_device_path(split_path, cfg):
         assert torch.equal(oh.view(torch.int16), ref.cpu().view(torch.int16))
 
 
+@pytest.mark.parametrize("cfg", [GRID[5], GRID[6]], ids=_cid)
+def test_layers_on_two_streams_run_independently(split_path, cfg):
+    # moe_layer calls alternating over two streams, each with its own
+    # workspace and inputs, issued without host synchronisation, so that their
+    # launches can overlap on the GPU: the chain keeps no state outside its
+    # workspace, and each output equals its own call's alone, bit for bit
+    shape = shape_of(cfg)
+    wts = _weights(cfg)
+    x, logits, sl = device_inputs(cfg)
+    flip = lambda t: t.flip(0).contiguous() if t is not None else None  # noqa: E731
+    inputs = [(x, logits, sl), (flip(x), flip(logits), flip(sl))]
+    ws0 = moe.workspace(shape)
+    refs = []
+    for xx, lg, s_ in inputs:
+        out, ids, w = moe.moe_layer(shape, lg, s_, xx, wts, ws0)
+        refs.append((out.clone(), ids.clone(), w.clone()))
+    torch.cuda.synchronize()
+    wss = [moe.workspace(shape), moe.workspace(shape)]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    results = []
+    for i in range(6):
+        xx, lg, s_ = inputs[i % 2]
+        with torch.cuda.stream(streams[i % 2]):
+            results.append(moe.moe_layer(shape, lg, s_, xx, wts, wss[i % 2]))
+    torch.cuda.synchronize()
+    for i, (out, ids, w) in enumerate(results):
+        r_out, r_ids, r_w = refs[i % 2]
+        assert torch.equal(ids, r_ids), i
+        assert torch.equal(w, r_w), i
+        assert torch.equal(out.view(torch.int16), r_out.view(torch.int16)), i
+    for w_ in wss:
+        assert moe.moe_get_status(w_) == (0, 0)
+
+
 def test_host_buffer_calls_on_two_streams(split_path):
     # consecutive moe_layer_host calls alternating over two caller streams,
     # each stream with its own workspace, different inputs per stream and no
