@@ -1,9 +1,11 @@
 """The GEMM2 gate and its two paths, through the C ABI (marked gpu).
 
-"[FlashInfer] Device-side gating for the MoE GEMM2 path": a one-warp kernel
-after the sort picks split (FC2 writes each routed row, the combine sums a
-token's rows) or dense (FC2's epilogue reduces w * Y into an fp32 [T, H]
-accumulator, the combine converts it), in one fixed launch chain.  Each path
+"[FlashInfer] Device-side gating for the MoE GEMM2 path": a device-side
+decision, taken once the sorted row count is known (here by the sort's
+placement thread, in the launch that writes the table's header), picks split
+(FC2 writes each routed row, the combine sums a token's rows) or dense (FC2's
+epilogue reduces w * Y into an fp32 [T, H] accumulator, the combine converts
+it), in one fixed launch chain.  Each path
 is forced through the gate here and must meet the layer's output bar against
 the oracle (relative L2 <= 1e-2, max-abs <= 2e-2; the page itself accepts a
 different summation order between the paths).  The gate's own rule is
@@ -29,6 +31,10 @@ CASES = [
     SMALL.replace(T=200, block_n=128, top_k=8, num_shared=1),
     SMALL.replace(T=256, block_n=16, E_local=32, expert_offset=16),  # EP slice: tokens without local rows
     synth.CONFIGS["tiny"],
+    # every token on experts 0 .. k-1 (Zipf s = 30): the dense path's
+    # reductions of four experts' tiles all land on the same token rows
+    SMALL.replace(T=600, block_n=32, zipf_s=30.0),
+    SMALL.replace(T=1000, block_n=128, num_shared=1, zipf_s=30.0),
 ]
 
 

@@ -264,6 +264,34 @@ def test_decode_long_batches_vs_oracle(cfg):
     check_layer(cfg, tokens=spread_tokens(cfg.T, 32))
 
 
+# Every token on the same experts: a Zipf popularity so steep (s = 30, logit
+# gaps of 20 and more between neighbouring ids against N(0, 1) noise) that
+# each token's top-k is experts 0 .. k-1 in that order.  Each of them holds all
+# T rows, cut into many virtual experts (tiles) of one expert: the most skewed
+# routing the method meets.  A slice that holds none of those experts gets no
+# routed row at all: its output is the shared expert's alone, or exactly zero.
+HOT = [
+    SMALL.replace(T=64, block_n=16, zipf_s=30.0),  # fused route + sort: 4 virtual experts per expert
+    SMALL.replace(T=300, block_n=32, num_shared=1, zipf_s=30.0),  # route launch + one-CTA token sort
+    SMALL.replace(T=600, block_n=32, zipf_s=30.0),  # general sort and the x quantiser's own launch
+    SMALL.replace(T=1000, block_n=128, num_shared=1, zipf_s=30.0),  # 128-row tiles: 8 per expert
+    SMALL.replace(T=200, block_n=32, E_local=32, expert_offset=32, zipf_s=30.0),  # no row at all
+    SMALL.replace(T=200, block_n=128, E_local=32, expert_offset=32, num_shared=1, zipf_s=30.0),  # shared rows only
+]
+
+
+@pytest.mark.parametrize("cfg", HOT, ids=_cid)
+def test_every_token_on_the_same_experts_vs_oracle(cfg):
+    orc = OracleCase(cfg)
+    np.testing.assert_array_equal(orc.ids[:, :cfg.top_k], np.tile(np.arange(cfg.top_k), (cfg.T, 1)))
+    local = [e for e in range(cfg.top_k) if cfg.expert_offset <= e < cfg.expert_offset + cfg.E_local]
+    counts = orc.sort["counts"]
+    assert sorted(counts[counts > 0].tolist()) == [cfg.T] * (len(local) + cfg.num_shared)
+    out = check_layer(cfg, tokens=spread_tokens(cfg.T, 24))
+    if not local and not cfg.num_shared:
+        assert not bf16_bits(out).any()  # no routed row: the output is +0 everywhere
+
+
 @pytest.mark.parametrize("cfg", FULL, ids=_cid)
 def test_layer_full_size_vs_oracle(cfg):
     # every token of the decode workloads; 64 tokens spread over the prefill
