@@ -292,6 +292,22 @@ def test_every_token_on_the_same_experts_vs_oracle(cfg):
         assert not bf16_bits(out).any()  # no routed row: the output is +0 everywhere
 
 
+# The largest routing shape the library takes: 1024 experts in all (1023 in the
+# local slice plus the shared one fill the 1024 local slots), top-32 plus the
+# shared expert (k' 33, the fused route + sort's limit), through the fused,
+# one-CTA and ballot sorts and the 128-row tiling.
+MAXR = SMALL.replace(E_global=1024, E_local=1023, expert_offset=1, top_k=32, num_shared=1, hidden=512, inter=128)
+MAX_ROUTING = [MAXR.replace(T=16, block_n=16), MAXR.replace(T=200, block_n=32), MAXR.replace(T=600, block_n=32),
+               MAXR.replace(T=300, block_n=128)]
+
+
+@pytest.mark.parametrize("cfg", MAX_ROUTING, ids=_cid)
+def test_largest_routing_shape_vs_oracle(cfg):
+    assert moe.moe_is_supported(shape_of(cfg))
+    assert not moe.moe_is_supported(shape_of(cfg.replace(E_local=1024, expert_offset=0)))  # 1025 local slots
+    check_layer(cfg, tokens=spread_tokens(cfg.T, 16))
+
+
 @pytest.mark.parametrize("cfg", FULL, ids=_cid)
 def test_layer_full_size_vs_oracle(cfg):
     # every token of the decode workloads; 64 tokens spread over the prefill
