@@ -308,6 +308,41 @@ def test_largest_routing_shape_vs_oracle(cfg):
     check_layer(cfg, tokens=spread_tokens(cfg.T, 16))
 
 
+@pytest.mark.parametrize("cfg", [SMALL.replace(T=37, block_n=32), SMALL.replace(T=600, block_n=16, num_shared=1),
+                                 SMALL.replace(T=300, block_n=128)], ids=_cid)
+def test_workspace_sized_for_a_larger_batch(cfg):
+    # A workspace carved for max_T 4096, first filled by a 4096-token call, then
+    # called with T tokens: the ids, weights and output equal those of a call on
+    # a workspace carved for exactly T -- bit for bit on the split path, within
+    # one bf16 step on the dense path (its reductions run in no fixed order).
+    # Nothing a call reads may come from a region sized by max_T but written
+    # only by an earlier, larger call.
+    wts = _weights(cfg)
+    x, logits, sl = device_inputs(cfg)
+    xb, lb, sb = device_inputs(cfg, T=4096)
+    exact, big = shape_of(cfg), shape_of(cfg)
+    big.max_T = 4096
+    full = shape_of(cfg, T=4096)
+    for path in (moe.GEMM2_SPLIT, moe.GEMM2_DENSE):
+        moe.moe_set_gemm2_path(path)
+        try:
+            ws_e, ws_b = moe.workspace(exact), moe.workspace(big)
+            a = moe.moe_layer(exact, logits, sl, x, wts, ws_e)
+            moe.moe_layer(full, lb, sb, xb, wts, ws_b)
+            b = moe.moe_layer(big, logits, sl, x, wts, ws_b)
+            torch.cuda.synchronize()
+        finally:
+            moe.moe_set_gemm2_path(moe.GEMM2_AUTO)
+        assert moe.moe_get_status(ws_e) == (0, 0) and moe.moe_get_status(ws_b) == (0, 0)
+        assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
+        if path == moe.GEMM2_SPLIT:
+            assert torch.equal(a[0].view(torch.int16), b[0].view(torch.int16))
+        else:
+            fa, fb = a[0].double().cpu().numpy(), b[0].double().cpu().numpy()
+            step = np.exp2(np.floor(np.log2(np.maximum(np.abs(fa), 1e-30))) - 7)
+            assert np.all(np.abs(fa - fb) <= step)
+
+
 @pytest.mark.parametrize("cfg", FULL, ids=_cid)
 def test_layer_full_size_vs_oracle(cfg):
     # every token of the decode workloads; 64 tokens spread over the prefill
