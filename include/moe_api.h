@@ -395,11 +395,11 @@ int moe_get_status(const void* workspace, int32_t* status, int32_t* detail);
  *                    converts it to bf16.  The reductions' order varies, so
  *                    the result is within the layer's tolerance but not
  *                    bit-reproducible.
- * The gate's own rule (MOE_GEMM2_AUTO, the default) takes dense when rows * H
- * <= 32 Mi and T * H * 4 bytes <= 32 MiB (the accumulator stays in L2, where
- * the reductions cost less than writing and re-reading the rows: the decode
- * batches), split otherwise (the long prefill); the chain of launches is the
- * same either way.  moe_set_gemm2_path forces one path for every later sort
+ * The gate's own rule (MOE_GEMM2_AUTO, the default) takes dense when the
+ * accumulator stays in L2, T * H * 4 bytes <= 32 MiB, and, at block_n 128
+ * (whose split rows are bf16, cheaper to write and re-read than the decode
+ * tilings' fp32 rows), rows * H <= 56 Mi; split otherwise (the long
+ * prefill); the chain of launches is the same either way.  moe_set_gemm2_path forces one path for every later sort
  * (moe_sort, moe_layer*) issued from this process (a captured graph keeps
  * the value of its capture); MOE_ERR_SHAPE for another value.  The path a
  * call took is header word 5 of its workspace (0 split, 1 dense). */

@@ -25,9 +25,10 @@ std::atomic<uint64_t> g_test_stall_ns{0};
 // placement thread decides the GEMM2 path)
 std::atomic<int> g_gemm2_path{MOE_GEMM2_AUTO};
 
-// The gate's rule: the dense GEMM2 path when rows * H <= this many fp32
-// reductions and the accumulator fits well inside L2 (rs::gemm2_path).
-constexpr int64_t kDenseMaxElems = int64_t(32) << 20;
+// The gate's rule at 128-row tiles: the dense GEMM2 path when rows * H <=
+// this many fp32 reductions and the accumulator fits well inside L2; the
+// decode tilings take dense whenever the accumulator fits (rs::gemm2_path).
+constexpr int64_t kDenseMaxElems = int64_t(56) << 20;
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;

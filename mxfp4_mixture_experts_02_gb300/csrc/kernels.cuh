@@ -51,7 +51,7 @@ struct SortParams {
     // the GEMM2 gate, decided where the expert placement writes the header
     int H;
     int gemm2_force;    // 0 the rule (rs::gemm2_path), 1 split, 2 dense
-    int64_t dense_max_elems;  // dense when rows * H <= this (and the accumulator fits)
+    int64_t dense_max_elems;  // 128-row tiles: dense when rows * H <= this (and the accumulator fits)
 };
 
 // Router GEMM (x bf16 [T, H] times router rows bf16 [Eg, H] -> fp32 logits).

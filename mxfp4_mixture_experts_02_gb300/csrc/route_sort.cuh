@@ -249,20 +249,26 @@ __device__ __forceinline__ void block_scan3(int a, int b, int c, int& ea, int& e
 //          accumulator at the L2 (the finalize fused into GEMM2); the combine
 //          only converts it to bf16.  The order of the reductions varies from
 //          run to run, so the last bits of the sums may too.
-// The rule: dense when the rows' reductions are few, R * H <= dense_max, and
-// the accumulator is small, T * H * 4 bytes <= 32 MiB (well inside the
-// 126 MiB L2, so the reductions run at the L2 and cost less than writing the
-// rows and reading them back); split otherwise.  Measured on GB300: dense is
-// faster at every decode workload, and 2x slower at the 32768-token prefill,
-// whose 470 MB accumulator lives in DRAM.  A caller may force either path.
-// The pages give the gate a one-warp launch after the sort; here the thread
-// that writes the sort's header decides, and the chain has no launch for it.
-__device__ __forceinline__ int gemm2_path(int R, int T, int H, int force, int64_t dense_max) {
+// The rule: dense needs the accumulator to stay in L2, T * H * 4 bytes <=
+// 32 MiB (well inside the 126 MiB L2: the reductions then run at the L2).
+// Within that, the split rows' format decides.  The decode tilings' split
+// rows are fp32 (8 bytes per element written and read back), which costs
+// more than the reductions at every such batch: dense.  The 128-row tiling's
+// rows are bf16 (4 bytes per element), cheaper than the reductions once
+// there are many: dense only while R * H <= dense_max_128.  Measured on
+// GB300 (H 3584, top-16): decode tilings dense faster at every T up to 2340
+// (742 against 848 us per layer there); 128-row tiles dense faster up to
+// T 1024 (R * H = 56 Mi; 470 against 475 us), split from T 1280 (484 against
+// 491 us) and 2x faster at the 32768-token prefill, whose 470 MB accumulator
+// lives in DRAM.  A caller may force either path.  The pages give the gate
+// a one-warp launch after the sort; here the thread that writes the sort's
+// header decides, and the chain has no launch for it.
+__device__ __forceinline__ int gemm2_path(int R, int T, int H, int B, int force, int64_t dense_max_128) {
     if (force == 1) return kPathSplit;
     if (force == 2) return kPathDense;
-    return (static_cast<int64_t>(R) * H <= dense_max && static_cast<int64_t>(T) * H * 4 <= (int64_t(32) << 20))
-               ? kPathDense
-               : kPathSplit;
+    const bool acc_in_l2 = static_cast<int64_t>(T) * H * 4 <= (int64_t(32) << 20);
+    const bool rows_ok = B < 128 || static_cast<int64_t>(R) * H <= dense_max_128;
+    return acc_in_l2 && rows_ok ? kPathDense : kPathSplit;
 }
 
 // Expert-level placement (one CTA of 1024 threads, thread tid = expert):
@@ -289,7 +295,7 @@ __device__ __forceinline__ void place_experts(const SortParams& p, int cnt, int*
         p.header[kHdrRows] = R;
         p.header[kHdrNumV] = V;
         p.header[kHdrNumGroups] = NG;
-        p.header[kHdrGemm2Path] = gemm2_path(R, p.T, p.H, p.gemm2_force, p.dense_max_elems);
+        p.header[kHdrGemm2Path] = gemm2_path(R, p.T, p.H, p.B, p.gemm2_force, p.dense_max_elems);
         if (!p.keep_status) {
             p.header[kHdrStatus] = 0;
             p.header[kHdrDetail] = 0;

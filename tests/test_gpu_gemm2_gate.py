@@ -76,8 +76,8 @@ def test_both_gemm2_paths_match_the_oracle(cfg):
 
 
 def test_gate_rule_on_the_workloads():
-    # dense where rows * H <= 32 Mi with a [T, H] fp32 accumulator of at most
-    # 32 MiB (every decode workload), split at the 32768-token prefill
+    # dense where the [T, H] fp32 accumulator is at most 32 MiB (every decode
+    # workload), split at the 32768-token prefill
     want = {"tiny": 1, "decode_t32": 1, "ep_slice_t64": 1, "skewed_shared_t256": 1, "prefill_t32768": 0}
     for name, path in want.items():
         cfg = synth.CONFIGS[name]
@@ -87,6 +87,23 @@ def test_gate_rule_on_the_workloads():
         moe.moe_layer(shape, logits, sl, x, device_weights(cfg), ws)
         torch.cuda.synchronize()
         assert int(moe.moe_get_views(shape, ws)["header"][5].item()) == path, name
+
+
+@pytest.mark.parametrize("T,block_n,path", [(2340, 32, 1), (2341, 32, 0), (2340, 16, 1), (1024, 128, 1),
+                                            (1025, 128, 0)])
+def test_gate_rule_boundaries(T, block_n, path):
+    # at the layer's shape (H 3584, 896 experts, top-16): the fp32 accumulator
+    # is 32 MiB at T 2340, one token more leaves L2 (split at every tiling);
+    # the 128-row tiling's rows * H reaches 56 Mi at T 1024 (R = 16 T)
+    shape = moe.MoeShape(T=T, max_T=T, E_global=896, E_local=896, expert_offset=0, top_k=16, num_shared=0,
+                         hidden=3584, inter=384, block_n=block_n)
+    rng = np.random.default_rng(T)
+    ids = np.argsort(rng.random((T, 896)), axis=1)[:, :16].astype(np.int32)  # 16 distinct experts per token
+    ws = moe.workspace(shape)
+    moe.moe_sort(shape, torch.from_numpy(ids).cuda(), ws)
+    torch.cuda.synchronize()
+    hdr = moe.moe_get_views(shape, ws)["header"].cpu().numpy()
+    assert hdr[0] == 16 * T and hdr[5] == path
 
 
 def test_dense_path_repeats_within_a_bf16_step():
