@@ -254,6 +254,32 @@ def rel_l2(a, b) -> float:
     return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30))
 
 
+def dense_repeat_bound(shape, ws_split, T: int):
+    """Per output element, how far two dense-path results may lie apart.  The
+    dense path sums a token's fp32 terms w * Y in no fixed order, so two runs'
+    fp32 sums each lie within (k' - 1) * 2^-24 * sum_j |w_j Y_j| of the exact
+    sum, then each is rounded to bf16 once.  sum_j |w_j Y_j| comes from the
+    split path's rows of the same inputs (the same fp32 products; at 128-row
+    tiles rounded to bf16, hence the 2^-7 margin).  Returns M; the bound is
+    one bf16 step of the larger result plus 2 k' 2^-24 M (1 + 2^-7)."""
+    v = moe.moe_get_views(shape, ws_split)
+    kp = shape.kp
+    cm = v["c_map"][:T * kp].view(T, kp).long()
+    y = v["y"].float()
+    M = torch.zeros((T, shape.hidden), dtype=torch.float64, device=y.device)
+    for j in range(kp):
+        rows = cm[:, j]
+        ok = rows >= 0
+        M[ok] += y[rows[ok]].abs().double()
+    return M.cpu().numpy() * 2 * kp * 2.0 ** -24 * (1 + 2.0 ** -7)
+
+
+def within_dense_repeat(a, b, slack) -> bool:
+    """a, b: bf16 outputs as float64 arrays."""
+    step = np.exp2(np.floor(np.log2(np.maximum(np.maximum(np.abs(a), np.abs(b)), 1e-30))) - 7)
+    return bool(np.all(np.abs(a - b) <= step + slack))
+
+
 E4M3_VALUES = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).double().numpy()
 
 
