@@ -399,8 +399,8 @@ __global__ void __cluster_dims__(kRouteCtas, 1, 1) __launch_bounds__(kSortThread
     }
 
     rank_by_token_masks(p, s_ids, s_mask, nullptr, s_off, s_tot, rp.w, fuse_x ? gp.row_w : nullptr, nullptr);
-    // The launches that follow read the work list only after their
-    // griddepcontrol.wait (the gate) or after a launch that waited (FC1).
+    // The launch that follows (FC1 at the decode tilings, the gather at
+    // 128-row tiles) reads the work list only after its griddepcontrol.wait.
     ptx::pdl_launch_dependents();
 }
 
