@@ -323,6 +323,33 @@ def test_largest_routing_shape_vs_oracle(cfg):
     check_layer(cfg, tokens=spread_tokens(cfg.T, 16))
 
 
+@pytest.mark.parametrize("cfg", [SMALL.replace(T=16, block_n=16, E_global=896, E_local=896, top_k=16),
+                                 SMALL.replace(T=100, block_n=32, E_global=896, E_local=896, top_k=16, num_shared=1),
+                                 SMALL.replace(T=200, block_n=128, top_k=8)], ids=_cid)
+def test_all_logits_equal_vs_oracle(cfg):
+    # every logit of every token equal (zero): the routing's heaviest tie
+    # (all experts candidates, the selection's fallback over all entries);
+    # ties go to the lower id, so each token takes experts 0 .. k-1 with
+    # weight 1/k, and the layer must still match the oracle
+    shape = shape_of(cfg)
+    x, logits, sl = device_inputs(cfg)
+    logits = torch.zeros_like(logits)
+    ws = moe.workspace(shape)
+    out, ids, w = moe.moe_layer(shape, logits, sl, x, _weights(cfg), ws)
+    torch.cuda.synchronize()
+    assert moe.moe_get_status(ws) == (0, 0)
+    orc = OracleCase(cfg, logits=np.zeros((cfg.T, cfg.E_global), np.float32))
+    np.testing.assert_array_equal(orc.ids[:, :cfg.top_k], np.tile(np.arange(cfg.top_k), (cfg.T, 1)))
+    np.testing.assert_array_equal(ids.cpu().numpy(), orc.ids)
+    wg = w.cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(wg - orc.w) <= 4e-6 * np.abs(orc.w) + 1e-7)
+    assert np.allclose(wg[:, :cfg.top_k], 1.0 / cfg.top_k, rtol=1e-6)
+    toks = spread_tokens(cfg.T, 8)
+    ref = orc.forward(toks)["out_f64"]
+    got = bf16_to_f64(bf16_bits(out)[toks])
+    assert rel_l2(got, ref) <= 1e-2 and float(np.max(np.abs(got - ref))) <= 2e-2
+
+
 # Wide layers: hidden 7168 and inter 2048 (14 / 16 K chunks per FC2 / FC1
 # item, 28 FC2 weight blocks and 16 FC1 blocks per expert), on both tilings
 # and both GEMM2 paths (nothing in the kernels is sized by H or I).
